@@ -1,0 +1,497 @@
+"""Benchmark: RMSNorm backward on GB300, one JSON line on stdout (rank 0).
+
+Default workload: plain RMSNorm backward, bf16, M=4096, N=4096, eps=1e-6,
+rstd from this library's forward; a step is one public backward call
+(row pass + cross-row weight-gradient reduction + fp32->bf16 cast), timed
+with CUDA events on the launching stream after the L2 has been flushed by
+writing a buffer twice the L2 size (outside the event pair).
+
+  value      algorithmic bytes / time, GB/s (whole job: summed over ranks,
+             divided by the slowest rank's time)
+  roofline   the row-pass kernel alone (events the library records around
+             it), against the measured HBM copy bandwidth
+  e2e        the same metric with host (pinned) inputs copied in and dx,
+             dweight copied out inside every timed step
+  cpu_baseline  the fp64 CPU oracle on the host cores, same workload
+
+`--impl reference` times the CPU oracle as the reference arm.
+Multi-GPU (torchrun): every rank runs an independent replica (the rows of
+this workload shard with no exchange but the weight-gradient sum, which a
+training framework's gradient all-reduce already performs).
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and achieved HBM GB/s (% of peak), RMSNorm & fused-add bwd, 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "bwd_row_kernel_bf16_4096x4096.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "rmsnorm_backward_bwd_gb300", "csrc", f)
+                  for f in ("bwd_row.cu", "common.cuh")]
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the row-pass kernel from the committed ncu
+    summary, if that summary was taken on the current kernel source."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            text = f.read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9,]+)", text)
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_tr.group(1).replace(",", ""))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a window."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inwin = [p for ts, p in rows if any(a - 0.15 <= ts <= b + 0.15 for a, b in self.windows)]
+        use = inwin if inwin else rows
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = sorted(x for x in (num(p[2]) for p in use) if x is not None)
+        mx = [x for x in (num(p[3]) for p in use) if x is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if p[6 + i] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use), "samples_in_window": len(inwin)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_case(name):
+    from rmsnorm_backward_bwd_gb300 import synth
+    table = {"plain_4096": synth.PLAIN_4096, "fused_4096": synth.FUSED_4096,
+             "fused_4096_nodres": synth.FUSED_4096_NODRES, "plain_16384x8192": synth.LARGE_PLAIN,
+             "fused_16384x8192": synth.LARGE_FUSED}
+    return table[name]
+
+
+class Problem:
+    """Device-resident inputs/outputs of one backward case, plus the call."""
+
+    def __init__(self, case, dev):
+        import torch
+        import rmsnorm_backward_bwd_gb300 as rn
+        from rmsnorm_backward_bwd_gb300 import synth
+        self.case = case
+        inp = synth.make_inputs(case, device=str(dev))
+        g = inp["gamma"]
+        if case.fused:
+            # the saved `added` and its rstd come from the fused forward
+            _, self.x, self.rstd = rn.fused_add_rmsnorm_fwd(inp["x"], inp["residual"], g, case.eps)
+            del inp["residual"]
+        else:
+            self.x = inp["x"]
+            _, self.rstd = rn.rmsnorm_fwd(self.x, g, case.eps)
+        self.g, self.dy, self.dres = g, inp["dy"], inp.get("dres")
+        self.dx = torch.empty_like(self.x)
+        self.dw32 = torch.empty(case.N, dtype=torch.float32, device=dev)
+        self.dw = torch.empty(case.N, dtype=self.x.dtype, device=dev)
+        self.ws = rn.bwd_workspace(case.M, case.N, self.x.dtype, dev)
+        self.bytes = synth.algorithmic_bytes(case.M, case.N, case.dtype, case.with_dres, True)
+        s = synth.ELEM_BYTES[case.dtype]
+        # the row pass alone: read x|added, dy, [dres], gamma, rstd; write dx
+        self.row_pass_bytes = (case.M * case.N * s * (4 if case.with_dres else 3)
+                               + case.N * s + 4 * case.M)
+        torch.cuda.synchronize()
+
+    def call(self):
+        import rmsnorm_backward_bwd_gb300 as rn
+        if self.case.fused:
+            rn.fused_add_rmsnorm_bwd(self.x, self.g, self.dy, self.rstd, self.dres, dx=self.dx,
+                                     dweight_f32=self.dw32, dweight=self.dw, workspace=self.ws)
+        else:
+            rn.rmsnorm_bwd(self.x, self.g, self.dy, self.rstd, dx=self.dx, dweight_f32=self.dw32,
+                           dweight=self.dw, workspace=self.ws)
+
+
+def launches_per_call(plan):
+    if "dw=atomic" in plan:
+        return 3  # zero, row pass, cast
+    return 2      # row pass, finalize (+cast)
+
+
+def time_calls(prob, steps, warmup, flush, ws, sampler=None, kernel_events=False):
+    """Per-call device time (ms) with an L2 flush before each call."""
+    import torch
+    from rmsnorm_backward_bwd_gb300 import native
+    for _ in range(warmup):
+        flush.zero_()
+        prob.call()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)] if kernel_events else None
+    t0 = time.time()
+    for i in range(steps):
+        flush.zero_()
+        if kev:
+            native.lib().rn_set_profile_events(kev[i][0].cuda_event, kev[i][1].cuda_event)
+        ev[i][0].record(st)
+        prob.call()
+        ev[i][1].record(st)
+    if kev:
+        native.lib().rn_set_profile_events(None, None)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(ws)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(t0, t1)
+    call_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev] if kev else None
+    return call_ms, kern_ms, t1 - t0
+
+
+def time_e2e(prob, steps, warmup, ws):
+    """Same call with inputs in pinned host memory copied in, and dx + dweight
+    copied out, inside every timed step (one stream, CUDA events)."""
+    import torch
+    c = prob.case
+    host = {k: getattr(prob, k).cpu().pin_memory() for k in ("x", "g", "dy", "rstd")}
+    if prob.dres is not None:
+        host["dres"] = prob.dres.cpu().pin_memory()
+    out_dx = torch.empty(prob.dx.shape, dtype=prob.dx.dtype).pin_memory()
+    out_dw = torch.empty(prob.dw.shape, dtype=prob.dw.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_dx.numel() * out_dx.element_size() + out_dw.numel() * out_dw.element_size()
+
+    def step():
+        for k, t in host.items():
+            getattr(prob, k).copy_(t, non_blocking=True)
+        prob.call()
+        out_dx.copy_(prob.dx, non_blocking=True)
+        out_dw.copy_(prob.dw, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(steps):
+        step()
+    b.record(st)
+    torch.cuda.synchronize()
+    barrier(ws)
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def oracle_rate(case, seconds, nthreads=0):
+    """fp64 CPU oracle on the case's full problem, repeated for ~`seconds`."""
+    import numpy as np
+    import torch
+    import oracle
+    from rmsnorm_backward_bwd_gb300 import synth
+    inp = synth.make_inputs(case)
+    g = inp["gamma"].to(torch.float64).numpy()
+    dy = inp["dy"].to(torch.float64).numpy()
+    if case.fused:
+        _, x, rstd = oracle.fused_add_rmsnorm_fwd(inp["x"].to(torch.float64).numpy(),
+                                                  inp["residual"].to(torch.float64).numpy(), g,
+                                                  np.float32(case.eps), case.dtype, nthreads)
+    else:
+        x = inp["x"].to(torch.float64).numpy()
+        _, rstd = oracle.rmsnorm_fwd(x, g, np.float32(case.eps), nthreads)
+    rstd = oracle.round_to(rstd, "f32")
+    dres = inp["dres"].to(torch.float64).numpy() if "dres" in inp else None
+    cores = oracle.max_threads() if nthreads <= 0 else nthreads
+    times = []
+    t_end = time.time() + seconds
+    while True:
+        t = time.perf_counter()
+        if case.fused:
+            oracle.fused_add_rmsnorm_bwd(x, g, dy, rstd, dres, nthreads)
+        else:
+            oracle.rmsnorm_bwd(x, g, dy, rstd, nthreads)
+        times.append(time.perf_counter() - t)
+        if time.time() >= t_end:
+            break
+    nbytes = synth.algorithmic_bytes(case.M, case.N, case.dtype, case.with_dres, True)
+    return nbytes * len(times) / sum(times) / 1e9, cores, len(times), sum(times)
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle, timed as it stands."""
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if ws > 1 and rank != 0:
+        return
+    import numpy as np
+    import torch
+    import oracle
+    from rmsnorm_backward_bwd_gb300 import synth
+    case = workload_case(args.workload)
+    inp = synth.make_inputs(case)
+    x = inp["x"].to(torch.float64).numpy()
+    g = inp["gamma"].to(torch.float64).numpy()
+    dy = inp["dy"].to(torch.float64).numpy()
+    if case.fused:
+        _, x, rstd = oracle.fused_add_rmsnorm_fwd(x, inp["residual"].to(torch.float64).numpy(),
+                                                  g, np.float32(case.eps), case.dtype)
+    else:
+        _, rstd = oracle.rmsnorm_fwd(x, g, np.float32(case.eps))
+    rstd = oracle.round_to(rstd, "f32")
+    dres = inp["dres"].to(torch.float64).numpy() if "dres" in inp else None
+    # each step: a bounded sample of the workload's rows (whole problem when
+    # it takes under ~0.5 s)
+    rows = case.M
+    call = (lambda xs, dys, rs, drs: oracle.fused_add_rmsnorm_bwd(xs, g, dys, rs, drs)
+            if case.fused else oracle.rmsnorm_bwd(xs, g, dys, rs))
+    t = time.perf_counter()
+    call(x[:256], dy[:256], rstd[:256], dres[:256] if dres is not None else None)
+    per_row = (time.perf_counter() - t) / 256
+    rows = int(min(case.M, max(1, 0.5 / max(per_row, 1e-9))))
+    xs, dys, rs = x[:rows], dy[:rows], rstd[:rows]
+    drs = dres[:rows] if dres is not None else None
+    for _ in range(args.warmup):
+        call(xs, dys, rs, drs)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        call(xs, dys, rs, drs)
+    dt = (time.perf_counter() - t) / args.steps
+    nbytes = synth.algorithmic_bytes(rows, case.N, case.dtype, case.with_dres, True)
+    gbs = nbytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": case.name, "M": case.M, "N": case.N, "eps": case.eps},
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": "%d of %d rows per step (fp64 C oracle, OpenMP)" % (rows, case.M)},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    from rmsnorm_backward_bwd_gb300 import native
+
+    ws, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or getattr(props, "l2_cache_size", 0) or (128 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    case = workload_case(args.workload)
+    prob = Problem(case, dev)
+    prob.call()
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    call_ms, _, wall = time_calls(prob, args.steps, args.warmup, flush, ws, sampler)
+    _, kern_ms, _ = time_calls(prob, args.steps, 3, flush, ws, sampler, kernel_events=True)
+    clocks = sampler.stop()
+
+    ms = float(np.mean(call_ms))
+    ms_max = max_over_ranks(ms, ws)
+    kms = max_over_ranks(float(np.mean(kern_ms)), ws)
+    value = prob.bytes * ws / (ms_max * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = prob.row_pass_bytes / (kms * 1e-3) / 1e9
+
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_ms, h2d, d2h = time_e2e(prob, e2e_steps, 3, ws)
+    e2e_ms = max_over_ranks(e2e_ms, ws)
+
+    extra = []
+    if not args.no_extra:
+        for name in ("fused_4096", "fused_4096_nodres", "plain_16384x8192", "fused_16384x8192"):
+            if name == args.workload:
+                continue
+            p2 = Problem(workload_case(name), dev)
+            cms, kms2, _ = time_calls(p2, max(20, args.steps // 4), args.warmup, flush, ws,
+                                      kernel_events=True)
+            t2 = float(np.mean(cms))
+            k2 = float(np.mean(kms2))
+            extra.append({"workload": p2.case.name, "us_per_call": round(t2 * 1e3, 2),
+                          "GBps": round(p2.bytes / (t2 * 1e-3) / 1e9, 1),
+                          "pct_of_peak": round(100 * p2.bytes / (t2 * 1e-3) / 1e9 / peak, 1),
+                          "row_pass_us": round(k2 * 1e3, 2),
+                          "row_pass_GBps": round(p2.row_pass_bytes / (k2 * 1e-3) / 1e9, 1),
+                          "plan": native.last_plan()})
+            del p2
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        rate, cores, n, secs = oracle_rate(case, args.cpu_seconds)
+        cpu = {"value": round(rate, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": "full %dx%d problem, %d calls in %.1f s (fp64 C oracle, OpenMP)" % (
+                   case.M, case.N, n, secs)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+            "us_per_call": round(ms_max * 1e3, 2),
+            "pct_of_peak": round(100 * value / ws / peak, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": case.dtype, "data": "synthetic",
+            "config": {"workload": case.name, "M": case.M, "N": case.N, "eps": case.eps,
+                       "step": "one backward call: row pass + weight-gradient reduction + cast",
+                       "l2": "flushed before every step (write of 2x L2 = %d MiB)" % (2 * l2 >> 20),
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": ncu_traffic(), "kernel": "bwd_row_kernel",
+                         "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": prob.row_pass_bytes,
+                         "us_per_launch": round(kms * 1e3, 2)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(prob.bytes * ws / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": launches_per_call(plan) * args.steps,
+            "clocks": clocks,
+            "plan": plan,
+            "extra": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="plain_4096",
+                    choices=["plain_4096", "fused_4096", "fused_4096_nodres", "plain_16384x8192",
+                             "fused_16384x8192"])
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import __graft_entry__
+    __graft_entry__.build()
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * rmsnorm_gb300.h -- C ABI of the GB300 (sm_103a) RMSNorm library.
+ *
+ * What it computes (FlyDSL pages):
+ *   forward, per row m of an [M,N] input:
+ *       rstd_m = 1 / sqrt(mean_j x_mj^2 + eps),   y_mj = x_mj * rstd_m * gamma_j
+ *     -- issue #769 "Add rmsnorm backward (+ forward saves rstd)", section
+ *        "Current state" (the per-row rrms), and PR #800's commit message
+ *        "Makes RMSNorm training-capable" (rstd is 1/RMS, fp32, shape (M,)).
+ *   backward, per row, with x_hat = x * rstd and wdy = dy * gamma:
+ *       c1 = mean_j(x_hat_j * wdy_j),  dx_j = (wdy_j - x_hat_j * c1) * rstd
+ *     and over all rows  dweight_j = sum_m dy_mj * x_hat_mj  (fp32, length N)
+ *     -- issue #769, section "Math (matches quack rmsnorm_bwd_ref)".
+ *   fused-add (prenorm): added = x + residual is saved (residual_out); the
+ *     backward runs on `added`, adds dresidual_out (if given) to dx, and dx is
+ *     also the gradient of residual (dx == dresidual)
+ *     -- PR #800 "Add fused-add / residual backward", section "What's included".
+ *
+ * Conventions shared by every call:
+ *   - All [M,N] tensors are row-major and contiguous (row stride N elements);
+ *     gamma, dweight are [N]; rstd is fp32 [M]; dweight_f32 is fp32 [N].
+ *   - One I/O dtype per call (rn_dtype) for x / residual / added / gamma /
+ *     dy / dresidual_out / y / out / residual_out / dx / dweight: the kernels
+ *     read every operand with that one element type. Every reduction and the
+ *     weight-gradient accumulation run in fp32; outputs are rounded to the
+ *     I/O dtype once, to nearest even.
+ *   - Pointers are DEVICE pointers on the calling thread's current CUDA
+ *     device; the caller owns every buffer. Nothing is allocated or freed.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *     asynchronous: they enqueue kernels on `stream` and return.
+ *   - Errors: argument checks run before anything is enqueued and return
+ *     RN_ERR_INVALID_ARG / RN_ERR_UNSUPPORTED / RN_ERR_WORKSPACE with nothing
+ *     launched; a failed launch returns RN_ERR_CUDA. rn_last_error() gives a
+ *     message for the calling thread's last failure.
+ *   - Output buffers must not overlap any input, except that the backward's
+ *     dx may be the very same buffer as dresidual_out (each element is read
+ *     before it is overwritten).
+ *   - N >= 1; M >= 0. M == 0 is a valid empty batch (the backward then writes
+ *     a zero dweight).
+ */
+#ifndef RMSNORM_GB300_H
+#define RMSNORM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rn_dtype { RN_F32 = 0, RN_F16 = 1, RN_BF16 = 2 } rn_dtype;
+
+typedef enum rn_status {
+    RN_OK = 0,
+    RN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad dtype code, bad option */
+    RN_ERR_UNSUPPORTED = 2,  /* shape/alignment no engine handles (e.g. N too large) */
+    RN_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    RN_ERR_WORKSPACE = 4,    /* workspace missing, misaligned or too small */
+    RN_ERR_TIMEOUT = 5       /* a device-side wait gave up (see rn_workspace_status) */
+} rn_status;
+
+/* Version of this ABI (increments on any incompatible change). */
+int rn_abi_version(void);
+
+/* Static text for a status code. */
+const char *rn_status_string(int status);
+
+/* Message describing the calling thread's most recent failure ("" if none). */
+const char *rn_last_error(void);
+
+/*
+ * Forward, plain RMSNorm (issue #769 "Current state"; PR #800 commit
+ * "Makes RMSNorm training-capable", store_rstd).
+ *   x      [M,N] dtype, in
+ *   gamma  [N]   dtype, in
+ *   eps    added to the mean square before the reciprocal square root
+ *   y      [M,N] dtype, out: x * rstd * gamma
+ *   rstd   [M] fp32, out, may be NULL (then not stored)
+ */
+rn_status rn_rmsnorm_fwd(const void *x, const void *gamma, float eps, void *y, float *rstd,
+                         int64_t M, int64_t N, int dtype, void *stream);
+
+/*
+ * Forward, fused-add (prenorm) RMSNorm (PR #800 "What's included").
+ *   x, residual   [M,N] dtype, in
+ *   gamma         [N] dtype, in
+ *   out           [M,N] dtype, out: added * rstd * gamma
+ *   residual_out  [M,N] dtype, out: added = x + residual, rounded to dtype;
+ *                 the statistic and `out` are computed from this rounded value
+ *   rstd          [M] fp32, out (of `added`), may be NULL
+ */
+rn_status rn_fused_add_rmsnorm_fwd(const void *x, const void *residual, const void *gamma,
+                                   float eps, void *out, void *residual_out, float *rstd,
+                                   int64_t M, int64_t N, int dtype, void *stream);
+
+/*
+ * Bytes of workspace the backward needs on the current device for an [M,N]
+ * problem (scratch partials of the weight gradient plus a 256-byte header
+ * holding a device status word). Needs a CUDA device; writes *bytes.
+ * The workspace must be 256-byte aligned and ZEROED ONCE when allocated; the
+ * library keeps its header consistent afterwards. Calls that share one
+ * workspace must be ordered on the GPU (one stream, or events).
+ */
+rn_status rn_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes);
+
+/*
+ * Backward, plain RMSNorm (issue #769 "Math").
+ *   x            [M,N] dtype, in (the forward's input)
+ *   gamma        [N] dtype, in
+ *   dy           [M,N] dtype, in (gradient of y)
+ *   rstd         [M] fp32, in: the statistic the forward saved (not recomputed)
+ *   dx           [M,N] dtype, out
+ *   dweight_f32  [N] fp32, out: fully overwritten with sum_m dy*x_hat
+ *   dweight      [N] dtype, out, may be NULL: dweight_f32 rounded to dtype
+ *   workspace    device buffer of >= rn_bwd_workspace_bytes(M,N,dtype) bytes
+ * Every step (zero, row pass, cross-row reduction, cast) runs inside this call.
+ */
+rn_status rn_rmsnorm_bwd(const void *x, const void *gamma, const void *dy, const float *rstd,
+                         void *dx, float *dweight_f32, void *dweight,
+                         void *workspace, size_t workspace_bytes,
+                         int64_t M, int64_t N, int dtype, void *stream);
+
+/*
+ * Backward, fused-add RMSNorm (PR #800 "What's included").
+ *   added          [M,N] dtype, in: the saved x + residual (residual_out)
+ *   gamma, dy, rstd as for rn_rmsnorm_bwd (rstd is the statistic of `added`)
+ *   dresidual_out  [M,N] dtype, in, may be NULL (read as zeros): gradient
+ *                  flowing into residual_out
+ *   dx             [M,N] dtype, out: (wdy - a_hat*c1)*rstd + dresidual_out;
+ *                  it is both the x gradient and the residual gradient. It may
+ *                  be the same buffer as dresidual_out.
+ *   dweight_f32, dweight, workspace as for rn_rmsnorm_bwd.
+ */
+rn_status rn_fused_add_rmsnorm_bwd(const void *added, const void *gamma, const void *dy,
+                                   const float *rstd, const void *dresidual_out, void *dx,
+                                   float *dweight_f32, void *dweight,
+                                   void *workspace, size_t workspace_bytes,
+                                   int64_t M, int64_t N, int dtype, void *stream);
+
+/*
+ * Read the device status word of a workspace: synchronises `stream`, copies
+ * the word to *status (0 = no device-side wait has given up; otherwise an
+ * rn_status code, e.g. RN_ERR_TIMEOUT). clear != 0 resets it to 0 afterwards.
+ */
+rn_status rn_workspace_status(void *workspace, int clear, int *status, void *stream);
+
+/*
+ * Tuning / test options. They are process-wide, not thread-safe, and apply
+ * to calls made after they are set; value 0 always means "automatic".
+ */
+typedef enum rn_option {
+    RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (bulk-copy pipeline), 2 = generic engine */
+    RN_OPT_DWEIGHT_MODE = 1,  /* 1 = scratch partials + finalize, 2 = fp32 atomics + cast */
+    RN_OPT_CHUNKS_PER_THREAD = 2, /* row engine: 16-byte chunks per thread per row: 1, 2, 4 */
+    RN_OPT_TEAMS_PER_CTA = 3, /* row engine: rows processed at once per CTA (1..15) */
+    RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8) */
+    RN_OPT_GRID = 5,          /* cap on the number of CTAs of the row pass */
+    RN_OPT_COUNT = 6
+} rn_option;
+
+rn_status rn_set_option(int option, int value);
+int rn_get_option(int option);
+
+/*
+ * Text describing the plan (engine, tile shape, grid, weight-gradient mode)
+ * the most recent backward call on this thread used; "" if none.
+ */
+const char *rn_last_plan(void);
+
+/*
+ * Timing hook: while both are non-NULL, every backward call records
+ * cudaEvent_t `ev_begin` just before its row-pass kernel and `ev_end` just
+ * after it, on the call's stream. Pass NULLs to switch off.
+ */
+rn_status rn_set_profile_events(void *ev_begin, void *ev_end);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_GB300_H */

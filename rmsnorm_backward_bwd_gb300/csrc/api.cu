@@ -1,0 +1,438 @@
+// C ABI of the library (declared in include/rmsnorm_gb300.h): argument
+// checks, engine selection, and the launch sequence of each call on the
+// caller's stream and current device.
+//
+// Backward launch sequences (the pages count the fp32 zero and the cast to
+// the parameter dtype inside the call -- FlyDSL PR #854 "Benchmark
+// contract"):
+//   scratch mode: row pass (partials -> workspace) -> finalize (sum + cast)
+//   atomic mode:  zero dweight_f32 -> row pass (fp32 atomics) -> [cast]
+// Kernels after the first are launched as programmatic dependents, so their
+// launch overlaps the tail of the kernel they wait for.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/rmsnorm_gb300.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace rn {
+
+static thread_local char g_err[512] = "";
+static thread_local char g_plan[256] = "";
+static int g_opts[RN_OPT_COUNT] = {0};
+static cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
+
+static rn_status fail(rn_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+static rn_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(RN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+    int num_sms = 0;
+    size_t smem_optin = 0;
+};
+
+static std::mutex g_mu;
+static std::unordered_map<int, DeviceInfo> g_devs;
+static std::unordered_map<long long, size_t> g_smem_set;  // (device, func) -> bytes set
+
+static cudaError_t device_info(DeviceInfo *out, int *dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev_out) *dev_out = dev;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_devs.find(dev);
+    if (it != g_devs.end()) {
+        *out = it->second;
+        return cudaSuccess;
+    }
+    DeviceInfo d;
+    int v = 0;
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    d.num_sms = v;
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    d.smem_optin = (size_t)v;
+    g_devs[dev] = d;
+    *out = d;
+    return cudaSuccess;
+}
+
+cudaError_t ensure_smem_attr(const void *func, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const long long key = ((long long)dev << 48) ^ (long long)(uintptr_t)func;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_smem_set.find(key);
+        if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
+    }
+    // Always set the kernel's cap to the device maximum we may ask for.
+    DeviceInfo d;
+    e = device_info(&d, nullptr);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)d.smem_optin);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_smem_set[key] = d.smem_optin;
+    return cudaSuccess;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Workspace partial rows the backward may use on a device.
+static int max_partial_rows(const DeviceInfo &d) { return 2 * d.num_sms; }
+
+static size_t ws_bytes_for(const DeviceInfo &d, int64_t N) {
+    return kWsHeaderBytes + (size_t)max_partial_rows(d) * (size_t)N * 4;
+}
+
+// ------------------------------------------------------------- planning
+static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
+    const int eb = elem_bytes(p.dtype);
+    const int row_bytes = p.N * eb;
+    if (row_bytes % 16) return false;
+    if (!aligned16(p.x) || !aligned16(p.dy) || !aligned16(p.gamma) || !aligned16(p.dx) ||
+        (p.dres && !aligned16(p.dres)))
+        return false;
+    const int nchunks = row_bytes / 16;
+    if (nchunks > kRowMaxChunks) return false;
+    const int nt = p.dres ? 3 : 2;
+
+    int cpt = g_opts[RN_OPT_CHUNKS_PER_THREAD];
+    int team;
+    if (cpt == 1 || cpt == 2 || cpt == 4) {
+        team = ((nchunks + cpt - 1) / cpt + 31) / 32 * 32;
+    } else {
+        // about 256 threads per row, 2 chunks each where possible
+        team = ((nchunks + 1) / 2 + 31) / 32 * 32;
+        if (team > 256) team = 256;
+        cpt = (nchunks + team - 1) / team;
+        cpt = cpt <= 1 ? 1 : (cpt <= 2 ? 2 : 4);
+        if (cpt == 4) team = ((nchunks + 3) / 4 + 31) / 32 * 32;
+    }
+    if (team > row_max_threads(cpt)) return false;
+
+    const size_t budget = (d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024);
+    const size_t stage = (size_t)nt * (size_t)((row_bytes + 127) / 128 * 128);
+    int teams = g_opts[RN_OPT_TEAMS_PER_CTA];
+    if (teams <= 0) {
+        teams = row_max_threads(cpt) / team;
+        if (teams > 15) teams = 15;
+        // keep at least 3 slots per team when the rows are long
+        while (teams > 1 && row_smem_bytes(teams, 3, nt, row_bytes) > budget) --teams;
+        // no more teams than rows per SM
+        int64_t rows_per_sm = (p.M + d.num_sms - 1) / d.num_sms;
+        if (rows_per_sm < 1) rows_per_sm = 1;
+        if (teams > rows_per_sm) teams = (int)rows_per_sm;
+    }
+    if (teams < 1 || teams > 15 || teams * team > row_max_threads(cpt)) return false;
+
+    int64_t grid = (p.M + teams - 1) / teams;
+    if (grid > d.num_sms) grid = d.num_sms;
+    if (g_opts[RN_OPT_GRID] > 0 && grid > g_opts[RN_OPT_GRID]) grid = g_opts[RN_OPT_GRID];
+    if (grid > max_partial_rows(d)) grid = max_partial_rows(d);
+    if (grid < 1) grid = 1;
+
+    int stages = g_opts[RN_OPT_STAGES];
+    if (stages <= 0) {
+        stages = (int)((budget - 2048) / (stage * teams));
+        if (stages > 8) stages = 8;
+        const int64_t rows_per_team = (p.M + grid * teams - 1) / (grid * teams);
+        if (stages > rows_per_team) stages = (int)(rows_per_team < 1 ? 1 : rows_per_team);
+    }
+    if (stages < 1 || stages > 8) return false;
+    const size_t smem = row_smem_bytes(teams, stages, nt, row_bytes);
+    if (smem > d.smem_optin) return false;
+
+    plan->cpt = cpt;
+    plan->team_threads = team;
+    plan->teams = teams;
+    plan->stages = stages;
+    plan->grid = (int)grid;
+    plan->smem = smem;
+    plan->atomic = false;
+    return true;
+}
+
+static void plan_generic(const BwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
+    plan->threads = p.N >= 4096 ? 512 : 256;
+    const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
+    plan->smem_dw = generic_smem_bytes(p.N, true) <= budget;
+    plan->smem = generic_smem_bytes(p.N, plan->smem_dw);
+    int64_t grid = p.M;
+    if (grid > max_partial_rows(d)) grid = max_partial_rows(d);
+    if (g_opts[RN_OPT_GRID] > 0 && grid > g_opts[RN_OPT_GRID]) grid = g_opts[RN_OPT_GRID];
+    if (grid < 1) grid = 1;
+    plan->grid = (int)grid;
+    plan->atomic = false;
+}
+
+// Weight-gradient mode: scratch partials + finalize by default (deterministic
+// and no separate zeroing); atomics only when asked for.
+static bool want_atomic(const BwdProblem &p) {
+    const int m = g_opts[RN_OPT_DWEIGHT_MODE];
+    if (m == 2) return aligned16(p.dw_f32);
+    return false;
+}
+
+static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
+    DeviceInfo d;
+    int dev = 0;
+    cudaError_t e = device_info(&d, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    if (p.ws == nullptr) return fail(RN_ERR_WORKSPACE, "workspace is NULL");
+    if (((uintptr_t)p.ws & 255u) != 0) return fail(RN_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    const size_t need = ws_bytes_for(d, p.N);
+    if (ws_bytes < need)
+        return fail(RN_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+
+    if (p.M == 0) {
+        e = launch_finalize(nullptr, 0, p.N, p.dw_f32, p.dw_cast, p.dtype, s, false);
+        snprintf(g_plan, sizeof(g_plan), "empty batch: finalize only");
+        return e == cudaSuccess ? RN_OK : cuda_fail(e, "finalize launch");
+    }
+
+    const int engine = g_opts[RN_OPT_BWD_ENGINE];
+    RowPlan rp;
+    GenericPlan gp;
+    bool use_row = false;
+    if (engine != 2) {
+        use_row = plan_row(p, d, &rp);
+        if (!use_row && engine == 1)
+            return fail(RN_ERR_UNSUPPORTED, "row engine cannot take N=%d dtype=%d here", p.N,
+                        p.dtype);
+    }
+    if (!use_row) plan_generic(p, d, &gp);
+    const bool atomic = want_atomic(p);
+    rp.atomic = gp.atomic = atomic;
+    if (!use_row && atomic) {
+        gp.smem_dw = true;
+        gp.smem = generic_smem_bytes(p.N, true);
+        if (gp.smem > d.smem_optin) return fail(RN_ERR_UNSUPPORTED, "atomic mode needs N*4 bytes of shared memory");
+    }
+    const int G = use_row ? rp.grid : gp.grid;
+    if (use_row)
+        snprintf(g_plan, sizeof(g_plan),
+                 "engine=row cpt=%d team_threads=%d teams=%d stages=%d grid=%d smem=%zu dw=%s",
+                 rp.cpt, rp.team_threads, rp.teams, rp.stages, rp.grid, rp.smem,
+                 atomic ? "atomic" : "scratch");
+    else
+        snprintf(g_plan, sizeof(g_plan), "engine=generic threads=%d grid=%d smem_dw=%d dw=%s",
+                 gp.threads, gp.grid, (int)gp.smem_dw, atomic ? "atomic" : "scratch");
+
+    if (atomic) {
+        e = launch_zero_f32(p.dw_f32, p.N, s);
+        if (e != cudaSuccess) return cuda_fail(e, "zero launch");
+    }
+    const bool prof = g_ev_begin && g_ev_end;
+    if (prof) {
+        e = cudaEventRecord(g_ev_begin, s);
+        if (e != cudaSuccess) return cuda_fail(e, "profile event");
+    }
+    e = use_row ? launch_bwd_row(p, rp, s, atomic) : launch_bwd_generic(p, gp, s, atomic);
+    if (e != cudaSuccess) return cuda_fail(e, "row pass launch");
+    if (prof) {
+        e = cudaEventRecord(g_ev_end, s);
+        if (e != cudaSuccess) return cuda_fail(e, "profile event");
+    }
+    if (atomic) {
+        if (p.dw_cast) {
+            e = launch_cast(p.dw_f32, p.dw_cast, p.N, p.dtype, s, !prof);
+            if (e != cudaSuccess) return cuda_fail(e, "cast launch");
+        }
+    } else {
+        e = launch_finalize(reinterpret_cast<const float *>(p.ws + kWsHeaderBytes), G, p.N,
+                            p.dw_f32, p.dw_cast, p.dtype, s, !prof);
+        if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+    }
+    return RN_OK;
+}
+
+static rn_status check_common(int64_t M, int64_t N, int dtype) {
+    if (dtype < RN_F32 || dtype > RN_BF16) return fail(RN_ERR_INVALID_ARG, "bad dtype code %d", dtype);
+    if (M < 0) return fail(RN_ERR_INVALID_ARG, "M must be >= 0 (got %lld)", (long long)M);
+    if (N < 1) return fail(RN_ERR_INVALID_ARG, "N must be >= 1 (got %lld)", (long long)N);
+    if (N > (int64_t)1 << 28) return fail(RN_ERR_UNSUPPORTED, "N too large (%lld)", (long long)N);
+    if (M > ((int64_t)1 << 62) / N) return fail(RN_ERR_INVALID_ARG, "M*N overflows");
+    return RN_OK;
+}
+
+static rn_status bwd_entry(const void *x, const void *gamma, const void *dy, const float *rstd,
+                           const void *dres, void *dx, float *dw_f32, void *dw_cast, void *ws,
+                           size_t ws_bytes, int64_t M, int64_t N, int dtype, void *stream) {
+    g_err[0] = 0;
+    g_plan[0] = 0;
+    rn_status st = check_common(M, N, dtype);
+    if (st != RN_OK) return st;
+    if (!gamma || !dw_f32) return fail(RN_ERR_INVALID_ARG, "gamma and dweight_f32 are required");
+    if (M > 0 && (!x || !dy || !rstd || !dx))
+        return fail(RN_ERR_INVALID_ARG, "x, dy, rstd and dx are required when M > 0");
+    if (M > 0 && (dx == x || dx == dy || (void *)dx == (void *)rstd))
+        return fail(RN_ERR_INVALID_ARG, "dx must not alias x, dy or rstd");
+    BwdProblem p;
+    p.x = x;
+    p.gamma = gamma;
+    p.dy = dy;
+    p.rstd = rstd;
+    p.dres = dres;
+    p.dx = dx;
+    p.dw_f32 = dw_f32;
+    p.dw_cast = dw_cast;
+    p.ws = static_cast<uint8_t *>(ws);
+    p.M = M;
+    p.N = (int)N;
+    p.dtype = dtype;
+    return run_bwd(p, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+static rn_status fwd_entry(const void *x, const void *residual, const void *gamma, float eps,
+                           void *y, void *residual_out, float *rstd, int64_t M, int64_t N,
+                           int dtype, void *stream, bool fused) {
+    g_err[0] = 0;
+    rn_status st = check_common(M, N, dtype);
+    if (st != RN_OK) return st;
+    if (!(eps >= 0.f)) return fail(RN_ERR_INVALID_ARG, "eps must be >= 0");
+    if (!gamma) return fail(RN_ERR_INVALID_ARG, "gamma is required");
+    if (M > 0 && (!x || !y)) return fail(RN_ERR_INVALID_ARG, "input and output are required");
+    if (fused && M > 0 && (!residual || !residual_out))
+        return fail(RN_ERR_INVALID_ARG, "residual and residual_out are required");
+    if (M == 0) return RN_OK;
+    DeviceInfo d;
+    cudaError_t e = device_info(&d, nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    FwdProblem p;
+    p.x = x;
+    p.residual = fused ? residual : nullptr;
+    p.gamma = gamma;
+    p.y = y;
+    p.residual_out = fused ? residual_out : nullptr;
+    p.rstd = rstd;
+    p.eps = eps;
+    p.M = M;
+    p.N = (int)N;
+    p.dtype = dtype;
+    const int eb = elem_bytes(dtype);
+    bool vec = ((N * eb) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y) &&
+               (!fused || (aligned16(residual) && aligned16(residual_out)));
+    e = launch_fwd(p, vec, d.num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
+}
+
+}  // namespace rn
+
+using namespace rn;
+
+extern "C" {
+
+int rn_abi_version(void) { return 1; }
+
+const char *rn_status_string(int s) {
+    switch (s) {
+    case RN_OK: return "ok";
+    case RN_ERR_INVALID_ARG: return "invalid argument";
+    case RN_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+    case RN_ERR_CUDA: return "CUDA error";
+    case RN_ERR_WORKSPACE: return "bad workspace";
+    case RN_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+    }
+}
+
+const char *rn_last_error(void) { return g_err; }
+
+const char *rn_last_plan(void) { return g_plan; }
+
+rn_status rn_set_option(int option, int value) {
+    if (option < 0 || option >= RN_OPT_COUNT) return fail(RN_ERR_INVALID_ARG, "bad option %d", option);
+    if (value < 0) return fail(RN_ERR_INVALID_ARG, "option values are >= 0");
+    g_opts[option] = value;
+    return RN_OK;
+}
+
+int rn_get_option(int option) {
+    if (option < 0 || option >= RN_OPT_COUNT) return -1;
+    return g_opts[option];
+}
+
+rn_status rn_set_profile_events(void *ev_begin, void *ev_end) {
+    g_ev_begin = static_cast<cudaEvent_t>(ev_begin);
+    g_ev_end = static_cast<cudaEvent_t>(ev_end);
+    return RN_OK;
+}
+
+rn_status rn_rmsnorm_fwd(const void *x, const void *gamma, float eps, void *y, float *rstd,
+                         int64_t M, int64_t N, int dtype, void *stream) {
+    return fwd_entry(x, nullptr, gamma, eps, y, nullptr, rstd, M, N, dtype, stream, false);
+}
+
+rn_status rn_fused_add_rmsnorm_fwd(const void *x, const void *residual, const void *gamma,
+                                   float eps, void *out, void *residual_out, float *rstd,
+                                   int64_t M, int64_t N, int dtype, void *stream) {
+    return fwd_entry(x, residual, gamma, eps, out, residual_out, rstd, M, N, dtype, stream, true);
+}
+
+rn_status rn_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes) {
+    g_err[0] = 0;
+    rn_status st = check_common(M, N, dtype);
+    if (st != RN_OK) return st;
+    if (!bytes) return fail(RN_ERR_INVALID_ARG, "bytes is NULL");
+    DeviceInfo d;
+    cudaError_t e = device_info(&d, nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    *bytes = ws_bytes_for(d, N);
+    return RN_OK;
+}
+
+rn_status rn_rmsnorm_bwd(const void *x, const void *gamma, const void *dy, const float *rstd,
+                         void *dx, float *dweight_f32, void *dweight, void *workspace,
+                         size_t workspace_bytes, int64_t M, int64_t N, int dtype, void *stream) {
+    return bwd_entry(x, gamma, dy, rstd, nullptr, dx, dweight_f32, dweight, workspace,
+                     workspace_bytes, M, N, dtype, stream);
+}
+
+rn_status rn_fused_add_rmsnorm_bwd(const void *added, const void *gamma, const void *dy,
+                                   const float *rstd, const void *dresidual_out, void *dx,
+                                   float *dweight_f32, void *dweight, void *workspace,
+                                   size_t workspace_bytes, int64_t M, int64_t N, int dtype,
+                                   void *stream) {
+    return bwd_entry(added, gamma, dy, rstd, dresidual_out, dx, dweight_f32, dweight, workspace,
+                     workspace_bytes, M, N, dtype, stream);
+}
+
+rn_status rn_workspace_status(void *workspace, int clear, int *status, void *stream) {
+    g_err[0] = 0;
+    if (!workspace || !status) return fail(RN_ERR_INVALID_ARG, "workspace and status are required");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    *status = v;
+    if (clear && v != 0) {
+        e = cudaMemsetAsync(workspace, 0, sizeof(int), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    }
+    return RN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rn {
+
+enum DType { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+inline int elem_bytes(int dt) { return dt == kF32 ? 4 : 2; }
+
+// One backward problem, already validated by the API layer.
+struct BwdProblem {
+    const void *x;        // x (plain) or added (fused-add)
+    const void *gamma;
+    const void *dy;
+    const float *rstd;
+    const void *dres;     // nullable
+    void *dx;
+    float *dw_f32;
+    void *dw_cast;        // nullable
+    uint8_t *ws;          // workspace (status word + partials)
+    int64_t M;
+    int N;
+    int dtype;
+};
+
+// Launch shape of the row engine.
+struct RowPlan {
+    int cpt;           // 16-byte chunks per thread per row (1, 2, 4)
+    int team_threads;  // threads that share one row (multiple of 32)
+    int teams;         // rows processed concurrently per CTA
+    int stages;        // bulk-copy ring depth per team
+    int grid;          // CTAs (persistent)
+    size_t smem;       // dynamic shared memory bytes
+    bool atomic;       // weight gradient via fp32 atomics (else scratch partials)
+};
+
+struct GenericPlan {
+    int threads;       // CTA size; one row per CTA at a time
+    int grid;
+    bool smem_dw;      // per-CTA weight-gradient partial in shared memory
+    size_t smem;
+    bool atomic;
+};
+
+// Row engine: largest chunk count per row and CTA thread cap for a cpt.
+constexpr int kRowMaxChunks = 2048;
+int row_max_threads(int cpt);
+size_t row_smem_bytes(int teams, int stages, int ntensors, int row_bytes);
+size_t generic_smem_bytes(int N, bool smem_dw);
+
+cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_t s,
+                           bool pdl_after_zero);
+cudaError_t launch_bwd_generic(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
+                               bool pdl_after_zero);
+// Scratch mode: dw_f32 = sum of G partial rows (fixed order), optional cast.
+cudaError_t launch_finalize(const float *partials, int G, int N, float *dw_f32, void *dw_cast,
+                            int dtype, cudaStream_t s, bool pdl);
+// Atomic mode: zero before the row pass, cast after it.
+cudaError_t launch_zero_f32(float *p, int N, cudaStream_t s);
+cudaError_t launch_cast(const float *dw_f32, void *dw_cast, int N, int dtype, cudaStream_t s,
+                        bool pdl);
+
+struct FwdProblem {
+    const void *x;
+    const void *residual;  // nullable: plain forward
+    const void *gamma;
+    void *y;
+    void *residual_out;    // fused-add only
+    float *rstd;           // nullable
+    float eps;
+    int64_t M;
+    int N;
+    int dtype;
+};
+
+cudaError_t launch_fwd(const FwdProblem &p, bool vector_ok, int num_sms, cudaStream_t s);
+
+// Set the dynamic shared memory cap of a kernel once per device.
+cudaError_t ensure_smem_attr(const void *func, size_t bytes);
+
+}  // namespace rn

@@ -1,0 +1,95 @@
+"""ctypes view of the C ABI declared in ``include/rmsnorm_gb300.h``.
+
+Loads ``_build/librn_gb300.so`` (built in-tree by ``build.py``). There is no
+fallback: if the library is missing or fails to load, every call raises.
+"""
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "librn_gb300.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "rmsnorm_gb300.h")
+
+RN_OK, RN_ERR_INVALID_ARG, RN_ERR_UNSUPPORTED, RN_ERR_CUDA, RN_ERR_WORKSPACE, RN_ERR_TIMEOUT = range(6)
+RN_F32, RN_F16, RN_BF16 = 0, 1, 2
+OPT_BWD_ENGINE, OPT_DWEIGHT_MODE, OPT_CHUNKS_PER_THREAD, OPT_TEAMS_PER_CTA, OPT_STAGES, OPT_GRID = range(6)
+
+_lib = None
+
+
+class RNError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__("%s (status %d): %s" % (status_string(status), status, msg))
+        self.status = status
+
+
+def _bind(lib):
+    vp, i64, ci, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.rn_abi_version.restype = ci
+    lib.rn_abi_version.argtypes = []
+    lib.rn_status_string.restype = ctypes.c_char_p
+    lib.rn_status_string.argtypes = [ci]
+    lib.rn_last_error.restype = ctypes.c_char_p
+    lib.rn_last_error.argtypes = []
+    lib.rn_last_plan.restype = ctypes.c_char_p
+    lib.rn_last_plan.argtypes = []
+    lib.rn_rmsnorm_fwd.restype = ci
+    lib.rn_rmsnorm_fwd.argtypes = [vp, vp, f32, vp, vp, i64, i64, ci, vp]
+    lib.rn_fused_add_rmsnorm_fwd.restype = ci
+    lib.rn_fused_add_rmsnorm_fwd.argtypes = [vp, vp, vp, f32, vp, vp, vp, i64, i64, ci, vp]
+    lib.rn_bwd_workspace_bytes.restype = ci
+    lib.rn_bwd_workspace_bytes.argtypes = [i64, i64, ci, ctypes.POINTER(sz)]
+    lib.rn_rmsnorm_bwd.restype = ci
+    lib.rn_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, ci, vp]
+    lib.rn_fused_add_rmsnorm_bwd.restype = ci
+    lib.rn_fused_add_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, ci, vp]
+    lib.rn_workspace_status.restype = ci
+    lib.rn_workspace_status.argtypes = [vp, ci, ctypes.POINTER(ci), vp]
+    lib.rn_set_option.restype = ci
+    lib.rn_set_option.argtypes = [ci, ci]
+    lib.rn_get_option.restype = ci
+    lib.rn_get_option.argtypes = [ci]
+    lib.rn_set_profile_events.restype = ci
+    lib.rn_set_profile_events.argtypes = [vp, vp]
+    return lib
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("CUDA library %s is not built; run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        _lib = _bind(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def status_string(st):
+    return lib().rn_status_string(int(st)).decode()
+
+
+def check(st):
+    if st != RN_OK:
+        raise RNError(st, lib().rn_last_error().decode())
+
+
+def header_functions():
+    """Names of the functions include/rmsnorm_gb300.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rn_[a-z0-9_]+)\s*\(", text)))
+
+
+def last_plan():
+    return lib().rn_last_plan().decode()
+
+
+def set_option(opt, value):
+    check(lib().rn_set_option(int(opt), int(value)))
+
+
+def get_option(opt):
+    return int(lib().rn_get_option(int(opt)))

@@ -1,0 +1,129 @@
+"""Parity helpers: oracle expectations for a case and the comparison rules.
+
+Tolerances (written here, used by every GPU parity test):
+  * f32 dx / y:  max|gpu - ref| / max|ref| <= 1e-5 over the tensor.
+  * f16/bf16 dx / y:  |gpu - ref| <= 1e-2 + 1.6e-2*|ref| elementwise, AND the
+    tighter |gpu - ref| <= ulp_dtype(ref) + 1e-5*max|ref| (one unit in the
+    last place of the I/O dtype, plus fp32 round-off relative to the tensor's
+    scale for elements near zero).
+  * dweight_f32: max|gpu - ref| / max|ref| <= 1e-4; the cast dweight within
+    ulp_dtype(ref) + 1e-4*max|ref|.
+  * rstd (forward): |gpu - ref| <= 4*2^-24*ref.
+  * residual_out (fused forward): bit-exact (one correctly rounded add).
+ref is the fp64 oracle on the same inputs; inputs and the saved rstd come
+from the seeded generator and the oracle, never from the GPU.
+"""
+import numpy as np
+import torch
+
+import oracle
+from rmsnorm_backward_bwd_gb300 import synth
+
+P_BITS = {"f32": 24, "f16": 11, "bf16": 8}
+E_MIN = {"f32": -126, "f16": -14, "bf16": -126}
+
+
+def ulp(ref, dtype):
+    a = np.abs(np.asarray(ref, np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(np.where(a > 0, e, E_MIN[dtype]), E_MIN[dtype])
+    return np.ldexp(1.0, (e - (P_BITS[dtype] - 1)).astype(np.int64))
+
+
+def to64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def check_tensor(name, got, ref, dtype, kind="dx"):
+    """Compare one GPU output (torch tensor) with the fp64 reference (numpy)."""
+    g = to64(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert g.shape == ref.shape, (name, g.shape, ref.shape)
+    assert np.all(np.isfinite(g)), "%s has non-finite values" % name
+    scale = float(np.max(np.abs(ref))) if ref.size else 0.0
+    err = np.abs(g - ref)
+    if ref.size == 0:
+        return
+    if kind == "dweight_f32":
+        rel = float(np.max(err)) / max(scale, 1e-30)
+        assert rel <= 1e-4, "%s: max rel err %.3g > 1e-4" % (name, rel)
+        return
+    if kind == "dweight":
+        bound = ulp(ref, dtype) + 1e-4 * scale
+        bad = err > bound
+        assert not bad.any(), "%s: %d elements beyond 1 ulp (worst %.3g vs bound %.3g)" % (
+            name, int(bad.sum()), float(err[bad].max()), float(bound[bad][np.argmax(err[bad])]))
+        return
+    if dtype == "f32":
+        rel = float(np.max(err)) / max(scale, 1e-30)
+        assert rel <= 1e-5, "%s: max rel err %.3g > 1e-5" % (name, rel)
+        return
+    loose = err <= 1e-2 + 1.6e-2 * np.abs(ref)
+    assert loose.all(), "%s: %d elements outside atol 1e-2 / rtol 1.6e-2" % (name, int((~loose).sum()))
+    bound = ulp(ref, dtype) + 1e-5 * scale
+    bad = err > bound
+    assert not bad.any(), "%s: %d elements beyond 1 ulp (worst excess %.3g)" % (
+        name, int(bad.sum()), float((err - bound)[bad].max()))
+
+
+class Expected:
+    """Inputs (CPU tensors in the I/O dtype) and the oracle's outputs."""
+
+
+def expected_bwd(case, nthreads=0):
+    """Draw the case's inputs; compute `added` (fused) and the saved fp32
+    rstd with the oracle's forward; then the oracle's backward."""
+    inp = synth.make_inputs(case)
+    dt = case.dtype
+    tdt = synth.TORCH_DTYPES[dt]
+    ex = Expected()
+    ex.case = case
+    g64 = inp["gamma"].to(torch.float64).numpy()
+    x64 = inp["x"].to(torch.float64).numpy()
+    if case.fused:
+        r64 = inp["residual"].to(torch.float64).numpy()
+        _, a64, rstd64 = oracle.fused_add_rmsnorm_fwd(x64, r64, g64, np.float32(case.eps), dt,
+                                                      nthreads)
+        ex.x = torch.from_numpy(a64).to(tdt)     # exact: a64 is dtype-rounded
+        del r64
+    else:
+        _, rstd64 = oracle.rmsnorm_fwd(x64, g64, np.float32(case.eps), nthreads)
+        a64 = x64
+        ex.x = inp["x"]
+    rstd32 = oracle.round_to(rstd64, "f32")
+    ex.rstd = torch.from_numpy(rstd32).to(torch.float32)
+    ex.gamma = inp["gamma"]
+    ex.dy = inp["dy"]
+    dy64 = inp["dy"].to(torch.float64).numpy()
+    ex.dres = inp.get("dres")
+    if case.fused:
+        dres64 = ex.dres.to(torch.float64).numpy() if ex.dres is not None else None
+        ex.dx, ex.dw = oracle.fused_add_rmsnorm_bwd(a64, g64, dy64, rstd32, dres64, nthreads)
+    else:
+        ex.dx, ex.dw = oracle.rmsnorm_bwd(a64, g64, dy64, rstd32, nthreads)
+    return ex
+
+
+def run_gpu_bwd(ex, dev="cuda", dx_out=None):
+    import rmsnorm_backward_bwd_gb300 as rn
+    x = ex.x.to(dev)
+    g = ex.gamma.to(dev)
+    dy = ex.dy.to(dev)
+    rstd = ex.rstd.to(dev)
+    if ex.case.fused:
+        dres = ex.dres.to(dev) if ex.dres is not None else None
+        dx, dres_out, dw, dw32 = rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, dres, dx=dx_out)
+        assert dres_out.data_ptr() == dx.data_ptr()
+    else:
+        dx, dw, dw32 = rn.rmsnorm_bwd(x, g, dy, rstd, dx=dx_out)
+    torch.cuda.synchronize()
+    return dx, dw, dw32
+
+
+def check_bwd(ex, dx, dw, dw32, tag=""):
+    dt = ex.case.dtype
+    check_tensor("dx" + tag, dx, ex.dx, dt, "dx")
+    check_tensor("dweight_f32" + tag, dw32, ex.dw, dt, "dweight_f32")
+    if dw is not None:
+        check_tensor("dweight" + tag, dw, ex.dw, dt, "dweight")

@@ -1,0 +1,74 @@
+"""The C ABI on the host: the library loads, exports what the header
+declares, and rejects bad arguments before touching the GPU (CPU only)."""
+import ctypes
+
+import pytest
+import torch
+
+from rmsnorm_backward_bwd_gb300 import native
+
+
+def test_library_exports_every_declared_function():
+    lib = native.lib()
+    names = native.header_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), "%s declared in the header but not exported" % n
+
+
+def test_abi_version_and_status_strings():
+    lib = native.lib()
+    assert lib.rn_abi_version() == 1
+    for st in range(6):
+        assert native.status_string(st)
+
+
+def _bwd(lib, **kw):
+    a = dict(x=None, g=None, dy=None, rstd=None, dx=None, dw32=None, dw=None, ws=None,
+             wsb=0, M=4, N=8, dt=2)
+    a.update(kw)
+    return lib.rn_rmsnorm_bwd(a["x"], a["g"], a["dy"], a["rstd"], a["dx"], a["dw32"], a["dw"],
+                              a["ws"], a["wsb"], a["M"], a["N"], a["dt"], None)
+
+
+def test_argument_checks_fail_before_any_launch():
+    lib = native.lib()
+    fake = ctypes.c_void_p(0x1000)
+    assert _bwd(lib) == native.RN_ERR_INVALID_ARG                       # gamma missing
+    assert b"required" in lib.rn_last_error()
+    assert _bwd(lib, dt=7, g=fake, dw32=fake) == native.RN_ERR_INVALID_ARG
+    assert _bwd(lib, N=0, g=fake, dw32=fake) == native.RN_ERR_INVALID_ARG
+    assert _bwd(lib, M=-1, g=fake, dw32=fake) == native.RN_ERR_INVALID_ARG
+    assert _bwd(lib, g=fake, dw32=fake) == native.RN_ERR_INVALID_ARG     # x/dy/rstd/dx missing
+    assert _bwd(lib, x=fake, g=fake, dy=fake, rstd=fake, dx=fake, dw32=fake) == \
+        native.RN_ERR_INVALID_ARG                                          # dx aliases x
+    assert _bwd(lib, N=1 << 40, g=fake, dw32=fake) == native.RN_ERR_UNSUPPORTED
+    assert lib.rn_rmsnorm_fwd(None, None, 1e-6, None, None, 4, 8, 2, None) == native.RN_ERR_INVALID_ARG
+    assert lib.rn_rmsnorm_fwd(fake, fake, -1.0, fake, None, 4, 8, 2, None) == native.RN_ERR_INVALID_ARG
+    assert lib.rn_fused_add_rmsnorm_fwd(fake, None, fake, 1e-6, fake, fake, None, 4, 8, 2,
+                                        None) == native.RN_ERR_INVALID_ARG
+    assert lib.rn_workspace_status(None, 0, None, None) == native.RN_ERR_INVALID_ARG
+
+
+def test_options_round_trip():
+    for opt in range(6):
+        native.set_option(opt, 3)
+        assert native.get_option(opt) == 3
+        native.set_option(opt, 0)
+    assert native.lib().rn_set_option(99, 1) == native.RN_ERR_INVALID_ARG
+    assert native.lib().rn_set_option(0, -1) == native.RN_ERR_INVALID_ARG
+    assert native.get_option(99) == -1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_device_queries_report_cuda_error_without_gpu():
+    n = ctypes.c_size_t(0)
+    st = native.lib().rn_bwd_workspace_bytes(4, 8, 2, ctypes.byref(n))
+    assert st == native.RN_ERR_CUDA
+
+
+def test_python_guards_reject_mismatched_dtypes_on_cpu_tensors():
+    import rmsnorm_backward_bwd_gb300 as rn
+    x = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="dtype mismatch"):
+        rn.rmsnorm_bwd(x, torch.zeros(8, dtype=torch.float16), x, torch.zeros(4))

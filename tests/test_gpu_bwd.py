@@ -1,0 +1,192 @@
+"""Backward parity: the CUDA library (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from rmsnorm_backward_bwd_gb300 import native, synth
+from rmsnorm_backward_bwd_gb300.synth import Case
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _reset_options():
+    for opt in range(6):
+        native.set_option(opt, 0)
+    yield
+    for opt in range(6):
+        native.set_option(opt, 0)
+
+
+WORKLOADS = [synth.SMALL_F32, synth.PLAIN_4096, synth.FUSED_4096, synth.FUSED_4096_NODRES,
+             *synth.edge_cases()]
+
+
+@pytest.mark.parametrize("case", WORKLOADS, ids=lambda c: c.name)
+def test_bwd_matches_oracle(case):
+    ex = parity.expected_bwd(case)
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    parity.check_bwd(ex, dx, dw, dw32)
+    assert "engine=" in native.last_plan()
+
+
+@pytest.mark.parametrize("case", [synth.LARGE_PLAIN, synth.LARGE_FUSED], ids=lambda c: c.name)
+def test_bwd_large_training_shape(case):
+    """16384 x 8192 bf16: the whole tensor against the oracle (all rows)."""
+    ex = parity.expected_bwd(case)
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    parity.check_bwd(ex, dx, dw, dw32)
+    assert native.last_plan().startswith("engine=row")
+
+
+SWEEP = [
+    Case("bf16 M=33 N=4096", 33, 4096, "bf16"),
+    Case("bf16 M=300 N=2048 fused", 300, 2048, "bf16", fused=True, with_dres=True),
+    Case("f32 M=7 N=3000", 7, 3000, "f32"),
+    Case("f16 M=65 N=1024 fused nodres", 65, 1024, "f16", fused=True),
+    Case("bf16 M=5 N=64", 5, 64, "bf16"),
+    Case("f32 M=200 N=8", 200, 8, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=lambda c: c.name)
+@pytest.mark.parametrize("engine,mode", [(1, 1), (1, 2), (2, 1), (2, 2)],
+                         ids=["row-scratch", "row-atomic", "generic-scratch", "generic-atomic"])
+def test_forced_engines(case, engine, mode):
+    native.set_option(native.OPT_BWD_ENGINE, engine)
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    ex = parity.expected_bwd(case)
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    parity.check_bwd(ex, dx, dw, dw32)
+    plan = native.last_plan()
+    assert ("engine=row" if engine == 1 else "engine=generic") in plan, plan
+    assert ("dw=atomic" if mode == 2 else "dw=scratch") in plan, plan
+
+
+@pytest.mark.parametrize("cpt", [1, 2, 4])
+@pytest.mark.parametrize("teams,stages", [(1, 1), (1, 8), (2, 3), (3, 4)])
+def test_row_engine_tile_shapes(cpt, teams, stages):
+    case = Case("bf16 M=97 N=2048 fused", 97, 2048, "bf16", fused=True, with_dres=True)
+    native.set_option(native.OPT_BWD_ENGINE, 1)
+    native.set_option(native.OPT_CHUNKS_PER_THREAD, cpt)
+    native.set_option(native.OPT_TEAMS_PER_CTA, teams)
+    native.set_option(native.OPT_STAGES, stages)
+    ex = parity.expected_bwd(case)
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    parity.check_bwd(ex, dx, dw, dw32)
+    plan = native.last_plan()
+    assert "cpt=%d" % cpt in plan and "teams=%d" % teams in plan and "stages=%d" % stages in plan
+
+
+@pytest.mark.parametrize("grid", [1, 3, 152])
+def test_row_engine_grid_caps(grid):
+    native.set_option(native.OPT_GRID, grid)
+    case = Case("bf16 M=1000 N=4096", 1000, 4096, "bf16")
+    ex = parity.expected_bwd(case)
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    parity.check_bwd(ex, dx, dw, dw32)
+
+
+def test_scratch_mode_is_bitwise_repeatable():
+    ex = parity.expected_bwd(Case("bf16 M=2048 N=4096", 2048, 4096, "bf16"))
+    a = parity.run_gpu_bwd(ex)
+    b = parity.run_gpu_bwd(ex)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2]) and torch.equal(a[1], b[1])
+
+
+def test_fused_dx_may_alias_dresidual_out():
+    import rmsnorm_backward_bwd_gb300 as rn
+    case = Case("bf16 M=257 N=4096 fused", 257, 4096, "bf16", fused=True, with_dres=True)
+    ex = parity.expected_bwd(case)
+    x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
+    dres = ex.dres.cuda()
+    ref_dx, _, ref_dw, ref_dw32 = rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, dres.clone())
+    buf = dres.clone()
+    dx, dres_grad, dw, dw32 = rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, buf, dx=buf)
+    torch.cuda.synchronize()
+    assert dx.data_ptr() == buf.data_ptr() == dres_grad.data_ptr()
+    assert torch.equal(dx, ref_dx) and torch.equal(dw32, ref_dw32)
+    parity.check_bwd(ex, dx, dw, dw32)
+
+
+def test_fused_with_zero_residual_grad_equals_plain():
+    import rmsnorm_backward_bwd_gb300 as rn
+    ex = parity.expected_bwd(Case("bf16 M=128 N=4096", 128, 4096, "bf16"))
+    x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
+    dx, dw, dw32 = rn.rmsnorm_bwd(x, g, dy, rstd)
+    for dres in (None, torch.zeros_like(x)):
+        fdx, _, fdw, fdw32 = rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, dres)
+        assert torch.equal(fdx, dx) and torch.equal(fdw32, dw32) and torch.equal(fdw, dw)
+
+
+def test_empty_batch_zeroes_dweight():
+    import rmsnorm_backward_bwd_gb300 as rn
+    g = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
+    x = torch.empty(0, 4096, dtype=torch.bfloat16, device="cuda")
+    rstd = torch.empty(0, dtype=torch.float32, device="cuda")
+    dw32 = torch.full((4096,), 7.0, device="cuda")
+    dw = torch.full((4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    rn.rmsnorm_bwd(x, g, x, rstd, dweight_f32=dw32, dweight=dw)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dw32).item() == 0 and torch.count_nonzero(dw).item() == 0
+
+
+@pytest.mark.parametrize("M,N,dt", [(1, 1, "f32"), (3, 7, "bf16"), (9, 33, "f16"),
+                                    (17, 1001, "bf16"), (2, 4099, "f32"), (40, 16384, "bf16"),
+                                    (3, 16392, "bf16"), (2, 60000, "f32"), (5, 131072, "bf16")])
+@pytest.mark.parametrize("fused", [False, True])
+def test_odd_and_extreme_widths(M, N, dt, fused):
+    case = Case("%s M=%d N=%d" % (dt, M, N), M, N, dt, fused=fused, with_dres=fused)
+    ex = parity.expected_bwd(case)
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    parity.check_bwd(ex, dx, dw, dw32)
+
+
+def test_misaligned_pointers_take_generic_path():
+    import rmsnorm_backward_bwd_gb300 as rn
+    case = Case("bf16 M=64 N=4096", 64, 4096, "bf16")
+    ex = parity.expected_bwd(case)
+    M, N = case.M, case.N
+    # storage shifted by one element: rows stay contiguous, bases are 2 mod 16
+    def shifted(t):
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device="cuda")
+        v = buf[1:].view(t.shape)
+        v.copy_(t.cuda())
+        return v
+    x, dy = shifted(ex.x), shifted(ex.dy)
+    g, rstd = ex.gamma.cuda(), ex.rstd.cuda()
+    dx = torch.empty(M * N + 1, dtype=x.dtype, device="cuda")[1:].view(M, N)
+    dx, dw, dw32 = rn.rmsnorm_bwd(x, g, dy, rstd, dx=dx)
+    torch.cuda.synchronize()
+    assert native.last_plan().startswith("engine=generic")
+    parity.check_bwd(ex, dx, dw, dw32)
+
+
+def test_workspace_status_stays_clean():
+    import rmsnorm_backward_bwd_gb300 as rn
+    ex = parity.expected_bwd(Case("bf16 M=512 N=4096", 512, 4096, "bf16"))
+    parity.run_gpu_bwd(ex)
+    ws = rn.bwd_workspace(512, 4096, torch.bfloat16, "cuda")
+    assert rn.workspace_status(ws) == 0
+
+
+def test_invariant_holds_at_full_size():
+    """sum_j x_j*dx_j = eps*rstd^3*sum_j x_j*gamma_j*dy_j per row (any size),
+    here with rstd computed by the oracle for 4096 x 4096 bf16."""
+    case = synth.PLAIN_4096
+    ex = parity.expected_bwd(case)
+    dx, _, _ = parity.run_gpu_bwd(ex)
+    x = parity.to64(ex.x)
+    d = parity.to64(dx)
+    g = parity.to64(ex.gamma)
+    dy = parity.to64(ex.dy)
+    r = parity.to64(ex.rstd)
+    lhs = np.sum(x * d, axis=1)
+    rhs = np.float32(case.eps) * r ** 3 * np.sum(x * g * dy, axis=1)
+    # dx is bf16-rounded: each term carries up to half an ulp of error
+    bound = np.sum(np.abs(x) * parity.ulp(d, "bf16"), axis=1) + 1e-6 * np.sum(np.abs(x * d), axis=1)
+    # rstd is fp32 (not exactly (ms+eps)^-1/2): the identity then holds up to that rounding
+    bound += 4 * 2.0**-24 * np.abs(np.sum(x * g * dy, axis=1)) * r
+    assert np.all(np.abs(lhs - rhs) <= bound)

@@ -1,0 +1,87 @@
+"""Forward parity (plain and fused-add) and the small fwd+bwd chain."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+import rmsnorm_backward_bwd_gb300 as rn
+from rmsnorm_backward_bwd_gb300 import native, synth
+from rmsnorm_backward_bwd_gb300.synth import Case
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(128, 1024, "f32"), (4096, 4096, "bf16"), (1, 4096, "bf16"), (512, 2048, "bf16"),
+          (512, 3000, "f32"), (128, 4096, "f16"), (7, 1001, "bf16"), (3, 33, "f16"),
+          (16, 16384, "bf16"), (2, 40000, "f32")]
+
+
+def _check_rstd(got, ref64):
+    g = parity.to64(got)
+    assert np.all(np.abs(g - ref64) <= 4 * 2.0**-24 * ref64), float(np.max(np.abs(g / ref64 - 1)))
+
+
+@pytest.mark.parametrize("M,N,dt", SHAPES, ids=lambda v: str(v))
+@pytest.mark.parametrize("eps", [1e-5, 1e-6, 1e-2])
+def test_fwd_matches_oracle(M, N, dt, eps):
+    inp = synth.make_inputs(Case("fwd", M, N, dt, eps=eps))
+    x64 = parity.to64(inp["x"])
+    g64 = parity.to64(inp["gamma"])
+    y64, rstd64 = oracle.rmsnorm_fwd(x64, g64, np.float32(eps))
+    y, rstd = rn.rmsnorm_fwd(inp["x"].cuda(), inp["gamma"].cuda(), eps)
+    torch.cuda.synchronize()
+    _check_rstd(rstd, rstd64)
+    parity.check_tensor("y", y, y64, dt, "y")
+
+
+@pytest.mark.parametrize("M,N,dt", SHAPES, ids=lambda v: str(v))
+def test_fused_fwd_matches_oracle(M, N, dt):
+    inp = synth.make_inputs(Case("fused fwd", M, N, dt, fused=True))
+    x64, r64, g64 = (parity.to64(inp[k]) for k in ("x", "residual", "gamma"))
+    out64, add64, rstd64 = oracle.fused_add_rmsnorm_fwd(x64, r64, g64, np.float32(1e-6), dt)
+    out, res_out, rstd = rn.fused_add_rmsnorm_fwd(inp["x"].cuda(), inp["residual"].cuda(),
+                                                  inp["gamma"].cuda(), 1e-6)
+    torch.cuda.synchronize()
+    assert np.array_equal(parity.to64(res_out), add64)   # one correctly rounded add
+    _check_rstd(rstd, rstd64)
+    parity.check_tensor("out", out, out64, dt, "y")
+
+
+def test_eps_is_honoured():
+    inp = synth.make_inputs(Case("eps", 64, 256, "f32"))
+    x, g = inp["x"].cuda() * 1e-2, inp["gamma"].cuda()
+    r = [rn.rmsnorm_fwd(x, g, eps)[1] for eps in (1e-5, 1e-6, 1e-2)]
+    assert not torch.equal(r[0], r[1]) and not torch.equal(r[0], r[2])
+
+
+def test_small_fwd_bwd_chain():
+    """128 x 1024 f32, eps 1e-5: GPU forward, then GPU backward on the GPU's
+    own rstd, against the oracle's forward and backward."""
+    case = synth.SMALL_F32
+    inp = synth.make_inputs(case)
+    x64, g64, dy64 = (parity.to64(inp[k]) for k in ("x", "gamma", "dy"))
+    y64, rstd64 = oracle.rmsnorm_fwd(x64, g64, np.float32(case.eps))
+    dx64, dw64 = oracle.rmsnorm_bwd(x64, g64, dy64, oracle.round_to(rstd64, "f32"))
+    x, g, dy = inp["x"].cuda(), inp["gamma"].cuda(), inp["dy"].cuda()
+    y, rstd = rn.rmsnorm_fwd(x, g, case.eps)
+    dx, dw, dw32 = rn.rmsnorm_bwd(x, g, dy, rstd)
+    torch.cuda.synchronize()
+    parity.check_tensor("y", y, y64, "f32", "y")
+    _check_rstd(rstd, rstd64)
+    parity.check_tensor("dx", dx, dx64, "f32", "dx")
+    parity.check_tensor("dweight_f32", dw32, dw64, "f32", "dweight_f32")
+
+
+def test_fwd_3d_input_and_guards():
+    x = torch.randn(2, 3, 512, device="cuda", dtype=torch.bfloat16)
+    g = torch.ones(512, device="cuda", dtype=torch.bfloat16)
+    y, rstd = rn.rmsnorm_fwd(x, g, 1e-6)
+    assert y.shape == x.shape and rstd.shape == (6,)
+    with pytest.raises(ValueError, match="dtype mismatch"):
+        rn.rmsnorm_fwd(x, g.to(torch.float16), 1e-6)
+    with pytest.raises(ValueError, match="weight has shape"):
+        rn.rmsnorm_fwd(x, g[:256], 1e-6)
+    with pytest.raises(ValueError, match="contiguous"):
+        rn.rmsnorm_fwd(x.transpose(0, 1), g, 1e-6)
+    with pytest.raises(ValueError, match="dtype mismatch"):
+        rn.fused_add_rmsnorm_fwd(x, x.to(torch.float16), g, 1e-6)
