@@ -231,6 +231,13 @@ def time_calls(prob, steps, warmup, flush, ws, sampler=None, kernel_events=False
           for _ in range(steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)] if kernel_events else None
+    if kev:
+        # torch creates the CUDA event on its first record: do that here, so
+        # that the handles passed to the library are real events
+        for a, b in kev:
+            a.record(st)
+            b.record(st)
+        torch.cuda.synchronize()
     t0 = time.time()
     for i in range(steps):
         flush.zero_()

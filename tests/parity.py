@@ -12,6 +12,14 @@ Tolerances (written here, used by every GPU parity test):
   * residual_out (fused forward): bit-exact (one correctly rounded add).
 ref is the fp64 oracle on the same inputs; inputs and the saved rstd come
 from the seeded generator and the oracle, never from the GPU.
+
+Ill-conditioned elements: where dx is a near-total cancellation of its two
+terms (wdy - x_hat*c1; e.g. N = 1, where x_hat^2 = ms/(ms+eps) is 1 - O(eps)),
+fp32 arithmetic cannot reach a bound relative to |dx| itself. Such an element
+also passes when its error is within fp32 round-off of the terms it is made
+of: 2^-24 * rstd * (16*(|wdy| + |x_hat*c1|) + 4*sqrt(N)*|x_hat|*rstd*mean|x*wdy|)
+(pointwise roundings plus the c1 reduction); this scale is computed in fp64
+from the inputs for the failing elements only.
 """
 import numpy as np
 import torch
@@ -35,8 +43,10 @@ def to64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def check_tensor(name, got, ref, dtype, kind="dx"):
-    """Compare one GPU output (torch tensor) with the fp64 reference (numpy)."""
+def check_tensor(name, got, ref, dtype, kind="dx", roundoff=None):
+    """Compare one GPU output (torch tensor) with the fp64 reference (numpy).
+    roundoff(mask) -> per-element fp32 round-off bound for the masked
+    elements (dx only; see the module docstring)."""
     g = to64(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert g.shape == ref.shape, (name, g.shape, ref.shape)
@@ -56,13 +66,18 @@ def check_tensor(name, got, ref, dtype, kind="dx"):
             name, int(bad.sum()), float(err[bad].max()), float(bound[bad][np.argmax(err[bad])]))
         return
     if dtype == "f32":
-        rel = float(np.max(err)) / max(scale, 1e-30)
-        assert rel <= 1e-5, "%s: max rel err %.3g > 1e-5" % (name, rel)
+        bad = err > 1e-5 * scale
+        if bad.any() and roundoff is not None:
+            bad[bad] = err[bad] > roundoff(bad)
+        assert not bad.any(), "%s: %d elements beyond rel err 1e-5 (max rel %.3g)" % (
+            name, int(bad.sum()), float(np.max(err)) / max(scale, 1e-30))
         return
     loose = err <= 1e-2 + 1.6e-2 * np.abs(ref)
     assert loose.all(), "%s: %d elements outside atol 1e-2 / rtol 1.6e-2" % (name, int((~loose).sum()))
     bound = ulp(ref, dtype) + 1e-5 * scale
     bad = err > bound
+    if bad.any() and roundoff is not None:
+        bad[bad] = err[bad] > ulp(ref[bad], dtype) + roundoff(bad)
     assert not bad.any(), "%s: %d elements beyond 1 ulp (worst excess %.3g)" % (
         name, int(bad.sum()), float((err - bound)[bad].max()))
 
@@ -102,7 +117,28 @@ def expected_bwd(case, nthreads=0):
         ex.dx, ex.dw = oracle.fused_add_rmsnorm_bwd(a64, g64, dy64, rstd32, dres64, nthreads)
     else:
         ex.dx, ex.dw = oracle.rmsnorm_bwd(a64, g64, dy64, rstd32, nthreads)
+    ex.a64, ex.g64, ex.dy64, ex.rstd64 = a64, g64, dy64, rstd32
     return ex
+
+
+def roundoff_bound(ex):
+    """fp32 round-off scale of dx's terms, for the elements of a mask."""
+    def fn(mask):
+        rows, cols = np.nonzero(mask.reshape(ex.a64.shape))
+        urows = np.unique(rows)
+        N = ex.a64.shape[1]
+        xr = ex.a64[urows]
+        r = ex.rstd64[urows][:, None]
+        wdy_r = ex.dy64[urows] * ex.g64
+        c1 = np.mean(xr * r * wdy_r, axis=1)
+        mabs = np.mean(np.abs(xr * wdy_r), axis=1)
+        pos = np.searchsorted(urows, rows)
+        xh = ex.a64[rows, cols] * ex.rstd64[rows]
+        wdy = ex.dy64[rows, cols] * ex.g64[cols]
+        rs = ex.rstd64[rows]
+        return 2.0**-24 * rs * (16 * (np.abs(wdy) + np.abs(xh * c1[pos]))
+                                + 4 * np.sqrt(N) * np.abs(xh) * rs * mabs[pos])
+    return fn
 
 
 def run_gpu_bwd(ex, dev="cuda", dx_out=None):
@@ -123,7 +159,7 @@ def run_gpu_bwd(ex, dev="cuda", dx_out=None):
 
 def check_bwd(ex, dx, dw, dw32, tag=""):
     dt = ex.case.dtype
-    check_tensor("dx" + tag, dx, ex.dx, dt, "dx")
+    check_tensor("dx" + tag, dx, ex.dx, dt, "dx", roundoff=roundoff_bound(ex))
     check_tensor("dweight_f32" + tag, dw32, ex.dw, dt, "dweight_f32")
     if dw is not None:
         check_tensor("dweight" + tag, dw, ex.dw, dt, "dweight")
