@@ -55,8 +55,7 @@ typedef enum rn_status {
     RN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad dtype code, bad option */
     RN_ERR_UNSUPPORTED = 2,  /* shape/alignment no engine handles (e.g. N too large) */
     RN_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
-    RN_ERR_WORKSPACE = 4,    /* workspace missing, misaligned or too small */
-    RN_ERR_TIMEOUT = 5       /* a device-side wait gave up (see rn_workspace_status) */
+    RN_ERR_WORKSPACE = 4     /* workspace missing, misaligned or too small */
 } rn_status;
 
 /* Version of this ABI (increments on any incompatible change). */
@@ -95,10 +94,10 @@ rn_status rn_fused_add_rmsnorm_fwd(const void *x, const void *residual, const vo
 
 /*
  * Bytes of workspace the backward needs on the current device for an [M,N]
- * problem (scratch partials of the weight gradient plus a 256-byte header
- * holding a device status word). Needs a CUDA device; writes *bytes.
- * The workspace must be 256-byte aligned and ZEROED ONCE when allocated; the
- * library keeps its header consistent afterwards. Calls that share one
+ * problem: a 256-byte header plus up to two fp32 rows of N per SM (the
+ * per-CTA partials of the weight gradient). Needs a CUDA device; writes
+ * *bytes. The workspace must be 256-byte aligned; its contents need no
+ * initialisation and are scratch between calls. Calls that share one
  * workspace must be ordered on the GPU (one stream, or events).
  */
 rn_status rn_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes);
@@ -138,23 +137,16 @@ rn_status rn_fused_add_rmsnorm_bwd(const void *added, const void *gamma, const v
                                    int64_t M, int64_t N, int dtype, void *stream);
 
 /*
- * Read the device status word of a workspace: synchronises `stream`, copies
- * the word to *status (0 = no device-side wait has given up; otherwise an
- * rn_status code, e.g. RN_ERR_TIMEOUT). clear != 0 resets it to 0 afterwards.
- */
-rn_status rn_workspace_status(void *workspace, int clear, int *status, void *stream);
-
-/*
  * Tuning / test options. They are process-wide, not thread-safe, and apply
  * to calls made after they are set; value 0 always means "automatic".
  */
 typedef enum rn_option {
-    RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (bulk-copy pipeline), 2 = generic engine */
+    RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (async-copy ring), 2 = generic engine */
     RN_OPT_DWEIGHT_MODE = 1,  /* 1 = scratch partials + finalize, 2 = fp32 atomics + cast */
     RN_OPT_CHUNKS_PER_THREAD = 2, /* row engine: 16-byte chunks per thread per row: 1, 2, 4 */
     RN_OPT_TEAMS_PER_CTA = 3, /* row engine: rows processed at once per CTA (1..15) */
     RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8) */
-    RN_OPT_GRID = 5,          /* cap on the number of CTAs of the row pass */
+    RN_OPT_GRID = 5,          /* CTAs of the row pass (default: one per SM; at most 2 per SM) */
     RN_OPT_COUNT = 6
 } rn_option;
 

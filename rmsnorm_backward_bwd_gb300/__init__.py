@@ -4,7 +4,7 @@ The compute runs in a CUDA library for sm_103a (``csrc/``, C ABI in
 ``include/rmsnorm_gb300.h``); this package is its thin PyTorch binding.
 """
 from .ops import (bwd_workspace, fused_add_rmsnorm_bwd, fused_add_rmsnorm_fwd, rmsnorm_bwd,
-                  rmsnorm_fwd, workspace_status)
+                  rmsnorm_fwd)
 
 __all__ = ["rmsnorm_fwd", "rmsnorm_bwd", "fused_add_rmsnorm_fwd", "fused_add_rmsnorm_bwd",
-           "bwd_workspace", "workspace_status"]
+           "bwd_workspace"]

@@ -132,13 +132,14 @@ static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
     if (team > row_max_threads(cpt)) return false;
 
     const size_t budget = (d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024);
-    const size_t stage = (size_t)nt * (size_t)((row_bytes + 127) / 128 * 128);
+    const int tc = cpt * team;  // 16-byte chunks per tensor row in a team's slot
+    const size_t stage = (size_t)nt * tc * 16;
     int teams = g_opts[RN_OPT_TEAMS_PER_CTA];
     if (teams <= 0) {
         teams = row_max_threads(cpt) / team;
         if (teams > 15) teams = 15;
         // keep at least 3 slots per team when the rows are long
-        while (teams > 1 && row_smem_bytes(teams, 3, nt, row_bytes) > budget) --teams;
+        while (teams > 1 && row_smem_bytes(teams, 3, nt, tc) > budget) --teams;
         // no more teams than rows per SM
         int64_t rows_per_sm = (p.M + d.num_sms - 1) / d.num_sms;
         if (rows_per_sm < 1) rows_per_sm = 1;
@@ -146,21 +147,22 @@ static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
     }
     if (teams < 1 || teams > 15 || teams * team > row_max_threads(cpt)) return false;
 
+    // one CTA per SM unless the grid option asks for another count
+    int64_t cap = g_opts[RN_OPT_GRID] > 0 ? g_opts[RN_OPT_GRID] : d.num_sms;
+    if (cap > max_partial_rows(d)) cap = max_partial_rows(d);
     int64_t grid = (p.M + teams - 1) / teams;
-    if (grid > d.num_sms) grid = d.num_sms;
-    if (g_opts[RN_OPT_GRID] > 0 && grid > g_opts[RN_OPT_GRID]) grid = g_opts[RN_OPT_GRID];
-    if (grid > max_partial_rows(d)) grid = max_partial_rows(d);
+    if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
 
     int stages = g_opts[RN_OPT_STAGES];
     if (stages <= 0) {
-        stages = (int)((budget - 2048) / (stage * teams));
+        stages = (int)((budget - 256) / (stage * teams));
         if (stages > 8) stages = 8;
         const int64_t rows_per_team = (p.M + grid * teams - 1) / (grid * teams);
         if (stages > rows_per_team) stages = (int)(rows_per_team < 1 ? 1 : rows_per_team);
     }
     if (stages < 1 || stages > 8) return false;
-    const size_t smem = row_smem_bytes(teams, stages, nt, row_bytes);
+    const size_t smem = row_smem_bytes(teams, stages, nt, tc);
     if (smem > d.smem_optin) return false;
 
     plan->cpt = cpt;
@@ -352,7 +354,6 @@ const char *rn_status_string(int s) {
     case RN_ERR_UNSUPPORTED: return "unsupported shape or alignment";
     case RN_ERR_CUDA: return "CUDA error";
     case RN_ERR_WORKSPACE: return "bad workspace";
-    case RN_ERR_TIMEOUT: return "device-side wait timed out";
     default: return "unknown status";
     }
 }
@@ -416,23 +417,6 @@ rn_status rn_fused_add_rmsnorm_bwd(const void *added, const void *gamma, const v
                                    void *stream) {
     return bwd_entry(added, gamma, dy, rstd, dresidual_out, dx, dweight_f32, dweight, workspace,
                      workspace_bytes, M, N, dtype, stream);
-}
-
-rn_status rn_workspace_status(void *workspace, int clear, int *status, void *stream) {
-    g_err[0] = 0;
-    if (!workspace || !status) return fail(RN_ERR_INVALID_ARG, "workspace and status are required");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int v = 0;
-    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_fail(e, "status read");
-    *status = v;
-    if (clear && v != 0) {
-        e = cudaMemsetAsync(workspace, 0, sizeof(int), s);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-        if (e != cudaSuccess) return cuda_fail(e, "status clear");
-    }
-    return RN_OK;
 }
 
 }  // extern "C"

@@ -9,25 +9,29 @@
 //   * Persistent grid, one CTA per SM. A CTA holds `teams` teams; a team of
 //     team_threads threads owns one row at a time. Team t of CTA b walks rows
 //     b*teams + t, then strides by gridDim.x*teams.
-//   * Each team keeps a ring of `stages` shared-memory slots. Its leader
-//     thread fills a slot with one bulk asynchronous copy per tensor row
-//     (x|added, dy, [dresidual_out]) completing on the slot's mbarrier, so
-//     several rows per team are in flight while the current row is reduced.
-//     Every row is read from HBM exactly once.
 //   * Thread tt of a team owns 16-byte chunks tt, tt+team_threads, ... of the
-//     row (consecutive threads -> consecutive 16 B: conflict-free shared
-//     reads, coalesced 128-bit dx stores). It keeps those chunks in registers
-//     across the c1 reduction (warp shuffles, then one named barrier across
-//     the team's warps), so dx needs no second read.
+//     row (consecutive threads -> consecutive 16 B: coalesced loads and
+//     128-bit dx stores, conflict-free shared accesses).
+//   * Each thread streams its own chunks of the next `stages-1` rows into a
+//     private ring of shared-memory slots with 16-byte asynchronous copies
+//     (cp.async, L2 evict-first). A thread only ever reads back what it copied
+//     itself, so the ring needs no barrier or mbarrier: per-thread commit
+//     groups order everything, and no wait in this kernel can spin forever.
+//     Every input byte is read from HBM exactly once.
+//   * Pass 1 reduces sum_j x_j*dy_j*gamma_j (warp shuffles, then one named
+//     barrier across the team's warps); pass 2 reads the slot again and
+//     stores dx. The arithmetic runs on packed fp32 pairs (f32x2 FMA / MUL /
+//     ADD: one instruction per two elements); for bf16/f16 the products
+//     x*dy and dy*gamma come exact from mixed-precision FMAs on the packed
+//     16-bit halves.
 //   * The weight-gradient partial of the thread's columns lives in fp32
 //     registers for every row the team handles; at the end the CTA's teams
 //     add theirs in a fixed order in shared memory and the CTA either stores
 //     one partial row to the workspace (deterministic; a finalize kernel sums
 //     the rows and casts) or adds it with fp32 vector atomics into a zeroed
 //     dweight_f32.
-//   * Every mbarrier wait is bounded (~1 s); on timeout the whole team stops,
-//     waits (bounded) for its copies in flight, and the CTA writes
-//     RN_ERR_TIMEOUT into the workspace status word.
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -39,16 +43,10 @@ template <int CPT> struct RowBounds {
     static constexpr int kMaxThreads = CPT <= 1 ? 1024 : (CPT == 2 ? 768 : 512);
 };
 
-constexpr int kBarBytes = 1024;      // up to 15 teams x 8 stages of 8-byte mbarriers
-constexpr int kRedOffset = 1024;     // [2 parities][32 warps] fp32 partial sums
-constexpr int kFlagOffset = 1280;    // [2 parities][32 warps] timeout flags
-constexpr int kStageOffset = 2048;
+constexpr int kRingOffset = 256;  // after [2 parities][32 warps] fp32 partial sums
 
-static inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
-
-size_t row_smem_bytes(int teams, int stages, int ntensors, int row_bytes) {
-    return (size_t)kStageOffset +
-           (size_t)teams * stages * ntensors * (size_t)round_up(row_bytes, 128);
+size_t row_smem_bytes(int teams, int stages, int ntensors, int team_chunks) {
+    return (size_t)kRingOffset + (size_t)teams * stages * ntensors * (size_t)team_chunks * 16;
 }
 
 struct RowArgs {
@@ -59,28 +57,119 @@ struct RowArgs {
     const uint8_t *dres;
     uint8_t *dx;
     float *dw_out;   // scratch: partial rows [gridDim.x][N]; atomic: dweight_f32
-    int *status;
     int64_t M;
     int N;
     int nchunks;
     int row_bytes;
-    int row_pitch;
     int team_threads;
     int teams;
     int stages;
     float inv_n;
 };
 
+// Per-chunk arithmetic of the two passes, by I/O dtype, on packed fp32
+// pairs (one f32x2 instruction per two elements). For bf16/f16 the products
+// x*dy and dy*gamma come exact from mixed-precision FMAs on the packed
+// 16-bit halves, so the inputs are never unpacked for them.
+template <typename T> struct RowMath;
+
+template <> struct RowMath<float> {
+    static constexpr int kPairs = 2;
+    static constexpr bool kNeedsGammaF = true;  // the fp32 path always reads gamma as fp32
+    // part2 + (x*dy)*g, pairwise
+    static __device__ __forceinline__ f32x2 pass1(const uint4 &x, const uint4 &dy, const uint4 &,
+                                                  const f32x2 *g2, f32x2 part2) {
+        const f32x2 x0 = f2_make(__uint_as_float(x.x), __uint_as_float(x.y));
+        const f32x2 x1 = f2_make(__uint_as_float(x.z), __uint_as_float(x.w));
+        const f32x2 d0 = f2_make(__uint_as_float(dy.x), __uint_as_float(dy.y));
+        const f32x2 d1 = f2_make(__uint_as_float(dy.z), __uint_as_float(dy.w));
+        part2 = f2_fma(f2_mul(x0, d0), g2[0], part2);
+        return f2_fma(f2_mul(x1, d1), g2[1], part2);
+    }
+    // dx = wdy*rs + x*b (rounded to the dtype); acc += (x*dy)*rs
+    template <bool HAS_DRES>
+    static __device__ __forceinline__ uint4 pass2(const uint4 &x, const uint4 &dy, const uint4 &r,
+                                                  const uint4 &, const f32x2 *g2, f32x2 rs2,
+                                                  f32x2 b2, f32x2 *acc2) {
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, dw[4] = {dy.x, dy.y, dy.z, dy.w};
+        const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const f32x2 x2 = f2_make(__uint_as_float(xw[2 * q]), __uint_as_float(xw[2 * q + 1]));
+            const f32x2 d2 = f2_make(__uint_as_float(dw[2 * q]), __uint_as_float(dw[2 * q + 1]));
+            acc2[q] = f2_fma(f2_mul(x2, d2), rs2, acc2[q]);
+            f32x2 v = f2_fma(x2, b2, f2_mul(f2_mul(d2, g2[q]), rs2));
+            if (HAS_DRES)
+                v = f2_add(v, f2_make(__uint_as_float(rw[2 * q]), __uint_as_float(rw[2 * q + 1])));
+            float lo, hi;
+            f2_split(v, lo, hi);
+            o[2 * q] = __float_as_uint(lo);
+            o[2 * q + 1] = __float_as_uint(hi);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+};
+
+template <typename T> struct RowMath16 {
+    static constexpr int kPairs = 4;
+    static constexpr bool kNeedsGammaF = false;
+    static constexpr bool kBF = std::is_same<T, __nv_bfloat16>::value;
+    static __device__ __forceinline__ f32x2 mul(uint32_t a, uint32_t b) {
+        return kBF ? mul_bf16x2(a, b) : mul_f16x2(a, b);
+    }
+    static __device__ __forceinline__ f32x2 widen(uint32_t a) {
+        return kBF ? widen_bf16x2(a) : widen_f16x2(a);
+    }
+    static __device__ __forceinline__ uint32_t pack(f32x2 v) {
+        float lo, hi;
+        f2_split(v, lo, hi);
+        return kBF ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+    }
+    // part2 + (x*dy)*g pairwise; without fp32 gamma (g2 == nullptr): x*(dy*gamma)
+    static __device__ __forceinline__ f32x2 pass1(const uint4 &x, const uint4 &dy,
+                                                  const uint4 &gp, const f32x2 *g2, f32x2 part2) {
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, dw[4] = {dy.x, dy.y, dy.z, dy.w};
+        const uint32_t gw[4] = {gp.x, gp.y, gp.z, gp.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (g2) part2 = f2_fma(mul(xw[q], dw[q]), g2[q], part2);
+            else part2 = f2_fma(widen(xw[q]), mul(dw[q], gw[q]), part2);
+        }
+        return part2;
+    }
+    template <bool HAS_DRES>
+    static __device__ __forceinline__ uint4 pass2(const uint4 &x, const uint4 &dy, const uint4 &r,
+                                                  const uint4 &gp, const f32x2 *, f32x2 rs2,
+                                                  f32x2 b2, f32x2 *acc2) {
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, dw[4] = {dy.x, dy.y, dy.z, dy.w};
+        const uint32_t gw[4] = {gp.x, gp.y, gp.z, gp.w}, rw[4] = {r.x, r.y, r.z, r.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            acc2[q] = f2_fma(mul(xw[q], dw[q]), rs2, acc2[q]);                 // += dy*x_hat
+            f32x2 v = f2_fma(widen(xw[q]), b2, f2_mul(mul(dw[q], gw[q]), rs2)); // wdy*rs + x*b
+            if (HAS_DRES) v = f2_add(v, widen(rw[q]));
+            o[q] = pack(v);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+};
+template <> struct RowMath<__nv_bfloat16> : RowMath16<__nv_bfloat16> {};
+template <> struct RowMath<__half> : RowMath16<__half> {};
+
 template <typename T, int CPT, bool HAS_DRES, bool ATOMIC>
 __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
     bwd_row_kernel(const RowArgs a) {
     constexpr int V = Traits<T>::kVec;
+    constexpr int P = RowMath<T>::kPairs;  // fp32 pairs per chunk
     constexpr int NT = HAS_DRES ? 3 : 2;
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    float *red = reinterpret_cast<float *>(smem + kRedOffset);
-    int *redflag = reinterpret_cast<int *>(smem + kFlagOffset);
-    uint8_t *stage_base = smem + kStageOffset;
+    // gamma is also kept as fp32 pairs when the math needs it or when that
+    // fits the register budget
+    constexpr bool kGammaF = RowMath<T>::kNeedsGammaF || CPT * V <= 8;
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *red = reinterpret_cast<float *>(smem);
+    uint8_t *ring = smem + kRingOffset;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -89,154 +178,126 @@ __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
     const int team_warps = a.team_threads >> 5;
     const int first_warp = team * team_warps;
     const int S = a.stages;
-    const int stage_bytes = NT * a.row_pitch;
 
-    if (tid == 0) {
-        for (int i = 0; i < a.teams * S; ++i) mbar_init(smem_addr(&bars[i]), 1);
-        fence_mbarrier_init();
-    }
-    __syncthreads();
+    // This thread's ring: chunk kk of tensor t in slot s lives at
+    // my0 + s*slot_bytes + t*tensor_bytes + kk*kk_bytes.
+    const int tc = CPT * a.team_threads;
+    const uint32_t kk_bytes = 16u * a.team_threads;
+    const uint32_t tensor_bytes = 16u * tc;
+    const uint32_t slot_bytes = NT * tensor_bytes;
+    const uint32_t my0 = smem_addr(ring) + (uint32_t)team * S * slot_bytes + 16u * tt;
 
     const int64_t team_stride = (int64_t)gridDim.x * a.teams;
     const int64_t row0 = (int64_t)blockIdx.x * a.teams + team;
     const int64_t nrows = row0 < a.M ? (a.M - 1 - row0) / team_stride + 1 : 0;
-    uint8_t *my_stages = stage_base + (size_t)team * S * stage_bytes;
-    const uint32_t my_bars = smem_addr(&bars[team * S]);
-    const uint32_t tx_bytes = (uint32_t)(NT * a.row_bytes);
+    const uint64_t policy = l2_policy_evict_first();
 
-    uint64_t policy = 0;
-    if (tt == 0) policy = l2_policy_evict_first();
-
-    // Leader only: load this team's k-th row into slot k % S.
-    auto issue = [&](int64_t k) {
-        const int s = (int)(k % S);
-        const int64_t row = row0 + k * team_stride;
-        const uint32_t bar = my_bars + 8u * s;
-        const uint32_t dst = smem_addr(my_stages + (size_t)s * stage_bytes);
-        const size_t off = (size_t)row * a.row_bytes;
-        mbar_arrive_expect_tx(bar, tx_bytes);
-        bulk_copy_g2s(dst, a.x + off, a.row_bytes, bar, policy);
-        bulk_copy_g2s(dst + a.row_pitch, a.dy + off, a.row_bytes, bar, policy);
-        if (HAS_DRES) bulk_copy_g2s(dst + 2 * a.row_pitch, a.dres + off, a.row_bytes, bar, policy);
-    };
-
-    if (tt == 0) {
-        const int64_t n0 = nrows < S ? nrows : S;
-        for (int64_t k = 0; k < n0; ++k) issue(k);
-    }
-
-    uint4 g[CPT];
+    // byte offset of this thread's chunk kk within a row, and whether it exists
+    uint32_t coff[CPT];
+    bool cok[CPT];
 #pragma unroll
     for (int kk = 0; kk < CPT; ++kk) {
         const int c = tt + kk * a.team_threads;
-        g[kk] = c < a.nchunks ? ld_global_nc_v4(a.gamma + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
+        coff[kk] = 16u * c;
+        cok[kk] = c < a.nchunks;
     }
-    float acc[CPT][V];
+
+    // Copy this thread's chunks of row `row` into slot `s`.
+    auto issue = [&](int64_t row, int s) {
+        const size_t off = (size_t)row * a.row_bytes;
+        const uint8_t *xr = a.x + off, *dr = a.dy + off, *rr = HAS_DRES ? a.dres + off : nullptr;
+        const uint32_t d = my0 + (uint32_t)s * slot_bytes;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            if (cok[kk]) {
+                cp_async16(d + kk * kk_bytes, xr + coff[kk], policy);
+                cp_async16(d + tensor_bytes + kk * kk_bytes, dr + coff[kk], policy);
+                if (HAS_DRES) cp_async16(d + 2 * tensor_bytes + kk * kk_bytes, rr + coff[kk], policy);
+            }
+        }
+    };
+    for (int j = 0; j < S - 1; ++j) {
+        if (j < nrows) issue(row0 + j * team_stride, j);
+        cp_async_commit();
+    }
+
+    uint4 gp[CPT];
+    f32x2 g2[kGammaF ? CPT : 1][kGammaF ? P : 1];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        gp[kk] = cok[kk] ? ld_global_nc_v4(a.gamma + coff[kk]) : make_uint4(0, 0, 0, 0);
+        if (kGammaF) {
+            float gf[V];
+            chunk_to_float<T>(gp[kk], gf);
+#pragma unroll
+            for (int q = 0; q < P; ++q)
+                g2[kGammaF ? kk : 0][kGammaF ? q : 0] = f2_make(gf[2 * q], gf[2 * q + 1]);
+        }
+    }
+    f32x2 acc2[CPT][P];
 #pragma unroll
     for (int kk = 0; kk < CPT; ++kk)
 #pragma unroll
-        for (int e = 0; e < V; ++e) acc[kk][e] = 0.f;
+        for (int q = 0; q < P; ++q) acc2[kk][q] = f2_make(0.f, 0.f);
 
+    const int64_t ahead = (int64_t)(S - 1) * team_stride;
     float rs_next = nrows > 0 ? __ldg(a.rstd + row0) : 0.f;
-    int64_t k = 0;
-    bool failed = false;
-    for (; k < nrows; ++k) {
-        const int s = (int)(k % S);
-        const uint32_t parity = (uint32_t)((k / S) & 1);
-        const int64_t row = row0 + k * team_stride;
+    int slot = 0, fill = S - 1;
+    int64_t row = row0;
+    for (int64_t k = 0; k < nrows; ++k, row += team_stride) {
+        // Refill: row k+S-1 goes into the slot this thread finished with in
+        // the previous iteration; then wait until row k's copies have landed.
+        if (k + S - 1 < nrows) issue(row + ahead, fill);
+        cp_async_commit();
         const float rs = rs_next;
         if (k + 1 < nrows) rs_next = __ldg(a.rstd + row + team_stride);
+        cp_async_wait_pending(S - 1);
+        const uint32_t sb = my0 + (uint32_t)slot * slot_bytes;
 
-        const bool ok = mbar_wait_bounded(my_bars + 8u * s, parity, kWaitLimitCycles);
-        const uint32_t sb = smem_addr(my_stages + (size_t)s * stage_bytes);
-
-        uint4 xv[CPT], dv[CPT], rv[CPT];
-        float part = 0.f;
+        f32x2 part2 = f2_make(0.f, 0.f);
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
-            const int c = tt + kk * a.team_threads;
-            if (c < a.nchunks) {
-                xv[kk] = ld_shared_v4(sb + 16u * c);
-                dv[kk] = ld_shared_v4(sb + a.row_pitch + 16u * c);
-                if (HAS_DRES) rv[kk] = ld_shared_v4(sb + 2 * a.row_pitch + 16u * c);
-                float xf[V], df[V], gf[V];
-                chunk_to_float<T>(xv[kk], xf);
-                chunk_to_float<T>(dv[kk], df);
-                chunk_to_float<T>(g[kk], gf);
-#pragma unroll
-                for (int e = 0; e < V; ++e) part = fmaf(xf[e], df[e] * gf[e], part);
-            }
+            if (cok[kk])
+                part2 = RowMath<T>::pass1(ld_shared_v4(sb + kk * kk_bytes),
+                                          ld_shared_v4(sb + tensor_bytes + kk * kk_bytes), gp[kk],
+                                          kGammaF ? g2[kGammaF ? kk : 0] : nullptr, part2);
         }
-        // c1 reduction across the team; the same barrier also tells the
-        // leader that every thread has finished reading slot s.
-        part = warp_sum(part);
-        int any_fail;
+        float plo, phi;
+        f2_split(part2, plo, phi);
+        float part = warp_sum(plo + phi);
         if (team_warps > 1) {
             const int base = (int)(k & 1) * 32;
-            if (lane == 0) {
-                red[base + warp] = part;
-                redflag[base + warp] = ok ? 0 : 1;
-            }
+            if (lane == 0) red[base + warp] = part;
             named_barrier_sync(1 + team, a.team_threads);
             float tot = 0.f;
-            int fl = 0;
-            for (int w = 0; w < team_warps; ++w) {
-                tot += red[base + first_warp + w];
-                fl |= redflag[base + first_warp + w];
-            }
+            for (int w = 0; w < team_warps; ++w) tot += red[base + first_warp + w];
             part = tot;
-            any_fail = fl;
-        } else {
-            any_fail = __any_sync(0xFFFFFFFFu, !ok);
-            __syncwarp();
-        }
-        if (any_fail) {
-            failed = true;
-            break;
-        }
-        if (tt == 0 && k + S < nrows) {
-            fence_proxy_async_shared();
-            issue(k + S);
         }
 
+        // dx = (wdy - x_hat*c1)*rstd = wdy*rstd + x*b with b = -rstd^2*c1
         const float c1 = rs * part * a.inv_n;
+        const float b = -rs * rs * c1;
+        const f32x2 rs2 = f2_make(rs, rs), b2 = f2_make(b, b);
         uint8_t *dxrow = a.dx + (size_t)row * a.row_bytes;
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
-            const int c = tt + kk * a.team_threads;
-            if (c < a.nchunks) {
-                float xf[V], df[V], gf[V], rf[V], o[V];
-                chunk_to_float<T>(xv[kk], xf);
-                chunk_to_float<T>(dv[kk], df);
-                chunk_to_float<T>(g[kk], gf);
-                if (HAS_DRES) chunk_to_float<T>(rv[kk], rf);
-#pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float xh = xf[e] * rs;
-                    const float wdy = df[e] * gf[e];
-                    float d = fmaf(-xh, c1, wdy) * rs;
-                    if (HAS_DRES) d += rf[e];
-                    o[e] = d;
-                    acc[kk][e] = fmaf(df[e], xh, acc[kk][e]);
-                }
-                st_global_v4(dxrow + 16u * c, float_to_chunk<T>(o));
+            if (cok[kk]) {
+                const uint4 r = HAS_DRES ? ld_shared_v4(sb + 2 * tensor_bytes + kk * kk_bytes)
+                                         : make_uint4(0, 0, 0, 0);
+                const uint4 o = RowMath<T>::template pass2<HAS_DRES>(
+                    ld_shared_v4(sb + kk * kk_bytes), ld_shared_v4(sb + tensor_bytes + kk * kk_bytes),
+                    r, gp[kk], kGammaF ? g2[kGammaF ? kk : 0] : nullptr, rs2, b2, acc2[kk]);
+                st_global_v4(dxrow + coff[kk], o);
             }
         }
-    }
-
-    if (failed && tt == 0) {
-        // Let the copies this team still has in flight land before exiting.
-        for (int64_t j = k; j < nrows && j < k + S; ++j) {
-            const int s = (int)(j % S);
-            mbar_wait_bounded(my_bars + 8u * s, (uint32_t)((j / S) & 1), kWaitLimitCycles);
-        }
-        atomicExch(a.status, 5 /* RN_ERR_TIMEOUT */);
+        if (++slot == S) slot = 0;
+        if (++fill == S) fill = 0;
     }
 
     pdl_launch_dependents();
 
     // ---- weight-gradient partial of this CTA
-    __syncthreads();  // all teams are done with their slots
+    __syncthreads();  // every team is done with its ring (all real copies waited for)
     float *out_row = ATOMIC ? a.dw_out : a.dw_out + (size_t)blockIdx.x * a.N;
     if (ATOMIC) pdl_wait();  // the zeroing kernel ahead of this one has finished
     if (a.teams == 1) {
@@ -246,8 +307,9 @@ __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
             if (c < a.nchunks) {
 #pragma unroll
                 for (int q = 0; q < V / 4; ++q) {
-                    float4 v = make_float4(acc[kk][4 * q], acc[kk][4 * q + 1], acc[kk][4 * q + 2],
-                                           acc[kk][4 * q + 3]);
+                    float4 v;
+                    f2_split(acc2[kk][2 * q], v.x, v.y);
+                    f2_split(acc2[kk][2 * q + 1], v.z, v.w);
                     float4 *dst = reinterpret_cast<float4 *>(out_row + (size_t)c * V + 4 * q);
                     if (ATOMIC) atomicAdd(dst, v);
                     else *dst = v;
@@ -256,7 +318,11 @@ __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
         }
         return;
     }
-    float *sdw = reinterpret_cast<float *>(stage_base);
+    // Teams add their partials in a fixed order (deterministic). Layout: the
+    // float4 `q` of chunk c sits at float4 index q*tc + c, so a warp's 16-byte
+    // accesses for one (kk, q) are consecutive (no bank conflicts).
+    constexpr int Q = V / 4;
+    float4 *sdw = reinterpret_cast<float4 *>(ring);
     for (int t = 0; t < a.teams; ++t) {
         if (team == t) {
 #pragma unroll
@@ -264,18 +330,29 @@ __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
                 const int c = tt + kk * a.team_threads;
                 if (c < a.nchunks) {
 #pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        float *p = sdw + (size_t)c * V + e;
-                        *p = (t == 0) ? acc[kk][e] : *p + acc[kk][e];
+                    for (int q = 0; q < Q; ++q) {
+                        float4 *p = sdw + (size_t)q * tc + c;
+                        float4 v;
+                        f2_split(acc2[kk][2 * q], v.x, v.y);
+                        f2_split(acc2[kk][2 * q + 1], v.z, v.w);
+                        if (t > 0) {
+                            const float4 o = *p;
+                            v.x += o.x;
+                            v.y += o.y;
+                            v.z += o.z;
+                            v.w += o.w;
+                        }
+                        *p = v;
                     }
                 }
             }
         }
         __syncthreads();
     }
-    for (int i = tid * 4; i < a.N; i += blockDim.x * 4) {
-        float4 v = *reinterpret_cast<const float4 *>(sdw + i);
-        float4 *dst = reinterpret_cast<float4 *>(out_row + i);
+    for (int i = tid; i < a.N / 4; i += blockDim.x) {
+        const int c = i / Q, q = i - c * Q;
+        const float4 v = sdw[(size_t)q * tc + c];
+        float4 *dst = reinterpret_cast<float4 *>(out_row) + i;
         if (ATOMIC) atomicAdd(dst, v);
         else *dst = v;
     }
@@ -332,12 +409,10 @@ cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_
     a.dres = static_cast<const uint8_t *>(p.dres);
     a.dx = static_cast<uint8_t *>(p.dx);
     a.dw_out = plan.atomic ? p.dw_f32 : reinterpret_cast<float *>(p.ws + kWsHeaderBytes);
-    a.status = reinterpret_cast<int *>(p.ws);
     a.M = p.M;
     a.N = p.N;
     a.row_bytes = p.N * eb;
     a.nchunks = a.row_bytes / 16;
-    a.row_pitch = round_up(a.row_bytes, 128);
     a.team_threads = plan.team_threads;
     a.teams = plan.teams;
     a.stages = plan.stages;

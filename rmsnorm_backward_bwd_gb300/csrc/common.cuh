@@ -1,7 +1,7 @@
 // Shared device helpers for the sm_103a RMSNorm kernels: I/O dtype traits,
-// 16-byte chunk packing, warp reductions, and inline-PTX wrappers for
-// mbarriers, bulk async copies (global -> shared) and programmatic dependent
-// launch.
+// 16-byte chunk packing, warp reductions, and inline-PTX wrappers for async
+// 16-byte copies, mixed-precision (bf16/f16 x bf16/f16 + fp32) arithmetic
+// and programmatic dependent launch.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -127,6 +127,15 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void *p) {
     return v;
 }
 
+// Same, with an L2 eviction policy (createpolicy).
+__device__ __forceinline__ uint4 ld_global_nc_v4_hint(const void *p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
 __device__ __forceinline__ void st_global_v4(void *p, const uint4 &v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
@@ -146,66 +155,141 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// ------------------------------------------------------------- mbarriers
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbarrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// Order this thread's earlier generic-proxy shared-memory accesses before
-// later async-proxy (bulk copy) accesses to the same memory.
-__device__ __forceinline__ void fence_proxy_async_shared() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+// ----------------------------------------------------- async 16-byte copies
+// One 16-byte asynchronous copy global -> shared through the load/store
+// path (L1 bypassed), with an L2 eviction policy. Completion is tracked per
+// thread with commit / wait groups: a thread that reads back only what it
+// copied itself needs no other synchronisation.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(src), "l"(policy)
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Wait for phase `parity` of an mbarrier to complete, giving up after
-// `limit_cycles` SM clock cycles. Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  long long limit_cycles) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > limit_cycles) return false;
+// Wait until at most `pending` of this thread's newest commit groups are
+// still in flight (0 <= pending <= 7).
+__device__ __forceinline__ void cp_async_wait_pending(int pending) {
+    switch (pending) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
     }
-}
-
-// One bulk asynchronous copy global -> this CTA's shared memory; completion
-// is signalled as transaction bytes on `bar`. dst, src 16-byte aligned;
-// bytes a multiple of 16.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                              uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-        : "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// ------------------------------------------------ mixed-precision arithmetic
+// d_lo = a_lo*b_lo + c_lo and d_hi = a_hi*b_hi + c_hi on the two 16-bit
+// halves of packed words, with an fp32 addend and result and one rounding
+// (the product of two bf16 or two f16 values is exact in fp32).
+__device__ __forceinline__ void fma2_bf16(uint32_t a, uint32_t b, float c0, float c1, float &d0,
+                                          float &d1) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %4;\n\tfma.rn.f32.bf16 %1, ah, bh, %5;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(a), "r"(b), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ void fma2_f16(uint32_t a, uint32_t b, float c0, float c1, float &d0,
+                                         float &d1) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %4;\n\tfma.rn.f32.f16 %1, ah, bh, %5;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(a), "r"(b), "f"(c0), "f"(c1));
+}
+
+// d = a + c with a a 16-bit half of a packed word and c fp32 (one rounding).
+__device__ __forceinline__ void add2_bf16(uint32_t a, float c0, float c1, float &d0, float &d1) {
+    asm("{\n\t.reg .b16 al, ah;\n\tmov.b32 {al, ah}, %2;\n\t"
+        "add.rn.f32.bf16 %0, al, %3;\n\tadd.rn.f32.bf16 %1, ah, %4;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(a), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ void add2_f16(uint32_t a, float c0, float c1, float &d0, float &d1) {
+    asm("{\n\t.reg .b16 al, ah;\n\tmov.b32 {al, ah}, %2;\n\t"
+        "add.rn.f32.f16 %0, al, %3;\n\tadd.rn.f32.f16 %1, ah, %4;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(a), "f"(c0), "f"(c1));
+}
+
+// ------------------------------------------------------ packed fp32 pairs
+// Two fp32 values in one 64-bit register pair; one f32x2 instruction does
+// both lanes (each lane rounded exactly as the scalar fp32 operation).
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f32x2 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Exact products of the two 16-bit halves of packed words, as an fp32 pair
+// (mixed-precision FMA with a zero addend; bf16*bf16 and f16*f16 products
+// are exact in fp32).
+__device__ __forceinline__ f32x2 mul_bf16x2(uint32_t a, uint32_t b) {
+    f32x2 d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 lo, al, bl, 0f00000000;\n\t"
+        "fma.rn.f32.bf16 hi, ah, bh, 0f00000000;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(d)
+        : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 mul_f16x2(uint32_t a, uint32_t b) {
+    f32x2 d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 lo, al, bl, 0f00000000;\n\t"
+        "fma.rn.f32.f16 hi, ah, bh, 0f00000000;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(d)
+        : "r"(a), "r"(b));
+    return d;
+}
+// The two 16-bit halves of a packed word, widened to an fp32 pair.
+__device__ __forceinline__ f32x2 widen_bf16x2(uint32_t w) {
+    return f2_make(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ f32x2 widen_f16x2(uint32_t w) {
+    float lo, hi;
+    f16x2_to_float(w, lo, hi);
+    return f2_make(lo, hi);
 }
 
 // ------------------------------------------- programmatic dependent launch
@@ -218,10 +302,8 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ~1 s at GB300 clocks: the limit on any device-side wait.
-constexpr long long kWaitLimitCycles = 2000000000LL;
-
-// Workspace header: status word at byte 0; partials start at byte 256.
+// Workspace: the partial rows start after a 256-byte header (kept free so
+// that the partials stay 256-byte aligned).
 constexpr size_t kWsHeaderBytes = 256;
 
 }  // namespace rn

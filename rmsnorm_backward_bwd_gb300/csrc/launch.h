@@ -22,7 +22,7 @@ struct BwdProblem {
     void *dx;
     float *dw_f32;
     void *dw_cast;        // nullable
-    uint8_t *ws;          // workspace (status word + partials)
+    uint8_t *ws;          // workspace (header + partial rows)
     int64_t M;
     int N;
     int dtype;
@@ -33,7 +33,7 @@ struct RowPlan {
     int cpt;           // 16-byte chunks per thread per row (1, 2, 4)
     int team_threads;  // threads that share one row (multiple of 32)
     int teams;         // rows processed concurrently per CTA
-    int stages;        // bulk-copy ring depth per team
+    int stages;        // async-copy ring depth per thread (rows in flight + 1)
     int grid;          // CTAs (persistent)
     size_t smem;       // dynamic shared memory bytes
     bool atomic;       // weight gradient via fp32 atomics (else scratch partials)
@@ -50,7 +50,7 @@ struct GenericPlan {
 // Row engine: largest chunk count per row and CTA thread cap for a cpt.
 constexpr int kRowMaxChunks = 2048;
 int row_max_threads(int cpt);
-size_t row_smem_bytes(int teams, int stages, int ntensors, int row_bytes);
+size_t row_smem_bytes(int teams, int stages, int ntensors, int team_chunks);
 size_t generic_smem_bytes(int N, bool smem_dw);
 
 cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_t s,

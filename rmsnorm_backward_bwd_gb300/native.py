@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "librn_gb300.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "rmsnorm_gb300.h")
 
-RN_OK, RN_ERR_INVALID_ARG, RN_ERR_UNSUPPORTED, RN_ERR_CUDA, RN_ERR_WORKSPACE, RN_ERR_TIMEOUT = range(6)
+RN_OK, RN_ERR_INVALID_ARG, RN_ERR_UNSUPPORTED, RN_ERR_CUDA, RN_ERR_WORKSPACE = range(5)
 RN_F32, RN_F16, RN_BF16 = 0, 1, 2
 OPT_BWD_ENGINE, OPT_DWEIGHT_MODE, OPT_CHUNKS_PER_THREAD, OPT_TEAMS_PER_CTA, OPT_STAGES, OPT_GRID = range(6)
 
@@ -44,8 +44,6 @@ def _bind(lib):
     lib.rn_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, ci, vp]
     lib.rn_fused_add_rmsnorm_bwd.restype = ci
     lib.rn_fused_add_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, ci, vp]
-    lib.rn_workspace_status.restype = ci
-    lib.rn_workspace_status.argtypes = [vp, ci, ctypes.POINTER(ci), vp]
     lib.rn_set_option.restype = ci
     lib.rn_set_option.argtypes = [ci, ci]
     lib.rn_get_option.restype = ci

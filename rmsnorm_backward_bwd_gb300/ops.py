@@ -63,8 +63,8 @@ _WS = {}
 
 
 def bwd_workspace(M, N, dtype, device):
-    """A zero-initialised workspace for the backward on `device`, cached per
-    (device, stream) so that calls sharing it are ordered on the GPU."""
+    """A workspace for the backward on `device`, cached per (device, stream)
+    so that calls sharing it are ordered on the GPU."""
     device = torch.device(device)
     with torch.cuda.device(device):
         nbytes = ctypes.c_size_t(0)
@@ -73,18 +73,9 @@ def bwd_workspace(M, N, dtype, device):
         key = (device.index, torch.cuda.current_stream().cuda_stream)
         ws = _WS.get(key)
         if ws is None or ws.numel() < nbytes.value:
-            ws = torch.zeros(nbytes.value, dtype=torch.uint8, device=device)
+            ws = torch.empty(nbytes.value, dtype=torch.uint8, device=device)
             _WS[key] = ws
         return ws
-
-
-def workspace_status(ws, clear=False):
-    """The device status word of a workspace (0 = fine), see rn_workspace_status."""
-    st = ctypes.c_int(0)
-    with torch.cuda.device(ws.device):
-        native.check(native.lib().rn_workspace_status(_ptr(ws), int(bool(clear)),
-                                                      ctypes.byref(st), _stream()))
-    return st.value
 
 
 def rmsnorm_fwd(x, gamma, eps, *, y=None, rstd=None, store_rstd=True):

@@ -164,12 +164,15 @@ def test_misaligned_pointers_take_generic_path():
     parity.check_bwd(ex, dx, dw, dw32)
 
 
-def test_workspace_status_stays_clean():
+def test_workspace_contents_do_not_matter():
+    """The workspace is scratch: garbage left in it changes nothing."""
     import rmsnorm_backward_bwd_gb300 as rn
     ex = parity.expected_bwd(Case("bf16 M=512 N=4096", 512, 4096, "bf16"))
-    parity.run_gpu_bwd(ex)
+    a = parity.run_gpu_bwd(ex)
     ws = rn.bwd_workspace(512, 4096, torch.bfloat16, "cuda")
-    assert rn.workspace_status(ws) == 0
+    ws.fill_(0x7F)
+    b = parity.run_gpu_bwd(ex)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2])
 
 
 def test_invariant_holds_at_full_size():
