@@ -137,6 +137,30 @@ rn_status rn_fused_add_rmsnorm_bwd(const void *added, const void *gamma, const v
                                    int64_t M, int64_t N, int dtype, void *stream);
 
 /*
+ * Backward, plain RMSNorm, without a caller workspace. (This call has no
+ * counterpart on the FlyDSL pages; it exists for callers that cannot
+ * allocate device memory when they run the backward -- e.g. code running
+ * while a caching allocator or memory pool is locked or being torn down, or
+ * an embedder that fixes every device allocation up front.)
+ *   Arguments, layouts, outputs and results are those of rn_rmsnorm_bwd.
+ *   The scratch comes from a fixed 16 MiB array inside the library's device
+ *   image, held by every GPU that loads the library until the process exits.
+ *   Problems needing more scratch than that (rn_bwd_workspace_bytes(M, N,
+ *   dtype) > 16 MiB, i.e. N above ~13,800 on a 152-SM GB300) are refused
+ *   with RN_ERR_UNSUPPORTED and a message in rn_last_error(); nothing is
+ *   launched. The call allocates nothing and frees nothing.
+ *   The first call on a device looks up the array's device address on that
+ *   device (cudaGetSymbolAddress); make that first call before any stream
+ *   capture. All calls share the one array: nothing in it needs to start at
+ *   zero (every call overwrites the part it reads), but calls that could run
+ *   at the same time on the GPU (different streams without ordering) race on
+ *   it and give wrong results. Order such calls on one stream or with events.
+ */
+rn_status rn_rmsnorm_bwd_noalloc(const void *x, const void *gamma, const void *dy,
+                                 const float *rstd, void *dx, float *dweight_f32, void *dweight,
+                                 int64_t M, int64_t N, int dtype, void *stream);
+
+/*
  * Tuning / test options. They are process-wide, not thread-safe, and apply
  * to calls made after they are set; value 0 always means "automatic".
  */

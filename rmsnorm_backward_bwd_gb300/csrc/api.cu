@@ -36,6 +36,8 @@ static rn_status fail(rn_status st, const char *fmt, ...) {
     return st;
 }
 
+void set_last_error(const char *msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 static rn_status cuda_fail(cudaError_t e, const char *what) {
     return fail(RN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }

@@ -80,6 +80,9 @@ struct FwdProblem {
 
 cudaError_t launch_fwd(const FwdProblem &p, bool vector_ok, int num_sms, cudaStream_t s);
 
+// Replace the calling thread's message returned by rn_last_error().
+void set_last_error(const char *msg);
+
 // Set the dynamic shared memory cap of a kernel once per device.
 cudaError_t ensure_smem_attr(const void *func, size_t bytes);
 

@@ -44,6 +44,8 @@ def _bind(lib):
     lib.rn_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, ci, vp]
     lib.rn_fused_add_rmsnorm_bwd.restype = ci
     lib.rn_fused_add_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, ci, vp]
+    lib.rn_rmsnorm_bwd_noalloc.restype = ci
+    lib.rn_rmsnorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, vp]
     lib.rn_set_option.restype = ci
     lib.rn_set_option.argtypes = [ci, ci]
     lib.rn_get_option.restype = ci
