@@ -166,7 +166,9 @@ rn_status rn_rmsnorm_bwd_noalloc(const void *x, const void *gamma, const void *d
  */
 typedef enum rn_option {
     RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (async-copy ring), 2 = generic engine */
-    RN_OPT_DWEIGHT_MODE = 1,  /* 1 = scratch partials + finalize, 2 = fp32 atomics + cast */
+    RN_OPT_DWEIGHT_MODE = 1,  /* 1 = scratch partials + finalize (deterministic dweight),
+                                 2 = fp32 atomics + cast (the default where possible: faster,
+                                 summation order varies from call to call) */
     RN_OPT_CHUNKS_PER_THREAD = 2, /* row engine: 16-byte chunks per thread per row: 1, 2, 4 */
     RN_OPT_TEAMS_PER_CTA = 3, /* row engine: rows processed at once per CTA (1..15) */
     RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8) */

@@ -37,10 +37,10 @@
 
 namespace rn {
 
-int row_max_threads(int cpt) { return cpt <= 1 ? 1024 : (cpt == 2 ? 768 : 512); }
+int row_max_threads(int cpt) { return cpt <= 2 ? 768 : 512; }
 
 template <int CPT> struct RowBounds {
-    static constexpr int kMaxThreads = CPT <= 1 ? 1024 : (CPT == 2 ? 768 : 512);
+    static constexpr int kMaxThreads = CPT <= 2 ? 768 : 512;
 };
 
 constexpr int kRingOffset = 256;  // after [2 parities][32 warps] fp32 partial sums
@@ -158,6 +158,92 @@ template <typename T> struct RowMath16 {
 template <> struct RowMath<__nv_bfloat16> : RowMath16<__nv_bfloat16> {};
 template <> struct RowMath<__half> : RowMath16<__half> {};
 
+// The CTA's weight-gradient partial: teams add theirs in a fixed order in
+// shared memory (deterministic), then the CTA stores one partial row to the
+// workspace (scratch mode) or adds it with fp32 vector atomics into
+// dweight_f32 (atomic mode, after the zeroing kernel ahead has finished).
+// Layout in shared memory: the float4 `q` of chunk c sits at float4 index
+// q*tc + c, so a warp's 16-byte accesses for one (kk, q) are consecutive (no
+// bank conflicts). `scratch` must hold N floats and be free of other use.
+template <typename T, int CPT, bool ATOMIC>
+__device__ __forceinline__ void cta_partial_out(const f32x2 (&acc2)[CPT][RowMath<T>::kPairs],
+                                                const RowArgs &a, uint8_t *scratch, int team,
+                                                int tt) {
+    constexpr int V = Traits<T>::kVec;
+    float *out_row = ATOMIC ? a.dw_out : a.dw_out + (size_t)blockIdx.x * a.N;
+    if (ATOMIC) pdl_wait();
+    if (a.teams == 1) {
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = tt + kk * a.team_threads;
+            if (c < a.nchunks) {
+#pragma unroll
+                for (int q = 0; q < V / 4; ++q) {
+                    float4 v;
+                    f2_split(acc2[kk][2 * q], v.x, v.y);
+                    f2_split(acc2[kk][2 * q + 1], v.z, v.w);
+                    float4 *dst = reinterpret_cast<float4 *>(out_row + (size_t)c * V + 4 * q);
+                    if (ATOMIC) atomicAdd(dst, v);
+                    else *dst = v;
+                }
+            }
+        }
+        return;
+    }
+    constexpr int Q = V / 4;
+    const int tc = CPT * a.team_threads;
+    float4 *sdw = reinterpret_cast<float4 *>(scratch);
+    for (int t = 0; t < a.teams; ++t) {
+        if (team == t) {
+#pragma unroll
+            for (int kk = 0; kk < CPT; ++kk) {
+                const int c = tt + kk * a.team_threads;
+                if (c < a.nchunks) {
+#pragma unroll
+                    for (int q = 0; q < Q; ++q) {
+                        float4 *p = sdw + (size_t)q * tc + c;
+                        float4 v;
+                        f2_split(acc2[kk][2 * q], v.x, v.y);
+                        f2_split(acc2[kk][2 * q + 1], v.z, v.w);
+                        if (t > 0) {
+                            const float4 o = *p;
+                            v.x += o.x;
+                            v.y += o.y;
+                            v.z += o.z;
+                            v.w += o.w;
+                        }
+                        *p = v;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    for (int i = threadIdx.x; i < a.N / 4; i += blockDim.x) {
+        const int c = i / Q, q = i - c * Q;
+        const float4 v = sdw[(size_t)q * tc + c];
+        float4 *dst = reinterpret_cast<float4 *>(out_row) + i;
+        if (ATOMIC) atomicAdd(dst, v);
+        else *dst = v;
+    }
+}
+
+// Sum of one value per thread over a team of team_warps warps: warp
+// shuffles, then the warps' sums through shared memory (double-buffered by
+// `parity`) and one named barrier, then a second shuffle; every thread of
+// the team gets the same bits.
+__device__ __forceinline__ float team_sum(float v, float *red, int parity, int team, int warp,
+                                          int lane, int team_warps, int first_warp,
+                                          int team_threads) {
+    v = warp_sum(v);
+    if (team_warps == 1) return v;
+    float *slot = red + parity * 32;
+    if (lane == 0) slot[warp] = v;
+    named_barrier_sync(1 + team, team_threads);
+    float w = lane < team_warps ? slot[first_warp + lane] : 0.f;
+    return warp_sum(w);
+}
+
 template <typename T, int CPT, bool HAS_DRES, bool ATOMIC>
 __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
     bwd_row_kernel(const RowArgs a) {
@@ -264,15 +350,8 @@ __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
         }
         float plo, phi;
         f2_split(part2, plo, phi);
-        float part = warp_sum(plo + phi);
-        if (team_warps > 1) {
-            const int base = (int)(k & 1) * 32;
-            if (lane == 0) red[base + warp] = part;
-            named_barrier_sync(1 + team, a.team_threads);
-            float tot = 0.f;
-            for (int w = 0; w < team_warps; ++w) tot += red[base + first_warp + w];
-            part = tot;
-        }
+        const float part = team_sum(plo + phi, red, (int)(k & 1), team, warp, lane, team_warps,
+                                    first_warp, a.team_threads);
 
         // dx = (wdy - x_hat*c1)*rstd = wdy*rstd + x*b with b = -rstd^2*c1
         const float c1 = rs * part * a.inv_n;
@@ -295,67 +374,8 @@ __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
     }
 
     pdl_launch_dependents();
-
-    // ---- weight-gradient partial of this CTA
     __syncthreads();  // every team is done with its ring (all real copies waited for)
-    float *out_row = ATOMIC ? a.dw_out : a.dw_out + (size_t)blockIdx.x * a.N;
-    if (ATOMIC) pdl_wait();  // the zeroing kernel ahead of this one has finished
-    if (a.teams == 1) {
-#pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            const int c = tt + kk * a.team_threads;
-            if (c < a.nchunks) {
-#pragma unroll
-                for (int q = 0; q < V / 4; ++q) {
-                    float4 v;
-                    f2_split(acc2[kk][2 * q], v.x, v.y);
-                    f2_split(acc2[kk][2 * q + 1], v.z, v.w);
-                    float4 *dst = reinterpret_cast<float4 *>(out_row + (size_t)c * V + 4 * q);
-                    if (ATOMIC) atomicAdd(dst, v);
-                    else *dst = v;
-                }
-            }
-        }
-        return;
-    }
-    // Teams add their partials in a fixed order (deterministic). Layout: the
-    // float4 `q` of chunk c sits at float4 index q*tc + c, so a warp's 16-byte
-    // accesses for one (kk, q) are consecutive (no bank conflicts).
-    constexpr int Q = V / 4;
-    float4 *sdw = reinterpret_cast<float4 *>(ring);
-    for (int t = 0; t < a.teams; ++t) {
-        if (team == t) {
-#pragma unroll
-            for (int kk = 0; kk < CPT; ++kk) {
-                const int c = tt + kk * a.team_threads;
-                if (c < a.nchunks) {
-#pragma unroll
-                    for (int q = 0; q < Q; ++q) {
-                        float4 *p = sdw + (size_t)q * tc + c;
-                        float4 v;
-                        f2_split(acc2[kk][2 * q], v.x, v.y);
-                        f2_split(acc2[kk][2 * q + 1], v.z, v.w);
-                        if (t > 0) {
-                            const float4 o = *p;
-                            v.x += o.x;
-                            v.y += o.y;
-                            v.z += o.z;
-                            v.w += o.w;
-                        }
-                        *p = v;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
-    for (int i = tid; i < a.N / 4; i += blockDim.x) {
-        const int c = i / Q, q = i - c * Q;
-        const float4 v = sdw[(size_t)q * tc + c];
-        float4 *dst = reinterpret_cast<float4 *>(out_row) + i;
-        if (ATOMIC) atomicAdd(dst, v);
-        else *dst = v;
-    }
+    cta_partial_out<T, CPT, ATOMIC>(acc2, a, ring, team, tt);
 }
 
 template <typename T, int CPT, bool HAS_DRES, bool ATOMIC>

@@ -90,6 +90,7 @@ def test_row_engine_grid_caps(grid):
 
 
 def test_scratch_mode_is_bitwise_repeatable():
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)
     ex = parity.expected_bwd(Case("bf16 M=2048 N=4096", 2048, 4096, "bf16"))
     a = parity.run_gpu_bwd(ex)
     b = parity.run_gpu_bwd(ex)
@@ -98,6 +99,7 @@ def test_scratch_mode_is_bitwise_repeatable():
 
 def test_fused_dx_may_alias_dresidual_out():
     import rmsnorm_backward_bwd_gb300 as rn
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)  # bitwise comparison: deterministic dweight
     case = Case("bf16 M=257 N=4096 fused", 257, 4096, "bf16", fused=True, with_dres=True)
     ex = parity.expected_bwd(case)
     x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
@@ -113,6 +115,7 @@ def test_fused_dx_may_alias_dresidual_out():
 
 def test_fused_with_zero_residual_grad_equals_plain():
     import rmsnorm_backward_bwd_gb300 as rn
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)  # bitwise comparison: deterministic dweight
     ex = parity.expected_bwd(Case("bf16 M=128 N=4096", 128, 4096, "bf16"))
     x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
     dx, dw, dw32 = rn.rmsnorm_bwd(x, g, dy, rstd)
@@ -167,6 +170,7 @@ def test_misaligned_pointers_take_generic_path():
 def test_workspace_contents_do_not_matter():
     """The workspace is scratch: garbage left in it changes nothing."""
     import rmsnorm_backward_bwd_gb300 as rn
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)  # the mode that uses the workspace
     ex = parity.expected_bwd(Case("bf16 M=512 N=4096", 512, 4096, "bf16"))
     a = parity.run_gpu_bwd(ex)
     ws = rn.bwd_workspace(512, 4096, torch.bfloat16, "cuda")
@@ -193,3 +197,31 @@ def test_invariant_holds_at_full_size():
     # rstd is fp32 (not exactly (ms+eps)^-1/2): the identity then holds up to that rounding
     bound += 4 * 2.0**-24 * np.abs(np.sum(x * g * dy, axis=1)) * r
     assert np.all(np.abs(lhs - rhs) <= bound)
+
+
+@pytest.mark.parametrize("case", [synth.PLAIN_4096, synth.FUSED_4096], ids=lambda c: c.name)
+def test_atomic_and_scratch_dweight_modes_agree(case):
+    ex = parity.expected_bwd(case)
+    out = {}
+    for mode in (1, 2):
+        native.set_option(native.OPT_DWEIGHT_MODE, mode)
+        dx, dw, dw32 = parity.run_gpu_bwd(ex)
+        parity.check_bwd(ex, dx, dw, dw32)
+        assert ("dw=atomic" if mode == 2 else "dw=scratch") in native.last_plan()
+        out[mode] = (dx, dw32)
+    assert torch.equal(out[1][0], out[2][0])  # dx does not depend on the mode
+    parity.check_tensor("dweight_f32 atomic vs scratch", out[2][1], parity.to64(out[1][1]),
+                        case.dtype, "dweight_f32")
+
+
+def test_generic_engine_falls_back_to_scratch_partials_for_wide_rows():
+    """Rows too wide for the generic engine's shared-memory partial use the
+    scratch mode by default; forcing atomics there is refused."""
+    case = Case("f32 M=2 N=60001", 2, 60001, "f32")
+    ex = parity.expected_bwd(case)
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    parity.check_bwd(ex, dx, dw, dw32)
+    assert "engine=generic" in native.last_plan() and "dw=scratch" in native.last_plan()
+    native.set_option(native.OPT_DWEIGHT_MODE, 2)
+    with pytest.raises(native.RNError, match="atomic mode"):
+        parity.run_gpu_bwd(ex)
