@@ -86,15 +86,20 @@ cudaError_t ensure_smem_attr(const void *func, size_t bytes) {
         auto it = g_smem_set.find(key);
         if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
     }
-    // Always set the kernel's cap to the device maximum we may ask for.
+    // Set the kernel's cap to the most dynamic shared memory it can have:
+    // the device's opt-in limit minus the kernel's own static shared memory.
     DeviceInfo d;
     e = device_info(&d, nullptr);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)d.smem_optin);
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, func);
+    if (e != cudaSuccess) return e;
+    const size_t cap = d.smem_optin - fa.sharedSizeBytes;
+    if (bytes > cap) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cap);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_mu);
-    g_smem_set[key] = d.smem_optin;
+    g_smem_set[key] = cap;
     return cudaSuccess;
 }
 
