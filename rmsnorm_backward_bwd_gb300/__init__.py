@@ -5,6 +5,8 @@ The compute runs in a CUDA library for sm_103a (``csrc/``, C ABI in
 """
 from .ops import (bwd_workspace, fused_add_rmsnorm_bwd, fused_add_rmsnorm_fwd, rmsnorm_bwd,
                   rmsnorm_fwd)
+from .autograd import FusedAddRMSNormFunction, RMSNormFunction, fused_add_rmsnorm, rmsnorm
 
 __all__ = ["rmsnorm_fwd", "rmsnorm_bwd", "fused_add_rmsnorm_fwd", "fused_add_rmsnorm_bwd",
-           "bwd_workspace"]
+           "bwd_workspace", "rmsnorm", "fused_add_rmsnorm", "RMSNormFunction",
+           "FusedAddRMSNormFunction"]

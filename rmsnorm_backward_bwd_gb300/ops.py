@@ -29,6 +29,9 @@ def _need(name, t, ref, shape=None, dtype=None):
         raise ValueError("%s is required" % name)
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cuda":
+        # the library takes device pointers only; there is no CPU path
+        raise ValueError("%s is on %s: these ops run on CUDA devices only" % (name, t.device))
     if t.device != ref.device:
         raise ValueError("%s is on %s, expected %s" % (name, t.device, ref.device))
     want = ref.dtype if dtype is None else dtype

@@ -66,8 +66,15 @@ def test_device_queries_report_cuda_error_without_gpu():
     assert st == native.RN_ERR_CUDA
 
 
-def test_python_guards_reject_mismatched_dtypes_on_cpu_tensors():
+def test_python_guards_refuse_host_tensors():
+    """Host pointers never reach the library: CPU tensors are refused before
+    any call (there is no CPU path)."""
     import rmsnorm_backward_bwd_gb300 as rn
     x = torch.zeros(4, 8, dtype=torch.bfloat16)
-    with pytest.raises(ValueError, match="dtype mismatch"):
-        rn.rmsnorm_bwd(x, torch.zeros(8, dtype=torch.float16), x, torch.zeros(4))
+    for call in (lambda: rn.rmsnorm_bwd(x, torch.zeros(8, dtype=torch.float16), x, torch.zeros(4)),
+                 lambda: rn.rmsnorm_fwd(x, torch.zeros(8, dtype=torch.bfloat16), 1e-6),
+                 lambda: rn.fused_add_rmsnorm_fwd(x, x, torch.zeros(8, dtype=torch.bfloat16), 1e-6),
+                 lambda: rn.fused_add_rmsnorm_bwd(x, torch.zeros(8, dtype=torch.bfloat16), x,
+                                                  torch.zeros(4))):
+        with pytest.raises(ValueError, match="CUDA devices only"):
+            call()

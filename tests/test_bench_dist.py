@@ -40,7 +40,7 @@ def _worker(rank, ws, port, out):
 
 def test_replicas_take_the_slowest_rank():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
