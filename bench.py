@@ -187,6 +187,11 @@ def whole_job_gbs(bytes_per_rank, ws, slowest_ms):
     return bytes_per_rank * ws / (slowest_ms * 1e-3) / 1e9
 
 
+def synth_bytes(case):
+    from rmsnorm_backward_bwd_gb300 import synth
+    return synth.algorithmic_bytes(case.M, case.N, case.dtype, case.with_dres, True)
+
+
 def workload_case(name):
     from rmsnorm_backward_bwd_gb300 import synth
     table = {"plain_4096": synth.PLAIN_4096, "fused_4096": synth.FUSED_4096,
@@ -316,6 +321,64 @@ def time_e2e(prob, steps, warmup, ws):
     torch.cuda.synchronize()
     barrier(ws)
     return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def autograd_problem(case, dev, impl):
+    """Forward graph of one case built once (outside timing): returns
+    (outputs, inputs, grad_outputs) for torch.autograd.grad. impl "ours" uses
+    this package's autograd wrappers, "torch_eager" torch's own rms_norm."""
+    import torch
+    import rmsnorm_backward_bwd_gb300 as rn
+    from rmsnorm_backward_bwd_gb300 import synth
+    inp = synth.make_inputs(case, device=str(dev))
+    x = inp["x"].requires_grad_()
+    w = inp["gamma"].requires_grad_()
+    if not case.fused:
+        if impl == "ours":
+            y = rn.rmsnorm(x, w, case.eps)
+        else:
+            y = torch.nn.functional.rms_norm(x, (case.N,), w, case.eps)
+        return (y,), (x, w), (inp["dy"],)
+    r = inp["residual"].requires_grad_()
+    if impl == "ours":
+        out, res_out = rn.fused_add_rmsnorm(x, r, w, case.eps)
+    else:
+        res_out = x + r
+        out = torch.nn.functional.rms_norm(res_out, (case.N,), w, case.eps)
+    return (out, res_out), (x, r, w), (inp["dy"], inp["dres"])
+
+
+def time_autograd(graph, steps, warmup, flush, queued=False):
+    """Mean time (ms) between CUDA events around torch.autograd.grad over the
+    saved graph, with an L2 flush before each call; output allocation, the
+    fp32 dweight zero and the cast are inside the timed region.
+
+    queued=False: the host issues the call right after the flush, so host-side
+    time (autograd engine, Python, launches) shows wherever it exceeds the GPU
+    work. queued=True: a GPU sleep of ~0.5 ms after the flush keeps the device
+    busy while the host issues the whole backward, so the events bracket the
+    device work alone."""
+    import numpy as np
+    import torch
+    outs, ins, gos = graph
+    for _ in range(warmup):
+        flush()
+        torch.autograd.grad(outs, ins, gos, retain_graph=True)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        if queued:
+            torch.cuda._sleep(1_000_000)
+        a.record(st)
+        torch.autograd.grad(outs, ins, gos, retain_graph=True)
+        b.record(st)
+        if queued:
+            b.synchronize()   # keep the host from running ahead of the sleep
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ev]))
 
 
 def oracle_rate(case, seconds, nthreads=0):
@@ -462,6 +525,36 @@ def run_ours(args):
             del p2
             torch.cuda.empty_cache()
 
+    autograd = []
+    if not args.no_extra:
+        for name in ("plain_4096", "fused_4096"):
+            c2 = workload_case(name)
+            nbytes = synth_bytes(c2)
+            row = {"workload": c2.name}
+            grads = {}
+            for impl in ("ours", "torch_eager"):
+                g = autograd_problem(c2, dev, impl)
+                grads[impl] = [t.float() for t in torch.autograd.grad(*g, retain_graph=True)]
+                n3 = max(20, args.steps // 4)
+                t = time_autograd(g, n3, args.warmup, flush)
+                tq = time_autograd(g, n3, args.warmup, flush, queued=True)
+                row[impl + "_us"] = round(t * 1e3, 2)
+                row[impl + "_GBps"] = round(nbytes / (t * 1e-3) / 1e9, 1)
+                row[impl + "_device_us"] = round(tq * 1e3, 2)
+                row[impl + "_device_GBps"] = round(nbytes / (tq * 1e-3) / 1e9, 1)
+                del g
+                torch.cuda.empty_cache()
+            # gradients compared before timing is reported (largest difference
+            # relative to the tensor's largest magnitude, over x/residual/weight)
+            row["max_rel_diff_vs_torch_eager"] = float("%.3g" % max(
+                float((a - b).abs().max() / b.abs().max().clamp_min(1e-30))
+                for a, b in zip(grads["ours"], grads["torch_eager"])))
+            del grads
+            row["speedup_vs_torch_eager"] = round(row["torch_eager_us"] / row["ours_us"], 2)
+            row["device_speedup_vs_torch_eager"] = round(
+                row["torch_eager_device_us"] / row["ours_device_us"], 2)
+            autograd.append(row)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         rate, cores, n, secs = oracle_rate(case, args.cpu_seconds)
@@ -496,6 +589,7 @@ def run_ours(args):
             "clocks": clocks,
             "plan": plan,
             "extra": extra,
+            "autograd": autograd,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -25,27 +25,28 @@ def _code(t):
 
 
 def _need(name, t, ref, shape=None, dtype=None):
-    if t is None:
-        raise ValueError("%s is required" % name)
     if not isinstance(t, torch.Tensor):
+        if t is None:
+            raise ValueError("%s is required" % name)
         raise TypeError("%s must be a torch.Tensor" % name)
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         # the library takes device pointers only; there is no CPU path
         raise ValueError("%s is on %s: these ops run on CUDA devices only" % (name, t.device))
-    if t.device != ref.device:
+    if t is not ref and t.get_device() != ref.get_device():
         raise ValueError("%s is on %s, expected %s" % (name, t.device, ref.device))
     want = ref.dtype if dtype is None else dtype
     if t.dtype != want:
         raise ValueError("dtype mismatch: %s is %s, expected %s" % (name, t.dtype, want))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != shape:
         raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
     return t
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    # plain ints: the bound argtypes (c_void_p) convert them
+    return t.data_ptr() if t is not None else None
 
 
 def _rows(x, gamma):
@@ -58,27 +59,73 @@ def _rows(x, gamma):
     return M, N
 
 
-def _stream():
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+# The raw handle of the current stream without building a Stream object (a
+# few microseconds per call saved); the public query is the fallback.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(index):
+    if _raw_stream is not None:
+        return _raw_stream(index)
+    return torch.cuda.current_stream(index).cuda_stream
+
+
+class _on_device:
+    """Make `index` the current device for the block (no-op when it is)."""
+
+    __slots__ = ("index", "prev")
+
+    def __init__(self, index):
+        self.index = index
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.index:
+            self.prev = cur
+            torch.cuda.set_device(self.index)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
 
 
 _WS = {}
+_WS_BYTES = {}
+
+
+def _ws_bytes(M, N, code, index):
+    """Workspace size the library asks for (it depends on the shape, dtype and
+    the device's SM count only), cached."""
+    key = (M, N, code, index)
+    n = _WS_BYTES.get(key)
+    if n is None:
+        nbytes = ctypes.c_size_t(0)
+        native.check(native.lib().rn_bwd_workspace_bytes(int(M), int(N), code,
+                                                         ctypes.byref(nbytes)))
+        n = _WS_BYTES[key] = nbytes.value
+    return n
+
+
+def _workspace(M, N, code, index):
+    # index is the current device here
+    n = _ws_bytes(M, N, code, index)
+    key = (index, _stream_handle(index))
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < n:
+        ws = torch.empty(n, dtype=torch.uint8, device=torch.device("cuda", index))
+        _WS[key] = ws
+    return ws
 
 
 def bwd_workspace(M, N, dtype, device):
     """A workspace for the backward on `device`, cached per (device, stream)
     so that calls sharing it are ordered on the GPU."""
     device = torch.device(device)
-    with torch.cuda.device(device):
-        nbytes = ctypes.c_size_t(0)
-        native.check(native.lib().rn_bwd_workspace_bytes(
-            int(M), int(N), _CODES[dtype], ctypes.byref(nbytes)))
-        key = (device.index, torch.cuda.current_stream().cuda_stream)
-        ws = _WS.get(key)
-        if ws is None or ws.numel() < nbytes.value:
-            ws = torch.empty(nbytes.value, dtype=torch.uint8, device=device)
-            _WS[key] = ws
-        return ws
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    with _on_device(index):
+        return _workspace(M, N, _CODES[dtype], index)
 
 
 def rmsnorm_fwd(x, gamma, eps, *, y=None, rstd=None, store_rstd=True):
@@ -87,7 +134,7 @@ def rmsnorm_fwd(x, gamma, eps, *, y=None, rstd=None, store_rstd=True):
     _need("x", x, x)
     _need("gamma", gamma, x)
     M, N = _rows(x, gamma)
-    with torch.cuda.device(x.device):
+    with _on_device(x.get_device()):
         y = torch.empty_like(x) if y is None else _need("y", y, x, x.shape)
         if store_rstd:
             rstd = (torch.empty(M, dtype=torch.float32, device=x.device) if rstd is None
@@ -95,7 +142,7 @@ def rmsnorm_fwd(x, gamma, eps, *, y=None, rstd=None, store_rstd=True):
         else:
             rstd = None
         native.check(native.lib().rn_rmsnorm_fwd(_ptr(x), _ptr(gamma), float(eps), _ptr(y),
-                                                 _ptr(rstd), M, N, _code(x), _stream()))
+                                                 _ptr(rstd), M, N, _code(x), _stream_handle(x.get_device())))
     return y, rstd
 
 
@@ -107,7 +154,7 @@ def fused_add_rmsnorm_fwd(x, residual, gamma, eps, *, out=None, residual_out=Non
     _need("residual", residual, x, x.shape)
     _need("gamma", gamma, x)
     M, N = _rows(x, gamma)
-    with torch.cuda.device(x.device):
+    with _on_device(x.get_device()):
         out = torch.empty_like(x) if out is None else _need("out", out, x, x.shape)
         residual_out = (torch.empty_like(x) if residual_out is None
                         else _need("residual_out", residual_out, x, x.shape))
@@ -118,7 +165,7 @@ def fused_add_rmsnorm_fwd(x, residual, gamma, eps, *, out=None, residual_out=Non
             rstd = None
         native.check(native.lib().rn_fused_add_rmsnorm_fwd(
             _ptr(x), _ptr(residual), _ptr(gamma), float(eps), _ptr(out), _ptr(residual_out),
-            _ptr(rstd), M, N, _code(x), _stream()))
+            _ptr(rstd), M, N, _code(x), _stream_handle(x.get_device())))
     return out, residual_out, rstd
 
 
@@ -143,12 +190,12 @@ def rmsnorm_bwd(x, gamma, dy, rstd, *, dx=None, dweight_f32=None, dweight=None,
     _need("dy", dy, x, x.shape)
     M, N = _rows(x, gamma)
     _need("rstd", rstd, x, (M,), torch.float32)
-    with torch.cuda.device(x.device):
+    with _on_device(x.get_device()):
         dx, dweight_f32, dweight = _bwd_outputs(x, M, N, dx, dweight_f32, dweight, want_cast)
-        ws = bwd_workspace(M, N, x.dtype, x.device) if workspace is None else workspace
+        ws = _workspace(M, N, _code(x), x.get_device()) if workspace is None else workspace
         native.check(native.lib().rn_rmsnorm_bwd(
             _ptr(x), _ptr(gamma), _ptr(dy), _ptr(rstd), _ptr(dx), _ptr(dweight_f32),
-            _ptr(dweight), _ptr(ws), ws.numel(), M, N, _code(x), _stream()))
+            _ptr(dweight), _ptr(ws), ws.numel(), M, N, _code(x), _stream_handle(x.get_device())))
     return dx, dweight, dweight_f32
 
 
@@ -165,11 +212,12 @@ def fused_add_rmsnorm_bwd(added, gamma, dy, rstd, dresidual_out=None, *, dx=None
     _need("rstd", rstd, added, (M,), torch.float32)
     if dresidual_out is not None:
         _need("dresidual_out", dresidual_out, added, added.shape)
-    with torch.cuda.device(added.device):
+    with _on_device(added.get_device()):
         dx, dweight_f32, dweight = _bwd_outputs(added, M, N, dx, dweight_f32, dweight, want_cast)
-        ws = bwd_workspace(M, N, added.dtype, added.device) if workspace is None else workspace
+        ws = (_workspace(M, N, _code(added), added.get_device()) if workspace is None
+              else workspace)
         native.check(native.lib().rn_fused_add_rmsnorm_bwd(
             _ptr(added), _ptr(gamma), _ptr(dy), _ptr(rstd), _ptr(dresidual_out), _ptr(dx),
             _ptr(dweight_f32), _ptr(dweight), _ptr(ws), ws.numel(), M, N, _code(added),
-            _stream()))
+            _stream_handle(added.get_device())))
     return dx, dx, dweight, dweight_f32
