@@ -1,4 +1,5 @@
-"""CPU oracle for RMSNorm forward / backward (plain and fused-add), fp64.
+"""CPU oracle for RMSNorm forward / backward (plain and fused-add) and for
+LayerNorm forward / backward, fp64.
 
 TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
 benchmark's ``cpu_baseline`` / ``--impl reference`` legs are the only callers.
@@ -8,7 +9,8 @@ package imports nothing from them.
 This module is argument marshalling over ``rmsnorm_oracle.c`` (numpy float64
 arrays in, float64 arrays out); all arithmetic lives in the C file, which
 cites the FlyDSL pages it follows (issue #769 "Math" section; PR #800
-"What's included").
+"What's included"; for LayerNorm, issue #769's plan, which mirrors the RMSNorm
+backward with mean handling and dbias -- the formulas are the textbook ones).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 (symbolic gradients, finite differences, the closed-form invariant, library
@@ -58,6 +60,9 @@ class Oracle:
         lib.oracle_rmsnorm_bwd.argtypes = [_dp, _dp, _dp, _dp, i64, i64, _dp, _dp, ci]
         lib.oracle_fused_add_rmsnorm_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, i64, i64,
                                                      _dp, _dp, ci]
+        lib.oracle_layernorm_fwd.argtypes = [_dp, _dp, _dp, dbl, i64, i64, _dp, _dp, _dp, ci]
+        lib.oracle_layernorm_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, i64, i64, _dp, _dp, _dp,
+                                             ci]
         self._lib = lib
         self.path = libpath
 
@@ -121,6 +126,34 @@ class Oracle:
                                                _p(dx), _p(dw), nthreads)
         return dx, dw
 
+    def layernorm_fwd(self, x, gamma, beta, eps, nthreads=0):
+        """Return (y, mean, rstd) in fp64; beta may be None (no bias)."""
+        x = _arr(x)
+        M, N = x.shape
+        g = _arr(gamma, (N,))
+        b = _arr(beta, (N,)) if beta is not None else None
+        y = np.empty_like(x)
+        mean = np.empty(M, np.float64)
+        rstd = np.empty(M, np.float64)
+        self._lib.oracle_layernorm_fwd(_p(x), _p(g), _p(b), float(eps), M, N, _p(y), _p(mean),
+                                       _p(rstd), nthreads)
+        return y, mean, rstd
+
+    def layernorm_bwd(self, x, gamma, dy, mean, rstd, nthreads=0):
+        """Return (dx, dgamma, dbeta) in fp64 from the given saved mean and rstd."""
+        x = _arr(x)
+        M, N = x.shape
+        g = _arr(gamma, (N,))
+        d = _arr(dy, (M, N))
+        mu = _arr(mean, (M,))
+        r = _arr(rstd, (M,))
+        dx = np.empty_like(x)
+        dg = np.empty(N, np.float64)
+        db = np.empty(N, np.float64)
+        self._lib.oracle_layernorm_bwd(_p(x), _p(g), _p(d), _p(mu), _p(r), M, N, _p(dx), _p(dg),
+                                       _p(db), nthreads)
+        return dx, dg, db
+
 
 _default = None
 
@@ -155,3 +188,11 @@ def rmsnorm_bwd(x, gamma, dy, rstd, nthreads=0):
 
 def fused_add_rmsnorm_bwd(added, gamma, dy, rstd, dresidual_out=None, nthreads=0):
     return default().fused_add_rmsnorm_bwd(added, gamma, dy, rstd, dresidual_out, nthreads)
+
+
+def layernorm_fwd(x, gamma, beta, eps, nthreads=0):
+    return default().layernorm_fwd(x, gamma, beta, eps, nthreads)
+
+
+def layernorm_bwd(x, gamma, dy, mean, rstd, nthreads=0):
+    return default().layernorm_bwd(x, gamma, dy, mean, rstd, nthreads)

@@ -1,5 +1,6 @@
 /*
- * RMSNorm forward / backward oracle -- plain, slow, obviously correct CPU code.
+ * RMSNorm (and LayerNorm) forward / backward oracle -- plain, slow, obviously
+ * correct CPU code.
  *
  * TEST INFRASTRUCTURE ONLY. Nothing in the product path may link, load or
  * call this file: only the test suite, the smoke check and the benchmark's
@@ -21,8 +22,8 @@
  *           dresidual_out, dx == dresidual) and its squashed commit
  *           messages (rstd is fp32 of shape (M,), all reductions fp32).
  *
- * Layout: every [M,N] array is row-major contiguous; gamma, dweight are [N];
- * rstd is [M]. Nothing is blocked, fused or reordered beyond the definitions:
+ * Layout: every [M,N] array is row-major contiguous; gamma, beta, dweight,
+ * dgamma, dbeta are [N]; rstd and mean are [M]. Nothing is blocked, fused or reordered beyond the definitions:
  * each sum runs j = 0..N-1 (row sums) or m = 0..M-1 (column sums) in order.
  * OpenMP only splits independent rows (dx) or independent columns (dweight);
  * each column is still summed over m in ascending order, so results do not
@@ -204,4 +205,96 @@ void oracle_fused_add_rmsnorm_bwd(const double *added, const double *gamma, cons
                                   int64_t M, int64_t N, double *dx, double *dweight, int nthreads)
 {
     bwd_core(added, gamma, dy, rstd, dresidual_out, M, N, dx, dweight, nthreads);
+}
+
+/*
+ * LayerNorm forward. The pages leave LayerNorm's formulas to its textbook
+ * definition: its backward "mirrors" the RMSNorm one "adding mean handling +
+ * dbias", and its forward saves mean and rstd ([I769] "Proposed approach"
+ * item 6 and the plan's "PR 5 -- LayerNorm backward"; [I769] status notes on
+ * PR #801). Per row:
+ *   mean = (1/N) sum_j x_j
+ *   var  = (1/N) sum_j (x_j - mean)^2          (biased, divide by N)
+ *   rstd = 1/sqrt(var + eps)
+ *   y_j  = (x_j - mean) * rstd * gamma_j + beta_j    (beta may be NULL: no bias)
+ * mean[m] and rstd[m] receive the fp64 statistics.
+ */
+void oracle_layernorm_fwd(const double *x, const double *gamma, const double *beta, double eps,
+                          int64_t M, int64_t N, double *y, double *mean, double *rstd,
+                          int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        const double *xr = x + m * N;
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j) s += xr[j];
+        double mu = s / (double)N;
+        double v = 0.0;
+        for (int64_t j = 0; j < N; ++j) v += (xr[j] - mu) * (xr[j] - mu);
+        double var = v / (double)N;
+        double r = 1.0 / sqrt(var + eps);
+        mean[m] = mu;
+        rstd[m] = r;
+        for (int64_t j = 0; j < N; ++j) {
+            double yv = (xr[j] - mu) * r * gamma[j];
+            if (beta) yv += beta[j];
+            y[m * N + j] = yv;
+        }
+    }
+}
+
+/*
+ * LayerNorm backward, the gradient of the forward above with the saved mean
+ * and rstd taken as given. Per row, x_hat = (x - mean) * rstd, wdy = dy * gamma:
+ *   c1 = (1/N) sum_j x_hat_j * wdy_j
+ *   c2 = (1/N) sum_j wdy_j
+ *   dx_j = (wdy_j - c2 - x_hat_j * c1) * rstd
+ * and over all rows dgamma_j = sum_m dy_mj * x_hat_mj, dbeta_j = sum_m dy_mj.
+ */
+void oracle_layernorm_bwd(const double *x, const double *gamma, const double *dy,
+                          const double *mean, const double *rstd, int64_t M, int64_t N,
+                          double *dx, double *dgamma, double *dbeta, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        const double mu = mean[m], r = rstd[m];
+        double a1 = 0.0, a2 = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double x_hat = (x[m * N + j] - mu) * r;
+            double wdy = dy[m * N + j] * gamma[j];
+            a1 += x_hat * wdy;
+            a2 += wdy;
+        }
+        double c1 = a1 / (double)N;
+        double c2 = a2 / (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            double x_hat = (x[m * N + j] - mu) * r;
+            double wdy = dy[m * N + j] * gamma[j];
+            dx[m * N + j] = (wdy - c2 - x_hat * c1) * r;
+        }
+    }
+
+    for (int64_t j = 0; j < N; ++j) {
+        dgamma[j] = 0.0;
+        dbeta[j] = 0.0;
+    }
+#pragma omp parallel
+    {
+        int64_t t = 0, T = 1;
+#ifdef _OPENMP
+        t = omp_get_thread_num();
+        T = omp_get_num_threads();
+#endif
+        int64_t j0 = N * t / T, j1 = N * (t + 1) / T;
+        for (int64_t m = 0; m < M; ++m) {
+            const double mu = mean[m], r = rstd[m];
+            for (int64_t j = j0; j < j1; ++j) {
+                double x_hat = (x[m * N + j] - mu) * r;
+                dgamma[j] += dy[m * N + j] * x_hat;
+                dbeta[j] += dy[m * N + j];
+            }
+        }
+    }
 }

@@ -16,6 +16,12 @@ What each pin ties the oracle to:
   * hand_cases       -- tests/golden/rmsnorm_hand_cases.txt (worked on paper)
   * special cases    -- fused with residual = 0, dres = 0 is plain; exact
                         power-of-two scaling; row permutation
+  * ln_*             -- LayerNorm: torch fp64 layer_norm and its autograd,
+                        numpy mean/var, sympy's exact derivative, finite
+                        differences, the per-row invariants sum dx = 0 and
+                        sum x_hat*dx = N*eps*c1*rstd^3, zero-mean rows reducing
+                        to RMSNorm, shift invariance, and
+                        tests/golden/layernorm_hand_cases.txt
 """
 import os
 from fractions import Fraction
@@ -368,6 +374,213 @@ def hand_cases(orc):
         assert np.allclose(dw, c["dweight"], rtol=1e-15, atol=1e-15), c["name"]
 
 
+# ----------------------------------------------------------------- LayerNorm
+LN_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                         "layernorm_hand_cases.txt")
+
+
+def ln_fwd_vs_torch(orc):
+    """torch.nn.functional.layer_norm in fp64 (with and without bias); mean and
+    rstd against numpy's mean and (biased) variance."""
+    rng = np.random.default_rng(21)
+    for (M, N, eps) in ((7, 33, 1e-5), (3, 1000, 1e-6), (2, 1, 1e-2)):
+        x = rng.standard_normal((M, N)) * 3 + 1.5
+        g = 1 + 0.1 * rng.standard_normal(N)
+        b = 0.1 * rng.standard_normal(N)
+        for beta in (b, None):
+            y, mean, rstd = orc.layernorm_fwd(x, g, beta, eps)
+            ref = torch.nn.functional.layer_norm(
+                torch.from_numpy(x), (N,), torch.from_numpy(g),
+                torch.from_numpy(beta) if beta is not None else None, eps).numpy()
+            assert _rel(y, ref) < 1e-13, (M, N, beta is None)
+        assert _rel(mean, np.mean(x, axis=1)) < 1e-14
+        assert _rel(rstd, 1 / np.sqrt(np.var(x, axis=1) + eps)) < 1e-13
+
+
+def _ln_sym_grads(M, N, x, g, b, dy, eps):
+    """Exact gradients of L = sum(y*dy) with y from the LayerNorm definition (sympy)."""
+    import sympy as sp
+    X = sp.Matrix(M, N, lambda i, j: sp.Symbol("x_%d_%d" % (i, j)))
+    G = [sp.Symbol("g_%d" % j) for j in range(N)]
+    B = [sp.Symbol("b_%d" % j) for j in range(N)]
+    L = 0
+    for i in range(M):
+        mu = sum(X[i, j] for j in range(N)) / N
+        var = sum((X[i, j] - mu) ** 2 for j in range(N)) / N
+        rs = (var + eps) ** sp.Rational(-1, 2)
+        for j in range(N):
+            L += ((X[i, j] - mu) * rs * G[j] + B[j]) * dy[i][j]
+    subs = {X[i, j]: x[i][j] for i in range(M) for j in range(N)}
+    subs.update({G[j]: g[j] for j in range(N)})
+    subs.update({B[j]: b[j] for j in range(N)})
+    ev = lambda e: float(e.subs(subs).evalf(30))
+    dX = np.array([[ev(sp.diff(L, X[i, j])) for j in range(N)] for i in range(M)])
+    dG = np.array([ev(sp.diff(L, G[j])) for j in range(N)])
+    dB = np.array([ev(sp.diff(L, B[j])) for j in range(N)])
+    return dX, dG, dB
+
+
+def ln_bwd_symbolic(orc):
+    import sympy as sp
+    Q = sp.Rational
+    M, N = 2, 3
+    x = [[Q(1, 2), Q(-3, 4), Q(2)], [Q(5, 4), Q(1, 8), Q(-1)]]
+    g = [Q(9, 10), Q(11, 10), Q(5, 4)]
+    b = [Q(1, 10), Q(-1, 5), Q(0)]
+    dy = [[Q(1), Q(-2), Q(1, 2)], [Q(3, 4), Q(1, 4), Q(-1)]]
+    eps = Q(1, 100)
+    dX, dG, dB = _ln_sym_grads(M, N, x, g, b, dy, eps)
+    f = lambda a: np.array(a, dtype=np.float64)
+    mean = np.array([float(sum(row) / N) for row in x])
+    rstd = np.array([float((sum((v - sum(row) / N) ** 2 for v in row) / N + eps) ** Q(-1, 2))
+                     for row in x])
+    dx, dg, db = orc.layernorm_bwd(f(x), f(g), f(dy), mean, rstd)
+    assert _rel(dx, dX) < 1e-13 and _rel(dg, dG) < 1e-13 and _rel(db, dB) < 1e-13, (dx, dX)
+
+
+def _ln_loss(orc, x, g, b, dy, eps):
+    y, _, _ = orc.layernorm_fwd(x, g, b, eps)
+    return float(np.sum(y * dy))
+
+
+def ln_bwd_fd(orc):
+    rng = np.random.default_rng(22)
+    for (M, N, eps) in ((3, 16, 1e-5), (2, 5, 1e-2)):
+        x = rng.standard_normal((M, N)) + 0.7
+        g = 1 + 0.1 * rng.standard_normal(N)
+        b = 0.1 * rng.standard_normal(N)
+        dy = rng.standard_normal((M, N))
+        _, mean, rstd = orc.layernorm_fwd(x, g, b, eps)
+        dx, dg, db = orc.layernorm_bwd(x, g, dy, mean, rstd)
+        h = 1e-6
+
+        def fd(arr, setter):
+            out = np.zeros(arr.shape)
+            for idx in np.ndindex(arr.shape):
+                ap, am = arr.copy(), arr.copy()
+                ap[idx] += h
+                am[idx] -= h
+                out[idx] = (setter(ap) - setter(am)) / (2 * h)
+            return out
+        fdx = fd(x, lambda v: _ln_loss(orc, v, g, b, dy, eps))
+        fdg = fd(g, lambda v: _ln_loss(orc, x, v, b, dy, eps))
+        fdb = fd(b, lambda v: _ln_loss(orc, x, g, v, dy, eps))
+        assert _rel(dx, fdx) < 1e-6 and _rel(dg, fdg) < 1e-6 and _rel(db, fdb) < 1e-6
+
+
+def ln_bwd_torch_autograd(orc):
+    rng = np.random.default_rng(23)
+    M, N, eps = 16, 300, 1e-5
+    x = rng.standard_normal((M, N)) * 2 - 0.5
+    g = 1 + 0.1 * rng.standard_normal(N)
+    b = 0.1 * rng.standard_normal(N)
+    dy = rng.standard_normal((M, N))
+    xt = torch.from_numpy(x).requires_grad_(True)
+    gt = torch.from_numpy(g).requires_grad_(True)
+    bt = torch.from_numpy(b).requires_grad_(True)
+    torch.nn.functional.layer_norm(xt, (N,), gt, bt, eps).backward(torch.from_numpy(dy))
+    _, mean, rstd = orc.layernorm_fwd(x, g, b, eps)
+    dx, dg, db = orc.layernorm_bwd(x, g, dy, mean, rstd)
+    assert _rel(dx, xt.grad.numpy()) < 1e-12
+    assert _rel(dg, gt.grad.numpy()) < 1e-12 and _rel(db, bt.grad.numpy()) < 1e-12
+
+
+def ln_bwd_invariants(orc):
+    """Per row, with the exact statistics: sum_j dx_j = 0 (sum_j x_hat_j = 0),
+    and sum_j x_hat_j*dx_j = N*eps*c1*rstd^3 (derivation: rstd*(N*c1 - c2*0 -
+    c1*N*var*rstd^2) with 1 - var*rstd^2 = eps*rstd^2). dbeta is the column
+    sum of dy."""
+    rng = np.random.default_rng(24)
+    M, N = 6, 50
+    x = rng.standard_normal((M, N)) + 2.0
+    g = 1 + 0.1 * rng.standard_normal(N)
+    dy = rng.standard_normal((M, N))
+    for eps in (1e-1, 1e-3, 0.0):
+        _, mean, rstd = orc.layernorm_fwd(x, g, None, eps)
+        dx, _, db = orc.layernorm_bwd(x, g, dy, mean, rstd)
+        scale = np.sum(np.abs(dx), axis=1)
+        assert np.all(np.abs(np.sum(dx, axis=1)) <= 1e-13 * scale)
+        xh = (x - mean[:, None]) * rstd[:, None]
+        c1 = np.mean(xh * dy * g, axis=1)
+        lhs = np.sum(xh * dx, axis=1)
+        rhs = N * eps * c1 * rstd ** 3
+        assert np.all(np.abs(lhs - rhs) <= 1e-13 * np.sum(np.abs(xh * dx), axis=1)), (eps,)
+        assert _rel(db, np.sum(dy, axis=0)) < 1e-14
+
+
+def ln_reduces_to_rms(orc):
+    """Rows with an exactly zero mean and no bias: LayerNorm is RMSNorm."""
+    rng = np.random.default_rng(25)
+    M, N, eps = 4, 32, 1e-6
+    half = rng.standard_normal((M, N // 2))
+    x = np.empty((M, N))
+    x[:, 0::2], x[:, 1::2] = half, -half           # a, -a, b, -b, ...: row sums are exactly 0
+    g = 1 + 0.1 * rng.standard_normal(N)
+    dy = rng.standard_normal((M, N))
+    y, mean, rstd = orc.layernorm_fwd(x, g, None, eps)
+    assert np.all(mean == 0.0)
+    y2, rstd2 = orc.rmsnorm_fwd(x, g, eps)
+    assert _rel(y, y2) < 1e-15 and _rel(rstd, rstd2) < 1e-15
+    dx, dg, _ = orc.layernorm_bwd(x, g, dy, mean, rstd)
+    dx2, dg2 = orc.rmsnorm_bwd(x, g, dy, rstd)
+    # the LayerNorm dx has the extra -c2*rstd term; on zero-mean rows it is the
+    # projection of the RMSNorm dx onto zero-sum vectors
+    c2 = np.mean(dy * g, axis=1)
+    assert _rel(dx, dx2 - (c2 * rstd)[:, None]) < 1e-13 and _rel(dg, dg2) < 1e-14
+
+
+def ln_shift_invariance(orc):
+    """Adding a constant to a row moves its mean and leaves y and dx unchanged."""
+    rng = np.random.default_rng(26)
+    M, N, eps = 5, 24, 1e-5
+    x = rng.standard_normal((M, N))
+    g = 1 + 0.1 * rng.standard_normal(N)
+    b = 0.1 * rng.standard_normal(N)
+    dy = rng.standard_normal((M, N))
+    shift = np.array([0.0, 1.0, -4.0, 8.0, 0.5])[:, None]
+    y, mean, rstd = orc.layernorm_fwd(x, g, b, eps)
+    y2, mean2, rstd2 = orc.layernorm_fwd(x + shift, g, b, eps)
+    assert _rel(y2, y) < 1e-13 and _rel(mean2, mean + shift[:, 0]) < 1e-14
+    dx, dg, db = orc.layernorm_bwd(x, g, dy, mean, rstd)
+    dxs, dgs, dbs = orc.layernorm_bwd(x + shift, g, dy, mean2, rstd2)
+    assert _rel(dxs, dx) < 1e-12 and _rel(dgs, dg) < 1e-12 and np.array_equal(dbs, db)
+
+
+def _parse_cases(path):
+    cases, cur = [], None
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "case":
+                cur = {"name": vals[0]}
+            elif key == "end":
+                cases.append(cur)
+                cur = None
+            elif key == "kind":
+                cur[key] = vals[0]
+            else:
+                cur[key] = np.array([float(Fraction(v)) for v in vals])
+    return cases
+
+
+def ln_hand_cases(orc):
+    for c in _parse_cases(LN_GOLDEN):
+        M, N = int(c["M"][0]), int(c["N"][0])
+        eps = float(c["eps"][0])
+        sh = lambda k: c[k].reshape(M, N)
+        y, mean, rstd = orc.layernorm_fwd(sh("x"), c["gamma"], c["beta"], eps)
+        assert np.allclose(mean, c["mean"], rtol=1e-15, atol=0), c["name"]
+        assert np.allclose(rstd, c["rstd"], rtol=1e-15, atol=0), c["name"]
+        assert np.allclose(y, sh("y"), rtol=1e-15, atol=1e-15), c["name"]
+        dx, dg, db = orc.layernorm_bwd(sh("x"), c["gamma"], sh("dy"), c["mean"], c["rstd"])
+        assert np.allclose(dx, sh("dx"), rtol=1e-15, atol=1e-15), c["name"]
+        assert np.allclose(dg, c["dgamma"], rtol=1e-15, atol=1e-15), c["name"]
+        assert np.allclose(db, c["dbeta"], rtol=1e-15, atol=1e-15), c["name"]
+
+
 PINS = [
     round_vs_torch_casts,
     round_direct_from_double,
@@ -382,4 +595,12 @@ PINS = [
     fused_reduces_to_plain,
     scaling_and_permutation,
     hand_cases,
+    ln_fwd_vs_torch,
+    ln_bwd_symbolic,
+    ln_bwd_fd,
+    ln_bwd_torch_autograd,
+    ln_bwd_invariants,
+    ln_reduces_to_rms,
+    ln_shift_invariance,
+    ln_hand_cases,
 ]

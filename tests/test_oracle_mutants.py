@@ -46,6 +46,31 @@ MUTANTS = [
     ("round_bf16_precision", "return round_format(v, 8, -126,", "return round_format(v, 9, -126,",
      None),
     ("round_no_overflow", "if (fabs(r) > maxf) return v > 0 ? INFINITY : -INFINITY;", "", None),
+    # LayerNorm
+    ("ln_mean_divisor", "double mu = s / (double)N;", "double mu = s / (double)(N - 1);", None),
+    ("ln_var_unbiased", "double var = v / (double)N;", "double var = v / (double)(N - 1);", None),
+    ("ln_var_uncentred", "v += (xr[j] - mu) * (xr[j] - mu);", "v += xr[j] * xr[j];", None),
+    ("ln_fwd_uncentred", "double yv = (xr[j] - mu) * r * gamma[j];",
+     "double yv = xr[j] * r * gamma[j];", None),
+    ("ln_fwd_beta_dropped", "if (beta) yv += beta[j];", "", None),
+    ("ln_drop_c2", "dx[m * N + j] = (wdy - c2 - x_hat * c1) * r;",
+     "dx[m * N + j] = (wdy - x_hat * c1) * r;", None),
+    ("ln_c2_sign", "dx[m * N + j] = (wdy - c2 - x_hat * c1) * r;",
+     "dx[m * N + j] = (wdy + c2 - x_hat * c1) * r;", None),
+    ("ln_drop_c1", "dx[m * N + j] = (wdy - c2 - x_hat * c1) * r;",
+     "dx[m * N + j] = (wdy - c2) * r;", None),
+    ("ln_c2_divisor", "double c2 = a2 / (double)N;", "double c2 = a2 / (double)(N + 1);", None),
+    ("ln_c1_uncentred", "double x_hat = (x[m * N + j] - mu) * r;",
+     "double x_hat = x[m * N + j] * r;", 0),
+    ("ln_dx_uncentred", "double x_hat = (x[m * N + j] - mu) * r;",
+     "double x_hat = x[m * N + j] * r;", 1),
+    ("ln_dgamma_uncentred", "double x_hat = (x[m * N + j] - mu) * r;",
+     "double x_hat = x[m * N + j] * r;", 2),
+    ("ln_dgamma_extra_gamma", "dgamma[j] += dy[m * N + j] * x_hat;",
+     "dgamma[j] += dy[m * N + j] * x_hat * gamma[j];", None),
+    ("ln_dbeta_times_xhat", "dbeta[j] += dy[m * N + j];", "dbeta[j] += dy[m * N + j] * x_hat;",
+     None),
+    ("ln_c2_ungamma", "a2 += wdy;", "a2 += dy[m * N + j];", None),
 ]
 
 
