@@ -1,5 +1,6 @@
 /*
- * rmsnorm_gb300.h -- C ABI of the GB300 (sm_103a) RMSNorm library.
+ * rmsnorm_gb300.h -- C ABI of the GB300 (sm_103a) RMSNorm library (with
+ * LayerNorm alongside).
  *
  * What it computes (FlyDSL pages):
  *   forward, per row m of an [M,N] input:
@@ -135,6 +136,65 @@ rn_status rn_fused_add_rmsnorm_bwd(const void *added, const void *gamma, const v
                                    float *dweight_f32, void *dweight,
                                    void *workspace, size_t workspace_bytes,
                                    int64_t M, int64_t N, int dtype, void *stream);
+
+/*
+ * LayerNorm. The FlyDSL pages plan its backward as the RMSNorm backward with
+ * mean handling and a bias gradient added, over a forward that saves the
+ * per-row mean and rstd (issue #769, plan item 6 "layernorm backward -- same
+ * pattern" and "PR 5 -- LayerNorm backward": "adding mean handling + dbias").
+ * The formulas are the textbook definition:
+ *   forward, per row:  mean = (1/N) sum_j x_j,  var = (1/N) sum_j (x_j - mean)^2,
+ *                      rstd = 1/sqrt(var + eps),
+ *                      y_j = (x_j - mean) * rstd * gamma_j + beta_j
+ *   backward, per row with x_hat = (x - mean)*rstd and wdy = dy*gamma:
+ *                      c1 = mean_j(x_hat_j*wdy_j),  c2 = mean_j(wdy_j),
+ *                      dx_j = (wdy_j - c2 - x_hat_j*c1) * rstd
+ *   over all rows:     dgamma_j = sum_m dy_mj*x_hat_mj,  dbeta_j = sum_m dy_mj
+ * The conventions above apply (one I/O dtype; device pointers; fp32 math).
+ */
+
+/*
+ * Forward, LayerNorm.
+ *   x      [M,N] dtype, in
+ *   gamma  [N] dtype, in
+ *   beta   [N] dtype, in, may be NULL (no bias)
+ *   eps    added to the variance before the reciprocal square root
+ *   y      [M,N] dtype, out
+ *   mean   [M] fp32, out, may be NULL (then not stored)
+ *   rstd   [M] fp32, out, may be NULL (then not stored)
+ */
+rn_status rn_layernorm_fwd(const void *x, const void *gamma, const void *beta, float eps, void *y,
+                           float *mean, float *rstd, int64_t M, int64_t N, int dtype,
+                           void *stream);
+
+/*
+ * Bytes of workspace rn_layernorm_bwd needs on the current device: a 256-byte
+ * header plus up to two fp32 rows of 2N per SM (per-CTA partials of dgamma
+ * and dbeta side by side). Same rules as rn_bwd_workspace_bytes.
+ */
+rn_status rn_layernorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes);
+
+/*
+ * Backward, LayerNorm.
+ *   x           [M,N] dtype, in (the forward's input)
+ *   gamma       [N] dtype, in
+ *   dy          [M,N] dtype, in (gradient of y)
+ *   mean, rstd  [M] fp32, in: the statistics the forward saved (not recomputed)
+ *   dx          [M,N] dtype, out; must not overlap any input
+ *   dgamma_f32  [N] fp32, out: fully overwritten with sum_m dy*x_hat
+ *   dbeta_f32   [N] fp32, out, may be NULL (no bias): sum_m dy; must not
+ *               overlap dgamma_f32
+ *   dgamma      [N] dtype, out, may be NULL: dgamma_f32 rounded to dtype
+ *   dbeta       [N] dtype, out, may be NULL: dbeta_f32 rounded to dtype
+ *               (needs dbeta_f32)
+ *   workspace   >= rn_layernorm_bwd_workspace_bytes(M,N,dtype) bytes
+ * Every step (zero, row pass, cross-row reduction, casts) runs inside this
+ * call; RN_OPT_* options apply as for the RMSNorm backward.
+ */
+rn_status rn_layernorm_bwd(const void *x, const void *gamma, const void *dy, const float *mean,
+                           const float *rstd, void *dx, float *dgamma_f32, float *dbeta_f32,
+                           void *dgamma, void *dbeta, void *workspace, size_t workspace_bytes,
+                           int64_t M, int64_t N, int dtype, void *stream);
 
 /*
  * Backward, plain RMSNorm, without a caller workspace. (This call has no

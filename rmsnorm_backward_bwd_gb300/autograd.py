@@ -1,5 +1,6 @@
 """Autograd wrappers over the backward calls: ``rmsnorm`` and
-``fused_add_rmsnorm`` as differentiable functions of (x, [residual], weight).
+``fused_add_rmsnorm`` as differentiable functions of (x, [residual], weight),
+and ``layernorm`` of (x, weight, [bias]).
 
 FlyDSL PR #800 ("Add fused-add / residual backward"), section "Summary" and
 its PR 1 notes: the forward saves the per-row fp32 rstd; ``RMSNormFunction``
@@ -14,7 +15,10 @@ approach" item 3: gradients flow through these wrappers transparently.
 
 Marshalling only: inputs are flattened to [M, N] (a view when the input is
 contiguous), gradients are made contiguous, and everything is computed by
-the CUDA library. CUDA tensors only; weight has the input's dtype.
+the CUDA library. CUDA tensors only; weight (and bias) have the input's
+dtype. ``LayerNormFunction`` follows the same pattern with the forward's mean
+and rstd saved (issue #769 plan, "PR 5 -- LayerNorm backward"); its default
+eps is torch's LayerNorm default, 1e-5 (the pages give none for it).
 """
 import torch
 
@@ -94,6 +98,35 @@ class FusedAddRMSNormFunction(torch.autograd.Function):
                 dweight if need_w else None, None)
 
 
+class LayerNormFunction(torch.autograd.Function):
+    """y = (x - mean) * rstd * weight + bias over the last dim (bias may be None)."""
+
+    @staticmethod
+    def forward(ctx, x, weight, bias, eps):
+        shape = x.shape
+        x2 = _rows2d(x, _width(x))
+        y, mean, rstd = ops.layernorm_fwd(x2, weight.contiguous(),
+                                          bias.contiguous() if bias is not None else None, eps)
+        ctx.save_for_backward(x2, weight, mean, rstd)
+        ctx.shape = shape
+        ctx.has_bias = bias is not None
+        return y.view(shape)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x2, weight, mean, rstd = ctx.saved_tensors
+        need_x, need_w, need_b = ctx.needs_input_grad[:3]
+        need_b = need_b and ctx.has_bias
+        if not (need_x or need_w or need_b):
+            return None, None, None, None
+        dy2 = _rows2d(dy, x2.shape[1])
+        dx, dgamma, dbeta, _, _ = ops.layernorm_bwd(
+            x2, weight.contiguous(), dy2, mean, rstd, want_dbeta=need_b,
+            want_cast=need_w or need_b)
+        return (dx.view(ctx.shape) if need_x else None, dgamma if need_w else None,
+                dbeta if need_b else None, None)
+
+
 def rmsnorm(x, weight, eps=1e-6):
     """Differentiable RMSNorm over the last dimension of x (any rank >= 1)."""
     return RMSNormFunction.apply(x, weight, eps)
@@ -104,3 +137,9 @@ def fused_add_rmsnorm(x, residual, weight, eps=1e-6, prenorm=True):
     returns (out, residual_out); otherwise out alone."""
     out, residual_out = FusedAddRMSNormFunction.apply(x, residual, weight, eps)
     return (out, residual_out) if prenorm else out
+
+
+def layernorm(x, weight, bias=None, eps=1e-5):
+    """Differentiable LayerNorm over the last dimension of x (any rank >= 1);
+    bias may be None."""
+    return LayerNormFunction.apply(x, weight, bias, eps)

@@ -113,44 +113,46 @@ static size_t ws_bytes_for(const DeviceInfo &d, int64_t N) {
 }
 
 // ------------------------------------------------------------- planning
-static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
-    const int eb = elem_bytes(p.dtype);
-    const int row_bytes = p.N * eb;
-    if (row_bytes % 16) return false;
-    if (!aligned16(p.x) || !aligned16(p.dy) || !aligned16(p.gamma) || !aligned16(p.dx) ||
-        (p.dres && !aligned16(p.dres)))
-        return false;
-    const int nchunks = row_bytes / 16;
+// Tile of the persistent row engine for rows of `nchunks` 16-byte chunks and
+// `nt` streamed tensors; `red_bytes` of shared memory precede the ring and
+// `max_cpt` caps the default chunks per thread.
+static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int max_cpt,
+                          int (*max_threads)(int cpt), const DeviceInfo &d, RowPlan *plan) {
     if (nchunks > kRowMaxChunks) return false;
-    const int nt = p.dres ? 3 : 2;
 
     // Tile (measured on GB300): 4 chunks per thread for rows of 512+ chunks
     // (bf16 N >= 4096), else 2, else 1 for very short rows.
     int cpt = g_opts[RN_OPT_CHUNKS_PER_THREAD];
-    if (cpt != 1 && cpt != 2 && cpt != 4) cpt = nchunks >= 512 ? 4 : (nchunks >= 64 ? 2 : 1);
+    if (cpt != 1 && cpt != 2 && cpt != 4) {
+        cpt = nchunks >= 512 ? 4 : (nchunks >= 64 ? 2 : 1);
+        while (cpt > max_cpt) cpt /= 2;
+    }
     int team = ((nchunks + cpt - 1) / cpt + 31) / 32 * 32;
-    if (team > row_max_threads(cpt)) return false;
+    if (team > max_threads(cpt)) return false;
 
     const size_t budget = (d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024);
     const int tc = cpt * team;  // 16-byte chunks per tensor row in a team's slot
     const size_t stage = (size_t)nt * tc * 16;
+    auto smem_for = [&](int teams_, int stages_) {
+        return red_bytes + (size_t)teams_ * stages_ * stage;
+    };
     int teams = g_opts[RN_OPT_TEAMS_PER_CTA];
     if (teams <= 0) {
-        teams = row_max_threads(cpt) / team;
+        teams = max_threads(cpt) / team;
         if (teams > 15) teams = 15;
         // room for at least 2 slots per team
-        while (teams > 1 && row_smem_bytes(teams, 2, nt, tc) > budget) --teams;
+        while (teams > 1 && smem_for(teams, 2) > budget) --teams;
         // no more teams than rows per SM
-        int64_t rows_per_sm = (p.M + d.num_sms - 1) / d.num_sms;
+        int64_t rows_per_sm = (M + d.num_sms - 1) / d.num_sms;
         if (rows_per_sm < 1) rows_per_sm = 1;
         if (teams > rows_per_sm) teams = (int)rows_per_sm;
     }
-    if (teams < 1 || teams > 15 || teams * team > row_max_threads(cpt)) return false;
+    if (teams < 1 || teams > 15 || teams * team > max_threads(cpt)) return false;
 
     // one CTA per SM unless the grid option asks for another count
     int64_t cap = g_opts[RN_OPT_GRID] > 0 ? g_opts[RN_OPT_GRID] : d.num_sms;
     if (cap > max_partial_rows(d)) cap = max_partial_rows(d);
-    int64_t grid = (p.M + teams - 1) / teams;
+    int64_t grid = (M + teams - 1) / teams;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
 
@@ -159,14 +161,14 @@ static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
     // its SM gets one row more.
     int stages = g_opts[RN_OPT_STAGES];
     if (stages <= 0) {
-        stages = (int)((budget - 256) / (stage * teams));
+        stages = (int)((budget - red_bytes) / (stage * teams));
         const int want = teams >= 2 ? 2 : 3;
         if (stages > want) stages = want;
-        const int64_t rows_per_team = (p.M + grid * teams - 1) / (grid * teams);
+        const int64_t rows_per_team = (M + grid * teams - 1) / (grid * teams);
         if (stages > rows_per_team) stages = (int)(rows_per_team < 1 ? 1 : rows_per_team);
     }
     if (stages < 1 || stages > 8) return false;
-    const size_t smem = row_smem_bytes(teams, stages, nt, tc);
+    const size_t smem = smem_for(teams, stages);
     if (smem > d.smem_optin) return false;
 
     plan->cpt = cpt;
@@ -177,6 +179,18 @@ static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
     plan->smem = smem;
     plan->atomic = false;
     return true;
+}
+
+static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
+    const int row_bytes = p.N * elem_bytes(p.dtype);
+    if (row_bytes % 16) return false;
+    if (!aligned16(p.x) || !aligned16(p.dy) || !aligned16(p.gamma) || !aligned16(p.dx) ||
+        (p.dres && !aligned16(p.dres)))
+        return false;
+    const int nt = p.dres ? 3 : 2;
+    // the kernel's reduction slots precede its ring: row_smem_bytes with no ring
+    return plan_row_tile(p.M, row_bytes / 16, nt, row_smem_bytes(0, 0, nt, 0), 4,
+                         row_max_threads, d, plan);
 }
 
 static void plan_generic(const BwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
@@ -282,6 +296,114 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
     return RN_OK;
 }
 
+// ------------------------------------------------------------- LayerNorm
+static size_t ln_ws_bytes_for(const DeviceInfo &d, int64_t N) {
+    return kWsHeaderBytes + (size_t)max_partial_rows(d) * (size_t)N * 8;
+}
+
+static bool plan_ln_row(const LnBwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
+    const int row_bytes = p.N * elem_bytes(p.dtype);
+    if (row_bytes % 16) return false;
+    if (!aligned16(p.x) || !aligned16(p.dy) || !aligned16(p.gamma) || !aligned16(p.dx))
+        return false;
+    return plan_row_tile(p.M, row_bytes / 16, 2, ln_row_smem_bytes(0, 0, 0), kLnMaxCpt,
+                         ln_row_max_threads, d, plan);
+}
+
+static void plan_ln_generic(const LnBwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
+    plan->threads = p.N >= 4096 ? 512 : 256;
+    const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
+    plan->smem_dw = ln_generic_smem_bytes(p.N, true) <= budget;
+    plan->smem = ln_generic_smem_bytes(p.N, plan->smem_dw);
+    int64_t grid = p.M;
+    if (grid > max_partial_rows(d)) grid = max_partial_rows(d);
+    if (g_opts[RN_OPT_GRID] > 0 && grid > g_opts[RN_OPT_GRID]) grid = g_opts[RN_OPT_GRID];
+    if (grid < 1) grid = 1;
+    plan->grid = (int)grid;
+    plan->atomic = false;
+}
+
+static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t s) {
+    DeviceInfo d;
+    int dev = 0;
+    cudaError_t e = device_info(&d, &dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    if (p.ws == nullptr) return fail(RN_ERR_WORKSPACE, "workspace is NULL");
+    if (((uintptr_t)p.ws & 255u) != 0) return fail(RN_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    const size_t need = ln_ws_bytes_for(d, p.N);
+    if (ws_bytes < need)
+        return fail(RN_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+    const float *partials = reinterpret_cast<const float *>(p.ws + kWsHeaderBytes);
+
+    if (p.M == 0) {
+        e = launch_finalize2(nullptr, 0, 2 * p.N, p.N, p.dg_f32, p.dg_cast, p.db_f32, p.db_cast,
+                             p.dtype, s, false);
+        snprintf(g_plan, sizeof(g_plan), "empty batch: finalize only");
+        return e == cudaSuccess ? RN_OK : cuda_fail(e, "finalize launch");
+    }
+
+    const int engine = g_opts[RN_OPT_BWD_ENGINE];
+    RowPlan rp;
+    GenericPlan gp;
+    bool use_row = false;
+    if (engine != 2) {
+        use_row = plan_ln_row(p, d, &rp);
+        if (!use_row && engine == 1)
+            return fail(RN_ERR_UNSUPPORTED, "row engine cannot take N=%d dtype=%d here", p.N,
+                        p.dtype);
+    }
+    if (!use_row) plan_ln_generic(p, d, &gp);
+    bool atomic = g_opts[RN_OPT_DWEIGHT_MODE] != 1 && aligned16(p.dg_f32) &&
+                  (p.db_f32 == nullptr || aligned16(p.db_f32));
+    if (!use_row && atomic && ln_generic_smem_bytes(p.N, true) > d.smem_optin) {
+        // the generic engine keeps its atomic-mode partials in shared memory
+        if (g_opts[RN_OPT_DWEIGHT_MODE] == 2)
+            return fail(RN_ERR_UNSUPPORTED, "atomic mode needs N*8 bytes of shared memory");
+        atomic = false;
+    }
+    rp.atomic = gp.atomic = atomic;
+    if (!use_row && atomic) {
+        gp.smem_dw = true;
+        gp.smem = ln_generic_smem_bytes(p.N, true);
+    }
+    const int G = use_row ? rp.grid : gp.grid;
+    if (use_row)
+        snprintf(g_plan, sizeof(g_plan),
+                 "engine=ln_row cpt=%d team_threads=%d teams=%d stages=%d grid=%d smem=%zu dw=%s",
+                 rp.cpt, rp.team_threads, rp.teams, rp.stages, rp.grid, rp.smem,
+                 atomic ? "atomic" : "scratch");
+    else
+        snprintf(g_plan, sizeof(g_plan), "engine=ln_generic threads=%d grid=%d smem_dw=%d dw=%s",
+                 gp.threads, gp.grid, (int)gp.smem_dw, atomic ? "atomic" : "scratch");
+
+    if (atomic) {
+        e = launch_zero_f32(p.dg_f32, p.N, s, p.db_f32);
+        if (e != cudaSuccess) return cuda_fail(e, "zero launch");
+    }
+    const bool prof = g_ev_begin && g_ev_end;
+    if (prof) {
+        e = cudaEventRecord(g_ev_begin, s);
+        if (e != cudaSuccess) return cuda_fail(e, "profile event");
+    }
+    e = use_row ? launch_ln_bwd_row(p, rp, s, atomic) : launch_ln_bwd_generic(p, gp, s, atomic);
+    if (e != cudaSuccess) return cuda_fail(e, "row pass launch");
+    if (prof) {
+        e = cudaEventRecord(g_ev_end, s);
+        if (e != cudaSuccess) return cuda_fail(e, "profile event");
+    }
+    if (atomic) {
+        if (p.dg_cast || p.db_cast) {
+            e = launch_cast(p.dg_f32, p.dg_cast, p.N, p.dtype, s, !prof, p.db_f32, p.db_cast);
+            if (e != cudaSuccess) return cuda_fail(e, "cast launch");
+        }
+    } else {
+        e = launch_finalize2(partials, G, 2 * p.N, p.N, p.dg_f32, p.dg_cast, p.db_f32, p.db_cast,
+                             p.dtype, s, !prof);
+        if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+    }
+    return RN_OK;
+}
+
 static rn_status check_common(int64_t M, int64_t N, int dtype) {
     if (dtype < RN_F32 || dtype > RN_BF16) return fail(RN_ERR_INVALID_ARG, "bad dtype code %d", dtype);
     if (M < 0) return fail(RN_ERR_INVALID_ARG, "M must be >= 0 (got %lld)", (long long)M);
@@ -350,6 +472,70 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
                (!fused || (aligned16(residual) && aligned16(residual_out)));
     e = launch_fwd(p, vec, d.num_sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
+}
+
+static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta, float eps,
+                              void *y, float *mean, float *rstd, int64_t M, int64_t N, int dtype,
+                              void *stream) {
+    g_err[0] = 0;
+    rn_status st = check_common(M, N, dtype);
+    if (st != RN_OK) return st;
+    if (!(eps >= 0.f)) return fail(RN_ERR_INVALID_ARG, "eps must be >= 0");
+    if (!gamma) return fail(RN_ERR_INVALID_ARG, "gamma is required");
+    if (M > 0 && (!x || !y)) return fail(RN_ERR_INVALID_ARG, "input and output are required");
+    if (M == 0) return RN_OK;
+    DeviceInfo d;
+    cudaError_t e = device_info(&d, nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    LnFwdProblem p;
+    p.x = x;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.y = y;
+    p.mean = mean;
+    p.rstd = rstd;
+    p.eps = eps;
+    p.M = M;
+    p.N = (int)N;
+    p.dtype = dtype;
+    const int eb = elem_bytes(dtype);
+    const bool vec = ((N * eb) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y) &&
+                     (!beta || aligned16(beta));
+    e = launch_ln_fwd(p, vec, d.num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
+}
+
+static rn_status ln_bwd_entry(const void *x, const void *gamma, const void *dy, const float *mean,
+                              const float *rstd, void *dx, float *dg_f32, float *db_f32,
+                              void *dg_cast, void *db_cast, void *ws, size_t ws_bytes, int64_t M,
+                              int64_t N, int dtype, void *stream) {
+    g_err[0] = 0;
+    g_plan[0] = 0;
+    rn_status st = check_common(M, N, dtype);
+    if (st != RN_OK) return st;
+    if (!gamma || !dg_f32) return fail(RN_ERR_INVALID_ARG, "gamma and dgamma_f32 are required");
+    if (db_cast && !db_f32) return fail(RN_ERR_INVALID_ARG, "dbeta needs dbeta_f32");
+    if (db_f32 == dg_f32) return fail(RN_ERR_INVALID_ARG, "dbeta_f32 must not alias dgamma_f32");
+    if (M > 0 && (!x || !dy || !mean || !rstd || !dx))
+        return fail(RN_ERR_INVALID_ARG, "x, dy, mean, rstd and dx are required when M > 0");
+    if (M > 0 && (dx == x || dx == dy || (void *)dx == (void *)mean || (void *)dx == (void *)rstd))
+        return fail(RN_ERR_INVALID_ARG, "dx must not alias x, dy, mean or rstd");
+    LnBwdProblem p;
+    p.x = x;
+    p.gamma = gamma;
+    p.dy = dy;
+    p.mean = mean;
+    p.rstd = rstd;
+    p.dx = dx;
+    p.dg_f32 = dg_f32;
+    p.db_f32 = db_f32;
+    p.dg_cast = dg_cast;
+    p.db_cast = db_cast;
+    p.ws = static_cast<uint8_t *>(ws);
+    p.M = M;
+    p.N = (int)N;
+    p.dtype = dtype;
+    return run_ln_bwd(p, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace rn
@@ -430,6 +616,32 @@ rn_status rn_fused_add_rmsnorm_bwd(const void *added, const void *gamma, const v
                                    void *stream) {
     return bwd_entry(added, gamma, dy, rstd, dresidual_out, dx, dweight_f32, dweight, workspace,
                      workspace_bytes, M, N, dtype, stream);
+}
+
+rn_status rn_layernorm_fwd(const void *x, const void *gamma, const void *beta, float eps, void *y,
+                           float *mean, float *rstd, int64_t M, int64_t N, int dtype,
+                           void *stream) {
+    return ln_fwd_entry(x, gamma, beta, eps, y, mean, rstd, M, N, dtype, stream);
+}
+
+rn_status rn_layernorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes) {
+    g_err[0] = 0;
+    rn_status st = check_common(M, N, dtype);
+    if (st != RN_OK) return st;
+    if (!bytes) return fail(RN_ERR_INVALID_ARG, "bytes is NULL");
+    DeviceInfo d;
+    cudaError_t e = device_info(&d, nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    *bytes = ln_ws_bytes_for(d, N);
+    return RN_OK;
+}
+
+rn_status rn_layernorm_bwd(const void *x, const void *gamma, const void *dy, const float *mean,
+                           const float *rstd, void *dx, float *dgamma_f32, float *dbeta_f32,
+                           void *dgamma, void *dbeta, void *workspace, size_t workspace_bytes,
+                           int64_t M, int64_t N, int dtype, void *stream) {
+    return ln_bwd_entry(x, gamma, dy, mean, rstd, dx, dgamma_f32, dbeta_f32, dgamma, dbeta,
+                        workspace, workspace_bytes, M, N, dtype, stream);
 }
 
 }  // extern "C"

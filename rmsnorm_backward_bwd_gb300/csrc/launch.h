@@ -60,10 +60,15 @@ cudaError_t launch_bwd_generic(const BwdProblem &p, const GenericPlan &plan, cud
 // Scratch mode: dw_f32 = sum of G partial rows (fixed order), optional cast.
 cudaError_t launch_finalize(const float *partials, int G, int N, float *dw_f32, void *dw_cast,
                             int dtype, cudaStream_t s, bool pdl);
-// Atomic mode: zero before the row pass, cast after it.
-cudaError_t launch_zero_f32(float *p, int N, cudaStream_t s);
+// The same over partial rows of ld floats holding two length-N outputs side
+// by side (dw2_f32 nullable: one output).
+cudaError_t launch_finalize2(const float *partials, int G, int ld, int N, float *dw_f32,
+                             void *dw_cast, float *dw2_f32, void *dw2_cast, int dtype,
+                             cudaStream_t s, bool pdl);
+// Atomic mode: zero before the row pass, cast after it (second buffers nullable).
+cudaError_t launch_zero_f32(float *p, int N, cudaStream_t s, float *p2 = nullptr);
 cudaError_t launch_cast(const float *dw_f32, void *dw_cast, int N, int dtype, cudaStream_t s,
-                        bool pdl);
+                        bool pdl, const float *dw2_f32 = nullptr, void *dw2_cast = nullptr);
 
 struct FwdProblem {
     const void *x;
@@ -79,6 +84,49 @@ struct FwdProblem {
 };
 
 cudaError_t launch_fwd(const FwdProblem &p, bool vector_ok, int num_sms, cudaStream_t s);
+
+// LayerNorm.
+struct LnFwdProblem {
+    const void *x;
+    const void *gamma;
+    const void *beta;      // nullable: no bias
+    void *y;
+    float *mean;           // nullable
+    float *rstd;           // nullable
+    float eps;
+    int64_t M;
+    int N;
+    int dtype;
+};
+
+struct LnBwdProblem {
+    const void *x;
+    const void *gamma;
+    const void *dy;
+    const float *mean;
+    const float *rstd;
+    void *dx;
+    float *dg_f32;
+    float *db_f32;         // nullable: no bias gradient
+    void *dg_cast;         // nullable
+    void *db_cast;         // nullable
+    uint8_t *ws;           // workspace (header + partial rows of 2N floats)
+    int64_t M;
+    int N;
+    int dtype;
+};
+
+cudaError_t launch_ln_fwd(const LnFwdProblem &p, bool vector_ok, int num_sms, cudaStream_t s);
+// Default chunks-per-thread cap of the LayerNorm row engine (two fp32
+// accumulators per element pair instead of one).
+constexpr int kLnMaxCpt = 2;
+int ln_row_max_threads(int cpt);
+size_t ln_row_smem_bytes(int teams, int stages, int team_chunks);
+size_t ln_generic_smem_bytes(int N, bool smem_dw);
+cudaError_t launch_ln_bwd_row(const LnBwdProblem &p, const RowPlan &plan, cudaStream_t s,
+                              bool pdl_after_zero);
+cudaError_t launch_ln_bwd_generic(const LnBwdProblem &p, const GenericPlan &plan,
+                                  cudaStream_t s, bool pdl_after_zero);
 
 // Replace the calling thread's message returned by rn_last_error().
 void set_last_error(const char *msg);

@@ -1,0 +1,795 @@
+// LayerNorm forward (saving mean and rstd) and backward (dx, dgamma, dbeta).
+//
+// The FlyDSL pages plan the LayerNorm backward as the RMSNorm backward with
+// mean handling and a bias gradient added, over a forward that saves the
+// per-row mean and rstd (issue #769, plan item 6 and "PR 5 -- LayerNorm
+// backward"). The formulas are the textbook ones:
+//   forward:  mean = (1/N) sum_j x_j,  var = (1/N) sum_j (x_j - mean)^2,
+//             rstd = 1/sqrt(var + eps),  y = (x - mean) * rstd * gamma + beta
+//   backward: x_hat = (x - mean) * rstd,  wdy = dy * gamma,
+//             c1 = mean_j(x_hat * wdy),  c2 = mean_j(wdy),
+//             dx = (wdy - c2 - x_hat * c1) * rstd,
+//             dgamma = sum_rows dy * x_hat,  dbeta = sum_rows dy   (fp32)
+//
+// The engines mirror the RMSNorm ones:
+//   * forward, aligned rows: a team of threads per row holds the row in
+//     registers; the sum and then the centred sum of squares are reduced over
+//     the team (warp shuffles + one named barrier each). Unaligned rows: one
+//     CTA per row, three sweeps.
+//   * backward, aligned rows: the persistent row engine -- per-thread
+//     cp.async ring of x and dy rows in shared memory, pass 1 reduces the two
+//     row sums (x - mean)*wdy and wdy together, pass 2 stores dx and adds dy*x_hat
+//     and dy into fp32 register partials; at the end the CTA's teams combine
+//     their partials in a fixed order in shared memory and the CTA adds them
+//     with fp32 vector atomics (atomic mode) or stores one partial row of
+//     [dgamma | dbeta] to the workspace for the finalize kernel (scratch mode).
+//   * backward, unaligned rows: one CTA per row, scalar, two passes; the
+//     partials live in shared memory when 2N floats fit, else in the CTA's
+//     workspace row.
+#include "common.cuh"
+#include "launch.h"
+
+namespace rn {
+
+// ------------------------------------------------------------------ forward
+struct LnFwdArgs {
+    const uint8_t *x;
+    const uint8_t *gamma;
+    const uint8_t *beta;  // nullable
+    uint8_t *y;
+    float *mean;          // nullable
+    float *rstd;          // nullable
+    int64_t M;
+    int N;
+    int nchunks;
+    int row_bytes;
+    int team_threads;
+    int teams;
+    float inv_n;
+    float eps;
+};
+
+// Team-wide sum (warp shuffles, then the warps' partials through shared
+// memory, double-buffered by `parity`, behind one named barrier).
+__device__ __forceinline__ float ln_team_sum(float v, float (*red)[32], int parity, int team,
+                                             int warp, int team_warps, int first_warp,
+                                             int team_threads, int lane) {
+    v = warp_sum(v);
+    if (team_warps == 1) return v;
+    if (lane == 0) red[parity][warp] = v;
+    named_barrier_sync(1 + team, team_threads);
+    float t = 0.f;
+    for (int w = 0; w < team_warps; ++w) t += red[parity][first_warp + w];
+    return t;
+}
+
+template <typename T, int CPT>
+__global__ void __launch_bounds__(512) ln_fwd_vec_kernel(const LnFwdArgs a) {
+    constexpr int V = Traits<T>::kVec;
+    __shared__ float red[2][32];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int team = tid / a.team_threads;
+    const int tt = tid - team * a.team_threads;
+    const int team_warps = a.team_threads >> 5;
+    const int first_warp = team * team_warps;
+
+    uint4 g[CPT], b[CPT];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        const int c = tt + kk * a.team_threads;
+        const bool ok = c < a.nchunks;
+        g[kk] = ok ? ld_global_nc_v4(a.gamma + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
+        b[kk] = ok && a.beta ? ld_global_nc_v4(a.beta + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
+    }
+    const int64_t stride = (int64_t)gridDim.x * a.teams;
+    int parity = 0;
+    for (int64_t row = (int64_t)blockIdx.x * a.teams + team; row < a.M; row += stride) {
+        const size_t off = (size_t)row * a.row_bytes;
+        float v[CPT][V];
+        float s = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = tt + kk * a.team_threads;
+            if (c < a.nchunks) {
+                chunk_to_float<T>(ld_global_nc_v4(a.x + off + 16u * c), v[kk]);
+#pragma unroll
+                for (int e = 0; e < V; ++e) s += v[kk][e];
+            }
+        }
+        s = ln_team_sum(s, red, parity, team, warp, team_warps, first_warp, a.team_threads, lane);
+        parity ^= 1;
+        const float mu = s * a.inv_n;
+        float q = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = tt + kk * a.team_threads;
+            if (c < a.nchunks) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const float d = v[kk][e] - mu;
+                    q = fmaf(d, d, q);
+                }
+            }
+        }
+        q = ln_team_sum(q, red, parity, team, warp, team_warps, first_warp, a.team_threads, lane);
+        parity ^= 1;
+        const float rs = rsqrtf(q * a.inv_n + a.eps);
+        if (tt == 0) {
+            if (a.mean) a.mean[row] = mu;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = tt + kk * a.team_threads;
+            if (c < a.nchunks) {
+                float gf[V], bf[V], o[V];
+                chunk_to_float<T>(g[kk], gf);
+                chunk_to_float<T>(b[kk], bf);
+#pragma unroll
+                for (int e = 0; e < V; ++e) o[e] = fmaf((v[kk][e] - mu) * rs, gf[e], bf[e]);
+                st_global_v4(a.y + off + 16u * c, float_to_chunk<T>(o));
+            }
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) ln_fwd_generic_kernel(const LnFwdArgs a) {
+    __shared__ float red[32];
+    const T *x = reinterpret_cast<const T *>(a.x);
+    const T *g = reinterpret_cast<const T *>(a.gamma);
+    const T *bt = reinterpret_cast<const T *>(a.beta);
+    T *y = reinterpret_cast<T *>(a.y);
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    const int N = a.N;
+    auto block_sum = [&](float v) {
+        v = warp_sum(v);
+        if (lane == 0) red[warp] = v;
+        __syncthreads();
+        float t = 0.f;
+        for (int w = 0; w < nwarps; ++w) t += red[w];
+        __syncthreads();  // red is rewritten by the next sum
+        return t;
+    };
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const T *xr = x + (size_t)row * N;
+        float s = 0.f;
+        for (int j = tid; j < N; j += nthr) s += to_f(xr[j]);
+        const float mu = block_sum(s) * a.inv_n;
+        float q = 0.f;
+        for (int j = tid; j < N; j += nthr) {
+            const float d = to_f(xr[j]) - mu;
+            q = fmaf(d, d, q);
+        }
+        const float rs = rsqrtf(block_sum(q) * a.inv_n + a.eps);
+        if (tid == 0) {
+            if (a.mean) a.mean[row] = mu;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+        T *yr = y + (size_t)row * N;
+        for (int j = tid; j < N; j += nthr) {
+            const float bv = bt ? to_f(bt[j]) : 0.f;
+            yr[j] = from_f<T>(fmaf((to_f(xr[j]) - mu) * rs, to_f(g[j]), bv));
+        }
+    }
+}
+
+template <typename T>
+static cudaError_t launch_ln_fwd_t(const LnFwdArgs &a0, bool vector_ok, int num_sms,
+                                   cudaStream_t s) {
+    LnFwdArgs a = a0;
+    if (vector_ok) {
+        // team shape: about 256 threads per row, up to 4 chunks per thread
+        int team = (a.nchunks + 1) / 2;
+        team = ((team + 31) / 32) * 32;
+        if (team > 256) team = 256;
+        int cpt = (a.nchunks + team - 1) / team;
+        cpt = cpt <= 1 ? 1 : (cpt <= 2 ? 2 : 4);
+        if (cpt == 4) team = (((a.nchunks + 3) / 4 + 31) / 32) * 32;
+        if (team <= 512) {
+            a.team_threads = team;
+            a.teams = 512 / team;
+            if (a.teams > 15) a.teams = 15;
+            const void *fn = nullptr;
+            if (cpt == 1) fn = (const void *)ln_fwd_vec_kernel<T, 1>;
+            else if (cpt == 2) fn = (const void *)ln_fwd_vec_kernel<T, 2>;
+            else fn = (const void *)ln_fwd_vec_kernel<T, 4>;
+            int per_sm = 0;
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &per_sm, fn, a.teams * a.team_threads, 0);
+            if (e != cudaSuccess) return e;
+            if (per_sm < 1) per_sm = 1;
+            int64_t need = (a.M + a.teams - 1) / a.teams;
+            int64_t grid = (int64_t)num_sms * per_sm;
+            if (grid > need) grid = need;
+            dim3 block(a.teams * a.team_threads);
+            if (cpt == 1) ln_fwd_vec_kernel<T, 1><<<(unsigned)grid, block, 0, s>>>(a);
+            else if (cpt == 2) ln_fwd_vec_kernel<T, 2><<<(unsigned)grid, block, 0, s>>>(a);
+            else ln_fwd_vec_kernel<T, 4><<<(unsigned)grid, block, 0, s>>>(a);
+            return cudaGetLastError();
+        }
+    }
+    int64_t grid = (int64_t)num_sms * 8;
+    if (grid > a.M) grid = a.M;
+    ln_fwd_generic_kernel<T><<<(unsigned)grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ln_fwd(const LnFwdProblem &p, bool vector_ok, int num_sms, cudaStream_t s) {
+    LnFwdArgs a;
+    a.x = static_cast<const uint8_t *>(p.x);
+    a.gamma = static_cast<const uint8_t *>(p.gamma);
+    a.beta = static_cast<const uint8_t *>(p.beta);
+    a.y = static_cast<uint8_t *>(p.y);
+    a.mean = p.mean;
+    a.rstd = p.rstd;
+    a.M = p.M;
+    a.N = p.N;
+    a.row_bytes = p.N * elem_bytes(p.dtype);
+    a.nchunks = a.row_bytes / 16;
+    a.team_threads = 0;
+    a.teams = 0;
+    a.inv_n = 1.0f / (float)p.N;
+    a.eps = p.eps;
+    switch (p.dtype) {
+    case kF32: return launch_ln_fwd_t<float>(a, vector_ok, num_sms, s);
+    case kF16: return launch_ln_fwd_t<__half>(a, vector_ok, num_sms, s);
+    case kBF16: return launch_ln_fwd_t<__nv_bfloat16>(a, vector_ok, num_sms, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// ------------------------------------------------------- backward, row engine
+// Two fp32 accumulators per element pair (dgamma, dbeta) need up to 128
+// registers a thread: at most 512 threads a CTA for every tile.
+int ln_row_max_threads(int) { return 512; }
+constexpr int kLnMaxThreads = 512;
+
+// [2 parities][2 sums][32 warps] fp32 partial sums, then the ring
+constexpr int kLnRingOffset = 512;
+
+size_t ln_row_smem_bytes(int teams, int stages, int team_chunks) {
+    return (size_t)kLnRingOffset + (size_t)teams * stages * 2 * (size_t)team_chunks * 16;
+}
+
+struct LnRowArgs {
+    const uint8_t *x;
+    const uint8_t *gamma;
+    const uint8_t *dy;
+    const float *mean;
+    const float *rstd;
+    uint8_t *dx;
+    // atomic: dgamma_f32 / dbeta_f32 (dbeta nullable);
+    // scratch: the workspace's partial rows [gridDim.x][2N], dgamma then dbeta
+    float *dg_out;
+    float *db_out;
+    int64_t M;
+    int N;
+    int nchunks;
+    int row_bytes;
+    int team_threads;
+    int teams;
+    int stages;
+    float inv_n;
+};
+
+// A 16-byte chunk as fp32 pairs.
+template <typename T> __device__ __forceinline__ void chunk_pairs(const uint4 &u, f32x2 *p);
+template <> __device__ __forceinline__ void chunk_pairs<float>(const uint4 &u, f32x2 *p) {
+    p[0] = f2_make(__uint_as_float(u.x), __uint_as_float(u.y));
+    p[1] = f2_make(__uint_as_float(u.z), __uint_as_float(u.w));
+}
+template <> __device__ __forceinline__ void chunk_pairs<__nv_bfloat16>(const uint4 &u, f32x2 *p) {
+    p[0] = widen_bf16x2(u.x);
+    p[1] = widen_bf16x2(u.y);
+    p[2] = widen_bf16x2(u.z);
+    p[3] = widen_bf16x2(u.w);
+}
+template <> __device__ __forceinline__ void chunk_pairs<__half>(const uint4 &u, f32x2 *p) {
+    p[0] = widen_f16x2(u.x);
+    p[1] = widen_f16x2(u.y);
+    p[2] = widen_f16x2(u.z);
+    p[3] = widen_f16x2(u.w);
+}
+
+// dy*gamma for a chunk, as fp32 pairs: for 16-bit types the exact products of
+// the packed halves (one mixed-precision FMA per element, no unpacking).
+template <typename T>
+__device__ __forceinline__ void mul_chunk_pairs(const uint4 &d, const uint4 &g, f32x2 *p);
+template <>
+__device__ __forceinline__ void mul_chunk_pairs<__nv_bfloat16>(const uint4 &d, const uint4 &g,
+                                                               f32x2 *p) {
+    p[0] = mul_bf16x2(d.x, g.x);
+    p[1] = mul_bf16x2(d.y, g.y);
+    p[2] = mul_bf16x2(d.z, g.z);
+    p[3] = mul_bf16x2(d.w, g.w);
+}
+template <>
+__device__ __forceinline__ void mul_chunk_pairs<__half>(const uint4 &d, const uint4 &g, f32x2 *p) {
+    p[0] = mul_f16x2(d.x, g.x);
+    p[1] = mul_f16x2(d.y, g.y);
+    p[2] = mul_f16x2(d.z, g.z);
+    p[3] = mul_f16x2(d.w, g.w);
+}
+
+// fp32 pairs back to a 16-byte chunk of T (round to nearest even).
+template <typename T> __device__ __forceinline__ uint4 pairs_chunk(const f32x2 *p);
+template <> __device__ __forceinline__ uint4 pairs_chunk<float>(const f32x2 *p) {
+    float a, b, c, d;
+    f2_split(p[0], a, b);
+    f2_split(p[1], c, d);
+    return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c),
+                      __float_as_uint(d));
+}
+template <> __device__ __forceinline__ uint4 pairs_chunk<__nv_bfloat16>(const f32x2 *p) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float lo, hi;
+        f2_split(p[q], lo, hi);
+        w[q] = pack_bf16x2(lo, hi);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <> __device__ __forceinline__ uint4 pairs_chunk<__half>(const f32x2 *p) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float lo, hi;
+        f2_split(p[q], lo, hi);
+        w[q] = pack_f16x2(lo, hi);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Two team-wide sums at once; every thread of the team gets the same bits.
+__device__ __forceinline__ void ln_team_sum2(float &u, float &v, float *red, int parity, int warp,
+                                             int lane, int team, int team_warps, int first_warp,
+                                             int team_threads) {
+    u = warp_sum(u);
+    v = warp_sum(v);
+    if (team_warps == 1) return;
+    float *slot = red + parity * 64;
+    if (lane == 0) {
+        slot[warp] = u;
+        slot[32 + warp] = v;
+    }
+    named_barrier_sync(1 + team, team_threads);
+    const float a = lane < team_warps ? slot[first_warp + lane] : 0.f;
+    const float b = lane < team_warps ? slot[32 + first_warp + lane] : 0.f;
+    u = warp_sum(a);
+    v = warp_sum(b);
+}
+
+// The CTA's partial of one accumulator (a team's registers, teams combined in
+// a fixed order through shared memory, float4 q of chunk c at q*tc + c):
+// added atomically into out (atomic mode) or stored as out's row (scratch).
+// `scratch` must hold N floats and be free of other use; the caller
+// synchronises the CTA before and after.
+template <int CPT, int P, bool ATOMIC>
+__device__ __forceinline__ void ln_cta_out(const f32x2 (&acc)[CPT][P], float *out,
+                                           const LnRowArgs &a, uint8_t *scratch, int team,
+                                           int tt) {
+    constexpr int Q = P / 2;  // float4 per chunk
+    if (a.teams == 1) {
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = tt + kk * a.team_threads;
+            if (c < a.nchunks) {
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    float4 v;
+                    f2_split(acc[kk][2 * q], v.x, v.y);
+                    f2_split(acc[kk][2 * q + 1], v.z, v.w);
+                    float4 *dst = reinterpret_cast<float4 *>(out + (size_t)c * (2 * P) + 4 * q);
+                    if (ATOMIC) atomicAdd(dst, v);
+                    else *dst = v;
+                }
+            }
+        }
+        return;
+    }
+    const int tc = CPT * a.team_threads;
+    float4 *sdw = reinterpret_cast<float4 *>(scratch);
+    for (int t = 0; t < a.teams; ++t) {
+        if (team == t) {
+#pragma unroll
+            for (int kk = 0; kk < CPT; ++kk) {
+                const int c = tt + kk * a.team_threads;
+                if (c < a.nchunks) {
+#pragma unroll
+                    for (int q = 0; q < Q; ++q) {
+                        float4 *p = sdw + (size_t)q * tc + c;
+                        float4 v;
+                        f2_split(acc[kk][2 * q], v.x, v.y);
+                        f2_split(acc[kk][2 * q + 1], v.z, v.w);
+                        if (t > 0) {
+                            const float4 o = *p;
+                            v.x += o.x;
+                            v.y += o.y;
+                            v.z += o.z;
+                            v.w += o.w;
+                        }
+                        *p = v;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    for (int i = threadIdx.x; i < a.N / 4; i += blockDim.x) {
+        const int c = i / Q, q = i - c * Q;
+        const float4 v = sdw[(size_t)q * tc + c];
+        float4 *dst = reinterpret_cast<float4 *>(out) + i;
+        if (ATOMIC) atomicAdd(dst, v);
+        else *dst = v;
+    }
+}
+
+template <typename T, int CPT, bool ATOMIC>
+__global__ void __launch_bounds__(kLnMaxThreads, 1) ln_bwd_row_kernel(const LnRowArgs a) {
+    constexpr int V = Traits<T>::kVec;
+    constexpr int P = V / 2;  // fp32 pairs per chunk
+    // fp32 gamma is kept as pairs; 16-bit gamma stays packed (see mul_chunk_pairs)
+    constexpr bool kF32 = sizeof(T) == 4;
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *red = reinterpret_cast<float *>(smem);
+    uint8_t *ring = smem + kLnRingOffset;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int team = tid / a.team_threads;
+    const int tt = tid - team * a.team_threads;
+    const int team_warps = a.team_threads >> 5;
+    const int first_warp = team * team_warps;
+    const int S = a.stages;
+
+    // This thread's ring: chunk kk of tensor t (0 = x, 1 = dy) in slot s at
+    // my0 + s*slot_bytes + t*tensor_bytes + kk*kk_bytes.
+    const int tc = CPT * a.team_threads;
+    const uint32_t kk_bytes = 16u * a.team_threads;
+    const uint32_t tensor_bytes = 16u * tc;
+    const uint32_t slot_bytes = 2 * tensor_bytes;
+    const uint32_t my0 = smem_addr(ring) + (uint32_t)team * S * slot_bytes + 16u * tt;
+
+    const int64_t team_stride = (int64_t)gridDim.x * a.teams;
+    const int64_t row0 = (int64_t)blockIdx.x * a.teams + team;
+    const int64_t nrows = row0 < a.M ? (a.M - 1 - row0) / team_stride + 1 : 0;
+    const uint64_t policy = l2_policy_evict_first();
+
+    uint32_t coff[CPT];
+    bool cok[CPT];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        const int c = tt + kk * a.team_threads;
+        coff[kk] = 16u * c;
+        cok[kk] = c < a.nchunks;
+    }
+
+    auto issue = [&](int64_t row, int s) {
+        const size_t off = (size_t)row * a.row_bytes;
+        const uint8_t *xr = a.x + off, *dr = a.dy + off;
+        const uint32_t d = my0 + (uint32_t)s * slot_bytes;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            if (cok[kk]) {
+                cp_async16(d + kk * kk_bytes, xr + coff[kk], policy);
+                cp_async16(d + tensor_bytes + kk * kk_bytes, dr + coff[kk], policy);
+            }
+        }
+    };
+    for (int j = 0; j < S - 1; ++j) {
+        if (j < nrows) issue(row0 + j * team_stride, j);
+        cp_async_commit();
+    }
+
+    uint4 gp[CPT];
+    f32x2 g2[kF32 ? CPT : 1][kF32 ? P : 1];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        gp[kk] = cok[kk] ? ld_global_nc_v4(a.gamma + coff[kk]) : make_uint4(0, 0, 0, 0);
+        if (kF32) chunk_pairs<T>(gp[kk], g2[kF32 ? kk : 0]);
+    }
+    // wdy = dy*gamma of chunk kk as fp32 pairs (d2: dy as pairs, fp32 only)
+    auto wdy = [&](int kk, const uint4 &dv, const f32x2 *d2, f32x2 *w) {
+        if (kF32) {
+#pragma unroll
+            for (int q = 0; q < P; ++q) w[q] = f2_mul(d2[q], g2[kF32 ? kk : 0][kF32 ? q : 0]);
+        } else {
+            mul_chunk_pairs<T>(dv, gp[kk], w);
+        }
+    };
+    f32x2 accg[CPT][P], accb[CPT][P];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk)
+#pragma unroll
+        for (int q = 0; q < P; ++q) accg[kk][q] = accb[kk][q] = f2_make(0.f, 0.f);
+
+    const int64_t ahead = (int64_t)(S - 1) * team_stride;
+    float mu_next = nrows > 0 ? __ldg(a.mean + row0) : 0.f;
+    float rs_next = nrows > 0 ? __ldg(a.rstd + row0) : 0.f;
+    int slot = 0, fill = S - 1;
+    int64_t row = row0;
+    for (int64_t k = 0; k < nrows; ++k, row += team_stride) {
+        if (k + S - 1 < nrows) issue(row + ahead, fill);
+        cp_async_commit();
+        const float mu = mu_next, rs = rs_next;
+        if (k + 1 < nrows) {
+            mu_next = __ldg(a.mean + row + team_stride);
+            rs_next = __ldg(a.rstd + row + team_stride);
+        }
+        cp_async_wait_pending(S - 1);
+        const uint32_t sb = my0 + (uint32_t)slot * slot_bytes;
+        const f32x2 nmu2 = f2_make(-mu, -mu);
+
+        // pass 1: sum (x - mean)*wdy and sum wdy over the row
+        f32x2 s1 = f2_make(0.f, 0.f), s2 = f2_make(0.f, 0.f);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            if (cok[kk]) {
+                f32x2 x2[P], d2[P], w[P];
+                const uint4 dv = ld_shared_v4(sb + tensor_bytes + kk * kk_bytes);
+                chunk_pairs<T>(ld_shared_v4(sb + kk * kk_bytes), x2);
+                if (kF32) chunk_pairs<T>(dv, d2);
+                wdy(kk, dv, d2, w);
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    s1 = f2_fma(f2_add(x2[q], nmu2), w[q], s1);
+                    s2 = f2_add(w[q], s2);
+                }
+            }
+        }
+        float u, v, uh, vh;
+        f2_split(s1, u, uh);
+        f2_split(s2, v, vh);
+        u += uh;
+        v += vh;
+        ln_team_sum2(u, v, red, (int)(k & 1), warp, lane, team, team_warps, first_warp,
+                     a.team_threads);
+
+        // dx = (wdy - c2 - x_hat*c1)*rstd = wdy*rstd + (x - mean)*B + A with
+        // c1 = rstd*u/N, c2 = v/N, B = -rstd^2*c1, A = -c2*rstd
+        const float c1 = rs * u * a.inv_n;
+        const float c2 = v * a.inv_n;
+        const float B = -rs * rs * c1, A = -c2 * rs;
+        const f32x2 rs2 = f2_make(rs, rs), B2 = f2_make(B, B), A2 = f2_make(A, A);
+        uint8_t *dxrow = a.dx + (size_t)row * a.row_bytes;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            if (cok[kk]) {
+                f32x2 x2[P], d2[P], w[P], o2[P];
+                const uint4 dv = ld_shared_v4(sb + tensor_bytes + kk * kk_bytes);
+                chunk_pairs<T>(ld_shared_v4(sb + kk * kk_bytes), x2);
+                chunk_pairs<T>(dv, d2);
+                wdy(kk, dv, d2, w);
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    const f32x2 xc = f2_add(x2[q], nmu2);
+                    o2[q] = f2_fma(w[q], rs2, f2_fma(xc, B2, A2));
+                    accg[kk][q] = f2_fma(d2[q], f2_mul(xc, rs2), accg[kk][q]);
+                    accb[kk][q] = f2_add(d2[q], accb[kk][q]);
+                }
+                st_global_v4(dxrow + coff[kk], pairs_chunk<T>(o2));
+            }
+        }
+        if (++slot == S) slot = 0;
+        if (++fill == S) fill = 0;
+    }
+
+    pdl_launch_dependents();
+    __syncthreads();  // every team is done with its ring (all real copies waited for)
+    if (ATOMIC) pdl_wait();  // the zeroing kernel ahead of this one has finished
+    float *dg = ATOMIC ? a.dg_out : a.dg_out + (size_t)blockIdx.x * 2 * a.N;
+    float *db = ATOMIC ? a.db_out : dg + a.N;
+    ln_cta_out<CPT, P, ATOMIC>(accg, dg, a, ring, team, tt);
+    if (db) {
+        __syncthreads();  // the shared scratch is reused
+        ln_cta_out<CPT, P, ATOMIC>(accb, db, a, ring, team, tt);
+    }
+}
+
+template <typename T, int CPT, bool ATOMIC>
+static cudaError_t launch_ln_row_t(const LnRowArgs &args, const RowPlan &plan, cudaStream_t s,
+                                   bool pdl) {
+    auto kern = ln_bwd_row_kernel<T, CPT, ATOMIC>;
+    cudaError_t e = ensure_smem_attr((const void *)kern, plan.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(plan.teams * plan.team_threads);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+template <typename T>
+static cudaError_t launch_ln_row_dt(const LnRowArgs &args, const RowPlan &plan, cudaStream_t s,
+                                    bool pdl) {
+    switch (plan.cpt) {
+    case 1:
+        return plan.atomic ? launch_ln_row_t<T, 1, true>(args, plan, s, pdl)
+                           : launch_ln_row_t<T, 1, false>(args, plan, s, pdl);
+    case 2:
+        return plan.atomic ? launch_ln_row_t<T, 2, true>(args, plan, s, pdl)
+                           : launch_ln_row_t<T, 2, false>(args, plan, s, pdl);
+    case 4:
+        return plan.atomic ? launch_ln_row_t<T, 4, true>(args, plan, s, pdl)
+                           : launch_ln_row_t<T, 4, false>(args, plan, s, pdl);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_ln_bwd_row(const LnBwdProblem &p, const RowPlan &plan, cudaStream_t s,
+                              bool pdl_after_zero) {
+    LnRowArgs a;
+    a.x = static_cast<const uint8_t *>(p.x);
+    a.gamma = static_cast<const uint8_t *>(p.gamma);
+    a.dy = static_cast<const uint8_t *>(p.dy);
+    a.mean = p.mean;
+    a.rstd = p.rstd;
+    a.dx = static_cast<uint8_t *>(p.dx);
+    if (plan.atomic) {
+        a.dg_out = p.dg_f32;
+        a.db_out = p.db_f32;
+    } else {
+        a.dg_out = reinterpret_cast<float *>(p.ws + kWsHeaderBytes);
+        a.db_out = nullptr;  // the kernel derives the dbeta half of each partial row
+    }
+    a.M = p.M;
+    a.N = p.N;
+    a.row_bytes = p.N * elem_bytes(p.dtype);
+    a.nchunks = a.row_bytes / 16;
+    a.team_threads = plan.team_threads;
+    a.teams = plan.teams;
+    a.stages = plan.stages;
+    a.inv_n = 1.0f / (float)p.N;
+    switch (p.dtype) {
+    case kF32: return launch_ln_row_dt<float>(a, plan, s, pdl_after_zero);
+    case kF16: return launch_ln_row_dt<__half>(a, plan, s, pdl_after_zero);
+    case kBF16: return launch_ln_row_dt<__nv_bfloat16>(a, plan, s, pdl_after_zero);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// -------------------------------------------------- backward, generic engine
+size_t ln_generic_smem_bytes(int N, bool smem_dw) {
+    return 512 + (smem_dw ? (size_t)N * 8 : 0);
+}
+
+struct LnGenArgs {
+    const void *x;
+    const void *gamma;
+    const void *dy;
+    const float *mean;
+    const float *rstd;
+    void *dx;
+    // scratch: partial rows [gridDim.x][2N] (dgamma | dbeta); atomic: the outputs
+    float *dg_out;
+    float *db_out;  // atomic mode only; nullable
+    int64_t M;
+    int N;
+    float inv_n;
+};
+
+template <typename T, bool ATOMIC, bool SMEM_DW>
+__global__ void __launch_bounds__(512) ln_bwd_generic_kernel(const LnGenArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *red = reinterpret_cast<float *>(smem);        // [2 sums][32 warps]
+    float *sdw = reinterpret_cast<float *>(smem + 512);  // 2N floats when SMEM_DW
+    const T *x = static_cast<const T *>(a.x);
+    const T *g = static_cast<const T *>(a.gamma);
+    const T *dy = static_cast<const T *>(a.dy);
+    T *dx = static_cast<T *>(a.dx);
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    const int N = a.N;
+    float *part = ATOMIC ? nullptr : a.dg_out + (size_t)blockIdx.x * 2 * N;
+    float *dw = SMEM_DW ? sdw : part;  // [dgamma | dbeta]; !SMEM_DW implies scratch mode
+
+    for (int j = tid; j < 2 * N; j += nthr) dw[j] = 0.f;
+
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const float mu = __ldg(a.mean + row), rs = __ldg(a.rstd + row);
+        const T *xr = x + (size_t)row * N;
+        const T *dyr = dy + (size_t)row * N;
+        float s1 = 0.f, s2 = 0.f;
+        for (int j = tid; j < N; j += nthr) {
+            const float w = to_f(dyr[j]) * to_f(g[j]);
+            s1 = fmaf(to_f(xr[j]) - mu, w, s1);
+            s2 += w;
+        }
+        s1 = warp_sum(s1);
+        s2 = warp_sum(s2);
+        if (lane == 0) {
+            red[warp] = s1;
+            red[32 + warp] = s2;
+        }
+        __syncthreads();
+        float t1 = 0.f, t2 = 0.f;
+        for (int w = 0; w < nwarps; ++w) {
+            t1 += red[w];
+            t2 += red[32 + w];
+        }
+        __syncthreads();  // red is rewritten by the next row
+        const float c1 = rs * t1 * a.inv_n, c2 = t2 * a.inv_n;
+        T *dxr = dx + (size_t)row * N;
+        for (int j = tid; j < N; j += nthr) {
+            const float dv = to_f(dyr[j]);
+            const float xh = (to_f(xr[j]) - mu) * rs;
+            const float w = dv * to_f(g[j]);
+            dxr[j] = from_f<T>((w - c2 - xh * c1) * rs);
+            dw[j] = fmaf(dv, xh, dw[j]);
+            dw[N + j] += dv;
+        }
+    }
+    pdl_launch_dependents();
+    if (SMEM_DW || ATOMIC) {
+        if (ATOMIC) {
+            pdl_wait();
+            for (int j = tid; j < N; j += nthr) {
+                atomicAdd(a.dg_out + j, dw[j]);
+                if (a.db_out) atomicAdd(a.db_out + j, dw[N + j]);
+            }
+        } else {
+            for (int j = tid; j < 2 * N; j += nthr) part[j] = dw[j];
+        }
+    }
+}
+
+template <typename T, bool ATOMIC, bool SMEM_DW>
+static cudaError_t launch_ln_gen_t(const LnGenArgs &args, const GenericPlan &plan,
+                                   cudaStream_t s, bool pdl) {
+    auto kern = ln_bwd_generic_kernel<T, ATOMIC, SMEM_DW>;
+    cudaError_t e = ensure_smem_attr((const void *)kern, plan.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(plan.threads);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+template <typename T>
+static cudaError_t launch_ln_gen_dt(const LnGenArgs &args, const GenericPlan &plan,
+                                    cudaStream_t s, bool pdl) {
+    if (plan.atomic) return launch_ln_gen_t<T, true, true>(args, plan, s, pdl);
+    if (plan.smem_dw) return launch_ln_gen_t<T, false, true>(args, plan, s, pdl);
+    return launch_ln_gen_t<T, false, false>(args, plan, s, pdl);
+}
+
+cudaError_t launch_ln_bwd_generic(const LnBwdProblem &p, const GenericPlan &plan,
+                                  cudaStream_t s, bool pdl_after_zero) {
+    LnGenArgs a;
+    a.x = p.x;
+    a.gamma = p.gamma;
+    a.dy = p.dy;
+    a.mean = p.mean;
+    a.rstd = p.rstd;
+    a.dx = p.dx;
+    a.dg_out = plan.atomic ? p.dg_f32 : reinterpret_cast<float *>(p.ws + kWsHeaderBytes);
+    a.db_out = plan.atomic ? p.db_f32 : nullptr;
+    a.M = p.M;
+    a.N = p.N;
+    a.inv_n = 1.0f / (float)p.N;
+    switch (p.dtype) {
+    case kF32: return launch_ln_gen_dt<float>(a, plan, s, pdl_after_zero);
+    case kF16: return launch_ln_gen_dt<__half>(a, plan, s, pdl_after_zero);
+    case kBF16: return launch_ln_gen_dt<__nv_bfloat16>(a, plan, s, pdl_after_zero);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rn

@@ -44,6 +44,13 @@ def _bind(lib):
     lib.rn_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, ci, vp]
     lib.rn_fused_add_rmsnorm_bwd.restype = ci
     lib.rn_fused_add_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, ci, vp]
+    lib.rn_layernorm_fwd.restype = ci
+    lib.rn_layernorm_fwd.argtypes = [vp, vp, vp, f32, vp, vp, vp, i64, i64, ci, vp]
+    lib.rn_layernorm_bwd_workspace_bytes.restype = ci
+    lib.rn_layernorm_bwd_workspace_bytes.argtypes = [i64, i64, ci, ctypes.POINTER(sz)]
+    lib.rn_layernorm_bwd.restype = ci
+    lib.rn_layernorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64,
+                                     ci, vp]
     lib.rn_rmsnorm_bwd_noalloc.restype = ci
     lib.rn_rmsnorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, vp]
     lib.rn_set_option.restype = ci

@@ -108,9 +108,20 @@ def _ws_bytes(M, N, code, index):
     return n
 
 
-def _workspace(M, N, code, index):
+def _ln_ws_bytes(M, N, code, index):
+    key = ("ln", M, N, code, index)
+    n = _WS_BYTES.get(key)
+    if n is None:
+        nbytes = ctypes.c_size_t(0)
+        native.check(native.lib().rn_layernorm_bwd_workspace_bytes(int(M), int(N), code,
+                                                                   ctypes.byref(nbytes)))
+        n = _WS_BYTES[key] = nbytes.value
+    return n
+
+
+def _workspace(M, N, code, index, layernorm=False):
     # index is the current device here
-    n = _ws_bytes(M, N, code, index)
+    n = _ln_ws_bytes(M, N, code, index) if layernorm else _ws_bytes(M, N, code, index)
     key = (index, _stream_handle(index))
     ws = _WS.get(key)
     if ws is None or ws.numel() < n:
@@ -221,3 +232,77 @@ def fused_add_rmsnorm_bwd(added, gamma, dy, rstd, dresidual_out=None, *, dx=None
             _ptr(dweight_f32), _ptr(dweight), _ptr(ws), ws.numel(), M, N, _code(added),
             _stream_handle(added.get_device())))
     return dx, dx, dweight, dweight_f32
+
+
+def layernorm_fwd(x, gamma, beta, eps, *, y=None, mean=None, rstd=None, store_stats=True):
+    """y = (x - mean) * rstd * gamma + beta per row, with mean and
+    rstd = 1/sqrt(var + eps) over the last dimension (biased variance).
+    beta may be None. Returns (y, mean, rstd); mean and rstd are fp32 [M]
+    (None when store_stats is False)."""
+    _need("x", x, x)
+    _need("gamma", gamma, x)
+    M, N = _rows(x, gamma)
+    if beta is not None:
+        _need("beta", beta, x, (N,))
+    with _on_device(x.get_device()):
+        y = torch.empty_like(x) if y is None else _need("y", y, x, x.shape)
+        if store_stats:
+            mean = (torch.empty(M, dtype=torch.float32, device=x.device) if mean is None
+                    else _need("mean", mean, x, (M,), torch.float32))
+            rstd = (torch.empty(M, dtype=torch.float32, device=x.device) if rstd is None
+                    else _need("rstd", rstd, x, (M,), torch.float32))
+        else:
+            mean = rstd = None
+        native.check(native.lib().rn_layernorm_fwd(
+            _ptr(x), _ptr(gamma), _ptr(beta), float(eps), _ptr(y), _ptr(mean), _ptr(rstd), M, N,
+            _code(x), _stream_handle(x.get_device())))
+    return y, mean, rstd
+
+
+def layernorm_bwd(x, gamma, dy, mean, rstd, *, dx=None, dgamma_f32=None, dbeta_f32=None,
+                  dgamma=None, dbeta=None, want_dbeta=True, want_cast=True, workspace=None):
+    """Gradients of y = layernorm(x) * gamma (+ beta) given dy and the saved
+    fp32 mean and rstd. Returns (dx, dgamma, dbeta, dgamma_f32, dbeta_f32):
+    the casts to the I/O dtype are None when want_cast is False (and no buffer
+    was passed); the dbeta pair is None when want_dbeta is False."""
+    _need("x", x, x)
+    _need("gamma", gamma, x)
+    _need("dy", dy, x, x.shape)
+    M, N = _rows(x, gamma)
+    _need("mean", mean, x, (M,), torch.float32)
+    _need("rstd", rstd, x, (M,), torch.float32)
+    with _on_device(x.get_device()):
+        dx = torch.empty_like(x) if dx is None else _need("dx", dx, x, x.shape)
+        f32 = dict(dtype=torch.float32, device=x.device)
+        dgamma_f32 = (torch.empty(N, **f32) if dgamma_f32 is None
+                      else _need("dgamma_f32", dgamma_f32, x, (N,), torch.float32))
+        if want_dbeta:
+            dbeta_f32 = (torch.empty(N, **f32) if dbeta_f32 is None
+                         else _need("dbeta_f32", dbeta_f32, x, (N,), torch.float32))
+        else:
+            dbeta_f32 = dbeta = None
+        if dgamma is None and want_cast:
+            dgamma = torch.empty(N, dtype=x.dtype, device=x.device)
+        elif dgamma is not None:
+            _need("dgamma", dgamma, x, (N,))
+        if want_dbeta:
+            if dbeta is None and want_cast:
+                dbeta = torch.empty(N, dtype=x.dtype, device=x.device)
+            elif dbeta is not None:
+                _need("dbeta", dbeta, x, (N,))
+        ws = (_workspace(M, N, _code(x), x.get_device(), layernorm=True) if workspace is None
+              else workspace)
+        native.check(native.lib().rn_layernorm_bwd(
+            _ptr(x), _ptr(gamma), _ptr(dy), _ptr(mean), _ptr(rstd), _ptr(dx), _ptr(dgamma_f32),
+            _ptr(dbeta_f32), _ptr(dgamma), _ptr(dbeta), _ptr(ws), ws.numel(), M, N, _code(x),
+            _stream_handle(x.get_device())))
+    return dx, dgamma, dbeta, dgamma_f32, dbeta_f32
+
+
+def layernorm_bwd_workspace(M, N, dtype, device):
+    """A workspace for layernorm_bwd on `device` (shared with the RMSNorm
+    backward's cache: one buffer per (device, stream), grown as needed)."""
+    device = torch.device(device)
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    with _on_device(index):
+        return _workspace(M, N, _CODES[dtype], index, layernorm=True)

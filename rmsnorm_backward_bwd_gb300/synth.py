@@ -55,6 +55,36 @@ def make_inputs(case: Case, device: str = "cpu") -> Dict[str, torch.Tensor]:
     return {k: v.to(dt).to(device) for k, v in out.items()}
 
 
+def make_ln_inputs(case: Case, x_shift: float = 0.5, device: str = "cpu") -> Dict[str, torch.Tensor]:
+    """LayerNorm inputs: one CPU generator seeded with case.seed draws fp32
+    normals in the order x, gamma, dy, beta; x is shifted by x_shift (rows
+    with a nonzero mean, so that the centring matters), gamma = 1 + 0.1*N(0,1),
+    dy is scaled by case.dy_scale, beta = 0.1*N(0,1); all cast to the dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(case.seed)
+    M, N = case.M, case.N
+    f32 = torch.float32
+    out = {}
+    out["x"] = torch.randn(M, N, generator=g, dtype=f32) + x_shift
+    out["gamma"] = 1.0 + 0.1 * torch.randn(N, generator=g, dtype=f32)
+    out["dy"] = torch.randn(M, N, generator=g, dtype=f32) * case.dy_scale
+    out["beta"] = 0.1 * torch.randn(N, generator=g, dtype=f32)
+    dt = TORCH_DTYPES[case.dtype]
+    return {k: v.to(dt).to(device) for k, v in out.items()}
+
+
+def ln_algorithmic_bytes(M: int, N: int, dtype: str, with_dbeta: bool, casts: bool) -> int:
+    """Bytes a LayerNorm backward call must move: read x, dy, gamma, mean and
+    rstd; write dx, dgamma_f32 [and dbeta_f32], and the casts when requested
+    and dtype != f32."""
+    s = ELEM_BYTES[dtype]
+    nout = 2 if with_dbeta else 1
+    b = M * N * s * 3 + N * s + 8 * M + 4 * N * nout
+    if casts and dtype != "f32":
+        b += N * s * nout
+    return b
+
+
 def algorithmic_bytes(M: int, N: int, dtype: str, with_dres: bool, dweight_cast: bool) -> int:
     """Bytes a backward call must move: read x|added, dy, [dres], gamma, rstd;
     write dx, dweight_f32 and (when requested and dtype != f32) the cast dweight."""
@@ -77,6 +107,9 @@ EDGE_SHAPES = [(1, 4096, "bf16"), (512, 2048, "bf16"), (512, 3000, "f32"), (128,
 LARGE_PLAIN = Case("rmsnorm_bwd bf16 M=16384 N=8192", 16384, 8192, "bf16")
 LARGE_FUSED = Case("fused_add_rmsnorm_bwd bf16 M=16384 N=8192 +dres", 16384, 8192, "bf16",
                    fused=True, with_dres=True)
+
+
+LN_4096 = Case("layernorm_bwd bf16 M=4096 N=4096", 4096, 4096, "bf16", eps=1e-5)
 
 
 def edge_cases() -> List[Case]:

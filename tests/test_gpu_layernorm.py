@@ -1,0 +1,250 @@
+"""LayerNorm forward and backward on the GPU, through the C ABI, against the
+fp64 oracle on the same seeded inputs.
+
+Tolerances: the backward's dx, dgamma/dbeta (fp32 and cast) use the rules of
+parity.py (the same ones as the RMSNorm backward). Forward: y as parity.py's
+"y"; the saved fp32 mean and rstd within 2^-24*(8 + 4*sqrt(N)) of the oracle
+(relative to mean|x| of the row for the mean, to rstd itself for rstd) -- the
+growth of an fp32 sum of N terms with a random-walk error, with margin.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+import rmsnorm_backward_bwd_gb300 as rn
+from rmsnorm_backward_bwd_gb300 import native, synth
+from rmsnorm_backward_bwd_gb300.synth import Case
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(4096, 4096, "bf16"), (1, 4096, "bf16"), (512, 2048, "bf16"), (512, 3000, "f32"),
+          (128, 4096, "f16"), (300, 768, "bf16"), (7, 1001, "bf16"), (3, 33, "f16"),
+          (16, 16384, "bf16"), (2, 40000, "f32"), (64, 8192, "f32")]
+
+
+@pytest.fixture(autouse=True)
+def _default_options():
+    yield
+    for opt in range(6):
+        native.set_option(opt, 0)
+
+
+def _stat_tol(N):
+    return 2.0**-24 * (8 + 4 * np.sqrt(N))
+
+
+class LnExpected:
+    pass
+
+
+def expected(case, with_bias=True):
+    inp = synth.make_ln_inputs(case)
+    ex = LnExpected()
+    ex.case = case
+    ex.inp = inp
+    x64, g64, dy64 = (parity.to64(inp[k]) for k in ("x", "gamma", "dy"))
+    b64 = parity.to64(inp["beta"]) if with_bias else None
+    ex.y64, ex.mean64, ex.rstd64 = oracle.layernorm_fwd(x64, g64, b64, np.float32(case.eps))
+    ex.mean32 = oracle.round_to(ex.mean64, "f32")
+    ex.rstd32 = oracle.round_to(ex.rstd64, "f32")
+    ex.dx, ex.dg, ex.db = oracle.layernorm_bwd(x64, g64, dy64, ex.mean32, ex.rstd32)
+    ex.x64, ex.g64, ex.dy64 = x64, g64, dy64
+    return ex
+
+
+def roundoff(ex):
+    """fp32 round-off scale of dx's terms, for the elements of a mask (the
+    LayerNorm counterpart of parity.roundoff_bound)."""
+    def fn(mask):
+        rows, cols = np.nonzero(mask.reshape(ex.x64.shape))
+        N = ex.x64.shape[1]
+        xc = ex.x64[rows] - ex.mean32[rows][:, None]
+        rs = ex.rstd32[rows]
+        w = ex.dy64[rows] * ex.g64
+        c1 = np.mean(xc * rs[:, None] * w, axis=1)
+        c2 = np.mean(w, axis=1)
+        mxw = np.mean(np.abs(xc * w), axis=1)
+        mw = np.mean(np.abs(w), axis=1)
+        xh = xc[np.arange(len(rows)), cols] * rs
+        wj = w[np.arange(len(rows)), cols]
+        return 2.0**-24 * rs * (16 * (np.abs(wj) + np.abs(c2) + np.abs(xh * c1))
+                                + 4 * np.sqrt(N) * (np.abs(xh) * rs * mxw + mw))
+    return fn
+
+
+def run_gpu(ex, with_dbeta=True, dev="cuda"):
+    x = ex.inp["x"].to(dev)
+    g = ex.inp["gamma"].to(dev)
+    dy = ex.inp["dy"].to(dev)
+    mean = torch.from_numpy(ex.mean32).float().to(dev)
+    rstd = torch.from_numpy(ex.rstd32).float().to(dev)
+    out = rn.layernorm_bwd(x, g, dy, mean, rstd, want_dbeta=with_dbeta)
+    torch.cuda.synchronize()
+    return out
+
+
+def check(ex, out, with_dbeta=True, tag=""):
+    dx, dg, db, dg32, db32 = out
+    dt = ex.case.dtype
+    parity.check_tensor("dx" + tag, dx, ex.dx, dt, "dx", roundoff=roundoff(ex))
+    parity.check_tensor("dgamma_f32" + tag, dg32, ex.dg, dt, "dweight_f32")
+    parity.check_tensor("dgamma" + tag, dg, ex.dg, dt, "dweight")
+    if with_dbeta:
+        parity.check_tensor("dbeta_f32" + tag, db32, ex.db, dt, "dweight_f32")
+        parity.check_tensor("dbeta" + tag, db, ex.db, dt, "dweight")
+    else:
+        assert db is None and db32 is None
+
+
+@pytest.mark.parametrize("M,N,dt", SHAPES, ids=lambda v: str(v))
+def test_layernorm_bwd_matches_oracle(M, N, dt):
+    ex = expected(Case("ln", M, N, dt, eps=1e-5))
+    check(ex, run_gpu(ex))
+
+
+@pytest.mark.parametrize("M,N,dt", [(512, 2048, "bf16"), (7, 1001, "bf16"), (64, 3000, "f32")],
+                         ids=lambda v: str(v))
+def test_layernorm_bwd_without_dbeta(M, N, dt):
+    ex = expected(Case("ln", M, N, dt, eps=1e-5, seed=4))
+    check(ex, run_gpu(ex, with_dbeta=False), with_dbeta=False)
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("M,N,dt", [(1000, 4096, "bf16"), (333, 1024, "f16"), (129, 2048, "f32")],
+                         ids=lambda v: str(v))
+def test_layernorm_forced_engines_and_modes(engine, mode, M, N, dt):
+    native.set_option(native.OPT_BWD_ENGINE, engine)
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    ex = expected(Case("ln", M, N, dt, eps=1e-5, seed=2))
+    out = run_gpu(ex)
+    plan = native.last_plan()
+    assert ("ln_row" if engine == 1 else "ln_generic") in plan, plan
+    assert ("atomic" if mode == 2 else "scratch") in plan, plan
+    check(ex, out, tag=" [%s]" % plan)
+
+
+@pytest.mark.parametrize("cpt,teams,stages", [(1, 1, 2), (2, 2, 2), (2, 1, 4), (4, 1, 2),
+                                              (1, 2, 3)])
+def test_layernorm_row_tiles(cpt, teams, stages):
+    native.set_option(native.OPT_BWD_ENGINE, 1)
+    native.set_option(native.OPT_CHUNKS_PER_THREAD, cpt)
+    native.set_option(native.OPT_TEAMS_PER_CTA, teams)
+    native.set_option(native.OPT_STAGES, stages)
+    ex = expected(Case("ln", 777, 2048, "bf16", eps=1e-5, seed=6))
+    out = run_gpu(ex)
+    plan = native.last_plan()
+    assert "cpt=%d" % cpt in plan and "teams=%d" % teams in plan and "stages=%d" % stages in plan
+    check(ex, out, tag=" [%s]" % plan)
+
+
+def test_layernorm_tile_over_thread_cap_is_refused():
+    """One chunk per thread and four teams of 256 threads would need 1024
+    threads a CTA; the LayerNorm row engine allows 512 and says so."""
+    native.set_option(native.OPT_BWD_ENGINE, 1)
+    native.set_option(native.OPT_CHUNKS_PER_THREAD, 1)
+    native.set_option(native.OPT_TEAMS_PER_CTA, 4)
+    ex = expected(Case("ln", 64, 2048, "bf16", eps=1e-5, seed=6))
+    with pytest.raises(native.RNError, match="row engine cannot take"):
+        run_gpu(ex)
+
+
+def test_layernorm_scratch_mode_is_repeatable_and_agrees_with_atomics():
+    ex = expected(Case("ln", 2048, 4096, "bf16", eps=1e-5, seed=8))
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)
+    a = run_gpu(ex)
+    b = run_gpu(ex)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    native.set_option(native.OPT_DWEIGHT_MODE, 2)
+    c = run_gpu(ex)
+    assert torch.equal(a[0], c[0])   # dx does not depend on the mode
+    check(ex, c)
+
+
+def test_layernorm_row_sum_invariant_full_size():
+    """sum_j dx_j = -c1*rstd^2*sum_j (x_j - mean32) per row (zero with the exact
+    mean); checked against that value from the fp32 statistics the kernel used."""
+    ex = expected(Case("ln", 4096, 4096, "bf16", eps=1e-5, seed=9))
+    dx = parity.to64(run_gpu(ex)[0])
+    xc = ex.x64 - ex.mean32[:, None]
+    c1 = np.mean(xc * ex.rstd32[:, None] * ex.dy64 * ex.g64, axis=1)
+    expect = -c1 * ex.rstd32 ** 2 * np.sum(xc, axis=1)
+    scale = np.sum(np.abs(dx), axis=1)
+    assert np.all(np.abs(np.sum(dx, axis=1) - expect) <= 2e-3 * scale)
+
+
+def test_layernorm_empty_batch():
+    x = torch.empty(0, 1024, device="cuda", dtype=torch.bfloat16)
+    g = torch.ones(1024, device="cuda", dtype=torch.bfloat16)
+    dy = torch.empty_like(x)
+    z = torch.empty(0, device="cuda", dtype=torch.float32)
+    dx, dg, db, dg32, db32 = rn.layernorm_bwd(x, g, dy, z, z)
+    torch.cuda.synchronize()
+    for t in (dg, db, dg32, db32):
+        assert torch.count_nonzero(t).item() == 0
+
+
+def test_layernorm_misaligned_pointers_use_generic_engine():
+    ex = expected(Case("ln", 64, 2048, "bf16", eps=1e-5, seed=10))
+    x = torch.empty(64 * 2048 + 1, dtype=torch.bfloat16, device="cuda")[1:].view(64, 2048)
+    x.copy_(ex.inp["x"].cuda())
+    mean = torch.from_numpy(ex.mean32).float().cuda()
+    rstd = torch.from_numpy(ex.rstd32).float().cuda()
+    out = rn.layernorm_bwd(x, ex.inp["gamma"].cuda(), ex.inp["dy"].cuda(), mean, rstd)
+    torch.cuda.synchronize()
+    assert "ln_generic" in native.last_plan()
+    check(ex, out)
+
+
+@pytest.mark.parametrize("M,N,dt", SHAPES, ids=lambda v: str(v))
+@pytest.mark.parametrize("with_bias", [True, False])
+def test_layernorm_fwd_matches_oracle(M, N, dt, with_bias):
+    ex = expected(Case("ln", M, N, dt, eps=1e-5, seed=11), with_bias)
+    beta = ex.inp["beta"].cuda() if with_bias else None
+    y, mean, rstd = rn.layernorm_fwd(ex.inp["x"].cuda(), ex.inp["gamma"].cuda(), beta, 1e-5)
+    torch.cuda.synchronize()
+    parity.check_tensor("y", y, ex.y64, dt, "y")
+    tol = _stat_tol(N)
+    mabs = np.mean(np.abs(ex.x64), axis=1)
+    assert np.all(np.abs(parity.to64(mean) - ex.mean64) <= tol * mabs)
+    assert np.all(np.abs(parity.to64(rstd) - ex.rstd64) <= tol * ex.rstd64)
+
+
+def test_layernorm_fwd_guards():
+    x = torch.randn(4, 256, device="cuda", dtype=torch.bfloat16)
+    g = torch.ones(256, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="dtype mismatch"):
+        rn.layernorm_fwd(x, g, torch.zeros(256, device="cuda"), 1e-5)
+    with pytest.raises(ValueError, match="beta has shape"):
+        rn.layernorm_fwd(x, g, g[:128], 1e-5)
+
+
+@pytest.mark.parametrize("shape,dt", [((2, 64, 1024), "f32"), ((4, 32, 4096), "bf16"),
+                                      ((3, 5, 1001), "bf16"), ((8, 2048), "f16")],
+                         ids=lambda v: str(v))
+@pytest.mark.parametrize("with_bias", [True, False])
+def test_layernorm_autograd_matches_oracle(shape, dt, with_bias):
+    M = int(np.prod(shape[:-1]))
+    case = Case("ln autograd", M, shape[-1], dt, eps=1e-5, seed=12)
+    inp = synth.make_ln_inputs(case)
+    x64, g64, dy64 = (parity.to64(inp[k]) for k in ("x", "gamma", "dy"))
+    b64 = parity.to64(inp["beta"]) if with_bias else None
+    y64, mean64, rstd64 = oracle.layernorm_fwd(x64, g64, b64, np.float32(case.eps))
+    ex = LnExpected()
+    ex.x64, ex.g64, ex.dy64 = x64, g64, dy64
+    ex.mean32, ex.rstd32 = oracle.round_to(mean64, "f32"), oracle.round_to(rstd64, "f32")
+    dx64, dg64, db64 = oracle.layernorm_bwd(x64, g64, dy64, ex.mean32, ex.rstd32)
+    x = inp["x"].cuda().reshape(shape).requires_grad_()
+    w = inp["gamma"].cuda().requires_grad_()
+    b = inp["beta"].cuda().requires_grad_() if with_bias else None
+    y = rn.layernorm(x, w, b, case.eps)
+    y.backward(inp["dy"].cuda().reshape(shape))
+    torch.cuda.synchronize()
+    parity.check_tensor("y", y.reshape(M, -1), y64, dt, "y")
+    parity.check_tensor("dx", x.grad.reshape(M, -1), dx64, dt, "dx", roundoff=roundoff(ex))
+    parity.check_tensor("dgamma", w.grad, dg64, dt, "dweight")
+    if with_bias:
+        parity.check_tensor("dbeta", b.grad, db64, dt, "dweight")
