@@ -189,6 +189,8 @@ def whole_job_gbs(bytes_per_rank, ws, slowest_ms):
 
 def synth_bytes(case):
     from rmsnorm_backward_bwd_gb300 import synth
+    if case.name.startswith("layernorm"):
+        return synth.ln_algorithmic_bytes(case.M, case.N, case.dtype, True, True)
     return synth.algorithmic_bytes(case.M, case.N, case.dtype, case.with_dres, True)
 
 
@@ -196,7 +198,7 @@ def workload_case(name):
     from rmsnorm_backward_bwd_gb300 import synth
     table = {"plain_4096": synth.PLAIN_4096, "fused_4096": synth.FUSED_4096,
              "fused_4096_nodres": synth.FUSED_4096_NODRES, "plain_16384x8192": synth.LARGE_PLAIN,
-             "fused_16384x8192": synth.LARGE_FUSED}
+             "fused_16384x8192": synth.LARGE_FUSED, "layernorm_4096": synth.LN_4096}
     return table[name]
 
 
@@ -237,6 +239,37 @@ class Problem:
         else:
             rn.rmsnorm_bwd(self.x, self.g, self.dy, self.rstd, dx=self.dx, dweight_f32=self.dw32,
                            dweight=self.dw, workspace=self.ws)
+
+
+class LnProblem:
+    """Device-resident inputs/outputs of one LayerNorm backward, plus the call
+    (mean and rstd from the GPU LayerNorm forward)."""
+
+    def __init__(self, case, dev):
+        import torch
+        import rmsnorm_backward_bwd_gb300 as rn
+        from rmsnorm_backward_bwd_gb300 import synth
+        self.case = case
+        inp = synth.make_ln_inputs(case, device=str(dev))
+        self.x, self.g, self.dy = inp["x"], inp["gamma"], inp["dy"]
+        _, self.mean, self.rstd = rn.layernorm_fwd(self.x, self.g, inp["beta"], case.eps)
+        N = case.N
+        self.dx = torch.empty_like(self.x)
+        self.dg32 = torch.empty(N, dtype=torch.float32, device=dev)
+        self.db32 = torch.empty(N, dtype=torch.float32, device=dev)
+        self.dg = torch.empty(N, dtype=self.x.dtype, device=dev)
+        self.db = torch.empty(N, dtype=self.x.dtype, device=dev)
+        self.ws = rn.layernorm_bwd_workspace(case.M, N, self.x.dtype, dev)
+        self.bytes = synth.ln_algorithmic_bytes(case.M, N, case.dtype, True, True)
+        s = synth.ELEM_BYTES[case.dtype]
+        self.row_pass_bytes = case.M * N * s * 3 + N * s + 8 * case.M
+        torch.cuda.synchronize()
+
+    def call(self):
+        import rmsnorm_backward_bwd_gb300 as rn
+        rn.layernorm_bwd(self.x, self.g, self.dy, self.mean, self.rstd, dx=self.dx,
+                         dgamma_f32=self.dg32, dbeta_f32=self.db32, dgamma=self.dg,
+                         dbeta=self.db, workspace=self.ws)
 
 
 def launches_per_call(plan):
@@ -330,6 +363,14 @@ def autograd_problem(case, dev, impl):
     import torch
     import rmsnorm_backward_bwd_gb300 as rn
     from rmsnorm_backward_bwd_gb300 import synth
+    if case.name.startswith("layernorm"):
+        inp = synth.make_ln_inputs(case, device=str(dev))
+        x, w, b = (inp[k].requires_grad_() for k in ("x", "gamma", "beta"))
+        if impl == "ours":
+            y = rn.layernorm(x, w, b, case.eps)
+        else:
+            y = torch.nn.functional.layer_norm(x, (case.N,), w, b, case.eps)
+        return (y,), (x, w, b), (inp["dy"],)
     inp = synth.make_inputs(case, device=str(dev))
     x = inp["x"].requires_grad_()
     w = inp["gamma"].requires_grad_()
@@ -524,10 +565,25 @@ def run_ours(args):
                           "plan": native.last_plan()})
             del p2
             torch.cuda.empty_cache()
+        from rmsnorm_backward_bwd_gb300 import synth as _synth
+        p3 = LnProblem(_synth.LN_4096, dev)
+        n3 = max(20, args.steps // 4)
+        cms, _, _ = time_calls(p3, n3, args.warmup, flush, ws)
+        _, kms3, _ = time_calls(p3, n3, 3, flush, ws, kernel_events=True)
+        t3, k3 = float(np.mean(cms)), float(np.mean(kms3))
+        extra.append({"workload": p3.case.name + " (dgamma + dbeta)",
+                      "us_per_call": round(t3 * 1e3, 2),
+                      "GBps": round(p3.bytes / (t3 * 1e-3) / 1e9, 1),
+                      "pct_of_peak": round(100 * p3.bytes / (t3 * 1e-3) / 1e9 / peak, 1),
+                      "row_pass_us": round(k3 * 1e3, 2),
+                      "row_pass_GBps": round(p3.row_pass_bytes / (k3 * 1e-3) / 1e9, 1),
+                      "plan": native.last_plan()})
+        del p3
+        torch.cuda.empty_cache()
 
     autograd = []
     if not args.no_extra:
-        for name in ("plain_4096", "fused_4096"):
+        for name in ("plain_4096", "fused_4096", "layernorm_4096"):
             c2 = workload_case(name)
             nbytes = synth_bytes(c2)
             row = {"workload": c2.name}

@@ -314,6 +314,57 @@ __device__ __forceinline__ void mul_chunk_pairs<__half>(const uint4 &d, const ui
     p[3] = mul_f16x2(d.w, g.w);
 }
 
+// x - mean for a chunk, as fp32 pairs: for 16-bit types one mixed-precision
+// FMA per element, x*1 + (-mean), rounded once -- the same value as widening
+// x and subtracting in fp32, without the unpacking.
+template <typename T>
+__device__ __forceinline__ void centre_chunk_pairs(const uint4 &x, f32x2 nmu2, float nmu, f32x2 *p);
+template <>
+__device__ __forceinline__ void centre_chunk_pairs<float>(const uint4 &x, f32x2 nmu2, float,
+                                                          f32x2 *p) {
+    chunk_pairs<float>(x, p);
+    p[0] = f2_add(p[0], nmu2);
+    p[1] = f2_add(p[1], nmu2);
+}
+__device__ __forceinline__ f32x2 centre_bf16x2(uint32_t w, float c) {
+    f32x2 d;
+    asm("{\n\t.reg .b16 xl, xh, one;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\tmov.b16 one, 0x3F80;\n\t"
+        "fma.rn.f32.bf16 lo, xl, one, %2;\n\t"
+        "fma.rn.f32.bf16 hi, xh, one, %2;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(d)
+        : "r"(w), "f"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 centre_f16x2(uint32_t w, float c) {
+    f32x2 d;
+    asm("{\n\t.reg .b16 xl, xh, one;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\tmov.b16 one, 0x3C00;\n\t"
+        "fma.rn.f32.f16 lo, xl, one, %2;\n\t"
+        "fma.rn.f32.f16 hi, xh, one, %2;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(d)
+        : "r"(w), "f"(c));
+    return d;
+}
+template <>
+__device__ __forceinline__ void centre_chunk_pairs<__nv_bfloat16>(const uint4 &x, f32x2,
+                                                                  float nmu, f32x2 *p) {
+    p[0] = centre_bf16x2(x.x, nmu);
+    p[1] = centre_bf16x2(x.y, nmu);
+    p[2] = centre_bf16x2(x.z, nmu);
+    p[3] = centre_bf16x2(x.w, nmu);
+}
+template <>
+__device__ __forceinline__ void centre_chunk_pairs<__half>(const uint4 &x, f32x2, float nmu,
+                                                           f32x2 *p) {
+    p[0] = centre_f16x2(x.x, nmu);
+    p[1] = centre_f16x2(x.y, nmu);
+    p[2] = centre_f16x2(x.z, nmu);
+    p[3] = centre_f16x2(x.w, nmu);
+}
+
 // fp32 pairs back to a 16-byte chunk of T (round to nearest even).
 template <typename T> __device__ __forceinline__ uint4 pairs_chunk(const f32x2 *p);
 template <> __device__ __forceinline__ uint4 pairs_chunk<float>(const f32x2 *p) {
@@ -363,16 +414,22 @@ __device__ __forceinline__ void ln_team_sum2(float &u, float &v, float *red, int
     v = warp_sum(b);
 }
 
-// The CTA's partial of one accumulator (a team's registers, teams combined in
-// a fixed order through shared memory, float4 q of chunk c at q*tc + c):
-// added atomically into out (atomic mode) or stored as out's row (scratch).
-// `scratch` must hold N floats and be free of other use; the caller
-// synchronises the CTA before and after.
+// The CTA's partials of dgamma and dbeta (each team's registers; with several
+// teams, combined in a fixed team order through shared memory, float4 q of
+// chunk c at q*tc + c, the dbeta copy after the dgamma one): added atomically
+// into dg / db (atomic mode) or stored there as the CTA's partial rows
+// (scratch). db may be NULL (no bias gradient). `scratch` must hold 2N floats
+// and be free of other use; the caller synchronises the CTA before.
 template <int CPT, int P, bool ATOMIC>
-__device__ __forceinline__ void ln_cta_out(const f32x2 (&acc)[CPT][P], float *out,
+__device__ __forceinline__ void ln_cta_out(const f32x2 (&accg)[CPT][P],
+                                           const f32x2 (&accb)[CPT][P], float *dg, float *db,
                                            const LnRowArgs &a, uint8_t *scratch, int team,
                                            int tt) {
     constexpr int Q = P / 2;  // float4 per chunk
+    auto put = [](float *dst4, const float4 &v) {
+        if (ATOMIC) atomicAdd(reinterpret_cast<float4 *>(dst4), v);
+        else *reinterpret_cast<float4 *>(dst4) = v;
+    };
     if (a.teams == 1) {
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
@@ -380,19 +437,34 @@ __device__ __forceinline__ void ln_cta_out(const f32x2 (&acc)[CPT][P], float *ou
             if (c < a.nchunks) {
 #pragma unroll
                 for (int q = 0; q < Q; ++q) {
+                    const size_t off = (size_t)c * (2 * P) + 4 * q;
                     float4 v;
-                    f2_split(acc[kk][2 * q], v.x, v.y);
-                    f2_split(acc[kk][2 * q + 1], v.z, v.w);
-                    float4 *dst = reinterpret_cast<float4 *>(out + (size_t)c * (2 * P) + 4 * q);
-                    if (ATOMIC) atomicAdd(dst, v);
-                    else *dst = v;
+                    f2_split(accg[kk][2 * q], v.x, v.y);
+                    f2_split(accg[kk][2 * q + 1], v.z, v.w);
+                    put(dg + off, v);
+                    if (db) {
+                        f2_split(accb[kk][2 * q], v.x, v.y);
+                        f2_split(accb[kk][2 * q + 1], v.z, v.w);
+                        put(db + off, v);
+                    }
                 }
             }
         }
         return;
     }
     const int tc = CPT * a.team_threads;
-    float4 *sdw = reinterpret_cast<float4 *>(scratch);
+    float4 *sg = reinterpret_cast<float4 *>(scratch);
+    float4 *sb = sg + (size_t)Q * tc;
+    auto acc4 = [](float4 *p, float4 v, bool add) {
+        if (add) {
+            const float4 o = *p;
+            v.x += o.x;
+            v.y += o.y;
+            v.z += o.z;
+            v.w += o.w;
+        }
+        *p = v;
+    };
     for (int t = 0; t < a.teams; ++t) {
         if (team == t) {
 #pragma unroll
@@ -401,18 +473,14 @@ __device__ __forceinline__ void ln_cta_out(const f32x2 (&acc)[CPT][P], float *ou
                 if (c < a.nchunks) {
 #pragma unroll
                     for (int q = 0; q < Q; ++q) {
-                        float4 *p = sdw + (size_t)q * tc + c;
+                        const size_t i = (size_t)q * tc + c;
                         float4 v;
-                        f2_split(acc[kk][2 * q], v.x, v.y);
-                        f2_split(acc[kk][2 * q + 1], v.z, v.w);
-                        if (t > 0) {
-                            const float4 o = *p;
-                            v.x += o.x;
-                            v.y += o.y;
-                            v.z += o.z;
-                            v.w += o.w;
-                        }
-                        *p = v;
+                        f2_split(accg[kk][2 * q], v.x, v.y);
+                        f2_split(accg[kk][2 * q + 1], v.z, v.w);
+                        acc4(sg + i, v, t > 0);
+                        f2_split(accb[kk][2 * q], v.x, v.y);
+                        f2_split(accb[kk][2 * q + 1], v.z, v.w);
+                        acc4(sb + i, v, t > 0);
                     }
                 }
             }
@@ -421,10 +489,9 @@ __device__ __forceinline__ void ln_cta_out(const f32x2 (&acc)[CPT][P], float *ou
     }
     for (int i = threadIdx.x; i < a.N / 4; i += blockDim.x) {
         const int c = i / Q, q = i - c * Q;
-        const float4 v = sdw[(size_t)q * tc + c];
-        float4 *dst = reinterpret_cast<float4 *>(out) + i;
-        if (ATOMIC) atomicAdd(dst, v);
-        else *dst = v;
+        const size_t j = (size_t)q * tc + c;
+        put(dg + 4 * (size_t)i, sg[j]);
+        if (db) put(db + 4 * (size_t)i, sb[j]);
     }
 }
 
@@ -529,14 +596,14 @@ __global__ void __launch_bounds__(kLnMaxThreads, 1) ln_bwd_row_kernel(const LnRo
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
             if (cok[kk]) {
-                f32x2 x2[P], d2[P], w[P];
+                f32x2 xc[P], d2[P], w[P];
                 const uint4 dv = ld_shared_v4(sb + tensor_bytes + kk * kk_bytes);
-                chunk_pairs<T>(ld_shared_v4(sb + kk * kk_bytes), x2);
+                centre_chunk_pairs<T>(ld_shared_v4(sb + kk * kk_bytes), nmu2, -mu, xc);
                 if (kF32) chunk_pairs<T>(dv, d2);
                 wdy(kk, dv, d2, w);
 #pragma unroll
                 for (int q = 0; q < P; ++q) {
-                    s1 = f2_fma(f2_add(x2[q], nmu2), w[q], s1);
+                    s1 = f2_fma(xc[q], w[q], s1);
                     s2 = f2_add(w[q], s2);
                 }
             }
@@ -559,16 +626,15 @@ __global__ void __launch_bounds__(kLnMaxThreads, 1) ln_bwd_row_kernel(const LnRo
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
             if (cok[kk]) {
-                f32x2 x2[P], d2[P], w[P], o2[P];
+                f32x2 xc[P], d2[P], w[P], o2[P];
                 const uint4 dv = ld_shared_v4(sb + tensor_bytes + kk * kk_bytes);
-                chunk_pairs<T>(ld_shared_v4(sb + kk * kk_bytes), x2);
+                centre_chunk_pairs<T>(ld_shared_v4(sb + kk * kk_bytes), nmu2, -mu, xc);
                 chunk_pairs<T>(dv, d2);
                 wdy(kk, dv, d2, w);
 #pragma unroll
                 for (int q = 0; q < P; ++q) {
-                    const f32x2 xc = f2_add(x2[q], nmu2);
-                    o2[q] = f2_fma(w[q], rs2, f2_fma(xc, B2, A2));
-                    accg[kk][q] = f2_fma(d2[q], f2_mul(xc, rs2), accg[kk][q]);
+                    o2[q] = f2_fma(w[q], rs2, f2_fma(xc[q], B2, A2));
+                    accg[kk][q] = f2_fma(d2[q], f2_mul(xc[q], rs2), accg[kk][q]);
                     accb[kk][q] = f2_add(d2[q], accb[kk][q]);
                 }
                 st_global_v4(dxrow + coff[kk], pairs_chunk<T>(o2));
@@ -583,11 +649,7 @@ __global__ void __launch_bounds__(kLnMaxThreads, 1) ln_bwd_row_kernel(const LnRo
     if (ATOMIC) pdl_wait();  // the zeroing kernel ahead of this one has finished
     float *dg = ATOMIC ? a.dg_out : a.dg_out + (size_t)blockIdx.x * 2 * a.N;
     float *db = ATOMIC ? a.db_out : dg + a.N;
-    ln_cta_out<CPT, P, ATOMIC>(accg, dg, a, ring, team, tt);
-    if (db) {
-        __syncthreads();  // the shared scratch is reused
-        ln_cta_out<CPT, P, ATOMIC>(accb, db, a, ring, team, tt);
-    }
+    ln_cta_out<CPT, P, ATOMIC>(accg, accb, dg, db, a, ring, team, tt);
 }
 
 template <typename T, int CPT, bool ATOMIC>
