@@ -38,7 +38,7 @@ METRIC = "µs/call and achieved HBM GB/s (% of peak), RMSNorm & fused-add bwd, 1
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "bwd_row_kernel_bf16_4096x4096.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "rmsnorm_backward_bwd_gb300", "csrc", f)
-                  for f in ("bwd_row.cu", "common.cuh")]
+                  for f in ("bwd_row.cu", "row_math.cuh", "common.cuh")]
 
 
 def kernel_source_hash():

@@ -225,7 +225,10 @@ rn_status rn_rmsnorm_bwd_noalloc(const void *x, const void *gamma, const void *d
  * to calls made after they are set; value 0 always means "automatic".
  */
 typedef enum rn_option {
-    RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (async-copy ring), 2 = generic engine */
+    RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (async-copy ring), 2 = generic engine,
+                                 3 = cluster engine (RMSNorm backward: a row split across a
+                                 thread-block cluster; chosen by default for aligned rows of
+                                 more than 2048 16-byte chunks) */
     RN_OPT_DWEIGHT_MODE = 1,  /* 1 = scratch partials + finalize (deterministic dweight),
                                  2 = fp32 atomics + cast (the default where possible: faster,
                                  summation order varies from call to call) */
@@ -233,7 +236,8 @@ typedef enum rn_option {
     RN_OPT_TEAMS_PER_CTA = 3, /* row engine: rows processed at once per CTA (1..15) */
     RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8) */
     RN_OPT_GRID = 5,          /* CTAs of the row pass (default: one per SM; at most 2 per SM) */
-    RN_OPT_COUNT = 6
+    RN_OPT_CLUSTER_SIZE = 6,  /* cluster engine: CTAs per cluster, 2, 4, 8 or 16 */
+    RN_OPT_COUNT = 7
 } rn_option;
 
 rn_status rn_set_option(int option, int value);

@@ -15,6 +15,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <string>
 #include <unordered_map>
 
 #include "../../include/rmsnorm_gb300.h"
@@ -193,6 +194,76 @@ static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
                          row_max_threads, d, plan);
 }
 
+// Cluster engine: the row split over `csize` CTAs of up to 2048 chunks each.
+// Cluster occupancy answers are cached per launch shape.
+static std::unordered_map<std::string, int> g_cluster_occ;
+
+static bool plan_cluster(const BwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
+                         ClusterPlan *plan) {
+    const int row_bytes = p.N * elem_bytes(p.dtype);
+    if (row_bytes % 16) return false;
+    if (!aligned16(p.x) || !aligned16(p.dy) || !aligned16(p.gamma) || !aligned16(p.dx) ||
+        (p.dres && !aligned16(p.dres)))
+        return false;
+    const int nchunks = row_bytes / 16;
+    if (nchunks <= kRowMaxChunks && !forced) return false;  // the row engine's range
+    int csize = g_opts[RN_OPT_CLUSTER_SIZE];
+    if (csize == 0) {
+        csize = 2;
+        while (csize < 16 && (nchunks + csize - 1) / csize > kRowMaxChunks) csize *= 2;
+    }
+    if (csize != 2 && csize != 4 && csize != 8 && csize != 16) return false;
+    const int slice = (nchunks + csize - 1) / csize;
+    if (slice > kRowMaxChunks) return false;
+    int cpt = g_opts[RN_OPT_CHUNKS_PER_THREAD];
+    if (cpt != 1 && cpt != 2 && cpt != 4) cpt = slice > 1024 ? 4 : (slice > 512 ? 2 : 1);
+    const int threads = ((slice + cpt - 1) / cpt + 31) / 32 * 32;
+    if (threads > 512) return false;
+    const int nt = p.dres ? 3 : 2;
+    const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
+    int stages = g_opts[RN_OPT_STAGES];
+    if (stages <= 0) {
+        stages = 4;
+        while (stages > 2 && cluster_smem_bytes(stages, nt, cpt, threads) > budget) --stages;
+    }
+    if (stages < 1 || stages > 8) return false;
+    const size_t smem = cluster_smem_bytes(stages, nt, cpt, threads);
+    if (smem > d.smem_optin) return false;
+    plan->csize = csize;
+    plan->slice = slice;
+    plan->cpt = cpt;
+    plan->threads = threads;
+    plan->stages = stages;
+    plan->smem = smem;
+    plan->atomic = atomic;
+
+    char key[96];
+    snprintf(key, sizeof(key), "%d/%d/%d/%d/%d/%d/%zu/%d", d.num_sms, p.dtype, cpt, (int)(p.dres != nullptr),
+             (int)atomic, csize, smem, threads);
+    int occ = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_cluster_occ.find(key);
+        if (it != g_cluster_occ.end()) occ = it->second;
+    }
+    if (occ == 0) {
+        if (cluster_max_active(p, *plan, &occ) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_cluster_occ[key] = occ;
+    }
+    int64_t clusters = occ;
+    if (clusters > p.M) clusters = p.M;
+    if (clusters > max_partial_rows(d)) clusters = max_partial_rows(d);
+    if (g_opts[RN_OPT_GRID] > 0 && clusters * csize > g_opts[RN_OPT_GRID])
+        clusters = g_opts[RN_OPT_GRID] / csize;
+    if (clusters < 1) return false;
+    plan->clusters = (int)clusters;
+    return true;
+}
+
 static void plan_generic(const BwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
@@ -238,15 +309,51 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
     const int engine = g_opts[RN_OPT_BWD_ENGINE];
     RowPlan rp;
     GenericPlan gp;
-    bool use_row = false;
-    if (engine != 2) {
+    ClusterPlan cp;
+    bool use_row = false, use_cluster = false;
+    bool atomic = want_atomic(p);
+    if (engine == 0 || engine == 1) {
         use_row = plan_row(p, d, &rp);
         if (!use_row && engine == 1)
             return fail(RN_ERR_UNSUPPORTED, "row engine cannot take N=%d dtype=%d here", p.N,
                         p.dtype);
     }
+    if (!use_row && (engine == 0 || engine == 3)) {
+        use_cluster = plan_cluster(p, d, atomic, engine == 3, &cp);
+        if (!use_cluster && engine == 3)
+            return fail(RN_ERR_UNSUPPORTED, "cluster engine cannot take N=%d dtype=%d here",
+                        p.N, p.dtype);
+    }
+    if (use_cluster) {
+        snprintf(g_plan, sizeof(g_plan),
+                 "engine=cluster csize=%d slice=%d cpt=%d threads=%d stages=%d clusters=%d "
+                 "smem=%zu dw=%s",
+                 cp.csize, cp.slice, cp.cpt, cp.threads, cp.stages, cp.clusters, cp.smem,
+                 atomic ? "atomic" : "scratch");
+        if (atomic) {
+            e = launch_zero_f32(p.dw_f32, p.N, s);
+            if (e != cudaSuccess) return cuda_fail(e, "zero launch");
+        }
+        const bool prof = g_ev_begin && g_ev_end;
+        if (prof) {
+            e = cudaEventRecord(g_ev_begin, s);
+            if (e != cudaSuccess) return cuda_fail(e, "profile event");
+        }
+        e = launch_bwd_cluster(p, cp, s, atomic);
+        if (e != cudaSuccess) return cuda_fail(e, "cluster pass launch");
+        if (prof) {
+            e = cudaEventRecord(g_ev_end, s);
+            if (e != cudaSuccess) return cuda_fail(e, "profile event");
+        }
+        if (atomic) {
+            if (p.dw_cast) e = launch_cast(p.dw_f32, p.dw_cast, p.N, p.dtype, s, !prof);
+        } else {
+            e = launch_finalize(reinterpret_cast<const float *>(p.ws + kWsHeaderBytes),
+                                cp.clusters, p.N, p.dw_f32, p.dw_cast, p.dtype, s, !prof);
+        }
+        return e == cudaSuccess ? RN_OK : cuda_fail(e, atomic ? "cast launch" : "finalize launch");
+    }
     if (!use_row) plan_generic(p, d, &gp);
-    bool atomic = want_atomic(p);
     if (!use_row && atomic && generic_smem_bytes(p.N, true) > d.smem_optin) {
         // the generic engine keeps its atomic-mode partial in shared memory
         if (g_opts[RN_OPT_DWEIGHT_MODE] == 2)

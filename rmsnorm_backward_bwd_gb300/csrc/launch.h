@@ -39,6 +39,18 @@ struct RowPlan {
     bool atomic;       // weight gradient via fp32 atomics (else scratch partials)
 };
 
+// Launch shape of the cluster engine (rows longer than one CTA's tile).
+struct ClusterPlan {
+    int csize;         // CTAs per cluster (2..16)
+    int slice;         // 16-byte chunks of a row per CTA
+    int cpt;           // chunks per thread (1, 2, 4)
+    int threads;       // threads per CTA (multiple of 32, <= 512)
+    int stages;        // async-copy ring depth per thread
+    int clusters;      // clusters launched (persistent)
+    size_t smem;       // dynamic shared memory bytes per CTA
+    bool atomic;
+};
+
 struct GenericPlan {
     int threads;       // CTA size; one row per CTA at a time
     int grid;
@@ -56,6 +68,11 @@ size_t generic_smem_bytes(int N, bool smem_dw);
 cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_t s,
                            bool pdl_after_zero);
 cudaError_t launch_bwd_generic(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
+                               bool pdl_after_zero);
+size_t cluster_smem_bytes(int stages, int ntensors, int cpt, int threads);
+// Clusters of plan's shape that fit on the device at once (occupancy query).
+cudaError_t cluster_max_active(const BwdProblem &p, const ClusterPlan &plan, int *clusters);
+cudaError_t launch_bwd_cluster(const BwdProblem &p, const ClusterPlan &plan, cudaStream_t s,
                                bool pdl_after_zero);
 // Scratch mode: dw_f32 = sum of G partial rows (fixed order), optional cast.
 cudaError_t launch_finalize(const float *partials, int G, int N, float *dw_f32, void *dw_cast,

@@ -50,7 +50,7 @@ def test_argument_checks_fail_before_any_launch():
 
 
 def test_options_round_trip():
-    for opt in range(6):
+    for opt in range(native.OPT_COUNT):
         native.set_option(opt, 3)
         assert native.get_option(opt) == 3
         native.set_option(opt, 0)

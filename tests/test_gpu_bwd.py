@@ -13,10 +13,10 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(autouse=True)
 def _reset_options():
-    for opt in range(6):
+    for opt in range(native.OPT_COUNT):
         native.set_option(opt, 0)
     yield
-    for opt in range(6):
+    for opt in range(native.OPT_COUNT):
         native.set_option(opt, 0)
 
 

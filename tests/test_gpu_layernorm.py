@@ -27,7 +27,7 @@ SHAPES = [(4096, 4096, "bf16"), (1, 4096, "bf16"), (512, 2048, "bf16"), (512, 30
 @pytest.fixture(autouse=True)
 def _default_options():
     yield
-    for opt in range(6):
+    for opt in range(native.OPT_COUNT):
         native.set_option(opt, 0)
 
 

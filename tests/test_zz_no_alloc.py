@@ -35,7 +35,7 @@ def _noalloc(x, g, dy, rstd, dx, dw32, dw):
 
 @pytest.fixture(autouse=True)
 def _default_options():
-    for opt in range(6):
+    for opt in range(native.OPT_COUNT):
         native.set_option(opt, 0)
     yield
 
