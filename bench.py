@@ -198,7 +198,8 @@ def workload_case(name):
     from rmsnorm_backward_bwd_gb300 import synth
     table = {"plain_4096": synth.PLAIN_4096, "fused_4096": synth.FUSED_4096,
              "fused_4096_nodres": synth.FUSED_4096_NODRES, "plain_16384x8192": synth.LARGE_PLAIN,
-             "fused_16384x8192": synth.LARGE_FUSED, "layernorm_4096": synth.LN_4096}
+             "fused_16384x8192": synth.LARGE_FUSED, "layernorm_4096": synth.LN_4096,
+             "plain_4096x32768": synth.LONG_ROWS}
     return table[name]
 
 
@@ -548,7 +549,8 @@ def run_ours(args):
 
     extra = []
     if not args.no_extra:
-        for name in ("fused_4096", "fused_4096_nodres", "plain_16384x8192", "fused_16384x8192"):
+        for name in ("fused_4096", "fused_4096_nodres", "plain_16384x8192", "fused_16384x8192",
+                     "plain_4096x32768"):
             if name == args.workload:
                 continue
             p2 = Problem(workload_case(name), dev)
