@@ -127,6 +127,8 @@ static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int 
     if (cpt != 1 && cpt != 2 && cpt != 4) {
         cpt = nchunks >= 512 ? 4 : (nchunks >= 64 ? 2 : 1);
         while (cpt > max_cpt) cpt /= 2;
+        // more chunks per thread when the row does not fit the capped tile
+        while (cpt < 4 && ((nchunks + cpt - 1) / cpt + 31) / 32 * 32 > max_threads(cpt)) cpt *= 2;
     }
     int team = ((nchunks + cpt - 1) / cpt + 31) / 32 * 32;
     if (team > max_threads(cpt)) return false;

@@ -248,3 +248,14 @@ def test_layernorm_autograd_matches_oracle(shape, dt, with_bias):
     parity.check_tensor("dgamma", w.grad, dg64, dt, "dweight")
     if with_bias:
         parity.check_tensor("dbeta", b.grad, db64, dt, "dweight")
+
+
+@pytest.mark.parametrize("M,N", [(48, 12288), (16, 16384)])
+def test_layernorm_rows_up_to_the_tile_limit_use_the_row_engine(M, N):
+    """Rows that do not fit the default 2-chunks-per-thread tile take 4
+    chunks per thread rather than the generic engine."""
+    ex = expected(Case("ln", M, N, "bf16", eps=1e-5, seed=13))
+    out = run_gpu(ex)
+    plan = native.last_plan()
+    assert "engine=ln_row" in plan and "cpt=4" in plan, plan
+    check(ex, out)
