@@ -663,7 +663,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="plain_4096",
                     choices=["plain_4096", "fused_4096", "fused_4096_nodres", "plain_16384x8192",
-                             "fused_16384x8192"])
+                             "fused_16384x8192", "plain_4096x32768"])
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
