@@ -1,0 +1,87 @@
+"""The backward on side streams and inside CUDA graphs.
+
+The library launches only on the caller's stream and allocates nothing; the
+binding keeps one workspace per (device, stream). So two streams may run
+backwards at once, and a call made once outside capture (first-call setup:
+device queries and kernel attributes) can then be captured into a CUDA graph
+and replayed.
+"""
+import pytest
+import torch
+
+import parity
+import rmsnorm_backward_bwd_gb300 as rn
+from rmsnorm_backward_bwd_gb300 import native
+from rmsnorm_backward_bwd_gb300.synth import Case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _reset_options():
+    for opt in range(native.OPT_COUNT):
+        native.set_option(opt, 0)
+    yield
+
+
+def _device_inputs(ex):
+    t = dict(x=ex.x.cuda(), g=ex.gamma.cuda(), dy=ex.dy.cuda(), rstd=ex.rstd.cuda())
+    if ex.case.fused and ex.dres is not None:
+        t["dres"] = ex.dres.cuda()
+    return t
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_two_streams_concurrently(mode):
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    exs = [parity.expected_bwd(Case("s%d" % i, 2048, 4096, "bf16", seed=i)) for i in range(2)]
+    ins = [_device_inputs(ex) for ex in exs]
+    streams = [torch.cuda.Stream() for _ in exs]
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(3):   # several rounds so the two streams overlap
+        outs = []
+        for st, t in zip(streams, ins):
+            with torch.cuda.stream(st):
+                outs.append(rn.rmsnorm_bwd(t["x"], t["g"], t["dy"], t["rstd"]))
+    torch.cuda.synchronize()
+    for ex, (dx, dw, dw32) in zip(exs, outs):
+        parity.check_bwd(ex, dx, dw, dw32)
+
+
+@pytest.mark.parametrize("case", [Case("graph plain", 1024, 4096, "bf16"),
+                                  Case("graph fused", 512, 3000, "f32", fused=True, with_dres=True),
+                                  Case("graph long rows", 8, 32768, "bf16")],
+                         ids=lambda c: c.name)
+@pytest.mark.parametrize("mode", [1, 2])
+def test_backward_captured_in_a_cuda_graph(case, mode):
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    ex = parity.expected_bwd(case)
+    t = _device_inputs(ex)
+    x, g, dy, rstd = t["x"], t["g"], t["dy"], t["rstd"]
+    dx = torch.empty_like(x)
+    dw32 = torch.empty(case.N, dtype=torch.float32, device="cuda")
+    dw = torch.empty(case.N, dtype=x.dtype, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ws = rn.bwd_workspace(case.M, case.N, x.dtype, x.device)
+
+        def call():
+            if case.fused:
+                rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, t.get("dres"), dx=dx, dweight_f32=dw32,
+                                         dweight=dw, workspace=ws)
+            else:
+                rn.rmsnorm_bwd(x, g, dy, rstd, dx=dx, dweight_f32=dw32, dweight=dw, workspace=ws)
+        call()   # first call outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        call()
+    for buf in (dx, dw32, dw):
+        buf.fill_(7)          # replays must rewrite every output
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    parity.check_bwd(ex, dx, dw, dw32)
