@@ -200,14 +200,11 @@ static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
 // Cluster occupancy answers are cached per launch shape.
 static std::unordered_map<std::string, int> g_cluster_occ;
 
-static bool plan_cluster(const BwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
+// Cluster size, slice, tile and ring depth for rows of `nchunks` chunks and
+// `nt` streamed tensors (the occupancy-dependent cluster count is left out).
+static bool cluster_tile(int nchunks, int nt, bool forced, const DeviceInfo &d,
+                         size_t (*smem_bytes)(int stages, int nt, int cpt, int threads),
                          ClusterPlan *plan) {
-    const int row_bytes = p.N * elem_bytes(p.dtype);
-    if (row_bytes % 16) return false;
-    if (!aligned16(p.x) || !aligned16(p.dy) || !aligned16(p.gamma) || !aligned16(p.dx) ||
-        (p.dres && !aligned16(p.dres)))
-        return false;
-    const int nchunks = row_bytes / 16;
     if (nchunks <= kRowMaxChunks && !forced) return false;  // the row engine's range
     int csize = g_opts[RN_OPT_CLUSTER_SIZE];
     if (csize == 0) {
@@ -221,15 +218,14 @@ static bool plan_cluster(const BwdProblem &p, const DeviceInfo &d, bool atomic, 
     if (cpt != 1 && cpt != 2 && cpt != 4) cpt = slice > 1024 ? 4 : (slice > 512 ? 2 : 1);
     const int threads = ((slice + cpt - 1) / cpt + 31) / 32 * 32;
     if (threads > 512) return false;
-    const int nt = p.dres ? 3 : 2;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
     int stages = g_opts[RN_OPT_STAGES];
     if (stages <= 0) {
         stages = 4;
-        while (stages > 2 && cluster_smem_bytes(stages, nt, cpt, threads) > budget) --stages;
+        while (stages > 2 && smem_bytes(stages, nt, cpt, threads) > budget) --stages;
     }
     if (stages < 1 || stages > 8) return false;
-    const size_t smem = cluster_smem_bytes(stages, nt, cpt, threads);
+    const size_t smem = smem_bytes(stages, nt, cpt, threads);
     if (smem > d.smem_optin) return false;
     plan->csize = csize;
     plan->slice = slice;
@@ -237,11 +233,18 @@ static bool plan_cluster(const BwdProblem &p, const DeviceInfo &d, bool atomic, 
     plan->threads = threads;
     plan->stages = stages;
     plan->smem = smem;
-    plan->atomic = atomic;
+    return true;
+}
 
-    char key[96];
-    snprintf(key, sizeof(key), "%d/%d/%d/%d/%d/%d/%zu/%d", d.num_sms, p.dtype, cpt, (int)(p.dres != nullptr),
-             (int)atomic, csize, smem, threads);
+// The persistent cluster count: what fits at once (queried once per launch
+// shape and cached), at most one cluster per row and the workspace's rows.
+static bool cluster_count(const char *kind, int64_t M, int dtype, bool dres, const DeviceInfo &d,
+                          ClusterPlan *plan, cudaError_t (*query)(const void *ctx,
+                                                                 const ClusterPlan &, int *),
+                          const void *ctx) {
+    char key[128];
+    snprintf(key, sizeof(key), "%s/%d/%d/%d/%d/%d/%d/%zu/%d", kind, d.num_sms, dtype, plan->cpt,
+             (int)dres, (int)plan->atomic, plan->csize, plan->smem, plan->threads);
     int occ = 0;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -249,7 +252,7 @@ static bool plan_cluster(const BwdProblem &p, const DeviceInfo &d, bool atomic, 
         if (it != g_cluster_occ.end()) occ = it->second;
     }
     if (occ == 0) {
-        if (cluster_max_active(p, *plan, &occ) != cudaSuccess) {
+        if (query(ctx, *plan, &occ) != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
@@ -257,13 +260,34 @@ static bool plan_cluster(const BwdProblem &p, const DeviceInfo &d, bool atomic, 
         g_cluster_occ[key] = occ;
     }
     int64_t clusters = occ;
-    if (clusters > p.M) clusters = p.M;
+    if (clusters > M) clusters = M;
     if (clusters > max_partial_rows(d)) clusters = max_partial_rows(d);
-    if (g_opts[RN_OPT_GRID] > 0 && clusters * csize > g_opts[RN_OPT_GRID])
-        clusters = g_opts[RN_OPT_GRID] / csize;
+    if (g_opts[RN_OPT_GRID] > 0 && clusters * plan->csize > g_opts[RN_OPT_GRID])
+        clusters = g_opts[RN_OPT_GRID] / plan->csize;
     if (clusters < 1) return false;
     plan->clusters = (int)clusters;
     return true;
+}
+
+static size_t rms_cluster_smem(int stages, int nt, int cpt, int threads) {
+    return cluster_smem_bytes(stages, nt, cpt, threads);
+}
+
+static cudaError_t rms_cluster_query(const void *ctx, const ClusterPlan &plan, int *n) {
+    return cluster_max_active(*static_cast<const BwdProblem *>(ctx), plan, n);
+}
+
+static bool plan_cluster(const BwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
+                         ClusterPlan *plan) {
+    const int row_bytes = p.N * elem_bytes(p.dtype);
+    if (row_bytes % 16) return false;
+    if (!aligned16(p.x) || !aligned16(p.dy) || !aligned16(p.gamma) || !aligned16(p.dx) ||
+        (p.dres && !aligned16(p.dres)))
+        return false;
+    if (!cluster_tile(row_bytes / 16, p.dres ? 3 : 2, forced, d, rms_cluster_smem, plan))
+        return false;
+    plan->atomic = atomic;
+    return cluster_count("rms", p.M, p.dtype, p.dres != nullptr, d, plan, rms_cluster_query, &p);
 }
 
 static void plan_generic(const BwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
@@ -419,6 +443,25 @@ static bool plan_ln_row(const LnBwdProblem &p, const DeviceInfo &d, RowPlan *pla
                          ln_row_max_threads, d, plan);
 }
 
+static size_t ln_cluster_smem(int stages, int, int cpt, int threads) {
+    return ln_cluster_smem_bytes(stages, cpt, threads);
+}
+
+static cudaError_t ln_cluster_query(const void *ctx, const ClusterPlan &plan, int *n) {
+    return ln_cluster_max_active(*static_cast<const LnBwdProblem *>(ctx), plan, n);
+}
+
+static bool plan_ln_cluster(const LnBwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
+                            ClusterPlan *plan) {
+    const int row_bytes = p.N * elem_bytes(p.dtype);
+    if (row_bytes % 16) return false;
+    if (!aligned16(p.x) || !aligned16(p.dy) || !aligned16(p.gamma) || !aligned16(p.dx))
+        return false;
+    if (!cluster_tile(row_bytes / 16, 2, forced, d, ln_cluster_smem, plan)) return false;
+    plan->atomic = atomic;
+    return cluster_count("ln", p.M, p.dtype, false, d, plan, ln_cluster_query, &p);
+}
+
 static void plan_ln_generic(const LnBwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
@@ -454,16 +497,53 @@ static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t
     const int engine = g_opts[RN_OPT_BWD_ENGINE];
     RowPlan rp;
     GenericPlan gp;
-    bool use_row = false;
-    if (engine != 2) {
+    ClusterPlan cp;
+    bool use_row = false, use_cluster = false;
+    bool atomic = g_opts[RN_OPT_DWEIGHT_MODE] != 1 && aligned16(p.dg_f32) &&
+                  (p.db_f32 == nullptr || aligned16(p.db_f32));
+    if (engine == 0 || engine == 1) {
         use_row = plan_ln_row(p, d, &rp);
         if (!use_row && engine == 1)
             return fail(RN_ERR_UNSUPPORTED, "row engine cannot take N=%d dtype=%d here", p.N,
                         p.dtype);
     }
+    if (!use_row && (engine == 0 || engine == 3)) {
+        use_cluster = plan_ln_cluster(p, d, atomic, engine == 3, &cp);
+        if (!use_cluster && engine == 3)
+            return fail(RN_ERR_UNSUPPORTED, "cluster engine cannot take N=%d dtype=%d here",
+                        p.N, p.dtype);
+    }
+    if (use_cluster) {
+        snprintf(g_plan, sizeof(g_plan),
+                 "engine=ln_cluster csize=%d slice=%d cpt=%d threads=%d stages=%d clusters=%d "
+                 "smem=%zu dw=%s",
+                 cp.csize, cp.slice, cp.cpt, cp.threads, cp.stages, cp.clusters, cp.smem,
+                 atomic ? "atomic" : "scratch");
+        if (atomic) {
+            e = launch_zero_f32(p.dg_f32, p.N, s, p.db_f32);
+            if (e != cudaSuccess) return cuda_fail(e, "zero launch");
+        }
+        const bool prof = g_ev_begin && g_ev_end;
+        if (prof) {
+            e = cudaEventRecord(g_ev_begin, s);
+            if (e != cudaSuccess) return cuda_fail(e, "profile event");
+        }
+        e = launch_ln_bwd_cluster(p, cp, s, atomic);
+        if (e != cudaSuccess) return cuda_fail(e, "cluster pass launch");
+        if (prof) {
+            e = cudaEventRecord(g_ev_end, s);
+            if (e != cudaSuccess) return cuda_fail(e, "profile event");
+        }
+        if (atomic) {
+            if (p.dg_cast || p.db_cast)
+                e = launch_cast(p.dg_f32, p.dg_cast, p.N, p.dtype, s, !prof, p.db_f32, p.db_cast);
+        } else {
+            e = launch_finalize2(partials, cp.clusters, 2 * p.N, p.N, p.dg_f32, p.dg_cast,
+                                 p.db_f32, p.db_cast, p.dtype, s, !prof);
+        }
+        return e == cudaSuccess ? RN_OK : cuda_fail(e, atomic ? "cast launch" : "finalize launch");
+    }
     if (!use_row) plan_ln_generic(p, d, &gp);
-    bool atomic = g_opts[RN_OPT_DWEIGHT_MODE] != 1 && aligned16(p.dg_f32) &&
-                  (p.db_f32 == nullptr || aligned16(p.db_f32));
     if (!use_row && atomic && ln_generic_smem_bytes(p.N, true) > d.smem_optin) {
         // the generic engine keeps its atomic-mode partials in shared memory
         if (g_opts[RN_OPT_DWEIGHT_MODE] == 2)

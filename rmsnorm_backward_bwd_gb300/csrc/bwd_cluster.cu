@@ -24,6 +24,7 @@
 //     (scratch: one partial row per cluster; atomic: fp32 vector atomics).
 //   * A last cluster barrier keeps every CTA alive until its peers have read
 //     its partial slots.
+#include "cluster.cuh"
 #include "common.cuh"
 #include "launch.h"
 #include "row_math.cuh"
@@ -52,41 +53,6 @@ struct ClusterArgs {
     int stages;
     float inv_n;
 };
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_count_x() {
-    uint32_t n;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(n));
-    return n;
-}
-__device__ __forceinline__ uint32_t cluster_index_x() {
-    uint32_t i;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(i));
-    return i;
-}
-__device__ __forceinline__ uint32_t cluster_size_x() {
-    uint32_t n;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-    return n;
-}
-// Every thread of every CTA of the cluster arrives; shared-memory writes
-// before it are visible to the cluster after it.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile(
-        "barrier.cluster.arrive.release.aligned;\n\t"
-        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote;
-    float v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
 
 template <typename T, int CPT, bool HAS_DRES, bool ATOMIC>
 __global__ void __launch_bounds__(512, 1) bwd_cluster_kernel(const ClusterArgs a) {

@@ -144,6 +144,10 @@ cudaError_t launch_ln_bwd_row(const LnBwdProblem &p, const RowPlan &plan, cudaSt
                               bool pdl_after_zero);
 cudaError_t launch_ln_bwd_generic(const LnBwdProblem &p, const GenericPlan &plan,
                                   cudaStream_t s, bool pdl_after_zero);
+size_t ln_cluster_smem_bytes(int stages, int cpt, int threads);
+cudaError_t ln_cluster_max_active(const LnBwdProblem &p, const ClusterPlan &plan, int *clusters);
+cudaError_t launch_ln_bwd_cluster(const LnBwdProblem &p, const ClusterPlan &plan, cudaStream_t s,
+                                  bool pdl_after_zero);
 
 // Replace the calling thread's message returned by rn_last_error().
 void set_last_error(const char *msg);

@@ -23,9 +23,14 @@
 //     their partials in a fixed order in shared memory and the CTA adds them
 //     with fp32 vector atomics (atomic mode) or stores one partial row of
 //     [dgamma | dbeta] to the workspace for the finalize kernel (scratch mode).
+//   * backward, aligned rows longer than one CTA's tile: the cluster engine
+//     of the RMSNorm backward (a row split across a thread-block cluster, the
+//     two row sums exchanged through distributed shared memory behind one
+//     cluster barrier per row), with the LayerNorm arithmetic.
 //   * backward, unaligned rows: one CTA per row, scalar, two passes; the
 //     partials live in shared memory when 2N floats fit, else in the CTA's
 //     workspace row.
+#include "cluster.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -716,6 +721,343 @@ cudaError_t launch_ln_bwd_row(const LnBwdProblem &p, const RowPlan &plan, cudaSt
     case kF32: return launch_ln_row_dt<float>(a, plan, s, pdl_after_zero);
     case kF16: return launch_ln_row_dt<__half>(a, plan, s, pdl_after_zero);
     case kBF16: return launch_ln_row_dt<__nv_bfloat16>(a, plan, s, pdl_after_zero);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// -------------------------------------------------- backward, cluster engine
+// [2 parities][2 sums][16 warps] fp32 warp sums, then the ring
+constexpr int kLnClusterRingOffset = 512;
+
+size_t ln_cluster_smem_bytes(int stages, int cpt, int threads) {
+    return (size_t)kLnClusterRingOffset + (size_t)stages * 2 * cpt * threads * 16;
+}
+
+struct LnClusterArgs {
+    const uint8_t *x;
+    const uint8_t *gamma;
+    const uint8_t *dy;
+    const float *mean;
+    const float *rstd;
+    uint8_t *dx;
+    // atomic: dgamma_f32 / dbeta_f32 (dbeta nullable);
+    // scratch: partial rows [clusters][2N], dgamma then dbeta
+    float *dg_out;
+    float *db_out;
+    int64_t M;
+    int N;
+    int nchunks;
+    int row_bytes;
+    int slice;  // chunks per CTA slice
+    int stages;
+    float inv_n;
+};
+
+template <typename T, int CPT, bool ATOMIC>
+__global__ void __launch_bounds__(512, 1) ln_bwd_cluster_kernel(const LnClusterArgs a) {
+    constexpr int V = Traits<T>::kVec;
+    constexpr int P = V / 2;
+    constexpr int Q = P / 2;  // float4 per chunk
+    constexpr bool kF32 = sizeof(T) == 4;
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *red = reinterpret_cast<float *>(smem);
+    uint8_t *ring = smem + kLnClusterRingOffset;
+
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    const uint32_t crank = cluster_rank();
+    const int csize = (int)cluster_size_x();
+    const int64_t cid = cluster_index_x();
+    const int64_t ncl = cluster_count_x();
+    const int S = a.stages;
+
+    const int c0 = (int)crank * a.slice;
+    int c1 = c0 + a.slice;
+    if (c1 > a.nchunks) c1 = a.nchunks;
+
+    const uint32_t kk_bytes = 16u * nthr;
+    const uint32_t tensor_bytes = kk_bytes * CPT;
+    const uint32_t slot_bytes = 2 * tensor_bytes;
+    const uint32_t my0 = smem_addr(ring) + 16u * tid;
+    const uint32_t red_addr = smem_addr(red);
+
+    const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
+    const uint64_t policy = l2_policy_evict_first();
+
+    uint32_t coff[CPT];
+    bool cok[CPT];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        const int c = c0 + tid + kk * nthr;
+        coff[kk] = 16u * c;
+        cok[kk] = c < c1;
+    }
+
+    auto issue = [&](int64_t row, int s) {
+        const size_t off = (size_t)row * a.row_bytes;
+        const uint8_t *xr = a.x + off, *dr = a.dy + off;
+        const uint32_t d = my0 + (uint32_t)s * slot_bytes;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            if (cok[kk]) {
+                cp_async16(d + kk * kk_bytes, xr + coff[kk], policy);
+                cp_async16(d + tensor_bytes + kk * kk_bytes, dr + coff[kk], policy);
+            }
+        }
+    };
+    for (int j = 0; j < S - 1; ++j) {
+        if (j < nrows) issue(cid + j * ncl, j);
+        cp_async_commit();
+    }
+
+    uint4 gp[CPT];
+    f32x2 g2[kF32 ? CPT : 1][kF32 ? P : 1];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        gp[kk] = cok[kk] ? ld_global_nc_v4(a.gamma + coff[kk]) : make_uint4(0, 0, 0, 0);
+        if (kF32) chunk_pairs<T>(gp[kk], g2[kF32 ? kk : 0]);
+    }
+    auto wdy = [&](int kk, const uint4 &dv, const f32x2 *d2, f32x2 *w) {
+        if (kF32) {
+#pragma unroll
+            for (int q = 0; q < P; ++q) w[q] = f2_mul(d2[q], g2[kF32 ? kk : 0][kF32 ? q : 0]);
+        } else {
+            mul_chunk_pairs<T>(dv, gp[kk], w);
+        }
+    };
+    f32x2 accg[CPT][P], accb[CPT][P];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk)
+#pragma unroll
+        for (int q = 0; q < P; ++q) accg[kk][q] = accb[kk][q] = f2_make(0.f, 0.f);
+
+    const int64_t ahead = (int64_t)(S - 1) * ncl;
+    const int nparts = csize * nwarps;  // <= 16 x 16
+    float mu_next = nrows > 0 ? __ldg(a.mean + cid) : 0.f;
+    float rs_next = nrows > 0 ? __ldg(a.rstd + cid) : 0.f;
+    int slot = 0, fill = S - 1;
+    int64_t row = cid;
+    for (int64_t k = 0; k < nrows; ++k, row += ncl) {
+        if (k + S - 1 < nrows) issue(row + ahead, fill);
+        cp_async_commit();
+        const float mu = mu_next, rs = rs_next;
+        if (k + 1 < nrows) {
+            mu_next = __ldg(a.mean + row + ncl);
+            rs_next = __ldg(a.rstd + row + ncl);
+        }
+        cp_async_wait_pending(S - 1);
+        const uint32_t sb = my0 + (uint32_t)slot * slot_bytes;
+        const f32x2 nmu2 = f2_make(-mu, -mu);
+
+        // pass 1: this thread's share of sum (x - mean)*wdy and sum wdy
+        f32x2 s1 = f2_make(0.f, 0.f), s2 = f2_make(0.f, 0.f);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            if (cok[kk]) {
+                f32x2 xc[P], d2[P], w[P];
+                const uint4 dv = ld_shared_v4(sb + tensor_bytes + kk * kk_bytes);
+                centre_chunk_pairs<T>(ld_shared_v4(sb + kk * kk_bytes), nmu2, -mu, xc);
+                if (kF32) chunk_pairs<T>(dv, d2);
+                wdy(kk, dv, d2, w);
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    s1 = f2_fma(xc[q], w[q], s1);
+                    s2 = f2_add(w[q], s2);
+                }
+            }
+        }
+        float u, v, uh, vh;
+        f2_split(s1, u, uh);
+        f2_split(s2, v, vh);
+        u = warp_sum(u + uh);
+        v = warp_sum(v + vh);
+        const int par = (int)(k & 1) * 32;
+        if (lane == 0) {
+            red[par + warp] = u;
+            red[par + 16 + warp] = v;
+        }
+        cluster_sync_all();
+        // lane l reads partial l of the cluster's C x warps partials
+        float tu = 0.f, tv = 0.f;
+        for (int i = lane; i < nparts; i += 32) {
+            const int r = i / nwarps, w = i - r * nwarps;
+            tu += ld_peer_f32(red_addr + 4u * (par + w), (uint32_t)r);
+            tv += ld_peer_f32(red_addr + 4u * (par + 16 + w), (uint32_t)r);
+        }
+        u = warp_sum(tu);
+        v = warp_sum(tv);
+
+        const float c1v = rs * u * a.inv_n;
+        const float c2 = v * a.inv_n;
+        const float B = -rs * rs * c1v, A = -c2 * rs;
+        const f32x2 rs2 = f2_make(rs, rs), B2 = f2_make(B, B), A2 = f2_make(A, A);
+        uint8_t *dxrow = a.dx + (size_t)row * a.row_bytes;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            if (cok[kk]) {
+                f32x2 xc[P], d2[P], w[P], o2[P];
+                const uint4 dv = ld_shared_v4(sb + tensor_bytes + kk * kk_bytes);
+                centre_chunk_pairs<T>(ld_shared_v4(sb + kk * kk_bytes), nmu2, -mu, xc);
+                chunk_pairs<T>(dv, d2);
+                wdy(kk, dv, d2, w);
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    o2[q] = f2_fma(w[q], rs2, f2_fma(xc[q], B2, A2));
+                    accg[kk][q] = f2_fma(d2[q], f2_mul(xc[q], rs2), accg[kk][q]);
+                    accb[kk][q] = f2_add(d2[q], accb[kk][q]);
+                }
+                st_global_v4(dxrow + coff[kk], pairs_chunk<T>(o2));
+            }
+        }
+        if (++slot == S) slot = 0;
+        if (++fill == S) fill = 0;
+    }
+    // peers may still read this CTA's partial slots of the last row
+    cluster_sync_all();
+
+    pdl_launch_dependents();
+    if (ATOMIC) pdl_wait();  // the zeroing kernel ahead of this one has finished
+    float *dg = ATOMIC ? a.dg_out : a.dg_out + (size_t)cid * 2 * a.N;
+    float *db = ATOMIC ? a.db_out : dg + a.N;
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        if (cok[kk]) {
+            const int c = c0 + tid + kk * nthr;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const size_t off = (size_t)c * V + 4 * q;
+                float4 vg, vb;
+                f2_split(accg[kk][2 * q], vg.x, vg.y);
+                f2_split(accg[kk][2 * q + 1], vg.z, vg.w);
+                f2_split(accb[kk][2 * q], vb.x, vb.y);
+                f2_split(accb[kk][2 * q + 1], vb.z, vb.w);
+                if (ATOMIC) {
+                    atomicAdd(reinterpret_cast<float4 *>(dg + off), vg);
+                    if (db) atomicAdd(reinterpret_cast<float4 *>(db + off), vb);
+                } else {
+                    *reinterpret_cast<float4 *>(dg + off) = vg;
+                    *reinterpret_cast<float4 *>(db + off) = vb;
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int CPT, bool ATOMIC>
+static const void *ln_cluster_ptr() {
+    return (const void *)ln_bwd_cluster_kernel<T, CPT, ATOMIC>;
+}
+
+template <typename T>
+static const void *ln_cluster_kernel_for(int cpt, bool atomic) {
+    if (cpt == 1) return atomic ? ln_cluster_ptr<T, 1, true>() : ln_cluster_ptr<T, 1, false>();
+    if (cpt == 2) return atomic ? ln_cluster_ptr<T, 2, true>() : ln_cluster_ptr<T, 2, false>();
+    return atomic ? ln_cluster_ptr<T, 4, true>() : ln_cluster_ptr<T, 4, false>();
+}
+
+static const void *ln_cluster_kernel_dt(int dtype, int cpt, bool atomic) {
+    switch (dtype) {
+    case kF32: return ln_cluster_kernel_for<float>(cpt, atomic);
+    case kF16: return ln_cluster_kernel_for<__half>(cpt, atomic);
+    case kBF16: return ln_cluster_kernel_for<__nv_bfloat16>(cpt, atomic);
+    default: return nullptr;
+    }
+}
+
+static cudaError_t ln_cluster_prepare(const void *kern, const ClusterPlan &plan) {
+    cudaError_t e = ensure_smem_attr(kern, plan.smem);
+    if (e != cudaSuccess) return e;
+    if (plan.csize > 8)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+cudaError_t ln_cluster_max_active(const LnBwdProblem &p, const ClusterPlan &plan, int *clusters) {
+    const void *kern = ln_cluster_kernel_dt(p.dtype, plan.cpt, plan.atomic);
+    if (!kern) return cudaErrorInvalidValue;
+    cudaError_t e = ln_cluster_prepare(kern, plan);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.csize);
+    cfg.blockDim = dim3(plan.threads);
+    cfg.dynamicSmemBytes = plan.smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = plan.csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
+}
+
+template <typename T, int CPT, bool ATOMIC>
+static cudaError_t launch_ln_cluster_t(const LnClusterArgs &args, const ClusterPlan &plan,
+                                       cudaStream_t s, bool pdl) {
+    auto kern = ln_bwd_cluster_kernel<T, CPT, ATOMIC>;
+    cudaError_t e = ln_cluster_prepare((const void *)kern, plan);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.clusters * plan.csize);
+    cfg.blockDim = dim3(plan.threads);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = plan.csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+template <typename T>
+static cudaError_t launch_ln_cluster_dt(const LnClusterArgs &args, const ClusterPlan &plan,
+                                        cudaStream_t s, bool pdl) {
+    switch (plan.cpt) {
+    case 1:
+        return plan.atomic ? launch_ln_cluster_t<T, 1, true>(args, plan, s, pdl)
+                           : launch_ln_cluster_t<T, 1, false>(args, plan, s, pdl);
+    case 2:
+        return plan.atomic ? launch_ln_cluster_t<T, 2, true>(args, plan, s, pdl)
+                           : launch_ln_cluster_t<T, 2, false>(args, plan, s, pdl);
+    case 4:
+        return plan.atomic ? launch_ln_cluster_t<T, 4, true>(args, plan, s, pdl)
+                           : launch_ln_cluster_t<T, 4, false>(args, plan, s, pdl);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_ln_bwd_cluster(const LnBwdProblem &p, const ClusterPlan &plan, cudaStream_t s,
+                                  bool pdl_after_zero) {
+    LnClusterArgs a;
+    a.x = static_cast<const uint8_t *>(p.x);
+    a.gamma = static_cast<const uint8_t *>(p.gamma);
+    a.dy = static_cast<const uint8_t *>(p.dy);
+    a.mean = p.mean;
+    a.rstd = p.rstd;
+    a.dx = static_cast<uint8_t *>(p.dx);
+    if (plan.atomic) {
+        a.dg_out = p.dg_f32;
+        a.db_out = p.db_f32;
+    } else {
+        a.dg_out = reinterpret_cast<float *>(p.ws + kWsHeaderBytes);
+        a.db_out = nullptr;  // the kernel derives the dbeta half of each partial row
+    }
+    a.M = p.M;
+    a.N = p.N;
+    a.row_bytes = p.N * elem_bytes(p.dtype);
+    a.nchunks = a.row_bytes / 16;
+    a.slice = plan.slice;
+    a.stages = plan.stages;
+    a.inv_n = 1.0f / (float)p.N;
+    switch (p.dtype) {
+    case kF32: return launch_ln_cluster_dt<float>(a, plan, s, pdl_after_zero);
+    case kF16: return launch_ln_cluster_dt<__half>(a, plan, s, pdl_after_zero);
+    case kBF16: return launch_ln_cluster_dt<__nv_bfloat16>(a, plan, s, pdl_after_zero);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -259,3 +259,40 @@ def test_layernorm_rows_up_to_the_tile_limit_use_the_row_engine(M, N):
     plan = native.last_plan()
     assert "engine=ln_row" in plan and "cpt=4" in plan, plan
     check(ex, out)
+
+
+@pytest.mark.parametrize("M,N,dt,csize", [(24, 32768, "bf16", 2), (6, 65536, "bf16", 4),
+                                          (40, 16392, "bf16", 2), (16, 16384, "f32", 2),
+                                          (3, 131072, "f16", 8)],
+                         ids=lambda v: str(v))
+def test_layernorm_long_rows_take_the_cluster_engine(M, N, dt, csize):
+    ex = expected(Case("ln", M, N, dt, eps=1e-5, seed=14))
+    out = run_gpu(ex)
+    plan = native.last_plan()
+    assert "engine=ln_cluster" in plan and "csize=%d" % csize in plan, plan
+    check(ex, out, tag=" [%s]" % plan)
+
+
+@pytest.mark.parametrize("csize", [2, 4, 8, 16])
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("with_dbeta", [True, False])
+def test_layernorm_forced_cluster_sizes(csize, mode, with_dbeta):
+    native.set_option(native.OPT_BWD_ENGINE, 3)
+    native.set_option(native.OPT_CLUSTER_SIZE, csize)
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    ex = expected(Case("ln", 300, 4096, "bf16", eps=1e-5, seed=15 + csize))
+    out = run_gpu(ex, with_dbeta=with_dbeta)
+    plan = native.last_plan()
+    assert "ln_cluster" in plan and "csize=%d" % csize in plan, plan
+    check(ex, out, with_dbeta=with_dbeta, tag=" [%s]" % plan)
+
+
+def test_layernorm_cluster_scratch_mode_is_repeatable():
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)
+    ex = expected(Case("ln", 100, 32768, "bf16", eps=1e-5, seed=16))
+    a = run_gpu(ex)
+    b = run_gpu(ex)
+    assert "ln_cluster" in native.last_plan()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    check(ex, a)
