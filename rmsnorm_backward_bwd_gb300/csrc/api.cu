@@ -118,12 +118,15 @@ static size_t ws_bytes_for(const DeviceInfo &d, int64_t N) {
 // `nt` streamed tensors; `red_bytes` of shared memory precede the ring and
 // `max_cpt` caps the default chunks per thread.
 static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int max_cpt,
-                          int (*max_threads)(int cpt), const DeviceInfo &d, RowPlan *plan) {
+                          int (*max_threads)(int cpt), const DeviceInfo &d, RowPlan *plan,
+                          bool use_options = true) {
     if (nchunks > kRowMaxChunks) return false;
+    // RN_OPT_* shape the backward only
+    auto opt = [&](int o) { return use_options ? g_opts[o] : 0; };
 
     // Tile (measured on GB300): 4 chunks per thread for rows of 512+ chunks
     // (bf16 N >= 4096), else 2, else 1 for very short rows.
-    int cpt = g_opts[RN_OPT_CHUNKS_PER_THREAD];
+    int cpt = opt(RN_OPT_CHUNKS_PER_THREAD);
     if (cpt != 1 && cpt != 2 && cpt != 4) {
         cpt = nchunks >= 512 ? 4 : (nchunks >= 64 ? 2 : 1);
         while (cpt > max_cpt) cpt /= 2;
@@ -139,7 +142,7 @@ static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int 
     auto smem_for = [&](int teams_, int stages_) {
         return red_bytes + (size_t)teams_ * stages_ * stage;
     };
-    int teams = g_opts[RN_OPT_TEAMS_PER_CTA];
+    int teams = opt(RN_OPT_TEAMS_PER_CTA);
     if (teams <= 0) {
         teams = max_threads(cpt) / team;
         if (teams > 15) teams = 15;
@@ -153,7 +156,7 @@ static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int 
     if (teams < 1 || teams > 15 || teams * team > max_threads(cpt)) return false;
 
     // one CTA per SM unless the grid option asks for another count
-    int64_t cap = g_opts[RN_OPT_GRID] > 0 ? g_opts[RN_OPT_GRID] : d.num_sms;
+    int64_t cap = opt(RN_OPT_GRID) > 0 ? opt(RN_OPT_GRID) : d.num_sms;
     if (cap > max_partial_rows(d)) cap = max_partial_rows(d);
     int64_t grid = (M + teams - 1) / teams;
     if (grid > cap) grid = cap;
@@ -162,10 +165,17 @@ static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int 
     // A shallow ring (one row in flight per thread) measured best: the
     // first rows arrive sooner and more teams fit; a team that is alone on
     // its SM gets one row more.
-    int stages = g_opts[RN_OPT_STAGES];
+    int stages = opt(RN_OPT_STAGES);
     if (stages <= 0) {
         stages = (int)((budget - red_bytes) / (stage * teams));
-        const int want = teams >= 2 ? 2 : 3;
+        int want = teams >= 2 ? 2 : 3;
+        if (!use_options) {
+            // the forwards stream one or two tensors a row: about 64 KB a CTA in flight
+            const size_t per = stage * teams;
+            want = 1 + (int)((65536 + per - 1) / per);
+            if (want < 2) want = 2;
+            if (want > 8) want = 8;
+        }
         if (stages > want) stages = want;
         const int64_t rows_per_team = (M + grid * teams - 1) / (grid * teams);
         if (stages > rows_per_team) stages = (int)(rows_per_team < 1 ? 1 : rows_per_team);
@@ -657,9 +667,30 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
     p.N = (int)N;
     p.dtype = dtype;
     const int eb = elem_bytes(dtype);
-    bool vec = ((N * eb) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y) &&
-               (!fused || (aligned16(residual) && aligned16(residual_out)));
-    e = launch_fwd(p, vec, d.num_sms, static_cast<cudaStream_t>(stream));
+    const bool vec = ((N * eb) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y) &&
+                     (!fused || (aligned16(residual) && aligned16(residual_out)));
+    RowPlan rp;
+    const int nt = fused ? 2 : 1;
+    if (vec && plan_row_tile(M, (int)(N * eb / 16), nt, fwd_row_smem_bytes(0, 0, nt, 0), 4,
+                             row_max_threads, d, &rp, false)) {
+        FwdRowProblem q;
+        q.mode = fused ? kFwdFused : kFwdRms;
+        q.x = x;
+        q.residual = fused ? residual : nullptr;
+        q.gamma = gamma;
+        q.beta = nullptr;
+        q.y = y;
+        q.residual_out = fused ? residual_out : nullptr;
+        q.mean = nullptr;
+        q.rstd = rstd;
+        q.eps = eps;
+        q.M = M;
+        q.N = (int)N;
+        q.dtype = dtype;
+        e = launch_fwd_row(q, rp, static_cast<cudaStream_t>(stream));
+    } else {
+        e = launch_fwd(p, d.num_sms, static_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
 }
 
@@ -690,7 +721,27 @@ static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta
     const int eb = elem_bytes(dtype);
     const bool vec = ((N * eb) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y) &&
                      (!beta || aligned16(beta));
-    e = launch_ln_fwd(p, vec, d.num_sms, static_cast<cudaStream_t>(stream));
+    RowPlan rp;
+    if (vec && plan_row_tile(M, (int)(N * eb / 16), 1, fwd_row_smem_bytes(0, 0, 1, 0), 4,
+                             row_max_threads, d, &rp, false)) {
+        FwdRowProblem q;
+        q.mode = kFwdLn;
+        q.x = x;
+        q.residual = nullptr;
+        q.gamma = gamma;
+        q.beta = beta;
+        q.y = y;
+        q.residual_out = nullptr;
+        q.mean = mean;
+        q.rstd = rstd;
+        q.eps = eps;
+        q.M = M;
+        q.N = (int)N;
+        q.dtype = dtype;
+        e = launch_fwd_row(q, rp, static_cast<cudaStream_t>(stream));
+    } else {
+        e = launch_ln_fwd(p, d.num_sms, static_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
 }
 

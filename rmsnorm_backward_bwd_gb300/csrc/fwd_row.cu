@@ -1,0 +1,288 @@
+// Forward row engine for aligned rows: RMSNorm, fused-add RMSNorm and
+// LayerNorm forwards, each saving the statistics the backward consumes.
+//
+//   RMSNorm (FlyDSL issue #769, "Current state"; PR #800 commit message,
+//   store_rstd): rstd = 1/sqrt(mean_j x_j^2 + eps), y = x*rstd*gamma.
+//   Fused-add (PR #800, "What's included"): added = x + residual is rounded to
+//   the I/O dtype and stored as residual_out; the statistic and the output are
+//   taken from that rounded value (the tensor the backward reads).
+//   LayerNorm (issue #769 plan, "PR 5 -- LayerNorm backward": the forward
+//   saves mean and rstd): mean, then the centred variance (two passes over
+//   the row), rstd = 1/sqrt(var + eps), y = (x - mean)*rstd*gamma + beta.
+//
+// The structure is the backward row engine's: persistent CTAs of `teams`
+// teams, a team per row, each thread streaming its own 16-byte chunks of the
+// next rows into a private shared-memory ring with cp.async (no barrier
+// guards the ring: a thread reads back only what it copied). The row sums are
+// reduced over the team (warp shuffles, one named barrier, double-buffered
+// slots). Every input byte is read from HBM once.
+#include "common.cuh"
+#include "launch.h"
+
+namespace rn {
+
+constexpr int kFwdRingOffset = 256;  // [2 parities][32 warps] fp32 warp sums first
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :
+                 : "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+size_t fwd_row_smem_bytes(int teams, int stages, int ntensors, int team_chunks) {
+    return (size_t)kFwdRingOffset + (size_t)teams * stages * ntensors * (size_t)team_chunks * 16;
+}
+
+struct FwdRowArgs {
+    const uint8_t *x;
+    const uint8_t *res;    // fused-add only
+    const uint8_t *gamma;
+    const uint8_t *beta;   // LayerNorm, nullable
+    uint8_t *y;
+    uint8_t *res_out;      // fused-add only
+    float *mean;           // LayerNorm, nullable
+    float *rstd;           // nullable
+    int64_t M;
+    int nchunks;
+    int row_bytes;
+    int team_threads;
+    int teams;
+    int stages;
+    float inv_n;
+    float eps;
+};
+
+template <int CPT> struct FwdBounds {
+    static constexpr int kMaxThreads = CPT <= 2 ? 768 : 512;
+};
+
+// Sum over the team; every thread of the team gets the same bits.
+__device__ __forceinline__ float fwd_team_sum(float v, float *red, int parity, int team, int warp,
+                                              int lane, int team_warps, int first_warp,
+                                              int team_threads) {
+    v = warp_sum(v);
+    if (team_warps == 1) return v;
+    float *slot = red + parity * 32;
+    if (lane == 0) slot[warp] = v;
+    named_barrier_sync(1 + team, team_threads);
+    const float w = lane < team_warps ? slot[first_warp + lane] : 0.f;
+    return warp_sum(w);
+}
+
+template <typename T, int CPT, int MODE>
+__global__ void __launch_bounds__(FwdBounds<CPT>::kMaxThreads, 1) fwd_row_kernel(const FwdRowArgs a) {
+    constexpr int V = Traits<T>::kVec;
+    constexpr int NT = MODE == kFwdFused ? 2 : 1;
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *red = reinterpret_cast<float *>(smem);
+    uint8_t *ring = smem + kFwdRingOffset;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int team = tid / a.team_threads;
+    const int tt = tid - team * a.team_threads;
+    const int team_warps = a.team_threads >> 5;
+    const int first_warp = team * team_warps;
+    const int S = a.stages;
+
+    const int tc = CPT * a.team_threads;
+    const uint32_t kk_bytes = 16u * a.team_threads;
+    const uint32_t tensor_bytes = 16u * tc;
+    const uint32_t slot_bytes = NT * tensor_bytes;
+    const uint32_t my0 = smem_addr(ring) + (uint32_t)team * S * slot_bytes + 16u * tt;
+
+    const int64_t team_stride = (int64_t)gridDim.x * a.teams;
+    const int64_t row0 = (int64_t)blockIdx.x * a.teams + team;
+    const int64_t nrows = row0 < a.M ? (a.M - 1 - row0) / team_stride + 1 : 0;
+    const uint64_t policy = l2_policy_evict_first();
+
+    uint32_t coff[CPT];
+    bool cok[CPT];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        const int c = tt + kk * a.team_threads;
+        coff[kk] = 16u * c;
+        cok[kk] = c < a.nchunks;
+    }
+    auto issue = [&](int64_t row, int s) {
+        const size_t off = (size_t)row * a.row_bytes;
+        const uint32_t d = my0 + (uint32_t)s * slot_bytes;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            if (cok[kk]) {
+                cp_async16(d + kk * kk_bytes, a.x + off + coff[kk], policy);
+                if (MODE == kFwdFused)
+                    cp_async16(d + tensor_bytes + kk * kk_bytes, a.res + off + coff[kk], policy);
+            }
+        }
+    };
+    for (int j = 0; j < S - 1; ++j) {
+        if (j < nrows) issue(row0 + j * team_stride, j);
+        cp_async_commit();
+    }
+
+    uint4 gp[CPT], bp[CPT];
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        gp[kk] = cok[kk] ? ld_global_nc_v4(a.gamma + coff[kk]) : make_uint4(0, 0, 0, 0);
+        bp[kk] = (MODE == kFwdLn && cok[kk] && a.beta) ? ld_global_nc_v4(a.beta + coff[kk])
+                                                        : make_uint4(0, 0, 0, 0);
+    }
+
+    const int64_t ahead = (int64_t)(S - 1) * team_stride;
+    int slot = 0, fill = S - 1, parity = 0;
+    int64_t row = row0;
+    for (int64_t k = 0; k < nrows; ++k, row += team_stride) {
+        if (k + S - 1 < nrows) issue(row + ahead, fill);
+        cp_async_commit();
+        cp_async_wait_pending(S - 1);
+        const uint32_t sb = my0 + (uint32_t)slot * slot_bytes;
+        const size_t off = (size_t)row * a.row_bytes;
+
+        float mu = 0.f, rs;
+        if (MODE == kFwdLn) {
+            float s = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < CPT; ++kk) {
+                if (cok[kk]) {
+                    float v[V];
+                    chunk_to_float<T>(ld_shared_v4(sb + kk * kk_bytes), v);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) s += v[e];
+                }
+            }
+            mu = fwd_team_sum(s, red, parity, team, warp, lane, team_warps, first_warp,
+                              a.team_threads) * a.inv_n;
+            parity ^= 1;
+            float q = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < CPT; ++kk) {
+                if (cok[kk]) {
+                    float v[V];
+                    chunk_to_float<T>(ld_shared_v4(sb + kk * kk_bytes), v);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const float d = v[e] - mu;
+                        q = fmaf(d, d, q);
+                    }
+                }
+            }
+            q = fwd_team_sum(q, red, parity, team, warp, lane, team_warps, first_warp,
+                             a.team_threads);
+            parity ^= 1;
+            rs = rsqrtf(q * a.inv_n + a.eps);
+        } else {
+            float ss = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < CPT; ++kk) {
+                if (cok[kk]) {
+                    float v[V];
+                    uint4 xv = ld_shared_v4(sb + kk * kk_bytes);
+                    if (MODE == kFwdFused) {
+                        // added = x + residual, rounded to the dtype: stored as
+                        // residual_out and kept (in place of x) for the output
+                        float r[V];
+                        chunk_to_float<T>(xv, v);
+                        chunk_to_float<T>(ld_shared_v4(sb + tensor_bytes + kk * kk_bytes), r);
+#pragma unroll
+                        for (int e = 0; e < V; ++e) v[e] = v[e] + r[e];
+                        xv = float_to_chunk<T>(v);
+                        st_shared_v4(sb + kk * kk_bytes, xv);
+                        st_global_v4(a.res_out + off + coff[kk], xv);
+                    }
+                    chunk_to_float<T>(xv, v);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) ss = fmaf(v[e], v[e], ss);
+                }
+            }
+            ss = fwd_team_sum(ss, red, parity, team, warp, lane, team_warps, first_warp,
+                              a.team_threads);
+            parity ^= 1;
+            rs = rsqrtf(ss * a.inv_n + a.eps);
+        }
+        if (tt == 0) {
+            if (MODE == kFwdLn && a.mean) a.mean[row] = mu;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            if (cok[kk]) {
+                float v[V], g[V], o[V];
+                chunk_to_float<T>(ld_shared_v4(sb + kk * kk_bytes), v);
+                chunk_to_float<T>(gp[kk], g);
+                if (MODE == kFwdLn) {
+                    float b[V];
+                    chunk_to_float<T>(bp[kk], b);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) o[e] = fmaf((v[e] - mu) * rs, g[e], b[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) o[e] = v[e] * rs * g[e];
+                }
+                st_global_v4(a.y + off + coff[kk], float_to_chunk<T>(o));
+            }
+        }
+        if (++slot == S) slot = 0;
+        if (++fill == S) fill = 0;
+    }
+}
+
+template <typename T, int CPT, int MODE>
+static cudaError_t launch_fwd_row_t(const FwdRowArgs &args, const RowPlan &plan, cudaStream_t s) {
+    auto kern = fwd_row_kernel<T, CPT, MODE>;
+    cudaError_t e = ensure_smem_attr((const void *)kern, plan.smem);
+    if (e != cudaSuccess) return e;
+    kern<<<plan.grid, plan.teams * plan.team_threads, plan.smem, s>>>(args);
+    return cudaGetLastError();
+}
+
+template <typename T, int MODE>
+static cudaError_t launch_fwd_row_mode(const FwdRowArgs &args, const RowPlan &plan,
+                                       cudaStream_t s) {
+    switch (plan.cpt) {
+    case 1: return launch_fwd_row_t<T, 1, MODE>(args, plan, s);
+    case 2: return launch_fwd_row_t<T, 2, MODE>(args, plan, s);
+    case 4: return launch_fwd_row_t<T, 4, MODE>(args, plan, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+static cudaError_t launch_fwd_row_dt(const FwdRowArgs &args, const RowPlan &plan, int mode,
+                                     cudaStream_t s) {
+    switch (mode) {
+    case kFwdRms: return launch_fwd_row_mode<T, kFwdRms>(args, plan, s);
+    case kFwdFused: return launch_fwd_row_mode<T, kFwdFused>(args, plan, s);
+    case kFwdLn: return launch_fwd_row_mode<T, kFwdLn>(args, plan, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_fwd_row(const FwdRowProblem &p, const RowPlan &plan, cudaStream_t s) {
+    FwdRowArgs a;
+    a.x = static_cast<const uint8_t *>(p.x);
+    a.res = static_cast<const uint8_t *>(p.residual);
+    a.gamma = static_cast<const uint8_t *>(p.gamma);
+    a.beta = static_cast<const uint8_t *>(p.beta);
+    a.y = static_cast<uint8_t *>(p.y);
+    a.res_out = static_cast<uint8_t *>(p.residual_out);
+    a.mean = p.mean;
+    a.rstd = p.rstd;
+    a.M = p.M;
+    a.row_bytes = p.N * elem_bytes(p.dtype);
+    a.nchunks = a.row_bytes / 16;
+    a.team_threads = plan.team_threads;
+    a.teams = plan.teams;
+    a.stages = plan.stages;
+    a.inv_n = 1.0f / (float)p.N;
+    a.eps = p.eps;
+    switch (p.dtype) {
+    case kF32: return launch_fwd_row_dt<float>(a, plan, p.mode, s);
+    case kF16: return launch_fwd_row_dt<__half>(a, plan, p.mode, s);
+    case kBF16: return launch_fwd_row_dt<__nv_bfloat16>(a, plan, p.mode, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rn

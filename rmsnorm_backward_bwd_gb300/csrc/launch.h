@@ -100,7 +100,28 @@ struct FwdProblem {
     int dtype;
 };
 
-cudaError_t launch_fwd(const FwdProblem &p, bool vector_ok, int num_sms, cudaStream_t s);
+// Unaligned rows (and rows longer than the row engine's tile): one CTA per row.
+cudaError_t launch_fwd(const FwdProblem &p, int num_sms, cudaStream_t s);
+
+// Forward row engine (aligned rows): RMSNorm, fused-add RMSNorm, LayerNorm.
+enum FwdMode { kFwdRms = 0, kFwdFused = 1, kFwdLn = 2 };
+struct FwdRowProblem {
+    int mode;
+    const void *x;
+    const void *residual;   // fused-add
+    const void *gamma;
+    const void *beta;       // LayerNorm, nullable
+    void *y;
+    void *residual_out;     // fused-add
+    float *mean;            // LayerNorm, nullable
+    float *rstd;            // nullable
+    float eps;
+    int64_t M;
+    int N;
+    int dtype;
+};
+size_t fwd_row_smem_bytes(int teams, int stages, int ntensors, int team_chunks);
+cudaError_t launch_fwd_row(const FwdRowProblem &p, const RowPlan &plan, cudaStream_t s);
 
 // LayerNorm.
 struct LnFwdProblem {
@@ -133,7 +154,8 @@ struct LnBwdProblem {
     int dtype;
 };
 
-cudaError_t launch_ln_fwd(const LnFwdProblem &p, bool vector_ok, int num_sms, cudaStream_t s);
+// LayerNorm forward for unaligned rows (and rows longer than the row engine's tile).
+cudaError_t launch_ln_fwd(const LnFwdProblem &p, int num_sms, cudaStream_t s);
 // Default chunks-per-thread cap of the LayerNorm row engine (two fp32
 // accumulators per element pair instead of one).
 constexpr int kLnMaxCpt = 2;

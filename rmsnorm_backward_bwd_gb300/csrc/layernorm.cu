@@ -12,10 +12,9 @@
 //             dgamma = sum_rows dy * x_hat,  dbeta = sum_rows dy   (fp32)
 //
 // The engines mirror the RMSNorm ones:
-//   * forward, aligned rows: a team of threads per row holds the row in
-//     registers; the sum and then the centred sum of squares are reduced over
-//     the team (warp shuffles + one named barrier each). Unaligned rows: one
-//     CTA per row, three sweeps.
+//   * forward: aligned rows take the forward row engine (fwd_row.cu); here is
+//     the one-CTA-per-row version for the others, in three sweeps (sum,
+//     centred sum of squares, output).
 //   * backward, aligned rows: the persistent row engine -- per-thread
 //     cp.async ring of x and dy rows in shared memory, pass 1 reduces the two
 //     row sums (x - mean)*wdy and wdy together, pass 2 stores dx and adds dy*x_hat
@@ -46,98 +45,9 @@ struct LnFwdArgs {
     float *rstd;          // nullable
     int64_t M;
     int N;
-    int nchunks;
-    int row_bytes;
-    int team_threads;
-    int teams;
     float inv_n;
     float eps;
 };
-
-// Team-wide sum (warp shuffles, then the warps' partials through shared
-// memory, double-buffered by `parity`, behind one named barrier).
-__device__ __forceinline__ float ln_team_sum(float v, float (*red)[32], int parity, int team,
-                                             int warp, int team_warps, int first_warp,
-                                             int team_threads, int lane) {
-    v = warp_sum(v);
-    if (team_warps == 1) return v;
-    if (lane == 0) red[parity][warp] = v;
-    named_barrier_sync(1 + team, team_threads);
-    float t = 0.f;
-    for (int w = 0; w < team_warps; ++w) t += red[parity][first_warp + w];
-    return t;
-}
-
-template <typename T, int CPT>
-__global__ void __launch_bounds__(512) ln_fwd_vec_kernel(const LnFwdArgs a) {
-    constexpr int V = Traits<T>::kVec;
-    __shared__ float red[2][32];
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int team = tid / a.team_threads;
-    const int tt = tid - team * a.team_threads;
-    const int team_warps = a.team_threads >> 5;
-    const int first_warp = team * team_warps;
-
-    uint4 g[CPT], b[CPT];
-#pragma unroll
-    for (int kk = 0; kk < CPT; ++kk) {
-        const int c = tt + kk * a.team_threads;
-        const bool ok = c < a.nchunks;
-        g[kk] = ok ? ld_global_nc_v4(a.gamma + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
-        b[kk] = ok && a.beta ? ld_global_nc_v4(a.beta + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
-    }
-    const int64_t stride = (int64_t)gridDim.x * a.teams;
-    int parity = 0;
-    for (int64_t row = (int64_t)blockIdx.x * a.teams + team; row < a.M; row += stride) {
-        const size_t off = (size_t)row * a.row_bytes;
-        float v[CPT][V];
-        float s = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            const int c = tt + kk * a.team_threads;
-            if (c < a.nchunks) {
-                chunk_to_float<T>(ld_global_nc_v4(a.x + off + 16u * c), v[kk]);
-#pragma unroll
-                for (int e = 0; e < V; ++e) s += v[kk][e];
-            }
-        }
-        s = ln_team_sum(s, red, parity, team, warp, team_warps, first_warp, a.team_threads, lane);
-        parity ^= 1;
-        const float mu = s * a.inv_n;
-        float q = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            const int c = tt + kk * a.team_threads;
-            if (c < a.nchunks) {
-#pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float d = v[kk][e] - mu;
-                    q = fmaf(d, d, q);
-                }
-            }
-        }
-        q = ln_team_sum(q, red, parity, team, warp, team_warps, first_warp, a.team_threads, lane);
-        parity ^= 1;
-        const float rs = rsqrtf(q * a.inv_n + a.eps);
-        if (tt == 0) {
-            if (a.mean) a.mean[row] = mu;
-            if (a.rstd) a.rstd[row] = rs;
-        }
-#pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            const int c = tt + kk * a.team_threads;
-            if (c < a.nchunks) {
-                float gf[V], bf[V], o[V];
-                chunk_to_float<T>(g[kk], gf);
-                chunk_to_float<T>(b[kk], bf);
-#pragma unroll
-                for (int e = 0; e < V; ++e) o[e] = fmaf((v[kk][e] - mu) * rs, gf[e], bf[e]);
-                st_global_v4(a.y + off + 16u * c, float_to_chunk<T>(o));
-            }
-        }
-    }
-}
 
 template <typename T>
 __global__ void __launch_bounds__(256) ln_fwd_generic_kernel(const LnFwdArgs a) {
@@ -182,47 +92,14 @@ __global__ void __launch_bounds__(256) ln_fwd_generic_kernel(const LnFwdArgs a) 
 }
 
 template <typename T>
-static cudaError_t launch_ln_fwd_t(const LnFwdArgs &a0, bool vector_ok, int num_sms,
-                                   cudaStream_t s) {
-    LnFwdArgs a = a0;
-    if (vector_ok) {
-        // team shape: about 256 threads per row, up to 4 chunks per thread
-        int team = (a.nchunks + 1) / 2;
-        team = ((team + 31) / 32) * 32;
-        if (team > 256) team = 256;
-        int cpt = (a.nchunks + team - 1) / team;
-        cpt = cpt <= 1 ? 1 : (cpt <= 2 ? 2 : 4);
-        if (cpt == 4) team = (((a.nchunks + 3) / 4 + 31) / 32) * 32;
-        if (team <= 512) {
-            a.team_threads = team;
-            a.teams = 512 / team;
-            if (a.teams > 15) a.teams = 15;
-            const void *fn = nullptr;
-            if (cpt == 1) fn = (const void *)ln_fwd_vec_kernel<T, 1>;
-            else if (cpt == 2) fn = (const void *)ln_fwd_vec_kernel<T, 2>;
-            else fn = (const void *)ln_fwd_vec_kernel<T, 4>;
-            int per_sm = 0;
-            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &per_sm, fn, a.teams * a.team_threads, 0);
-            if (e != cudaSuccess) return e;
-            if (per_sm < 1) per_sm = 1;
-            int64_t need = (a.M + a.teams - 1) / a.teams;
-            int64_t grid = (int64_t)num_sms * per_sm;
-            if (grid > need) grid = need;
-            dim3 block(a.teams * a.team_threads);
-            if (cpt == 1) ln_fwd_vec_kernel<T, 1><<<(unsigned)grid, block, 0, s>>>(a);
-            else if (cpt == 2) ln_fwd_vec_kernel<T, 2><<<(unsigned)grid, block, 0, s>>>(a);
-            else ln_fwd_vec_kernel<T, 4><<<(unsigned)grid, block, 0, s>>>(a);
-            return cudaGetLastError();
-        }
-    }
+static cudaError_t launch_ln_fwd_t(const LnFwdArgs &a, int num_sms, cudaStream_t s) {
     int64_t grid = (int64_t)num_sms * 8;
     if (grid > a.M) grid = a.M;
     ln_fwd_generic_kernel<T><<<(unsigned)grid, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_ln_fwd(const LnFwdProblem &p, bool vector_ok, int num_sms, cudaStream_t s) {
+cudaError_t launch_ln_fwd(const LnFwdProblem &p, int num_sms, cudaStream_t s) {
     LnFwdArgs a;
     a.x = static_cast<const uint8_t *>(p.x);
     a.gamma = static_cast<const uint8_t *>(p.gamma);
@@ -232,16 +109,12 @@ cudaError_t launch_ln_fwd(const LnFwdProblem &p, bool vector_ok, int num_sms, cu
     a.rstd = p.rstd;
     a.M = p.M;
     a.N = p.N;
-    a.row_bytes = p.N * elem_bytes(p.dtype);
-    a.nchunks = a.row_bytes / 16;
-    a.team_threads = 0;
-    a.teams = 0;
     a.inv_n = 1.0f / (float)p.N;
     a.eps = p.eps;
     switch (p.dtype) {
-    case kF32: return launch_ln_fwd_t<float>(a, vector_ok, num_sms, s);
-    case kF16: return launch_ln_fwd_t<__half>(a, vector_ok, num_sms, s);
-    case kBF16: return launch_ln_fwd_t<__nv_bfloat16>(a, vector_ok, num_sms, s);
+    case kF32: return launch_ln_fwd_t<float>(a, num_sms, s);
+    case kF16: return launch_ln_fwd_t<__half>(a, num_sms, s);
+    case kBF16: return launch_ln_fwd_t<__nv_bfloat16>(a, num_sms, s);
     default: return cudaErrorInvalidValue;
     }
 }
