@@ -671,8 +671,9 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
                      (!fused || (aligned16(residual) && aligned16(residual_out)));
     RowPlan rp;
     const int nt = fused ? 2 : 1;
-    if (vec && plan_row_tile(M, (int)(N * eb / 16), nt, fwd_row_smem_bytes(0, 0, nt, 0), 4,
-                             row_max_threads, d, &rp, false)) {
+    const bool row = vec && plan_row_tile(M, (int)(N * eb / 16), nt, fwd_row_smem_bytes(0, 0, nt, 0),
+                                          4, row_max_threads, d, &rp, false);
+    if (vec) {
         FwdRowProblem q;
         q.mode = fused ? kFwdFused : kFwdRms;
         q.x = x;
@@ -687,7 +688,8 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
         q.M = M;
         q.N = (int)N;
         q.dtype = dtype;
-        e = launch_fwd_row(q, rp, static_cast<cudaStream_t>(stream));
+        e = row ? launch_fwd_row(q, rp, static_cast<cudaStream_t>(stream))
+                : launch_fwd_long(q, d.num_sms, static_cast<cudaStream_t>(stream));
     } else {
         e = launch_fwd(p, d.num_sms, static_cast<cudaStream_t>(stream));
     }
@@ -722,8 +724,9 @@ static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta
     const bool vec = ((N * eb) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y) &&
                      (!beta || aligned16(beta));
     RowPlan rp;
-    if (vec && plan_row_tile(M, (int)(N * eb / 16), 1, fwd_row_smem_bytes(0, 0, 1, 0), 4,
-                             row_max_threads, d, &rp, false)) {
+    const bool row = vec && plan_row_tile(M, (int)(N * eb / 16), 1, fwd_row_smem_bytes(0, 0, 1, 0),
+                                          4, row_max_threads, d, &rp, false);
+    if (vec) {
         FwdRowProblem q;
         q.mode = kFwdLn;
         q.x = x;
@@ -738,7 +741,8 @@ static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta
         q.M = M;
         q.N = (int)N;
         q.dtype = dtype;
-        e = launch_fwd_row(q, rp, static_cast<cudaStream_t>(stream));
+        e = row ? launch_fwd_row(q, rp, static_cast<cudaStream_t>(stream))
+                : launch_fwd_long(q, d.num_sms, static_cast<cudaStream_t>(stream));
     } else {
         e = launch_ln_fwd(p, d.num_sms, static_cast<cudaStream_t>(stream));
     }

@@ -286,3 +286,162 @@ cudaError_t launch_fwd_row(const FwdRowProblem &p, const RowPlan &plan, cudaStre
 }
 
 }  // namespace rn
+
+namespace rn {
+
+// ---------------------------------------------------------- long rows
+// Aligned rows longer than the row engine's tile: one CTA per row at a time
+// (persistent, several CTAs per SM), 16-byte loads. Pass 1 reads the row from
+// HBM; the later passes re-read it from L2, where the CTAs' rows in flight
+// (a few MB) stay. Fused-add: pass 1 writes residual_out and pass 2 reads it
+// back (this thread's own writes). LayerNorm: sum, centred sum of squares,
+// output.
+// A coherent 16-byte global load (the fused path reads back what this thread
+// stored earlier in the kernel, which the read-only path may not see).
+__device__ __forceinline__ uint4 ld_global_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float fwd_block_sum(float v, float *red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    v = warp_sum(v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int w = 0; w < nwarps; ++w) t += red[w];
+    __syncthreads();  // red is rewritten by the next sum
+    return t;
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(512) fwd_long_kernel(const FwdRowArgs a) {
+    constexpr int V = Traits<T>::kVec;
+    __shared__ float red[32];
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const size_t off = (size_t)row * a.row_bytes;
+        const uint8_t *xr = a.x + off;
+        float mu = 0.f, rs;
+        if (MODE == kFwdLn) {
+            float s = 0.f;
+            for (int c = tid; c < a.nchunks; c += nthr) {
+                float v[V];
+                chunk_to_float<T>(ld_global_nc_v4(xr + 16u * c), v);
+#pragma unroll
+                for (int e = 0; e < V; ++e) s += v[e];
+            }
+            mu = fwd_block_sum(s, red) * a.inv_n;
+            float q = 0.f;
+            for (int c = tid; c < a.nchunks; c += nthr) {
+                float v[V];
+                chunk_to_float<T>(ld_global_nc_v4(xr + 16u * c), v);
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const float d = v[e] - mu;
+                    q = fmaf(d, d, q);
+                }
+            }
+            rs = rsqrtf(fwd_block_sum(q, red) * a.inv_n + a.eps);
+        } else {
+            float ss = 0.f;
+            for (int c = tid; c < a.nchunks; c += nthr) {
+                float v[V];
+                uint4 xv = ld_global_nc_v4(xr + 16u * c);
+                if (MODE == kFwdFused) {
+                    float r[V];
+                    chunk_to_float<T>(xv, v);
+                    chunk_to_float<T>(ld_global_nc_v4(a.res + off + 16u * c), r);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) v[e] = v[e] + r[e];
+                    xv = float_to_chunk<T>(v);
+                    st_global_v4(a.res_out + off + 16u * c, xv);
+                }
+                chunk_to_float<T>(xv, v);
+#pragma unroll
+                for (int e = 0; e < V; ++e) ss = fmaf(v[e], v[e], ss);
+            }
+            rs = rsqrtf(fwd_block_sum(ss, red) * a.inv_n + a.eps);
+        }
+        if (tid == 0) {
+            if (MODE == kFwdLn && a.mean) a.mean[row] = mu;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+        // fused: read back residual_out (this thread's own stores); else x
+        const uint8_t *src = MODE == kFwdFused ? a.res_out + off : xr;
+        for (int c = tid; c < a.nchunks; c += nthr) {
+            float v[V], g[V], o[V];
+            const uint4 xv = MODE == kFwdFused ? ld_global_v4(src + 16u * c)
+                                               : ld_global_nc_v4(src + 16u * c);
+            chunk_to_float<T>(xv, v);
+            chunk_to_float<T>(ld_global_nc_v4(a.gamma + 16u * c), g);
+            if (MODE == kFwdLn) {
+                float b[V];
+                if (a.beta) chunk_to_float<T>(ld_global_nc_v4(a.beta + 16u * c), b);
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    o[e] = fmaf((v[e] - mu) * rs, g[e], a.beta ? b[e] : 0.f);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) o[e] = v[e] * rs * g[e];
+            }
+            st_global_v4(a.y + off + 16u * c, float_to_chunk<T>(o));
+        }
+    }
+}
+
+template <typename T, int MODE>
+static cudaError_t launch_fwd_long_t(const FwdRowArgs &a, int num_sms, cudaStream_t s) {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, fwd_long_kernel<T, MODE>, 512, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)num_sms * per_sm;
+    if (grid > a.M) grid = a.M;
+    fwd_long_kernel<T, MODE><<<(unsigned)grid, 512, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_fwd_long_dt(const FwdRowArgs &a, int mode, int num_sms,
+                                      cudaStream_t s) {
+    switch (mode) {
+    case kFwdRms: return launch_fwd_long_t<T, kFwdRms>(a, num_sms, s);
+    case kFwdFused: return launch_fwd_long_t<T, kFwdFused>(a, num_sms, s);
+    case kFwdLn: return launch_fwd_long_t<T, kFwdLn>(a, num_sms, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_fwd_long(const FwdRowProblem &p, int num_sms, cudaStream_t s) {
+    FwdRowArgs a;
+    a.x = static_cast<const uint8_t *>(p.x);
+    a.res = static_cast<const uint8_t *>(p.residual);
+    a.gamma = static_cast<const uint8_t *>(p.gamma);
+    a.beta = static_cast<const uint8_t *>(p.beta);
+    a.y = static_cast<uint8_t *>(p.y);
+    a.res_out = static_cast<uint8_t *>(p.residual_out);
+    a.mean = p.mean;
+    a.rstd = p.rstd;
+    a.M = p.M;
+    a.row_bytes = p.N * elem_bytes(p.dtype);
+    a.nchunks = a.row_bytes / 16;
+    a.team_threads = 512;
+    a.teams = 1;
+    a.stages = 0;
+    a.inv_n = 1.0f / (float)p.N;
+    a.eps = p.eps;
+    switch (p.dtype) {
+    case kF32: return launch_fwd_long_dt<float>(a, p.mode, num_sms, s);
+    case kF16: return launch_fwd_long_dt<__half>(a, p.mode, num_sms, s);
+    case kBF16: return launch_fwd_long_dt<__nv_bfloat16>(a, p.mode, num_sms, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rn

@@ -122,6 +122,8 @@ struct FwdRowProblem {
 };
 size_t fwd_row_smem_bytes(int teams, int stages, int ntensors, int team_chunks);
 cudaError_t launch_fwd_row(const FwdRowProblem &p, const RowPlan &plan, cudaStream_t s);
+// Aligned rows longer than the row engine's tile: one CTA per row, 16-byte loads.
+cudaError_t launch_fwd_long(const FwdRowProblem &p, int num_sms, cudaStream_t s);
 
 // LayerNorm.
 struct LnFwdProblem {

@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = [(128, 1024, "f32"), (4096, 4096, "bf16"), (1, 4096, "bf16"), (512, 2048, "bf16"),
           (512, 3000, "f32"), (128, 4096, "f16"), (7, 1001, "bf16"), (3, 33, "f16"),
-          (16, 16384, "bf16"), (2, 40000, "f32")]
+          (16, 16384, "bf16"), (2, 40000, "f32"), (8, 32768, "bf16"), (3, 65536, "f16")]
 
 
 def _check_rstd(got, ref64):

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = [(4096, 4096, "bf16"), (1, 4096, "bf16"), (512, 2048, "bf16"), (512, 3000, "f32"),
           (128, 4096, "f16"), (300, 768, "bf16"), (7, 1001, "bf16"), (3, 33, "f16"),
-          (16, 16384, "bf16"), (2, 40000, "f32"), (64, 8192, "f32")]
+          (16, 16384, "bf16"), (2, 40000, "f32"), (64, 8192, "f32"), (8, 32768, "bf16")]
 
 
 @pytest.fixture(autouse=True)
