@@ -323,38 +323,77 @@ def time_calls(prob, steps, warmup, flush, ws, sampler=None, kernel_events=False
 
 
 def time_e2e(prob, steps, warmup, ws):
-    """Same call with inputs in pinned host memory copied in, and dx + dweight
-    copied out, inside every timed step (one stream, CUDA events)."""
+    """The same public call with its inputs in pinned host memory: every step
+    copies that step's inputs (x|added, gamma, dy, rstd, [dres]) host->device,
+    runs the backward and copies dx + dweight device->host, all inside the
+    timed region. Steps are pipelined the way an input stream would be: two
+    device buffer sets and three streams (copy in, compute, copy out), so the
+    copy-in of step i+1 and the copy-out of step i-1 overlap the backward of
+    step i. Returns (ms per step, host->device bytes, device->host bytes)."""
     import torch
+    import rmsnorm_backward_bwd_gb300 as rn
     c = prob.case
-    host = {k: getattr(prob, k).cpu().pin_memory() for k in ("x", "g", "dy", "rstd")}
-    if prob.dres is not None:
-        host["dres"] = prob.dres.cpu().pin_memory()
+    names = ["x", "g", "dy", "rstd"] + (["dres"] if prob.dres is not None else [])
+    host = {k: getattr(prob, k).cpu().pin_memory() for k in names}
     out_dx = torch.empty(prob.dx.shape, dtype=prob.dx.dtype).pin_memory()
     out_dw = torch.empty(prob.dw.shape, dtype=prob.dw.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_dx.numel() * out_dx.element_size() + out_dw.numel() * out_dw.element_size()
 
-    def step():
-        for k, t in host.items():
-            getattr(prob, k).copy_(t, non_blocking=True)
-        prob.call()
-        out_dx.copy_(prob.dx, non_blocking=True)
-        out_dw.copy_(prob.dw, non_blocking=True)
+    up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(comp):
+        ws_comp = rn.bwd_workspace(c.M, c.N, prob.x.dtype, prob.x.device)
+    sets = []
+    for _ in range(2):
+        d = {k: torch.empty_like(getattr(prob, k)) for k in names}
+        d["dx"] = torch.empty_like(prob.dx)
+        d["dw32"] = torch.empty_like(prob.dw32)
+        d["dw"] = torch.empty_like(prob.dw)
+        sets.append(d)
+    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("inp", "done", "out")}
+    torch.cuda.synchronize()
 
-    for _ in range(warmup):
-        step()
+    def step(i):
+        b, d = i % 2, sets[i % 2]
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(ev["done"][b])   # the backward of step i-2 read these inputs
+            for k in names:
+                d[k].copy_(host[k], non_blocking=True)
+            ev["inp"][b].record(up)
+        with torch.cuda.stream(comp):
+            comp.wait_event(ev["inp"][b])
+            if i >= 2:
+                comp.wait_event(ev["out"][b])  # step i-2's outputs have been copied out
+            if c.fused:
+                rn.fused_add_rmsnorm_bwd(d["x"], d["g"], d["dy"], d["rstd"], d.get("dres"),
+                                         dx=d["dx"], dweight_f32=d["dw32"], dweight=d["dw"],
+                                         workspace=ws_comp)
+            else:
+                rn.rmsnorm_bwd(d["x"], d["g"], d["dy"], d["rstd"], dx=d["dx"],
+                               dweight_f32=d["dw32"], dweight=d["dw"], workspace=ws_comp)
+            ev["done"][b].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(ev["done"][b])
+            out_dx.copy_(d["dx"], non_blocking=True)
+            out_dw.copy_(d["dw"], non_blocking=True)
+            ev["out"][b].record(down)
+
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     barrier(ws)
-    st = torch.cuda.current_stream()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(st)
-    for _ in range(steps):
-        step()
-    b.record(st)
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(up)
+    for i in range(steps):
+        step(i)
+    z.record(down)
     torch.cuda.synchronize()
     barrier(ws)
-    return a.elapsed_time(b) / steps, h2d, d2h
+    # the pipelined steps produced the same dx as the device-resident call
+    if not torch.equal(out_dx, prob.dx.cpu()):
+        raise RuntimeError("end-to-end steps disagree with the device-resident call")
+    return a.elapsed_time(z) / steps, h2d, d2h
 
 
 def autograd_problem(case, dev, impl):
