@@ -64,6 +64,25 @@ def _bind(lib):
     return lib
 
 
+# Process-wide overrides read from the environment when the library loads:
+#   RN_BWD_ENGINE   = auto | row | generic | cluster
+#   RN_DWEIGHT_MODE = auto | scratch (deterministic) | atomic
+ENV_OPTIONS = {
+    "RN_BWD_ENGINE": (0, {"auto": 0, "row": 1, "generic": 2, "cluster": 3}),
+    "RN_DWEIGHT_MODE": (1, {"auto": 0, "scratch": 1, "atomic": 2}),
+}
+
+
+def _apply_env(lib_):
+    for var, (opt, values) in ENV_OPTIONS.items():
+        v = os.environ.get(var)
+        if v is None:
+            continue
+        if v.lower() not in values:
+            raise ValueError("%s=%r: expected one of %s" % (var, v, ", ".join(values)))
+        lib_.rn_set_option(opt, values[v.lower()])
+
+
 def lib():
     """The loaded library; raises if it has not been built."""
     global _lib
@@ -71,7 +90,9 @@ def lib():
         if not os.path.exists(LIB_PATH):
             raise RuntimeError("CUDA library %s is not built; run "
                                "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
-        _lib = _bind(ctypes.CDLL(LIB_PATH))
+        loaded = _bind(ctypes.CDLL(LIB_PATH))
+        _apply_env(loaded)
+        _lib = loaded
     return _lib
 
 

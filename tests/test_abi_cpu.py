@@ -1,11 +1,14 @@
 """The C ABI on the host: the library loads, exports what the header
 declares, and rejects bad arguments before touching the GPU (CPU only)."""
 import ctypes
+import os
 
 import pytest
 import torch
 
 from rmsnorm_backward_bwd_gb300 import native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_library_exports_every_declared_function():
@@ -78,3 +81,27 @@ def test_python_guards_refuse_host_tensors():
                                                   torch.zeros(4))):
         with pytest.raises(ValueError, match="CUDA devices only"):
             call()
+
+
+@pytest.mark.parametrize("env,opt,want", [({"RN_BWD_ENGINE": "cluster"}, 0, 3),
+                                          ({"RN_BWD_ENGINE": "generic"}, 0, 2),
+                                          ({"RN_DWEIGHT_MODE": "scratch"}, 1, 1),
+                                          ({"RN_DWEIGHT_MODE": "ATOMIC"}, 1, 2)])
+def test_environment_overrides_options(env, opt, want):
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r); from rmsnorm_backward_bwd_gb300 import native; "
+            "print(native.get_option(%d))" % (ROOT, opt))
+    out = subprocess.run([sys.executable, "-c", code], env={**os.environ, **env},
+                         capture_output=True, text=True, check=True).stdout.strip()
+    assert int(out) == want
+
+
+def test_environment_override_rejects_unknown_values():
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r); from rmsnorm_backward_bwd_gb300 import native; "
+            "native.lib()" % ROOT)
+    r = subprocess.run([sys.executable, "-c", code], env={**os.environ, "RN_BWD_ENGINE": "warp"},
+                       capture_output=True, text=True)
+    assert r.returncode != 0 and "RN_BWD_ENGINE" in r.stderr
