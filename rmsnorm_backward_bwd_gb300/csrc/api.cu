@@ -325,6 +325,73 @@ static bool want_atomic(const BwdProblem &p) {
     return aligned16(p.dw_f32);
 }
 
+// Outputs of the weight-gradient reduction: one or two length-N fp32 results
+// (LayerNorm: dgamma, dbeta) with optional casts, and where the scratch
+// mode's partial rows are (G rows of ld floats).
+struct DwOutputs {
+    float *f32_1;
+    void *cast_1;
+    float *f32_2;
+    void *cast_2;
+    int N;
+    int dtype;
+    const float *partials;
+    int G;
+    int ld;
+};
+
+// The kernels of one backward call around its pass: in atomic mode, zero the
+// fp32 outputs, run the pass (`pass(true)`: a programmatic dependent of the
+// zeroing kernel) and cast; in scratch mode, run the pass and the finalize
+// that sums the partial rows and casts. Profile events bracket the pass when
+// set.
+template <typename Pass>
+static rn_status run_sequence(bool atomic, const DwOutputs &o, cudaStream_t s, Pass pass) {
+    cudaError_t e;
+    if (atomic) {
+        e = launch_zero_f32(o.f32_1, o.N, s, o.f32_2);
+        if (e != cudaSuccess) return cuda_fail(e, "zero launch");
+    }
+    const bool prof = g_ev_begin && g_ev_end;
+    if (prof) {
+        e = cudaEventRecord(g_ev_begin, s);
+        if (e != cudaSuccess) return cuda_fail(e, "profile event");
+    }
+    e = pass(atomic);
+    if (e != cudaSuccess) return cuda_fail(e, "backward pass launch");
+    if (prof) {
+        e = cudaEventRecord(g_ev_end, s);
+        if (e != cudaSuccess) return cuda_fail(e, "profile event");
+    }
+    if (atomic) {
+        if (!o.cast_1 && !o.cast_2) return RN_OK;
+        e = launch_cast(o.f32_1, o.cast_1, o.N, o.dtype, s, !prof, o.f32_2, o.cast_2);
+        return e == cudaSuccess ? RN_OK : cuda_fail(e, "cast launch");
+    }
+    e = launch_finalize2(o.partials, o.G, o.ld, o.N, o.f32_1, o.cast_1, o.f32_2, o.cast_2, o.dtype,
+                         s, !prof);
+    return e == cudaSuccess ? RN_OK : cuda_fail(e, "finalize launch");
+}
+
+static void plan_string_cluster(const ClusterPlan &cp, const char *engine, bool atomic) {
+    snprintf(g_plan, sizeof(g_plan),
+             "engine=%s csize=%d slice=%d cpt=%d threads=%d stages=%d clusters=%d smem=%zu dw=%s",
+             engine, cp.csize, cp.slice, cp.cpt, cp.threads, cp.stages, cp.clusters, cp.smem,
+             atomic ? "atomic" : "scratch");
+}
+
+static void plan_string_row(const RowPlan &rp, const char *engine, bool atomic) {
+    snprintf(g_plan, sizeof(g_plan),
+             "engine=%s cpt=%d team_threads=%d teams=%d stages=%d grid=%d smem=%zu dw=%s",
+             engine, rp.cpt, rp.team_threads, rp.teams, rp.stages, rp.grid, rp.smem,
+             atomic ? "atomic" : "scratch");
+}
+
+static void plan_string_generic(const GenericPlan &gp, const char *engine, bool atomic) {
+    snprintf(g_plan, sizeof(g_plan), "engine=%s threads=%d grid=%d smem_dw=%d dw=%s", engine,
+             gp.threads, gp.grid, (int)gp.smem_dw, atomic ? "atomic" : "scratch");
+}
+
 static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
     DeviceInfo d;
     int dev = 0;
@@ -360,34 +427,12 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
             return fail(RN_ERR_UNSUPPORTED, "cluster engine cannot take N=%d dtype=%d here",
                         p.N, p.dtype);
     }
+    const float *partials = reinterpret_cast<const float *>(p.ws + kWsHeaderBytes);
     if (use_cluster) {
-        snprintf(g_plan, sizeof(g_plan),
-                 "engine=cluster csize=%d slice=%d cpt=%d threads=%d stages=%d clusters=%d "
-                 "smem=%zu dw=%s",
-                 cp.csize, cp.slice, cp.cpt, cp.threads, cp.stages, cp.clusters, cp.smem,
-                 atomic ? "atomic" : "scratch");
-        if (atomic) {
-            e = launch_zero_f32(p.dw_f32, p.N, s);
-            if (e != cudaSuccess) return cuda_fail(e, "zero launch");
-        }
-        const bool prof = g_ev_begin && g_ev_end;
-        if (prof) {
-            e = cudaEventRecord(g_ev_begin, s);
-            if (e != cudaSuccess) return cuda_fail(e, "profile event");
-        }
-        e = launch_bwd_cluster(p, cp, s, atomic);
-        if (e != cudaSuccess) return cuda_fail(e, "cluster pass launch");
-        if (prof) {
-            e = cudaEventRecord(g_ev_end, s);
-            if (e != cudaSuccess) return cuda_fail(e, "profile event");
-        }
-        if (atomic) {
-            if (p.dw_cast) e = launch_cast(p.dw_f32, p.dw_cast, p.N, p.dtype, s, !prof);
-        } else {
-            e = launch_finalize(reinterpret_cast<const float *>(p.ws + kWsHeaderBytes),
-                                cp.clusters, p.N, p.dw_f32, p.dw_cast, p.dtype, s, !prof);
-        }
-        return e == cudaSuccess ? RN_OK : cuda_fail(e, atomic ? "cast launch" : "finalize launch");
+        plan_string_cluster(cp, "cluster", atomic);
+        const DwOutputs o = {p.dw_f32, p.dw_cast, nullptr, nullptr, p.N, p.dtype,
+                             partials, cp.clusters, p.N};
+        return run_sequence(atomic, o, s, [&](bool pdl) { return launch_bwd_cluster(p, cp, s, pdl); });
     }
     if (!use_row) plan_generic(p, d, &gp);
     if (!use_row && atomic && generic_smem_bytes(p.N, true) > d.smem_optin) {
@@ -401,42 +446,13 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
         gp.smem_dw = true;
         gp.smem = generic_smem_bytes(p.N, true);
     }
-    const int G = use_row ? rp.grid : gp.grid;
-    if (use_row)
-        snprintf(g_plan, sizeof(g_plan),
-                 "engine=row cpt=%d team_threads=%d teams=%d stages=%d grid=%d smem=%zu dw=%s",
-                 rp.cpt, rp.team_threads, rp.teams, rp.stages, rp.grid, rp.smem,
-                 atomic ? "atomic" : "scratch");
-    else
-        snprintf(g_plan, sizeof(g_plan), "engine=generic threads=%d grid=%d smem_dw=%d dw=%s",
-                 gp.threads, gp.grid, (int)gp.smem_dw, atomic ? "atomic" : "scratch");
-
-    if (atomic) {
-        e = launch_zero_f32(p.dw_f32, p.N, s);
-        if (e != cudaSuccess) return cuda_fail(e, "zero launch");
-    }
-    const bool prof = g_ev_begin && g_ev_end;
-    if (prof) {
-        e = cudaEventRecord(g_ev_begin, s);
-        if (e != cudaSuccess) return cuda_fail(e, "profile event");
-    }
-    e = use_row ? launch_bwd_row(p, rp, s, atomic) : launch_bwd_generic(p, gp, s, atomic);
-    if (e != cudaSuccess) return cuda_fail(e, "row pass launch");
-    if (prof) {
-        e = cudaEventRecord(g_ev_end, s);
-        if (e != cudaSuccess) return cuda_fail(e, "profile event");
-    }
-    if (atomic) {
-        if (p.dw_cast) {
-            e = launch_cast(p.dw_f32, p.dw_cast, p.N, p.dtype, s, !prof);
-            if (e != cudaSuccess) return cuda_fail(e, "cast launch");
-        }
-    } else {
-        e = launch_finalize(reinterpret_cast<const float *>(p.ws + kWsHeaderBytes), G, p.N,
-                            p.dw_f32, p.dw_cast, p.dtype, s, !prof);
-        if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
-    }
-    return RN_OK;
+    if (use_row) plan_string_row(rp, "row", atomic);
+    else plan_string_generic(gp, "generic", atomic);
+    const DwOutputs o = {p.dw_f32, p.dw_cast, nullptr, nullptr, p.N, p.dtype,
+                         partials, use_row ? rp.grid : gp.grid, p.N};
+    return run_sequence(atomic, o, s, [&](bool pdl) {
+        return use_row ? launch_bwd_row(p, rp, s, pdl) : launch_bwd_generic(p, gp, s, pdl);
+    });
 }
 
 // ------------------------------------------------------------- LayerNorm
@@ -524,34 +540,11 @@ static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t
                         p.N, p.dtype);
     }
     if (use_cluster) {
-        snprintf(g_plan, sizeof(g_plan),
-                 "engine=ln_cluster csize=%d slice=%d cpt=%d threads=%d stages=%d clusters=%d "
-                 "smem=%zu dw=%s",
-                 cp.csize, cp.slice, cp.cpt, cp.threads, cp.stages, cp.clusters, cp.smem,
-                 atomic ? "atomic" : "scratch");
-        if (atomic) {
-            e = launch_zero_f32(p.dg_f32, p.N, s, p.db_f32);
-            if (e != cudaSuccess) return cuda_fail(e, "zero launch");
-        }
-        const bool prof = g_ev_begin && g_ev_end;
-        if (prof) {
-            e = cudaEventRecord(g_ev_begin, s);
-            if (e != cudaSuccess) return cuda_fail(e, "profile event");
-        }
-        e = launch_ln_bwd_cluster(p, cp, s, atomic);
-        if (e != cudaSuccess) return cuda_fail(e, "cluster pass launch");
-        if (prof) {
-            e = cudaEventRecord(g_ev_end, s);
-            if (e != cudaSuccess) return cuda_fail(e, "profile event");
-        }
-        if (atomic) {
-            if (p.dg_cast || p.db_cast)
-                e = launch_cast(p.dg_f32, p.dg_cast, p.N, p.dtype, s, !prof, p.db_f32, p.db_cast);
-        } else {
-            e = launch_finalize2(partials, cp.clusters, 2 * p.N, p.N, p.dg_f32, p.dg_cast,
-                                 p.db_f32, p.db_cast, p.dtype, s, !prof);
-        }
-        return e == cudaSuccess ? RN_OK : cuda_fail(e, atomic ? "cast launch" : "finalize launch");
+        plan_string_cluster(cp, "ln_cluster", atomic);
+        const DwOutputs o = {p.dg_f32, p.dg_cast, p.db_f32, p.db_cast, p.N, p.dtype,
+                             partials, cp.clusters, 2 * p.N};
+        return run_sequence(atomic, o, s,
+                            [&](bool pdl) { return launch_ln_bwd_cluster(p, cp, s, pdl); });
     }
     if (!use_row) plan_ln_generic(p, d, &gp);
     if (!use_row && atomic && ln_generic_smem_bytes(p.N, true) > d.smem_optin) {
@@ -565,42 +558,13 @@ static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t
         gp.smem_dw = true;
         gp.smem = ln_generic_smem_bytes(p.N, true);
     }
-    const int G = use_row ? rp.grid : gp.grid;
-    if (use_row)
-        snprintf(g_plan, sizeof(g_plan),
-                 "engine=ln_row cpt=%d team_threads=%d teams=%d stages=%d grid=%d smem=%zu dw=%s",
-                 rp.cpt, rp.team_threads, rp.teams, rp.stages, rp.grid, rp.smem,
-                 atomic ? "atomic" : "scratch");
-    else
-        snprintf(g_plan, sizeof(g_plan), "engine=ln_generic threads=%d grid=%d smem_dw=%d dw=%s",
-                 gp.threads, gp.grid, (int)gp.smem_dw, atomic ? "atomic" : "scratch");
-
-    if (atomic) {
-        e = launch_zero_f32(p.dg_f32, p.N, s, p.db_f32);
-        if (e != cudaSuccess) return cuda_fail(e, "zero launch");
-    }
-    const bool prof = g_ev_begin && g_ev_end;
-    if (prof) {
-        e = cudaEventRecord(g_ev_begin, s);
-        if (e != cudaSuccess) return cuda_fail(e, "profile event");
-    }
-    e = use_row ? launch_ln_bwd_row(p, rp, s, atomic) : launch_ln_bwd_generic(p, gp, s, atomic);
-    if (e != cudaSuccess) return cuda_fail(e, "row pass launch");
-    if (prof) {
-        e = cudaEventRecord(g_ev_end, s);
-        if (e != cudaSuccess) return cuda_fail(e, "profile event");
-    }
-    if (atomic) {
-        if (p.dg_cast || p.db_cast) {
-            e = launch_cast(p.dg_f32, p.dg_cast, p.N, p.dtype, s, !prof, p.db_f32, p.db_cast);
-            if (e != cudaSuccess) return cuda_fail(e, "cast launch");
-        }
-    } else {
-        e = launch_finalize2(partials, G, 2 * p.N, p.N, p.dg_f32, p.dg_cast, p.db_f32, p.db_cast,
-                             p.dtype, s, !prof);
-        if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
-    }
-    return RN_OK;
+    if (use_row) plan_string_row(rp, "ln_row", atomic);
+    else plan_string_generic(gp, "ln_generic", atomic);
+    const DwOutputs o = {p.dg_f32, p.dg_cast, p.db_f32, p.db_cast, p.N, p.dtype,
+                         partials, use_row ? rp.grid : gp.grid, 2 * p.N};
+    return run_sequence(atomic, o, s, [&](bool pdl) {
+        return use_row ? launch_ln_bwd_row(p, rp, s, pdl) : launch_ln_bwd_generic(p, gp, s, pdl);
+    });
 }
 
 static rn_status check_common(int64_t M, int64_t N, int dtype) {
