@@ -396,6 +396,62 @@ def time_e2e(prob, steps, warmup, ws):
     return a.elapsed_time(z) / steps, h2d, d2h
 
 
+def time_forwards(dev, flush, steps, warmup, peak):
+    """The forwards (RMSNorm, fused-add, LayerNorm; bf16) at 4096x4096 and
+    16384x8192: mean device time per call with an L2 flush before each, the
+    algorithmic bytes (inputs read once, outputs and statistics written once)
+    over that time, and torch eager rms_norm on the same inputs beside them."""
+    import numpy as np
+    import torch
+    import rmsnorm_backward_bwd_gb300 as rn
+    from rmsnorm_backward_bwd_gb300 import synth
+    from rmsnorm_backward_bwd_gb300.synth import Case
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush()
+            fn()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            flush()
+            a.record(st)
+            fn()
+            b.record(st)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3
+
+    rows = []
+    for M, N in ((4096, 4096), (16384, 8192)):
+        inp = synth.make_inputs(Case("forward", M, N, "bf16", fused=True), device=str(dev))
+        x, r, g = inp["x"], inp["residual"], inp["gamma"]
+        y, ro = torch.empty_like(x), torch.empty_like(x)
+        mean = torch.empty(M, dtype=torch.float32, device=dev)
+        rstd = torch.empty(M, dtype=torch.float32, device=dev)
+        s = 2
+        plain = M * N * s * 2 + N * s + 4 * M
+        cases = [
+            ("rmsnorm_fwd", plain, lambda: rn.rmsnorm_fwd(x, g, 1e-6, y=y, rstd=rstd)),
+            ("fused_add_rmsnorm_fwd", M * N * s * 4 + N * s + 4 * M,
+             lambda: rn.fused_add_rmsnorm_fwd(x, r, g, 1e-6, out=y, residual_out=ro, rstd=rstd)),
+            ("layernorm_fwd (bias)", plain + N * s + 4 * M,
+             lambda: rn.layernorm_fwd(x, g, g, 1e-5, y=y, mean=mean, rstd=rstd)),
+        ]
+        for name, nbytes, fn in cases:
+            us = timed(fn)
+            rows.append({"workload": "%s bf16 M=%d N=%d" % (name, M, N), "us_per_call": round(us, 2),
+                         "GBps": round(nbytes / us / 1e3, 1),
+                         "pct_of_peak": round(100 * nbytes / us / 1e3 / peak, 1)})
+        us = timed(lambda: torch.nn.functional.rms_norm(x, (N,), g, 1e-6))
+        rows.append({"workload": "torch eager rms_norm bf16 M=%d N=%d" % (M, N),
+                     "us_per_call": round(us, 2)})
+        del inp, x, r, g, y, ro
+        torch.cuda.empty_cache()
+    return rows
+
+
 def autograd_problem(case, dev, impl):
     """Forward graph of one case built once (outside timing): returns
     (outputs, inputs, grad_outputs) for torch.autograd.grad. impl "ours" uses
@@ -622,6 +678,10 @@ def run_ours(args):
         del p3
         torch.cuda.empty_cache()
 
+    forward = []
+    if not args.no_extra:
+        forward = time_forwards(dev, flush, max(20, args.steps // 10), args.warmup, peak)
+
     autograd = []
     if not args.no_extra:
         for name in ("plain_4096", "fused_4096", "layernorm_4096"):
@@ -687,6 +747,7 @@ def run_ours(args):
             "plan": plan,
             "extra": extra,
             "autograd": autograd,
+            "forward": forward,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
