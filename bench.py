@@ -396,6 +396,55 @@ def time_e2e(prob, steps, warmup, ws):
     return a.elapsed_time(z) / steps, h2d, d2h
 
 
+# The shape table of the FlyDSL PR #854 backward benchmark ("Summary" table):
+# (op, M, N, dtype). The fused-add rows here pass a residual_out gradient.
+PAGES_AUTOGRAD_SHAPES = [(op, M, N, dt) for (M, N, dt) in
+                         ((1, 4096, "bf16"), (128, 4096, "bf16"), (4096, 4096, "bf16"),
+                          (512, 2048, "bf16"), (512, 3000, "f32"), (1024, 8192, "bf16"))
+                         for op in ("rmsnorm_bwd", "fused_add_bwd")]
+
+
+def autograd_pages_table(dev, steps=100, warmup=10):
+    """The public-autograd backward at the pages' benchmark shapes, this
+    package against torch eager on the same GPU, timed the pages' way: hot
+    cache, `warmup` calls, then the mean of `steps` calls between CUDA events;
+    backward allocations, the dweight zero and the cast are inside. Gradients
+    are compared before timing."""
+    import numpy as np
+    import torch
+    from rmsnorm_backward_bwd_gb300.synth import Case
+    rows = []
+    for op, M, N, dt in PAGES_AUTOGRAD_SHAPES:
+        case = Case(op, M, N, dt, fused=op == "fused_add_bwd", with_dres=op == "fused_add_bwd")
+        res = {"op": op, "M": M, "N": N, "dtype": dt}
+        grads = {}
+        for impl in ("ours", "torch_eager"):
+            outs, ins, gos = autograd_problem(case, dev, impl)
+            grads[impl] = [t.float() for t in torch.autograd.grad(outs, ins, gos, retain_graph=True)]
+            for _ in range(warmup):
+                torch.autograd.grad(outs, ins, gos, retain_graph=True)
+            torch.cuda.synchronize()
+            st = torch.cuda.current_stream()
+            ts = []
+            for _ in range(steps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                torch.autograd.grad(outs, ins, gos, retain_graph=True)
+                b.record(st)
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            res[impl + "_us"] = round(float(np.mean([a.elapsed_time(b) for a, b in ts])) * 1e3, 2)
+            del outs, ins, gos
+        res["max_rel_diff"] = float("%.3g" % max(
+            float((u - v).abs().max() / v.abs().max().clamp_min(1e-30))
+            for u, v in zip(grads["ours"], grads["torch_eager"])))
+        res["torch_over_ours"] = round(res["torch_eager_us"] / res["ours_us"], 2)
+        rows.append(res)
+        del grads
+        torch.cuda.empty_cache()
+    return rows
+
+
 def time_forwards(dev, flush, steps, warmup, peak):
     """The forwards (RMSNorm, fused-add, LayerNorm; bf16) at 4096x4096 and
     16384x8192: mean device time per call with an L2 flush before each, the
@@ -679,8 +728,10 @@ def run_ours(args):
         torch.cuda.empty_cache()
 
     forward = []
+    pages_table = []
     if not args.no_extra:
         forward = time_forwards(dev, flush, max(20, args.steps // 10), args.warmup, peak)
+        pages_table = autograd_pages_table(dev)
 
     autograd = []
     if not args.no_extra:
@@ -748,6 +799,7 @@ def run_ours(args):
             "extra": extra,
             "autograd": autograd,
             "forward": forward,
+            "autograd_pages_shapes": pages_table,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

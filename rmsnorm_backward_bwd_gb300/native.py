@@ -1,7 +1,9 @@
-"""ctypes view of the C ABI declared in ``include/rmsnorm_gb300.h``.
+"""ctypes view of the C ABI declared in ``include/rmsnorm_gb300.h``, and the
+loader of the PyTorch operator library over it.
 
-Loads ``_build/librn_gb300.so`` (built in-tree by ``build.py``). There is no
-fallback: if the library is missing or fails to load, every call raises.
+Loads ``_build/librn_gb300.so`` and ``_build/librn_torch.so`` (built in-tree
+by ``build.py``). There is no fallback: if a library is missing or fails to
+load, every call that needs it raises.
 """
 import ctypes
 import os
@@ -9,6 +11,7 @@ import re
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "librn_gb300.so")
+TORCH_LIB_PATH = os.path.join(HERE, "_build", "librn_torch.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "rmsnorm_gb300.h")
 
 RN_OK, RN_ERR_INVALID_ARG, RN_ERR_UNSUPPORTED, RN_ERR_CUDA, RN_ERR_WORKSPACE = range(5)
@@ -94,6 +97,26 @@ def lib():
         _apply_env(loaded)
         _lib = loaded
     return _lib
+
+
+_torch_ops = None
+
+
+def torch_ops():
+    """The operator namespace ``torch.ops.rn_gb300`` (the differentiable ops
+    and the raw calls as C++ PyTorch operators). The CUDA library is loaded
+    first, so that both views share one copy of it (one set of options)."""
+    global _torch_ops
+    if _torch_ops is None:
+        import torch
+        lib()
+        if not os.path.exists(TORCH_LIB_PATH):
+            raise RuntimeError("operator library %s is not built; run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`"
+                               % TORCH_LIB_PATH)
+        torch.ops.load_library(TORCH_LIB_PATH)
+        _torch_ops = torch.ops.rn_gb300
+    return _torch_ops
 
 
 def status_string(st):

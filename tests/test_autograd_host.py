@@ -1,11 +1,15 @@
-"""Host logic of the autograd wrappers (CPU only).
+"""Host logic of the C++ autograd functions (CPU only).
 
-The wrappers' own work is marshalling: flattening to [M, N], saving tensors,
-turning absent gradients into the right call, returning dx for both x and
-residual. Here the binding's calls are replaced by stand-ins built on the
-fp64 oracle so that this plumbing runs on the CPU, and the gradients that
-come out are compared with torch's own autograd of RMSNorm in fp64. The real
-calls refuse CPU tensors, which is checked too.
+The differentiable ops (``torch.ops.rn_gb300.rmsnorm`` / ``fused_add_rmsnorm``
+/ ``layernorm``, C++ in ``csrc/torch_ops.cpp``) do marshalling: flattening to
+[M, N], saving tensors, turning absent gradients into the right call,
+returning dx for both x and residual. They reach the computation through the
+raw operators (``rn_gb300::rmsnorm_fwd`` etc.), which the library registers
+for CUDA tensors only. Here a test-only CPU kernel for each raw operator,
+built on the fp64 oracle, is registered with the dispatcher for the length of
+a test, so that the C++ plumbing runs on the CPU; the gradients that come out
+are compared with torch's own autograd in fp64. The public functions refuse
+CPU tensors, which is checked too.
 """
 import numpy as np
 import pytest
@@ -14,14 +18,15 @@ import torch
 import oracle
 import rmsnorm_backward_bwd_gb300 as rn
 from rmsnorm_backward_bwd_gb300 import autograd as ag
+from rmsnorm_backward_bwd_gb300 import native
 
 
 def _np(t):
     return t.detach().to(torch.float64).numpy()
 
 
-class OracleOps:
-    """The four calls of the binding, computed by the oracle (fp32 I/O)."""
+class OracleKernels:
+    """CPU kernels of the raw operators, computed by the oracle (fp32 I/O)."""
 
     def __init__(self):
         self.calls = []
@@ -39,27 +44,54 @@ class OracleOps:
         return (torch.from_numpy(out).to(x.dtype), torch.from_numpy(added).to(x.dtype),
                 torch.from_numpy(oracle.round_to(rstd, "f32")).to(torch.float32))
 
-    def rmsnorm_bwd(self, x, gamma, dy, rstd, want_cast=True):
+    def rmsnorm_bwd(self, x, gamma, dy, rstd, want_cast):
         self.calls.append(("bwd", tuple(x.shape), want_cast))
         assert dy.is_contiguous() and dy.shape == x.shape
         dx, dw = oracle.rmsnorm_bwd(_np(x), _np(gamma), _np(dy), _np(rstd))
         dw32 = torch.from_numpy(dw).to(torch.float32)
         return (torch.from_numpy(dx).to(x.dtype), dw32.to(x.dtype) if want_cast else None, dw32)
 
-    def fused_add_rmsnorm_bwd(self, added, gamma, dy, rstd, dres=None, want_cast=True):
+    def fused_add_rmsnorm_bwd(self, added, gamma, dy, rstd, dres, want_cast):
         self.calls.append(("fused_bwd", tuple(added.shape), dres is not None, want_cast))
         dx, dw = oracle.fused_add_rmsnorm_bwd(_np(added), _np(gamma), _np(dy), _np(rstd),
                                               None if dres is None else _np(dres))
         dx = torch.from_numpy(dx).to(added.dtype)
         dw32 = torch.from_numpy(dw).to(torch.float32)
-        return dx, dx, dw32.to(added.dtype) if want_cast else None, dw32
+        return dx, dw32.to(added.dtype) if want_cast else None, dw32
+
+    def layernorm_fwd(self, x, gamma, beta, eps):
+        self.calls.append(("ln_fwd", tuple(x.shape), beta is not None))
+        y, mean, rstd = oracle.layernorm_fwd(_np(x), _np(gamma),
+                                             None if beta is None else _np(beta), np.float32(eps))
+        f32 = lambda a: torch.from_numpy(oracle.round_to(a, "f32")).to(torch.float32)  # noqa: E731
+        return torch.from_numpy(y).to(x.dtype), f32(mean), f32(rstd)
+
+    def layernorm_bwd(self, x, gamma, dy, mean, rstd, want_dbeta, want_cast):
+        self.calls.append(("ln_bwd", tuple(x.shape), want_dbeta, want_cast))
+        dx, dg, db = oracle.layernorm_bwd(_np(x), _np(gamma), _np(dy), _np(mean), _np(rstd))
+        dg32 = torch.from_numpy(dg).to(torch.float32)
+        db32 = torch.from_numpy(db).to(torch.float32) if want_dbeta else None
+        return (torch.from_numpy(dx).to(x.dtype), dg32.to(x.dtype) if want_cast else None,
+                db32.to(x.dtype) if (want_cast and want_dbeta) else None, dg32, db32)
+
+
+_RAW = ("rmsnorm_fwd", "rmsnorm_bwd", "fused_add_rmsnorm_fwd", "fused_add_rmsnorm_bwd",
+        "layernorm_fwd", "layernorm_bwd")
 
 
 @pytest.fixture
 def fake(monkeypatch):
-    ops = OracleOps()
-    monkeypatch.setattr(ag, "ops", ops)
-    return ops
+    native.torch_ops()   # the operators must exist before kernels are added to them
+    k = OracleKernels()
+    lib = torch.library.Library("rn_gb300", "IMPL")
+    for name in _RAW:
+        lib.impl(name, getattr(k, name), "CPU")
+    # let the public functions pass CPU tensors through to the operators
+    monkeypatch.setattr(ag, "_on_cuda", lambda name, t: None)
+    try:
+        yield k
+    finally:
+        lib._destroy()
 
 
 def _draw(shape, seed=0):
@@ -89,7 +121,7 @@ def test_rmsnorm_grads_any_rank(fake, shape):
     x, _, w, dy, _ = _draw(shape)
     eps = 1e-5
     xa, wa = x.clone().requires_grad_(), w.clone().requires_grad_()
-    y = ag.rmsnorm(xa, wa, eps)
+    y = rn.rmsnorm(xa, wa, eps)
     assert y.shape == x.shape
     (y * dy).sum().backward()
     x64, w64 = x.double().requires_grad_(), w.double().requires_grad_()
@@ -105,7 +137,7 @@ def test_rmsnorm_grads_any_rank(fake, shape):
 def test_rmsnorm_weight_grad_not_needed(fake):
     x, _, w, dy, _ = _draw((4, 32))
     xa = x.clone().requires_grad_()
-    y = ag.rmsnorm(xa, w, 1e-6)
+    y = rn.rmsnorm(xa, w, 1e-6)
     y.backward(dy)
     assert fake.calls[-1] == ("bwd", (4, 32), False)
     assert xa.grad is not None
@@ -114,7 +146,7 @@ def test_rmsnorm_weight_grad_not_needed(fake):
 def test_rmsnorm_noncontiguous_grad(fake):
     x, _, w, _, _ = _draw((5, 16))
     xa = x.clone().requires_grad_()
-    ag.rmsnorm(xa, w, 1e-6).sum().backward()   # dy is an expanded (stride 0) tensor
+    rn.rmsnorm(xa, w, 1e-6).sum().backward()   # dy is an expanded (stride 0) tensor
     x64 = x.double().requires_grad_()
     _torch_rms(x64, w.double(), 1e-6).sum().backward()
     _close(xa.grad, x64.grad)
@@ -139,7 +171,7 @@ def test_fused_grads(fake, use_out, use_res):
     x, r, w, dy, dres = _draw((2, 5, 48), seed=1)
     eps = 1e-6
     xa, ra, wa = (t.clone().requires_grad_() for t in (x, r, w))
-    out, res_out = ag.fused_add_rmsnorm(xa, ra, wa, eps)
+    out, res_out = rn.fused_add_rmsnorm(xa, ra, wa, eps)
     assert out.shape == x.shape and res_out.shape == x.shape
     loss = 0
     if use_out:
@@ -163,7 +195,7 @@ def test_fused_grads(fake, use_out, use_res):
 def test_fused_prenorm_false_returns_out_only(fake):
     x, r, w, dy, _ = _draw((3, 16), seed=2)
     xa = x.clone().requires_grad_()
-    out = ag.fused_add_rmsnorm(xa, r, w, 1e-6, prenorm=False)
+    out = rn.fused_add_rmsnorm(xa, r, w, 1e-6, prenorm=False)
     assert isinstance(out, torch.Tensor)
     (out * dy).sum().backward()
     _, _, gx, _, _ = _fused_reference(x, r, w, dy, dy, 1e-6, True, False)
@@ -185,3 +217,71 @@ def test_real_calls_refuse_cpu_tensors():
 def test_scalar_input_rejected():
     with pytest.raises(ValueError, match="at least one dimension"):
         rn.rmsnorm(torch.tensor(1.0), torch.ones(1))
+
+
+def _torch_ln(x64, w64, b64, eps):
+    return torch.nn.functional.layer_norm(x64, (x64.shape[-1],), w64, b64, eps)
+
+
+@pytest.mark.parametrize("with_bias", [True, False])
+@pytest.mark.parametrize("shape", [(6, 40), (2, 3, 24)])
+def test_layernorm_grads(fake, shape, with_bias):
+    x, _, w, dy, b = _draw(shape, seed=3)
+    b = b[(0,) * (len(shape) - 1)] if with_bias else None
+    eps = 1e-5
+    xa, wa = x.clone().requires_grad_(), w.clone().requires_grad_()
+    ba = b.clone().requires_grad_() if with_bias else None
+    y = rn.layernorm(xa, wa, ba, eps)
+    (y * dy).sum().backward()
+    x64, w64 = x.double().requires_grad_(), w.double().requires_grad_()
+    b64 = b.double().requires_grad_() if with_bias else None
+    (_torch_ln(x64, w64, b64, eps) * dy.double()).sum().backward()
+    _close(y, _torch_ln(x.double(), w.double(), None if b is None else b.double(), eps))
+    _close(xa.grad, x64.grad)
+    _close(wa.grad, w64.grad)
+    if with_bias:
+        _close(ba.grad, b64.grad)
+    M = int(np.prod(shape[:-1]))
+    assert fake.calls == [("ln_fwd", (M, shape[-1]), with_bias),
+                          ("ln_bwd", (M, shape[-1]), with_bias, True)]
+
+
+def test_layernorm_only_x_grad(fake):
+    x, _, w, dy, b = _draw((4, 16), seed=4)
+    xa = x.clone().requires_grad_()
+    rn.layernorm(xa, w, b[0]).backward(dy)
+    # neither weight nor bias needs a gradient: no dbeta, no casts
+    assert fake.calls[-1] == ("ln_bwd", (4, 16), False, False)
+    x64 = x.double().requires_grad_()
+    (_torch_ln(x64, w.double(), b[0].double(), 1e-5) * dy.double()).sum().backward()
+    _close(xa.grad, x64.grad)
+
+
+def test_no_input_needs_grad_skips_backward(fake):
+    x, _, w, _, _ = _draw((3, 8))
+    y = rn.rmsnorm(x, w)
+    assert not y.requires_grad
+    assert fake.calls == [("fwd", (3, 8))]
+
+
+def test_residual_shape_checked_by_the_autograd_layer(fake):
+    x, r, w, _, _ = _draw((3, 8))
+    with pytest.raises(ValueError, match="residual has shape"):
+        rn.fused_add_rmsnorm(x, r[:, :4], w)
+
+
+def test_raw_operators_have_no_cpu_kernel():
+    ops = native.torch_ops()
+    x = torch.randn(2, 8)
+    with pytest.raises(NotImplementedError):
+        ops.rmsnorm_fwd(x, torch.ones(8), 1e-6)
+    with pytest.raises(NotImplementedError):
+        ops.rmsnorm(x, torch.ones(8), 1e-6)
+
+
+def test_public_classes_forward_to_the_operators(fake):
+    x, r, w, _, b = _draw((2, 8), seed=5)
+    assert torch.equal(rn.RMSNormFunction.apply(x, w, 1e-6), rn.rmsnorm(x, w, 1e-6))
+    out, res = rn.FusedAddRMSNormFunction.apply(x, r, w, 1e-6)
+    assert torch.equal(res, x + r)
+    assert torch.equal(rn.LayerNormFunction.apply(x, w, b[0], 1e-5), rn.layernorm(x, w, b[0]))
