@@ -199,6 +199,7 @@ def workload_case(name):
     table = {"plain_4096": synth.PLAIN_4096, "fused_4096": synth.FUSED_4096,
              "fused_4096_nodres": synth.FUSED_4096_NODRES, "plain_16384x8192": synth.LARGE_PLAIN,
              "fused_16384x8192": synth.LARGE_FUSED, "layernorm_4096": synth.LN_4096,
+             "layernorm_16384x8192": synth.LN_LARGE,
              "plain_4096x32768": synth.LONG_ROWS}
     return table[name]
 
@@ -496,6 +497,9 @@ def time_forwards(dev, flush, steps, warmup, peak):
         us = timed(lambda: torch.nn.functional.rms_norm(x, (N,), g, 1e-6))
         rows.append({"workload": "torch eager rms_norm bf16 M=%d N=%d" % (M, N),
                      "us_per_call": round(us, 2)})
+        us = timed(lambda: torch.nn.functional.layer_norm(x, (N,), g, g, 1e-5))
+        rows.append({"workload": "torch eager layer_norm (bias) bf16 M=%d N=%d" % (M, N),
+                     "us_per_call": round(us, 2)})
         del inp, x, r, g, y, ro
         torch.cuda.empty_cache()
     return rows
@@ -712,20 +716,21 @@ def run_ours(args):
             del p2
             torch.cuda.empty_cache()
         from rmsnorm_backward_bwd_gb300 import synth as _synth
-        p3 = LnProblem(_synth.LN_4096, dev)
-        n3 = max(20, args.steps // 4)
-        cms, _, _ = time_calls(p3, n3, args.warmup, flush, ws)
-        _, kms3, _ = time_calls(p3, n3, 3, flush, ws, kernel_events=True)
-        t3, k3 = float(np.mean(cms)), float(np.mean(kms3))
-        extra.append({"workload": p3.case.name + " (dgamma + dbeta)",
-                      "us_per_call": round(t3 * 1e3, 2),
-                      "GBps": round(p3.bytes / (t3 * 1e-3) / 1e9, 1),
-                      "pct_of_peak": round(100 * p3.bytes / (t3 * 1e-3) / 1e9 / peak, 1),
-                      "row_pass_us": round(k3 * 1e3, 2),
-                      "row_pass_GBps": round(p3.row_pass_bytes / (k3 * 1e-3) / 1e9, 1),
-                      "plan": native.last_plan()})
-        del p3
-        torch.cuda.empty_cache()
+        for ln_case in (_synth.LN_4096, _synth.LN_LARGE):
+            p3 = LnProblem(ln_case, dev)
+            n3 = max(20, args.steps // 4)
+            cms, _, _ = time_calls(p3, n3, args.warmup, flush, ws)
+            _, kms3, _ = time_calls(p3, n3, 3, flush, ws, kernel_events=True)
+            t3, k3 = float(np.mean(cms)), float(np.mean(kms3))
+            extra.append({"workload": p3.case.name + " (dgamma + dbeta)",
+                          "us_per_call": round(t3 * 1e3, 2),
+                          "GBps": round(p3.bytes / (t3 * 1e-3) / 1e9, 1),
+                          "pct_of_peak": round(100 * p3.bytes / (t3 * 1e-3) / 1e9 / peak, 1),
+                          "row_pass_us": round(k3 * 1e3, 2),
+                          "row_pass_GBps": round(p3.row_pass_bytes / (k3 * 1e-3) / 1e9, 1),
+                          "plan": native.last_plan()})
+            del p3
+            torch.cuda.empty_cache()
 
     forward = []
     pages_table = []

@@ -93,6 +93,10 @@ class _on_device:
 
 _WS = {}
 _WS_BYTES = {}
+# Workspaces replaced by a larger one stay allocated: a CUDA graph captured
+# on that stream may still use the smaller buffer, and freeing it would let
+# the allocator hand the memory to someone else under the graph.
+_WS_RETIRED = []
 
 
 def _ws_bytes(M, N, code, index):
@@ -125,6 +129,8 @@ def _workspace(M, N, code, index, layernorm=False):
     key = (index, _stream_handle(index))
     ws = _WS.get(key)
     if ws is None or ws.numel() < n:
+        if ws is not None:
+            _WS_RETIRED.append(ws)
         ws = torch.empty(n, dtype=torch.uint8, device=torch.device("cuda", index))
         _WS[key] = ws
     return ws

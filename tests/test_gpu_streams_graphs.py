@@ -11,7 +11,7 @@ import torch
 
 import parity
 import rmsnorm_backward_bwd_gb300 as rn
-from rmsnorm_backward_bwd_gb300 import native
+from rmsnorm_backward_bwd_gb300 import native, ops
 from rmsnorm_backward_bwd_gb300.synth import Case
 
 pytestmark = pytest.mark.gpu
@@ -85,3 +85,40 @@ def test_backward_captured_in_a_cuda_graph(case, mode):
     graph.replay()
     torch.cuda.synchronize()
     parity.check_bwd(ex, dx, dw, dw32)
+
+
+def test_graph_keeps_its_workspace_after_the_cache_grows():
+    """A graph captured on a stream whose cached workspace then grows (a wider
+    call on the same stream) must still own its buffer: the binding keeps the
+    smaller workspace allocated, so no later tensor is placed under the
+    graph's scratch writes."""
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)      # scratch: the partials live in the workspace
+    ex = parity.expected_bwd(Case("graph ws small", 512, 1024, "bf16"))
+    t = _device_inputs(ex)
+    x, g, dy, rstd = t["x"], t["g"], t["dy"], t["rstd"]
+    dx = torch.empty_like(x)
+    dw32 = torch.empty(1024, dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        rn.rmsnorm_bwd(x, g, dy, rstd, dx=dx, dweight_f32=dw32)   # caches this stream's workspace
+        small_ws_bytes = ops._ws_bytes(512, 1024, native.RN_BF16, 0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        rn.rmsnorm_bwd(x, g, dy, rstd, dx=dx, dweight_f32=dw32)
+    # a wider call on the same stream replaces the cached workspace
+    wide = parity.expected_bwd(Case("graph ws wide", 64, 8192, "bf16"))
+    tw = _device_inputs(wide)
+    with torch.cuda.stream(side):
+        rn.rmsnorm_bwd(tw["x"], tw["g"], tw["dy"], tw["rstd"])
+    torch.cuda.synchronize()
+    # tensors of the small workspace's size: the allocator would hand them its block if freed
+    canaries = [torch.full((small_ws_bytes,), 0x5A, dtype=torch.uint8, device="cuda")
+                for _ in range(4)]
+    dx.fill_(7)
+    graph.replay()
+    torch.cuda.synchronize()
+    parity.check_bwd(ex, dx, None, dw32)
+    for c in canaries:
+        assert bool((c == 0x5A).all()), "a graph replay wrote into a later tensor"
