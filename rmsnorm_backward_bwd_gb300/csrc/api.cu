@@ -465,8 +465,24 @@ static bool plan_ln_row(const LnBwdProblem &p, const DeviceInfo &d, RowPlan *pla
     if (row_bytes % 16) return false;
     if (!aligned16(p.x) || !aligned16(p.dy) || !aligned16(p.gamma) || !aligned16(p.dx))
         return false;
-    return plan_row_tile(p.M, row_bytes / 16, 2, ln_row_smem_bytes(0, 0, 0), kLnMaxCpt,
-                         ln_row_max_threads, d, plan);
+    const int nchunks = row_bytes / 16;
+    const size_t red = ln_row_smem_bytes(0, 0, 0);
+    if (!plan_row_tile(p.M, nchunks, 2, red, kLnMaxCpt, ln_row_max_threads, d, plan)) return false;
+    const bool forced = g_opts[RN_OPT_CHUNKS_PER_THREAD] || g_opts[RN_OPT_TEAMS_PER_CTA];
+    // Measured on GB300 (bf16): when 2 chunks per thread leave one team per
+    // SM, 4 chunks per thread and two teams are faster (N = 8192: 131.9 vs
+    // 147.5 us at M = 16384, 42.1 vs 47.7 us at M = 4096).
+    if (plan->teams == 1 && plan->cpt == 2 && !forced) {
+        RowPlan wide;
+        if (plan_row_tile(p.M, nchunks, 2, red, 4, ln_row_max_threads, d, &wide) && wide.teams >= 2)
+            *plan = wide;
+    }
+    // A team alone on its SM: a 2-slot ring (N = 16384: 136.4 vs 140.1 us for 3 slots).
+    if (plan->teams == 1 && plan->stages > 2 && g_opts[RN_OPT_STAGES] == 0) {
+        plan->stages = 2;
+        plan->smem = ln_row_smem_bytes(plan->teams, 2, plan->cpt * plan->team_threads);
+    }
+    return true;
 }
 
 static size_t ln_cluster_smem(int stages, int, int cpt, int threads) {

@@ -261,6 +261,22 @@ def test_layernorm_rows_up_to_the_tile_limit_use_the_row_engine(M, N):
     check(ex, out)
 
 
+@pytest.mark.parametrize("M,N,dt,tile", [(1024, 8192, "bf16", "cpt=4 team_threads=256 teams=2"),
+                                         (700, 6144, "f16", "cpt=4 team_threads=192 teams=2"),
+                                         (600, 4096, "f32", "cpt=4 team_threads=256 teams=2"),
+                                         (1024, 16384, "bf16", "cpt=4 team_threads=512 teams=1 stages=2")],
+                         ids=lambda v: str(v))
+def test_layernorm_wide_rows_default_tile(M, N, dt, tile):
+    """Where 2 chunks per thread would leave one team per SM, the default
+    tile takes 4 chunks per thread and two teams; a team alone on its SM
+    gets a 2-slot ring."""
+    ex = expected(Case("ln", M, N, dt, eps=1e-5, seed=15))
+    out = run_gpu(ex)
+    plan = native.last_plan()
+    assert "engine=ln_row" in plan and tile in plan, plan
+    check(ex, out, tag=" [%s]" % plan)
+
+
 @pytest.mark.parametrize("M,N,dt,csize", [(24, 32768, "bf16", 2), (6, 65536, "bf16", 4),
                                           (40, 16392, "bf16", 2), (16, 16384, "f32", 2),
                                           (3, 131072, "f16", 8)],
