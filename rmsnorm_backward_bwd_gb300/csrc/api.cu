@@ -300,12 +300,36 @@ static bool plan_cluster(const BwdProblem &p, const DeviceInfo &d, bool atomic, 
     return cluster_count("rms", p.M, p.dtype, p.dres != nullptr, d, plan, rms_cluster_query, &p);
 }
 
+// The generic engine's vector variant needs every row tensor at the same
+// alignment phase (base addresses equal modulo 16, element-aligned) and the
+// weight-gradient partial in shared memory.
+static bool generic_vec_ok(const BwdProblem &p, const DeviceInfo &d) {
+    const uintptr_t S = (uintptr_t)elem_bytes(p.dtype);
+    const uintptr_t ph = (uintptr_t)p.x & 15u;
+    for (const void *q : {p.x, p.dy, static_cast<const void *>(p.dx), p.dres}) {
+        if (q == nullptr) continue;
+        if (((uintptr_t)q & 15u) != ph || ((uintptr_t)q % S) != 0) return false;
+    }
+    const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
+    return generic_vec_smem_bytes(p.N) <= budget;
+}
+
 static void plan_generic(const BwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
     plan->smem_dw = generic_smem_bytes(p.N, true) <= budget;
     plan->smem = generic_smem_bytes(p.N, plan->smem_dw);
-    int64_t grid = p.M;
+    plan->rows = 0;
+    if (generic_vec_ok(p, d)) {
+        // rows in flight per CTA iteration: 4 when a row's chunks leave most
+        // threads idle, else 2
+        const int chunks = (int)((int64_t)p.N * elem_bytes(p.dtype) / 16);
+        plan->threads = chunks >= 256 ? 512 : 256;
+        plan->rows = chunks * 2 < plan->threads ? 4 : 2;
+        plan->smem_dw = true;
+        plan->smem = generic_vec_smem_bytes(p.N);
+    }
+    int64_t grid = plan->rows ? (p.M + plan->rows - 1) / plan->rows : p.M;
     if (grid > max_partial_rows(d)) grid = max_partial_rows(d);
     if (g_opts[RN_OPT_GRID] > 0 && grid > g_opts[RN_OPT_GRID]) grid = g_opts[RN_OPT_GRID];
     if (grid < 1) grid = 1;
@@ -388,8 +412,12 @@ static void plan_string_row(const RowPlan &rp, const char *engine, bool atomic) 
 }
 
 static void plan_string_generic(const GenericPlan &gp, const char *engine, bool atomic) {
-    snprintf(g_plan, sizeof(g_plan), "engine=%s threads=%d grid=%d smem_dw=%d dw=%s", engine,
-             gp.threads, gp.grid, (int)gp.smem_dw, atomic ? "atomic" : "scratch");
+    if (gp.rows)
+        snprintf(g_plan, sizeof(g_plan), "engine=%s vec rows=%d threads=%d grid=%d dw=%s", engine,
+                 gp.rows, gp.threads, gp.grid, atomic ? "atomic" : "scratch");
+    else
+        snprintf(g_plan, sizeof(g_plan), "engine=%s threads=%d grid=%d smem_dw=%d dw=%s", engine,
+                 gp.threads, gp.grid, (int)gp.smem_dw, atomic ? "atomic" : "scratch");
 }
 
 static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
@@ -435,14 +463,14 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
         return run_sequence(atomic, o, s, [&](bool pdl) { return launch_bwd_cluster(p, cp, s, pdl); });
     }
     if (!use_row) plan_generic(p, d, &gp);
-    if (!use_row && atomic && generic_smem_bytes(p.N, true) > d.smem_optin) {
+    if (!use_row && atomic && !gp.rows && generic_smem_bytes(p.N, true) > d.smem_optin) {
         // the generic engine keeps its atomic-mode partial in shared memory
         if (g_opts[RN_OPT_DWEIGHT_MODE] == 2)
             return fail(RN_ERR_UNSUPPORTED, "atomic mode needs N*4 bytes of shared memory");
         atomic = false;
     }
     rp.atomic = gp.atomic = atomic;
-    if (!use_row && atomic) {
+    if (!use_row && atomic && !gp.rows) {
         gp.smem_dw = true;
         gp.smem = generic_smem_bytes(p.N, true);
     }

@@ -52,11 +52,12 @@ struct ClusterPlan {
 };
 
 struct GenericPlan {
-    int threads;       // CTA size; one row per CTA at a time
+    int threads;       // CTA size
     int grid;
     bool smem_dw;      // per-CTA weight-gradient partial in shared memory
     size_t smem;
     bool atomic;
+    int rows = 0;      // vector variant: rows in flight per CTA iteration (2, 4); 0 = scalar
 };
 
 // Row engine: largest chunk count per row and CTA thread cap for a cpt.
@@ -64,6 +65,7 @@ constexpr int kRowMaxChunks = 2048;
 int row_max_threads(int cpt);
 size_t row_smem_bytes(int teams, int stages, int ntensors, int team_chunks);
 size_t generic_smem_bytes(int N, bool smem_dw);
+size_t generic_vec_smem_bytes(int N);
 
 cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_t s,
                            bool pdl_after_zero);

@@ -225,3 +225,55 @@ def test_generic_engine_falls_back_to_scratch_partials_for_wide_rows():
     native.set_option(native.OPT_DWEIGHT_MODE, 2)
     with pytest.raises(native.RNError, match="atomic mode"):
         parity.run_gpu_bwd(ex)
+
+
+def test_mismatched_alignment_phases_take_the_scalar_generic_kernel():
+    """x one element off 16-byte alignment while dy and dx are not: no common
+    phase for 16-byte chunks, so the element-wise generic kernel runs."""
+    import rmsnorm_backward_bwd_gb300 as rn
+    case = Case("bf16 M=48 N=1000", 48, 1000, "bf16")
+    ex = parity.expected_bwd(case)
+    buf = torch.empty(ex.x.numel() + 1, dtype=ex.x.dtype, device="cuda")
+    x = buf[1:].view(ex.x.shape)
+    x.copy_(ex.x.cuda())
+    dx, dw, dw32 = rn.rmsnorm_bwd(x, ex.gamma.cuda(), ex.dy.cuda(), ex.rstd.cuda())
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert plan.startswith("engine=generic") and "vec" not in plan, plan
+    parity.check_bwd(ex, dx, dw, dw32)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("M,N,dt,fused,rows", [
+    (1000, 4095, "bf16", False, 2), (333, 4100, "bf16", True, 2), (97, 2999, "f32", False, 2),
+    (130, 1001, "f16", True, 4), (5, 7, "bf16", False, 4), (3, 3, "f32", True, 4),
+    (777, 8190, "f16", False, 2), (64, 515, "bf16", True, 4)],
+    ids=lambda v: str(v))
+def test_generic_vector_variant(M, N, dt, fused, rows, mode):
+    """Rows that are not 16-byte multiples, all tensors at one phase: 16-byte
+    chunks plus element-wise head and tail, several rows per CTA iteration
+    (M not a multiple of them), both weight-gradient modes."""
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    ex = parity.expected_bwd(Case("vec %s" % dt, M, N, dt, fused=fused, with_dres=fused, seed=21))
+    out = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    assert "engine=generic vec rows=%d" % rows in plan, plan
+    assert ("atomic" if mode == 2 else "scratch") in plan, plan
+    parity.check_bwd(ex, *out, tag=" [%s]" % plan)
+
+
+def test_generic_vector_variant_small_grid_and_dres_as_dx():
+    """Few CTAs for many rows (the grid option), and dx written over
+    dresidual_out in place."""
+    import rmsnorm_backward_bwd_gb300 as rn
+    native.set_option(native.OPT_GRID, 3)
+    ex = parity.expected_bwd(Case("vec grid", 501, 2047, "bf16", fused=True, with_dres=True,
+                                  seed=22))
+    x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
+    dres = ex.dres.cuda()
+    dx, dres_out, dw, dw32 = rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, dres, dx=dres)
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert "vec" in plan and "grid=3" in plan, plan
+    assert dx.data_ptr() == dres.data_ptr()
+    parity.check_bwd(ex, dx, dw, dw32)
