@@ -59,9 +59,23 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic():
+# The row-pass kernel each engine launches (from the plan string).
+ENGINE_KERNELS = {"row": "bwd_row_kernel", "cluster": "bwd_cluster_kernel",
+                  "generic vec": "bwd_generic_vec_kernel", "generic": "bwd_generic_kernel"}
+
+
+def row_pass_kernel(plan):
+    engine = plan.split("engine=", 1)[1].split(" threads=")[0].split(" rows=")[0] if plan else ""
+    engine = engine.split(" cpt=")[0].split(" csize=")[0]
+    return ENGINE_KERNELS.get(engine, engine)
+
+
+def ncu_traffic(workload):
     """DRAM bytes per launch of the row-pass kernel from the committed ncu
-    summary, if that summary was taken on the current kernel source."""
+    summary, if that summary covers this workload and was taken on the
+    current kernel source."""
+    if workload != "plain_4096":
+        return None
     try:
         with open(PROFILE_SUMMARY) as f:
             text = f.read()
@@ -200,7 +214,7 @@ def workload_case(name):
              "fused_4096_nodres": synth.FUSED_4096_NODRES, "plain_16384x8192": synth.LARGE_PLAIN,
              "fused_16384x8192": synth.LARGE_FUSED, "layernorm_4096": synth.LN_4096,
              "layernorm_16384x8192": synth.LN_LARGE,
-             "plain_4096x32768": synth.LONG_ROWS}
+             "plain_4096x32768": synth.LONG_ROWS, "plain_4096x4095": synth.UNALIGNED_ROWS}
     return table[name]
 
 
@@ -698,7 +712,7 @@ def run_ours(args):
     extra = []
     if not args.no_extra:
         for name in ("fused_4096", "fused_4096_nodres", "plain_16384x8192", "fused_16384x8192",
-                     "plain_4096x32768"):
+                     "plain_4096x32768", "plain_4096x4095"):
             if name == args.workload:
                 continue
             p2 = Problem(workload_case(name), dev)
@@ -790,7 +804,7 @@ def run_ours(args):
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": ncu_traffic(), "kernel": "bwd_row_kernel",
+                         "traffic": ncu_traffic(args.workload), "kernel": row_pass_kernel(plan),
                          "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": prob.row_pass_bytes,
                          "us_per_launch": round(kms * 1e3, 2)},
@@ -820,7 +834,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="plain_4096",
                     choices=["plain_4096", "fused_4096", "fused_4096_nodres", "plain_16384x8192",
-                             "fused_16384x8192", "plain_4096x32768"])
+                             "fused_16384x8192", "plain_4096x32768", "plain_4096x4095"])
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
