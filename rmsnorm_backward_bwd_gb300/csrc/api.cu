@@ -314,7 +314,43 @@ static bool generic_vec_ok(const BwdProblem &p, const DeviceInfo &d) {
     return generic_vec_smem_bytes(p.N) <= budget;
 }
 
+// The realigning engine: the vector variant's conditions, and a row of 1024
+// to 4 x 512 column blocks of 16 bytes (16 KB to 32 KB: bf16 N 8,185 to
+// 16,384) whose buffers fit the shared-memory budget. Measured on GB300 (L2
+// flushed, us per call, vector variant -> realigning engine): bf16 16384 x
+// 8190 292 -> 233 (fused 321 -> 275), f32 4096 x 4095 68 -> 58 (fused
+// 77 -> 67); below 1024 blocks the vector variant was faster (bf16 4096 x
+// 4100 48 vs 56, 4096 x 4095 51 vs 53).
+static bool plan_realign(const BwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
+    if (!generic_vec_ok(p, d)) return false;
+    const int nb = (int)(((int64_t)p.N * elem_bytes(p.dtype) + 15) / 16);
+    if (nb < 1024) return false;
+    int cpb = 2;
+    while (cpb < 4 && (nb + cpb - 1) / cpb > 512) cpb *= 2;
+    if ((nb + cpb - 1) / cpb > 512) return false;
+    const int rows = 1;  // rows per CTA iteration (the kernel's R)
+    const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
+    const size_t smem = realign_smem_bytes(p.N, p.dtype, rows, p.dres != nullptr);
+    if (smem > budget) return false;
+    plan->cpb = cpb;
+    plan->rows = rows;
+    plan->threads = ((nb + cpb - 1) / cpb + 31) / 32 * 32;
+    plan->smem_dw = false;
+    plan->smem = smem;
+    // two CTAs per SM when a CTA has at most 256 threads, else one
+    int64_t grid = (p.M + rows - 1) / rows;
+    const int64_t cap = plan->threads <= 256 ? max_partial_rows(d) : d.num_sms;
+    if (grid > cap) grid = cap;
+    if (g_opts[RN_OPT_GRID] > 0 && grid > g_opts[RN_OPT_GRID]) grid = g_opts[RN_OPT_GRID];
+    if (grid < 1) grid = 1;
+    plan->grid = (int)grid;
+    plan->atomic = false;
+    return true;
+}
+
 static void plan_generic(const BwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
+    plan->cpb = 0;
+    if (plan_realign(p, d, plan)) return;
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
     plan->smem_dw = generic_smem_bytes(p.N, true) <= budget;
@@ -412,7 +448,10 @@ static void plan_string_row(const RowPlan &rp, const char *engine, bool atomic) 
 }
 
 static void plan_string_generic(const GenericPlan &gp, const char *engine, bool atomic) {
-    if (gp.rows)
+    if (gp.cpb)
+        snprintf(g_plan, sizeof(g_plan), "engine=%s realign cpb=%d rows=%d threads=%d grid=%d dw=%s",
+                 engine, gp.cpb, gp.rows, gp.threads, gp.grid, atomic ? "atomic" : "scratch");
+    else if (gp.rows)
         snprintf(g_plan, sizeof(g_plan), "engine=%s vec rows=%d threads=%d grid=%d dw=%s", engine,
                  gp.rows, gp.threads, gp.grid, atomic ? "atomic" : "scratch");
     else
@@ -463,14 +502,15 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
         return run_sequence(atomic, o, s, [&](bool pdl) { return launch_bwd_cluster(p, cp, s, pdl); });
     }
     if (!use_row) plan_generic(p, d, &gp);
-    if (!use_row && atomic && !gp.rows && generic_smem_bytes(p.N, true) > d.smem_optin) {
+    if (!use_row && atomic && !gp.rows && !gp.cpb &&
+        generic_smem_bytes(p.N, true) > d.smem_optin) {
         // the generic engine keeps its atomic-mode partial in shared memory
         if (g_opts[RN_OPT_DWEIGHT_MODE] == 2)
             return fail(RN_ERR_UNSUPPORTED, "atomic mode needs N*4 bytes of shared memory");
         atomic = false;
     }
     rp.atomic = gp.atomic = atomic;
-    if (!use_row && atomic && !gp.rows) {
+    if (!use_row && atomic && !gp.rows && !gp.cpb) {
         gp.smem_dw = true;
         gp.smem = generic_smem_bytes(p.N, true);
     }
@@ -479,7 +519,8 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
     const DwOutputs o = {p.dw_f32, p.dw_cast, nullptr, nullptr, p.N, p.dtype,
                          partials, use_row ? rp.grid : gp.grid, p.N};
     return run_sequence(atomic, o, s, [&](bool pdl) {
-        return use_row ? launch_bwd_row(p, rp, s, pdl) : launch_bwd_generic(p, gp, s, pdl);
+        if (use_row) return launch_bwd_row(p, rp, s, pdl);
+        return gp.cpb ? launch_bwd_realign(p, gp, s, pdl) : launch_bwd_generic(p, gp, s, pdl);
     });
 }
 

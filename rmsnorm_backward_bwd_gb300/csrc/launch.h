@@ -58,6 +58,7 @@ struct GenericPlan {
     size_t smem;
     bool atomic;
     int rows = 0;      // vector variant: rows in flight per CTA iteration (2, 4); 0 = scalar
+    int cpb = 0;       // realigning engine: column blocks per thread (2, 4); 0 = not used
 };
 
 // Row engine: largest chunk count per row and CTA thread cap for a cpt.
@@ -70,6 +71,10 @@ size_t generic_vec_smem_bytes(int N);
 cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_t s,
                            bool pdl_after_zero);
 cudaError_t launch_bwd_generic(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
+                               bool pdl_after_zero);
+// Rows that are not 16-byte multiples, all row tensors at one alignment phase.
+size_t realign_smem_bytes(int N, int dtype, int rows, bool dres);
+cudaError_t launch_bwd_realign(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
                                bool pdl_after_zero);
 size_t cluster_smem_bytes(int stages, int ntensors, int cpt, int threads);
 // Clusters of plan's shape that fit on the device at once (occupancy query).

@@ -244,17 +244,40 @@ def test_mismatched_alignment_phases_take_the_scalar_generic_kernel():
 
 
 @pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("M,N,dt,fused,cpb", [
+    (777, 8190, "f16", False, 2), (300, 8190, "bf16", False, 2), (17, 8191, "bf16", True, 2),
+    (33, 4095, "f32", True, 2), (50, 12289, "bf16", True, 4), (40, 16383, "bf16", False, 4),
+    (9, 4097, "f32", False, 4)],
+    ids=lambda v: str(v))
+def test_generic_realigning_engine(M, N, dt, fused, cpb, mode):
+    """Rows of 16 to 32 KB that are not 16-byte multiples, all tensors at one
+    phase: aligned chunks through a shared row buffer, fixed column blocks
+    read back by the row's phase, dx out as aligned chunks (2 and 4 blocks per
+    thread; both weight-gradient modes)."""
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    ex = parity.expected_bwd(Case("realign %s" % dt, M, N, dt, fused=fused, with_dres=fused,
+                                  seed=21))
+    out = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    assert "engine=generic realign cpb=%d" % cpb in plan, plan
+    assert ("atomic" if mode == 2 else "scratch") in plan, plan
+    parity.check_bwd(ex, *out, tag=" [%s]" % plan)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("M,N,dt,fused,rows", [
     (1000, 4095, "bf16", False, 2), (333, 4100, "bf16", True, 2), (97, 2999, "f32", False, 2),
     (130, 1001, "f16", True, 4), (5, 7, "bf16", False, 4), (3, 3, "f32", True, 4),
-    (777, 8190, "f16", False, 2), (64, 515, "bf16", True, 4)],
+    (64, 515, "bf16", True, 4), (24, 20001, "bf16", False, 2), (16, 18001, "f16", True, 2)],
     ids=lambda v: str(v))
 def test_generic_vector_variant(M, N, dt, fused, rows, mode):
-    """Rows that are not 16-byte multiples, all tensors at one phase: 16-byte
-    chunks plus element-wise head and tail, several rows per CTA iteration
-    (M not a multiple of them), both weight-gradient modes."""
+    """Rows under 16 KB (or past the realigning engine's 32 KB) that are not
+    16-byte multiples, all tensors at one phase: 16-byte chunks plus
+    element-wise head and tail, several rows per CTA iteration (M not a
+    multiple of them), shared partial with atomic adds; both weight-gradient
+    modes."""
     native.set_option(native.OPT_DWEIGHT_MODE, mode)
-    ex = parity.expected_bwd(Case("vec %s" % dt, M, N, dt, fused=fused, with_dres=fused, seed=21))
+    ex = parity.expected_bwd(Case("vec %s" % dt, M, N, dt, fused=fused, with_dres=fused, seed=23))
     out = parity.run_gpu_bwd(ex)
     plan = native.last_plan()
     assert "engine=generic vec rows=%d" % rows in plan, plan
@@ -262,18 +285,18 @@ def test_generic_vector_variant(M, N, dt, fused, rows, mode):
     parity.check_bwd(ex, *out, tag=" [%s]" % plan)
 
 
-def test_generic_vector_variant_small_grid_and_dres_as_dx():
+def test_generic_realigning_small_grid_and_dres_as_dx():
     """Few CTAs for many rows (the grid option), and dx written over
     dresidual_out in place."""
     import rmsnorm_backward_bwd_gb300 as rn
     native.set_option(native.OPT_GRID, 3)
-    ex = parity.expected_bwd(Case("vec grid", 501, 2047, "bf16", fused=True, with_dres=True,
+    ex = parity.expected_bwd(Case("realign grid", 501, 8190, "bf16", fused=True, with_dres=True,
                                   seed=22))
     x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
     dres = ex.dres.cuda()
     dx, dres_out, dw, dw32 = rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, dres, dx=dres)
     torch.cuda.synchronize()
     plan = native.last_plan()
-    assert "vec" in plan and "grid=3" in plan, plan
+    assert "realign" in plan and "grid=3" in plan, plan
     assert dx.data_ptr() == dres.data_ptr()
     parity.check_bwd(ex, dx, dw, dw32)
