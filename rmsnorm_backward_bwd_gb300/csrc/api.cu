@@ -722,26 +722,26 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
     const int nt = fused ? 2 : 1;
     const bool row = vec && plan_row_tile(M, (int)(N * eb / 16), nt, fwd_row_smem_bytes(0, 0, nt, 0),
                                           4, row_max_threads, d, &rp, false);
-    if (vec) {
-        FwdRowProblem q;
-        q.mode = fused ? kFwdFused : kFwdRms;
-        q.x = x;
-        q.residual = fused ? residual : nullptr;
-        q.gamma = gamma;
-        q.beta = nullptr;
-        q.y = y;
-        q.residual_out = fused ? residual_out : nullptr;
-        q.mean = nullptr;
-        q.rstd = rstd;
-        q.eps = eps;
-        q.M = M;
-        q.N = (int)N;
-        q.dtype = dtype;
-        e = row ? launch_fwd_row(q, rp, static_cast<cudaStream_t>(stream))
-                : launch_fwd_long(q, d.num_sms, static_cast<cudaStream_t>(stream));
-    } else {
-        e = launch_fwd(p, d.num_sms, static_cast<cudaStream_t>(stream));
-    }
+    FwdRowProblem q;
+    q.mode = fused ? kFwdFused : kFwdRms;
+    q.x = x;
+    q.residual = fused ? residual : nullptr;
+    q.gamma = gamma;
+    q.beta = nullptr;
+    q.y = y;
+    q.residual_out = fused ? residual_out : nullptr;
+    q.mean = nullptr;
+    q.rstd = rstd;
+    q.eps = eps;
+    q.M = M;
+    q.N = (int)N;
+    q.dtype = dtype;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (vec)
+        e = row ? launch_fwd_row(q, rp, cs) : launch_fwd_long(q, d.num_sms, cs);
+    else
+        e = fwd_generic_vec_ok(q) ? launch_fwd_generic_vec(q, d.num_sms, cs)
+                                  : launch_fwd(p, d.num_sms, cs);
     return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
 }
 
@@ -775,26 +775,26 @@ static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta
     RowPlan rp;
     const bool row = vec && plan_row_tile(M, (int)(N * eb / 16), 1, fwd_row_smem_bytes(0, 0, 1, 0),
                                           4, row_max_threads, d, &rp, false);
-    if (vec) {
-        FwdRowProblem q;
-        q.mode = kFwdLn;
-        q.x = x;
-        q.residual = nullptr;
-        q.gamma = gamma;
-        q.beta = beta;
-        q.y = y;
-        q.residual_out = nullptr;
-        q.mean = mean;
-        q.rstd = rstd;
-        q.eps = eps;
-        q.M = M;
-        q.N = (int)N;
-        q.dtype = dtype;
-        e = row ? launch_fwd_row(q, rp, static_cast<cudaStream_t>(stream))
-                : launch_fwd_long(q, d.num_sms, static_cast<cudaStream_t>(stream));
-    } else {
-        e = launch_ln_fwd(p, d.num_sms, static_cast<cudaStream_t>(stream));
-    }
+    FwdRowProblem q;
+    q.mode = kFwdLn;
+    q.x = x;
+    q.residual = nullptr;
+    q.gamma = gamma;
+    q.beta = beta;
+    q.y = y;
+    q.residual_out = nullptr;
+    q.mean = mean;
+    q.rstd = rstd;
+    q.eps = eps;
+    q.M = M;
+    q.N = (int)N;
+    q.dtype = dtype;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (vec)
+        e = row ? launch_fwd_row(q, rp, cs) : launch_fwd_long(q, d.num_sms, cs);
+    else
+        e = fwd_generic_vec_ok(q) ? launch_fwd_generic_vec(q, d.num_sms, cs)
+                                  : launch_ln_fwd(p, d.num_sms, cs);
     return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
 }
 

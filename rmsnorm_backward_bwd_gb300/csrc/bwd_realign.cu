@@ -31,22 +31,6 @@ namespace {
 // [2 parities][2 rows][32 warps] fp32 warp sums, then the row buffers
 constexpr int kRealignRedBytes = 512;
 
-// Bytes [sh, sh + 16) of the 32 bytes lo|hi (byte 0 = lowest byte of lo.x).
-// sh is uniform across the CTA for a row: the switch does not diverge and
-// every word index is a constant.
-__device__ __forceinline__ uint4 shift_bytes(const uint4 &lo, const uint4 &hi, int sh) {
-    const int b = (sh & 3) * 8;
-    uint32_t a0, a1, a2, a3, a4;
-    switch (sh >> 2) {
-    case 0: a0 = lo.x; a1 = lo.y; a2 = lo.z; a3 = lo.w; a4 = hi.x; break;
-    case 1: a0 = lo.y; a1 = lo.z; a2 = lo.w; a3 = hi.x; a4 = hi.y; break;
-    case 2: a0 = lo.z; a1 = lo.w; a2 = hi.x; a3 = hi.y; a4 = hi.z; break;
-    default: a0 = lo.w; a1 = hi.x; a2 = hi.y; a3 = hi.z; a4 = hi.w; break;
-    }
-    return make_uint4(__funnelshift_r(a0, a1, b), __funnelshift_r(a1, a2, b),
-                      __funnelshift_r(a2, a3, b), __funnelshift_r(a3, a4, b));
-}
-
 // 16 bytes of shared memory starting at byte offset `start` of the buffer at
 // shared address `buf` (16-byte aligned; the buffer extends 16 bytes past
 // the last window read).

@@ -131,6 +131,10 @@ size_t fwd_row_smem_bytes(int teams, int stages, int ntensors, int team_chunks);
 cudaError_t launch_fwd_row(const FwdRowProblem &p, const RowPlan &plan, cudaStream_t s);
 // Aligned rows longer than the row engine's tile: one CTA per row, 16-byte loads.
 cudaError_t launch_fwd_long(const FwdRowProblem &p, int num_sms, cudaStream_t s);
+// Rows that are not 16-byte multiples, row tensors at one alignment phase and
+// gamma (beta) 16-byte aligned: 16-byte chunks plus element-wise head and tail.
+bool fwd_generic_vec_ok(const FwdRowProblem &p);
+cudaError_t launch_fwd_generic_vec(const FwdRowProblem &p, int num_sms, cudaStream_t s);
 
 // LayerNorm.
 struct LnFwdProblem {

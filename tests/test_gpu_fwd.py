@@ -85,3 +85,62 @@ def test_fwd_3d_input_and_guards():
         rn.rmsnorm_fwd(x.transpose(0, 1), g, 1e-6)
     with pytest.raises(ValueError, match="dtype mismatch"):
         rn.fused_add_rmsnorm_fwd(x, x.to(torch.float16), g, 1e-6)
+
+
+UNALIGNED = [(300, 4095, "bf16"), (97, 2999, "f32"), (64, 1001, "f16"), (5, 7, "bf16"),
+             (3, 3, "f32"), (40, 8190, "bf16"), (9, 16385, "f16")]
+
+
+def _shifted_like(t, shift):
+    """A CUDA copy of t whose storage starts `shift` elements into a buffer
+    (rows stay contiguous; the base moves off 16-byte alignment)."""
+    buf = torch.empty(t.numel() + shift, dtype=t.dtype, device="cuda")
+    v = buf[shift:].view(t.shape)
+    v.copy_(t.cuda() if not t.is_cuda else t)
+    return v
+
+
+@pytest.mark.parametrize("M,N,dt", UNALIGNED, ids=lambda v: str(v))
+@pytest.mark.parametrize("phase", ["same", "mismatched"])
+def test_fwds_on_unaligned_rows(M, N, dt, phase):
+    """Rows that are not 16-byte multiples: with all row tensors at one phase
+    (16-byte chunks plus element-wise head and tail), and with the output one
+    element off the input's phase (element-wise kernel). RMSNorm, fused-add
+    and LayerNorm against the oracle."""
+    inp = synth.make_inputs(Case("unaligned fwd", M, N, dt, fused=True, seed=31))
+    x64, r64, g64 = (parity.to64(inp[k]) for k in ("x", "residual", "gamma"))
+    x, r, g = inp["x"].cuda(), inp["residual"].cuda(), inp["gamma"].cuda()
+
+    def out_buf():
+        z = torch.empty(M, N, dtype=x.dtype)
+        return _shifted_like(z, 1) if phase == "mismatched" else z.cuda()
+
+    y, rstd = rn.rmsnorm_fwd(x, g, 1e-6, y=out_buf())
+    o, ro, frstd = rn.fused_add_rmsnorm_fwd(x, r, g, 1e-6, out=out_buf(), residual_out=out_buf())
+    yl, mean, lrstd = rn.layernorm_fwd(x, g, g, 1e-5, y=out_buf())
+    torch.cuda.synchronize()
+    y64, rstd64 = oracle.rmsnorm_fwd(x64, g64, np.float32(1e-6))
+    o64, a64, frstd64 = oracle.fused_add_rmsnorm_fwd(x64, r64, g64, np.float32(1e-6), dt)
+    yl64, mean64, lrstd64 = oracle.layernorm_fwd(x64, g64, g64, np.float32(1e-5))
+    parity.check_tensor("y", y, y64, dt, "y")
+    _check_rstd(rstd, rstd64)
+    assert np.array_equal(parity.to64(ro), a64)
+    parity.check_tensor("out", o, o64, dt, "y")
+    _check_rstd(frstd, frstd64)
+    parity.check_tensor("layernorm y", yl, yl64, dt, "y")
+    tol = 2.0**-24 * (8 + 4 * np.sqrt(N))
+    assert np.all(np.abs(parity.to64(mean) - mean64) <= tol * np.mean(np.abs(x64), axis=1))
+    assert np.all(np.abs(parity.to64(lrstd) - lrstd64) <= tol * lrstd64)
+
+
+def test_unaligned_fwd_gamma_off_16_bytes():
+    """gamma itself off 16-byte alignment: the element-wise kernel."""
+    M, N, dt = 33, 1001, "bf16"
+    inp = synth.make_inputs(Case("unaligned gamma", M, N, dt, seed=32))
+    x64, g64 = parity.to64(inp["x"]), parity.to64(inp["gamma"])
+    g = _shifted_like(inp["gamma"], 3)
+    y, rstd = rn.rmsnorm_fwd(inp["x"].cuda(), g, 1e-6)
+    torch.cuda.synchronize()
+    y64, rstd64 = oracle.rmsnorm_fwd(x64, g64, np.float32(1e-6))
+    parity.check_tensor("y", y, y64, dt, "y")
+    _check_rstd(rstd, rstd64)
