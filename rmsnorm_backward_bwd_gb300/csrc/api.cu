@@ -578,7 +578,21 @@ static void plan_ln_generic(const LnBwdProblem &p, const DeviceInfo &d, GenericP
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
     plan->smem_dw = ln_generic_smem_bytes(p.N, true) <= budget;
     plan->smem = ln_generic_smem_bytes(p.N, plan->smem_dw);
-    int64_t grid = p.M;
+    plan->rows = 0;
+    plan->cpb = 0;
+    // vector variant: x, dy and dx at one alignment phase (element-aligned)
+    const uintptr_t S = (uintptr_t)elem_bytes(p.dtype), ph = (uintptr_t)p.x & 15u;
+    bool vec = ln_generic_vec_smem_bytes(p.N) <= budget;
+    for (const void *q : {p.x, p.dy, static_cast<const void *>(p.dx)})
+        vec = vec && ((uintptr_t)q & 15u) == ph && ((uintptr_t)q % S) == 0;
+    if (vec) {
+        const int chunks = (int)((int64_t)p.N * elem_bytes(p.dtype) / 16);
+        plan->threads = chunks >= 256 ? 512 : 256;
+        plan->rows = chunks * 2 < plan->threads ? 4 : 2;
+        plan->smem_dw = true;
+        plan->smem = ln_generic_vec_smem_bytes(p.N);
+    }
+    int64_t grid = plan->rows ? (p.M + plan->rows - 1) / plan->rows : p.M;
     if (grid > max_partial_rows(d)) grid = max_partial_rows(d);
     if (g_opts[RN_OPT_GRID] > 0 && grid > g_opts[RN_OPT_GRID]) grid = g_opts[RN_OPT_GRID];
     if (grid < 1) grid = 1;
@@ -632,14 +646,14 @@ static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t
                             [&](bool pdl) { return launch_ln_bwd_cluster(p, cp, s, pdl); });
     }
     if (!use_row) plan_ln_generic(p, d, &gp);
-    if (!use_row && atomic && ln_generic_smem_bytes(p.N, true) > d.smem_optin) {
+    if (!use_row && atomic && !gp.rows && ln_generic_smem_bytes(p.N, true) > d.smem_optin) {
         // the generic engine keeps its atomic-mode partials in shared memory
         if (g_opts[RN_OPT_DWEIGHT_MODE] == 2)
             return fail(RN_ERR_UNSUPPORTED, "atomic mode needs N*8 bytes of shared memory");
         atomic = false;
     }
     rp.atomic = gp.atomic = atomic;
-    if (!use_row && atomic) {
+    if (!use_row && atomic && !gp.rows) {
         gp.smem_dw = true;
         gp.smem = ln_generic_smem_bytes(p.N, true);
     }

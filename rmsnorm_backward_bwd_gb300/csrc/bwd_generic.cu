@@ -18,9 +18,6 @@ size_t generic_smem_bytes(int N, bool smem_dw) {
     return 256 + (smem_dw ? (size_t)N * 4 : 0);
 }
 
-// Padded index of column c in the vector variant's shared arrays.
-__device__ __forceinline__ int vpad(int c) { return c + (c >> 5); }
-static size_t vec_words(int N) { return ((size_t)N + (size_t)(N >> 5) + 4) & ~(size_t)3; }
 size_t generic_vec_smem_bytes(int N) { return 512 + 2 * 4 * vec_words(N); }
 
 struct GenArgs {

@@ -168,6 +168,13 @@ __device__ __forceinline__ uint4 shift_bytes(const uint4 &lo, const uint4 &hi, i
                       __funnelshift_r(a2, a3, b), __funnelshift_r(a3, a4, b));
 }
 
+// The generic engines' per-column shared arrays are padded by one word per
+// 32 columns: a warp's lanes touch columns 16/s apart, which without the pad
+// share banks. vpad is column c's padded index; vec_words is the padded
+// length of one array (a multiple of 4 words, so arrays stay 16-byte aligned).
+__device__ __forceinline__ int vpad(int c) { return c + (c >> 5); }
+inline size_t vec_words(int N) { return ((size_t)N + (size_t)(N >> 5) + 4) & ~(size_t)3; }
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

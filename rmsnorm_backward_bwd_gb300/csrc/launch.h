@@ -175,6 +175,7 @@ constexpr int kLnMaxCpt = 2;
 int ln_row_max_threads(int cpt);
 size_t ln_row_smem_bytes(int teams, int stages, int team_chunks);
 size_t ln_generic_smem_bytes(int N, bool smem_dw);
+size_t ln_generic_vec_smem_bytes(int N);
 cudaError_t launch_ln_bwd_row(const LnBwdProblem &p, const RowPlan &plan, cudaStream_t s,
                               bool pdl_after_zero);
 cudaError_t launch_ln_bwd_generic(const LnBwdProblem &p, const GenericPlan &plan,

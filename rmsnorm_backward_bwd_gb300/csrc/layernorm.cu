@@ -953,6 +953,7 @@ struct LnGenArgs {
     int64_t M;
     int N;
     float inv_n;
+    int words;  // vector variant: padded length of each shared array
 };
 
 template <typename T, bool ATOMIC, bool SMEM_DW>
@@ -1020,6 +1021,191 @@ __global__ void __launch_bounds__(512) ln_bwd_generic_kernel(const LnGenArgs a) 
     }
 }
 
+// Vector variant of the generic engine (rows that are not 16-byte multiples,
+// x, dy and dx at one alignment phase), the LayerNorm counterpart of the
+// RMSNorm one: each row splits into a head, whole 16-byte chunks (128-bit
+// loads and stores) and a tail; R rows per CTA iteration, their two sums
+// reduced together; gamma as fp32 and the dgamma / dbeta partials in padded
+// shared memory (a column's owner thread changes with the row's phase, so
+// the partials take shared atomic adds).
+size_t ln_generic_vec_smem_bytes(int N) { return 1024 + 3 * 4 * vec_words(N); }
+
+template <typename T, bool ATOMIC, int R>
+__global__ void __launch_bounds__(512, 2) ln_bwd_generic_vec_kernel(const LnGenArgs a) {
+    constexpr int S = sizeof(T), V = 16 / S;
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *red = reinterpret_cast<float *>(smem);            // [R][2 sums][32 warps]
+    float *sg = reinterpret_cast<float *>(smem + 1024);      // gamma, fp32, padded columns
+    float *sdg = sg + a.words;                               // dgamma partial, padded
+    float *sdb = sdg + a.words;                              // dbeta partial, padded
+    const T *x = static_cast<const T *>(a.x);
+    const T *g = static_cast<const T *>(a.gamma);
+    const T *dy = static_cast<const T *>(a.dy);
+    T *dx = static_cast<T *>(a.dx);
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    const int N = a.N;
+
+    for (int j = tid; j < N; j += nthr) {
+        sdg[vpad(j)] = 0.f;
+        sdb[vpad(j)] = 0.f;
+        sg[vpad(j)] = to_f(g[j]);
+    }
+    __syncthreads();
+
+    for (int64_t row0 = (int64_t)blockIdx.x * R; row0 < a.M; row0 += (int64_t)gridDim.x * R) {
+        int h[R], nv[R], nt[R];
+        float mu[R], rs[R], s1[R], s2[R];
+        int nvmax = 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t row = row0 + r;
+            h[r] = nv[r] = nt[r] = 0;
+            mu[r] = rs[r] = s1[r] = s2[r] = 0.f;
+            if (row < a.M) {
+                const uintptr_t ad = reinterpret_cast<uintptr_t>(x + (size_t)row * N);
+                int hh = (int)(((16u - (unsigned)(ad & 15u)) & 15u) / S);
+                if (hh > N) hh = N;
+                h[r] = hh;
+                nv[r] = (N - hh) / V;
+                nt[r] = N - hh - nv[r] * V;
+                mu[r] = __ldg(a.mean + row);
+                rs[r] = __ldg(a.rstd + row);
+            }
+            if (nv[r] > nvmax) nvmax = nv[r];
+        }
+        // pass 1: sum (x - mean)*wdy and sum wdy of each row
+        for (int i = tid; i < nvmax; i += nthr) {
+            uint4 xv[R], dv[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (i < nv[r]) {
+                    const size_t e0 = (size_t)(row0 + r) * N + h[r] + (size_t)i * V;
+                    xv[r] = ld_global_nc_v4(x + e0);
+                    dv[r] = ld_global_nc_v4(dy + e0);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (i < nv[r]) {
+                    float xf[V], df[V];
+                    chunk_to_float<T>(xv[r], xf);
+                    chunk_to_float<T>(dv[r], df);
+                    const int c0 = h[r] + i * V;
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const float w = df[e] * sg[vpad(c0 + e)];
+                        s1[r] = fmaf(xf[e] - mu[r], w, s1[r]);
+                        s2[r] += w;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            // head and tail (fewer than V elements each)
+            if (tid < h[r] + nt[r]) {
+                const size_t base = (size_t)(row0 + r) * N;
+                const int j = tid < h[r] ? tid : h[r] + nv[r] * V + (tid - h[r]);
+                const float w = to_f(dy[base + j]) * sg[vpad(j)];
+                s1[r] = fmaf(to_f(x[base + j]) - mu[r], w, s1[r]);
+                s2[r] += w;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float w1 = warp_sum(s1[r]), w2 = warp_sum(s2[r]);
+            if (lane == 0) {
+                red[r * 64 + warp] = w1;
+                red[r * 64 + 32 + warp] = w2;
+            }
+        }
+        __syncthreads();
+        float B[R], A[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float t1 = 0.f, t2 = 0.f;
+            for (int w = 0; w < nwarps; ++w) {
+                t1 += red[r * 64 + w];
+                t2 += red[r * 64 + 32 + w];
+            }
+            // dx = (wdy - c2 - x_hat*c1)*rstd = wdy*rstd + (x - mean)*B + A
+            const float c1 = rs[r] * t1 * a.inv_n, c2 = t2 * a.inv_n;
+            B[r] = -rs[r] * rs[r] * c1;
+            A[r] = -c2 * rs[r];
+        }
+        __syncthreads();  // red is rewritten by the next rows
+        // pass 2: dx; dgamma / dbeta partials += dy*x_hat, dy
+        for (int i = tid; i < nvmax; i += nthr) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (i < nv[r]) {
+                    const int c0 = h[r] + i * V;
+                    const size_t e0 = (size_t)(row0 + r) * N + c0;
+                    float xf[V], df[V], o[V];
+                    chunk_to_float<T>(ld_global_nc_v4(x + e0), xf);
+                    chunk_to_float<T>(ld_global_nc_v4(dy + e0), df);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        const float xc = xf[e] - mu[r];
+                        const float w = df[e] * sg[vpad(c0 + e)];
+                        o[e] = fmaf(w, rs[r], fmaf(xc, B[r], A[r]));
+                        atomicAdd(sdg + vpad(c0 + e), df[e] * (xc * rs[r]));
+                        atomicAdd(sdb + vpad(c0 + e), df[e]);
+                    }
+                    st_global_v4(dx + e0, float_to_chunk<T>(o));
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (tid < h[r] + nt[r]) {
+                const size_t base = (size_t)(row0 + r) * N;
+                const int j = tid < h[r] ? tid : h[r] + nv[r] * V + (tid - h[r]);
+                const float xc = to_f(x[base + j]) - mu[r], dv = to_f(dy[base + j]);
+                const float w = dv * sg[vpad(j)];
+                dx[base + j] = from_f<T>(fmaf(w, rs[r], fmaf(xc, B[r], A[r])));
+                atomicAdd(sdg + vpad(j), dv * (xc * rs[r]));
+                atomicAdd(sdb + vpad(j), dv);
+            }
+        }
+    }
+    pdl_launch_dependents();
+    __syncthreads();  // every shared add of the partials is done
+    if (ATOMIC) {
+        pdl_wait();
+        for (int j = tid; j < N; j += nthr) {
+            atomicAdd(a.dg_out + j, sdg[vpad(j)]);
+            if (a.db_out) atomicAdd(a.db_out + j, sdb[vpad(j)]);
+        }
+    } else {
+        float *part = a.dg_out + (size_t)blockIdx.x * 2 * N;  // [dgamma | dbeta]
+        for (int j = tid; j < N; j += nthr) {
+            part[j] = sdg[vpad(j)];
+            part[N + j] = sdb[vpad(j)];
+        }
+    }
+}
+
+template <typename T, bool ATOMIC, int R>
+static cudaError_t launch_ln_gen_vec_t(const LnGenArgs &args, const GenericPlan &plan,
+                                       cudaStream_t s, bool pdl) {
+    auto kern = ln_bwd_generic_vec_kernel<T, ATOMIC, R>;
+    cudaError_t e = ensure_smem_attr((const void *)kern, plan.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(plan.threads);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
 template <typename T, bool ATOMIC, bool SMEM_DW>
 static cudaError_t launch_ln_gen_t(const LnGenArgs &args, const GenericPlan &plan,
                                    cudaStream_t s, bool pdl) {
@@ -1042,6 +1228,13 @@ static cudaError_t launch_ln_gen_t(const LnGenArgs &args, const GenericPlan &pla
 template <typename T>
 static cudaError_t launch_ln_gen_dt(const LnGenArgs &args, const GenericPlan &plan,
                                     cudaStream_t s, bool pdl) {
+    if (plan.rows) {
+        if (plan.atomic)
+            return plan.rows == 4 ? launch_ln_gen_vec_t<T, true, 4>(args, plan, s, pdl)
+                                  : launch_ln_gen_vec_t<T, true, 2>(args, plan, s, pdl);
+        return plan.rows == 4 ? launch_ln_gen_vec_t<T, false, 4>(args, plan, s, pdl)
+                              : launch_ln_gen_vec_t<T, false, 2>(args, plan, s, pdl);
+    }
     if (plan.atomic) return launch_ln_gen_t<T, true, true>(args, plan, s, pdl);
     if (plan.smem_dw) return launch_ln_gen_t<T, false, true>(args, plan, s, pdl);
     return launch_ln_gen_t<T, false, false>(args, plan, s, pdl);
@@ -1061,6 +1254,7 @@ cudaError_t launch_ln_bwd_generic(const LnBwdProblem &p, const GenericPlan &plan
     a.M = p.M;
     a.N = p.N;
     a.inv_n = 1.0f / (float)p.N;
+    a.words = (int)vec_words(p.N);
     switch (p.dtype) {
     case kF32: return launch_ln_gen_dt<float>(a, plan, s, pdl_after_zero);
     case kF16: return launch_ln_gen_dt<__half>(a, plan, s, pdl_after_zero);

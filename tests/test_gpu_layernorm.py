@@ -312,3 +312,37 @@ def test_layernorm_cluster_scratch_mode_is_repeatable():
     for u, v in zip(a, b):
         assert torch.equal(u, v)
     check(ex, a)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("with_dbeta", [True, False])
+@pytest.mark.parametrize("M,N,dt,rows", [(700, 4095, "bf16", 2), (97, 2999, "f32", 2),
+                                         (130, 1001, "f16", 4), (5, 7, "bf16", 4),
+                                         (40, 8190, "bf16", 2), (3, 3, "f32", 4)],
+                         ids=lambda v: str(v))
+def test_layernorm_generic_vector_variant(M, N, dt, rows, with_dbeta, mode):
+    """Rows that are not 16-byte multiples with x, dy and dx at one phase:
+    16-byte chunks plus element-wise head and tail, several rows per CTA
+    iteration, dgamma / dbeta partials in shared memory; both modes, with and
+    without the bias gradient."""
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    ex = expected(Case("ln vec", M, N, dt, eps=1e-5, seed=33))
+    out = run_gpu(ex, with_dbeta=with_dbeta)
+    plan = native.last_plan()
+    assert "engine=ln_generic vec rows=%d" % rows in plan, plan
+    check(ex, out, with_dbeta=with_dbeta, tag=" [%s]" % plan)
+
+
+def test_layernorm_mismatched_phases_take_the_scalar_generic_kernel():
+    """dx one element off x's alignment phase: element-wise kernel."""
+    M, N, dt = 48, 1000, "bf16"
+    ex = expected(Case("ln scalar", M, N, dt, eps=1e-5, seed=34))
+    x, g, dy = (ex.inp[k].cuda() for k in ("x", "gamma", "dy"))
+    mean = torch.from_numpy(ex.mean32).float().cuda()
+    rstd = torch.from_numpy(ex.rstd32).float().cuda()
+    dx = torch.empty(M * N + 1, dtype=x.dtype, device="cuda")[1:].view(M, N)
+    out = rn.layernorm_bwd(x, g, dy, mean, rstd, dx=dx)
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert plan.startswith("engine=ln_generic") and "vec" not in plan, plan
+    check(ex, out)
