@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kLnMaxThreads, 1) ln_bwd_row_kernel(const LnRo
     }
     // wdy = dy*gamma of chunk kk as fp32 pairs (d2: dy as pairs, fp32 only)
     auto wdy = [&](int kk, const uint4 &dv, const f32x2 *d2, f32x2 *w) {
-        if (kF32) {
+        if constexpr (kF32) {
 #pragma unroll
             for (int q = 0; q < P; ++q) w[q] = f2_mul(d2[q], g2[kF32 ? kk : 0][kF32 ? q : 0]);
         } else {
@@ -691,7 +691,7 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_cluster_kernel(const LnClusterA
         if (kF32) chunk_pairs<T>(gp[kk], g2[kF32 ? kk : 0]);
     }
     auto wdy = [&](int kk, const uint4 &dv, const f32x2 *d2, f32x2 *w) {
-        if (kF32) {
+        if constexpr (kF32) {
 #pragma unroll
             for (int q = 0; q < P; ++q) w[q] = f2_mul(d2[q], g2[kF32 ? kk : 0][kF32 ? q : 0]);
         } else {
