@@ -10,6 +10,7 @@
 // j % blockDim.x, so the partial needs no atomics: it lives in shared memory
 // when N fp32 values fit there, otherwise in the CTA's workspace row.
 #include "common.cuh"
+#include "unaligned.cuh"
 #include "launch.h"
 
 namespace rn {

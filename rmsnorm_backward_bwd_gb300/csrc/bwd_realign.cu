@@ -21,6 +21,7 @@
 // 16 to 32 KB), and the next iteration's rows are fetched into registers
 // while they are.
 #include "common.cuh"
+#include "unaligned.cuh"
 #include "launch.h"
 #include "row_math.cuh"
 

@@ -14,6 +14,7 @@
 // the row's phase, so they come from two aligned 16-byte loads and a funnel
 // shift (element by element for a window at the end of the vector).
 #include "common.cuh"
+#include "unaligned.cuh"
 #include "launch.h"
 
 namespace rn {

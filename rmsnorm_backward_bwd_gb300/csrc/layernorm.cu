@@ -31,6 +31,7 @@
 //     workspace row.
 #include "cluster.cuh"
 #include "common.cuh"
+#include "unaligned.cuh"
 #include "launch.h"
 
 namespace rn {
