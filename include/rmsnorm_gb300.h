@@ -244,8 +244,10 @@ rn_status rn_set_option(int option, int value);
 int rn_get_option(int option);
 
 /*
- * Text describing the plan (engine, tile shape, grid, weight-gradient mode)
- * the most recent backward call on this thread used; "" if none.
+ * Text describing the plan the most recent backward or forward call on this
+ * thread used: the engine, and for the row engines the tile shape and grid
+ * (for a backward also the weight-gradient mode); "" if none. Forward plans
+ * start with the operation ("rmsnorm_fwd", "fused_add_fwd", "layernorm_fwd").
  */
 const char *rn_last_plan(void);
 

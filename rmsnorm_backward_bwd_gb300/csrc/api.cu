@@ -459,6 +459,15 @@ static void plan_string_generic(const GenericPlan &gp, const char *engine, bool 
                  gp.threads, gp.grid, (int)gp.smem_dw, atomic ? "atomic" : "scratch");
 }
 
+static void plan_string_fwd(const char *op, bool vec, bool row, bool gvec, const RowPlan &rp) {
+    if (vec && row)
+        snprintf(g_plan, sizeof(g_plan), "%s engine=row cpt=%d team_threads=%d teams=%d stages=%d "
+                 "grid=%d", op, rp.cpt, rp.team_threads, rp.teams, rp.stages, rp.grid);
+    else
+        snprintf(g_plan, sizeof(g_plan), "%s engine=%s", op,
+                 vec ? "long" : (gvec ? "generic vec" : "generic"));
+}
+
 static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
     DeviceInfo d;
     int dev = 0;
@@ -707,6 +716,7 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
                            void *y, void *residual_out, float *rstd, int64_t M, int64_t N,
                            int dtype, void *stream, bool fused) {
     g_err[0] = 0;
+    g_plan[0] = 0;
     rn_status st = check_common(M, N, dtype);
     if (st != RN_OK) return st;
     if (!(eps >= 0.f)) return fail(RN_ERR_INVALID_ARG, "eps must be >= 0");
@@ -751,11 +761,12 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
     q.N = (int)N;
     q.dtype = dtype;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool gvec = !vec && fwd_generic_vec_ok(q);
+    plan_string_fwd(fused ? "fused_add_fwd" : "rmsnorm_fwd", vec, row, gvec, rp);
     if (vec)
         e = row ? launch_fwd_row(q, rp, cs) : launch_fwd_long(q, d.num_sms, cs);
     else
-        e = fwd_generic_vec_ok(q) ? launch_fwd_generic_vec(q, d.num_sms, cs)
-                                  : launch_fwd(p, d.num_sms, cs);
+        e = gvec ? launch_fwd_generic_vec(q, d.num_sms, cs) : launch_fwd(p, d.num_sms, cs);
     return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
 }
 
@@ -763,6 +774,7 @@ static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta
                               void *y, float *mean, float *rstd, int64_t M, int64_t N, int dtype,
                               void *stream) {
     g_err[0] = 0;
+    g_plan[0] = 0;
     rn_status st = check_common(M, N, dtype);
     if (st != RN_OK) return st;
     if (!(eps >= 0.f)) return fail(RN_ERR_INVALID_ARG, "eps must be >= 0");
@@ -804,11 +816,12 @@ static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta
     q.N = (int)N;
     q.dtype = dtype;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool gvec = !vec && fwd_generic_vec_ok(q);
+    plan_string_fwd("layernorm_fwd", vec, row, gvec, rp);
     if (vec)
         e = row ? launch_fwd_row(q, rp, cs) : launch_fwd_long(q, d.num_sms, cs);
     else
-        e = fwd_generic_vec_ok(q) ? launch_fwd_generic_vec(q, d.num_sms, cs)
-                                  : launch_ln_fwd(p, d.num_sms, cs);
+        e = gvec ? launch_fwd_generic_vec(q, d.num_sms, cs) : launch_ln_fwd(p, d.num_sms, cs);
     return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
 }
 

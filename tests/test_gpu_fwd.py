@@ -47,6 +47,19 @@ def test_fused_fwd_matches_oracle(M, N, dt):
     parity.check_tensor("out", out, out64, dt, "y")
 
 
+@pytest.mark.parametrize("M,N,engine", [(256, 4096, "row"), (8, 40000, "long")])
+def test_fwd_plan_names_the_engine(M, N, engine):
+    inp = synth.make_inputs(Case("fwd plan", M, N, "bf16", fused=True))
+    x, r, g = inp["x"].cuda(), inp["residual"].cuda(), inp["gamma"].cuda()
+    rn.rmsnorm_fwd(x, g, 1e-6)
+    assert native.last_plan().startswith("rmsnorm_fwd engine=%s" % engine), native.last_plan()
+    rn.fused_add_rmsnorm_fwd(x, r, g, 1e-6)
+    assert native.last_plan().startswith("fused_add_fwd engine=%s" % engine), native.last_plan()
+    rn.layernorm_fwd(x, g, None, 1e-5)
+    assert native.last_plan().startswith("layernorm_fwd engine=%s" % engine), native.last_plan()
+    torch.cuda.synchronize()
+
+
 def test_eps_is_honoured():
     inp = synth.make_inputs(Case("eps", 64, 256, "f32"))
     x, g = inp["x"].cuda() * 1e-2, inp["gamma"].cuda()
@@ -115,10 +128,17 @@ def test_fwds_on_unaligned_rows(M, N, dt, phase):
         z = torch.empty(M, N, dtype=x.dtype)
         return _shifted_like(z, 1) if phase == "mismatched" else z.cuda()
 
+    engine = "engine=generic vec" if phase == "same" else "engine=generic"
+    plans = []
     y, rstd = rn.rmsnorm_fwd(x, g, 1e-6, y=out_buf())
+    plans.append(native.last_plan())
     o, ro, frstd = rn.fused_add_rmsnorm_fwd(x, r, g, 1e-6, out=out_buf(), residual_out=out_buf())
+    plans.append(native.last_plan())
     yl, mean, lrstd = rn.layernorm_fwd(x, g, g, 1e-5, y=out_buf())
+    plans.append(native.last_plan())
     torch.cuda.synchronize()
+    for op, plan in zip(("rmsnorm_fwd", "fused_add_fwd", "layernorm_fwd"), plans):
+        assert plan == "%s %s" % (op, engine), plan
     y64, rstd64 = oracle.rmsnorm_fwd(x64, g64, np.float32(1e-6))
     o64, a64, frstd64 = oracle.fused_add_rmsnorm_fwd(x64, r64, g64, np.float32(1e-6), dt)
     yl64, mean64, lrstd64 = oracle.layernorm_fwd(x64, g64, g64, np.float32(1e-5))
