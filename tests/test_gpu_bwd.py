@@ -300,3 +300,33 @@ def test_generic_realigning_small_grid_and_dres_as_dx():
     assert "realign" in plan and "grid=3" in plan, plan
     assert dx.data_ptr() == dres.data_ptr()
     parity.check_bwd(ex, dx, dw, dw32)
+
+
+@pytest.mark.parametrize("N,dt,engine", [
+    (8183, "bf16", "engine=generic vec"),        # 1023 column blocks: under the realigning range
+    (8185, "bf16", "engine=generic realign cpb=2"),  # 1024 blocks
+    (16383, "bf16", "engine=generic realign cpb=4"),  # 2048 blocks
+    (16385, "bf16", "engine=generic vec"),       # 2049 blocks: past it
+    (4093, "f32", "engine=generic realign cpb=2"),   # 1024 blocks of f32
+    (4091, "f32", "engine=generic vec")],        # 1023
+    ids=lambda v: str(v))
+@pytest.mark.parametrize("M", [1, 3, 64])
+def test_generic_engine_thresholds(N, dt, engine, M):
+    """The width thresholds between the realigning engine and the vector
+    variant, on both sides, with few and several rows."""
+    ex = parity.expected_bwd(Case("threshold", M, N, dt, fused=True, with_dres=True, seed=41))
+    out = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    assert plan.startswith(engine), plan
+    parity.check_bwd(ex, *out, tag=" [%s]" % plan)
+
+
+def test_generic_engines_empty_batch():
+    """M = 0 on unaligned rows: nothing to read, a zero weight gradient."""
+    import rmsnorm_backward_bwd_gb300 as rn
+    for N in (4095, 8185):
+        x = torch.empty(0, N, dtype=torch.bfloat16, device="cuda")
+        g = torch.ones(N, dtype=torch.bfloat16, device="cuda")
+        dx, dw, dw32 = rn.rmsnorm_bwd(x, g, x, torch.empty(0, device="cuda"))
+        torch.cuda.synchronize()
+        assert dx.shape == (0, N) and torch.count_nonzero(dw32).item() == 0
