@@ -267,10 +267,13 @@ struct RMSNormFunction : public torch::autograd::Function<RMSNormFunction> {
         const bool need_x = ctx->needs_input_grad(0), need_w = ctx->needs_input_grad(1);
         if (!(need_x || need_w)) return {Tensor(), Tensor(), Tensor()};
         const Tensor &x2 = saved[0];
+        // an fp32 weight takes the fp32 accumulator itself: no cast launch
+        const bool f32 = x2.scalar_type() == at::kFloat;
         auto [dx, dw, dw32] = op.call(x2, saved[1], rows2d(grads[0], x2.size(1)), saved[2],
-                                      need_w);
+                                      need_w && !f32);
         const auto shape = ctx->saved_data["shape"].toIntVector();
-        return {need_x ? dx.view(shape) : Tensor(), need_w ? dw : Tensor(), Tensor()};
+        return {need_x ? dx.view(shape) : Tensor(), need_w ? (f32 ? dw32 : dw) : Tensor(),
+                Tensor()};
     }
 };
 
@@ -314,10 +317,13 @@ struct FusedAddRMSNormFunction : public torch::autograd::Function<FusedAddRMSNor
         }
         c10::optional<Tensor> dres;
         if (d_res.defined()) dres = rows2d(d_res, N);
-        auto [dx, dw, dw32] = op.call(added, saved[1], rows2d(d_out, N), saved[2], dres, need_w);
+        const bool f32 = added.scalar_type() == at::kFloat;
+        auto [dx, dw, dw32] = op.call(added, saved[1], rows2d(d_out, N), saved[2], dres,
+                                      need_w && !f32);
         const auto shape = ctx->saved_data["shape"].toIntVector();
         const Tensor g = dx.view(shape);
-        return {need_x ? g : Tensor(), need_r ? g : Tensor(), need_w ? dw : Tensor(), Tensor()};
+        return {need_x ? g : Tensor(), need_r ? g : Tensor(),
+                need_w ? (f32 ? dw32 : dw) : Tensor(), Tensor()};
     }
 };
 
@@ -351,11 +357,13 @@ struct LayerNormFunction : public torch::autograd::Function<LayerNormFunction> {
         const bool need_b = ctx->saved_data["has_bias"].toBool() && ctx->needs_input_grad(2);
         if (!(need_x || need_w || need_b)) return {Tensor(), Tensor(), Tensor(), Tensor()};
         const Tensor &x2 = saved[0];
+        const bool f32 = x2.scalar_type() == at::kFloat;
         auto [dx, dg, db, dg32, db32] = op.call(x2, saved[1], rows2d(grads[0], x2.size(1)),
-                                                saved[2], saved[3], need_b, need_w || need_b);
+                                                saved[2], saved[3], need_b,
+                                                (need_w || need_b) && !f32);
         const auto shape = ctx->saved_data["shape"].toIntVector();
-        return {need_x ? dx.view(shape) : Tensor(), need_w ? dg : Tensor(),
-                need_b ? db : Tensor(), Tensor()};
+        return {need_x ? dx.view(shape) : Tensor(), need_w ? (f32 ? dg32 : dg) : Tensor(),
+                need_b ? (f32 ? db32 : db) : Tensor(), Tensor()};
     }
 };
 

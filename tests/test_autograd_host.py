@@ -131,7 +131,23 @@ def test_rmsnorm_grads_any_rank(fake, shape):
     _close(xa.grad, x64.grad)
     _close(wa.grad, w64.grad)
     M = int(np.prod(shape[:-1]))
-    assert fake.calls == [("fwd", (M, shape[-1])), ("bwd", (M, shape[-1]), True)]
+    # fp32 weight: its gradient is the fp32 accumulator itself (no cast asked for)
+    assert fake.calls == [("fwd", (M, shape[-1])), ("bwd", (M, shape[-1]), False)]
+
+
+def test_bf16_weight_gradient_is_the_cast(fake):
+    """A 16-bit weight's gradient is the fp32 accumulator cast to its dtype;
+    an fp32 weight's is the accumulator itself."""
+    x, r, w, dy, _ = _draw((4, 32), seed=6)
+    for dt, cast in ((torch.bfloat16, True), (torch.float32, False)):
+        xa = x.to(dt).requires_grad_()
+        wa = w.to(dt).requires_grad_()
+        (rn.rmsnorm(xa, wa, 1e-6) * dy.to(dt)).sum().backward()
+        assert fake.calls[-1] == ("bwd", (4, 32), cast)
+        assert wa.grad.dtype == dt
+        out, _ = rn.fused_add_rmsnorm(xa.detach().requires_grad_(), r.to(dt), wa, 1e-6)
+        (out * dy.to(dt)).sum().backward()
+        assert fake.calls[-1] == ("fused_bwd", (4, 32), False, cast)
 
 
 def test_rmsnorm_weight_grad_not_needed(fake):
@@ -243,7 +259,7 @@ def test_layernorm_grads(fake, shape, with_bias):
         _close(ba.grad, b64.grad)
     M = int(np.prod(shape[:-1]))
     assert fake.calls == [("ln_fwd", (M, shape[-1]), with_bias),
-                          ("ln_bwd", (M, shape[-1]), with_bias, True)]
+                          ("ln_bwd", (M, shape[-1]), with_bias, False)]   # fp32: no cast
 
 
 def test_layernorm_only_x_grad(fake):
