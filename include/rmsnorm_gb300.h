@@ -225,10 +225,13 @@ rn_status rn_rmsnorm_bwd_noalloc(const void *x, const void *gamma, const void *d
  * to calls made after they are set; value 0 always means "automatic".
  */
 typedef enum rn_option {
-    RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (async-copy ring), 2 = generic engine,
-                                 3 = cluster engine (RMSNorm backward: a row split across a
-                                 thread-block cluster; chosen by default for aligned rows of
-                                 more than 2048 16-byte chunks) */
+    RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (async-copy ring), 2 = generic engines (the
+                                 default for rows that are not 16-byte multiples or bases off
+                                 16 bytes; which one runs depends on the row size and on whether
+                                 the row tensors share one alignment phase: realigning, vector
+                                 or element-wise kernel), 3 = cluster engine (RMSNorm backward:
+                                 a row split across a thread-block cluster; chosen by default
+                                 for aligned rows of more than 2048 16-byte chunks) */
     RN_OPT_DWEIGHT_MODE = 1,  /* 1 = scratch partials + finalize (deterministic dweight),
                                  2 = fp32 atomics + cast (the default where possible: faster,
                                  summation order varies from call to call) */
