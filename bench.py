@@ -61,12 +61,13 @@ def measured_peak():
 
 # The row-pass kernel each engine launches (from the plan string).
 ENGINE_KERNELS = {"row": "bwd_row_kernel", "cluster": "bwd_cluster_kernel",
+                  "generic phase": "bwd_phase_kernel", "generic realign": "bwd_realign_kernel",
                   "generic vec": "bwd_generic_vec_kernel", "generic": "bwd_generic_kernel"}
 
 
 def row_pass_kernel(plan):
     engine = plan.split("engine=", 1)[1].split(" threads=")[0].split(" rows=")[0] if plan else ""
-    engine = engine.split(" cpt=")[0].split(" csize=")[0]
+    engine = engine.split(" cpt=")[0].split(" csize=")[0].split(" cpb=")[0]
     return ENGINE_KERNELS.get(engine, engine)
 
 

@@ -240,7 +240,12 @@ typedef enum rn_option {
     RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8) */
     RN_OPT_GRID = 5,          /* CTAs of the row pass (default: one per SM; at most 2 per SM) */
     RN_OPT_CLUSTER_SIZE = 6,  /* cluster engine: CTAs per cluster, 2, 4, 8 or 16 */
-    RN_OPT_COUNT = 7
+    RN_OPT_GENERIC_KERNEL = 7, /* RMSNorm backward, generic engines: 1 = phase-class kernel,
+                                 2 = vector kernel, 3 = realigning kernel, 4 = element-wise
+                                 kernel. A kernel that cannot take the problem (its row-size
+                                 range, or tensors at different alignment phases) falls back
+                                 to the next one the automatic choice would make. */
+    RN_OPT_COUNT = 8
 } rn_option;
 
 rn_status rn_set_option(int option, int value);

@@ -343,15 +343,58 @@ static bool plan_realign(const BwdProblem &p, const DeviceInfo &d, GenericPlan *
     return true;
 }
 
-static void plan_generic(const BwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
+// The phase-class kernel: the vector variant's conditions (one alignment
+// phase) and at most 1024 whole 16-byte chunks per row (bf16 N ~8K, f32 N
+// ~4K); 1 chunk per thread up to 256 chunks, else 2. Its grid is the
+// kernel's resident CTAs on every SM, at most 2: scratch mode's partial rows
+// fill the workspace there, and in atomic mode every CTA adds N values at the
+// end. Measured on GB300 (L2 flushed, us per call, 2 CTAs per SM -> all
+// resident): f16 16384 x 1001 77.5 -> 101.8 (9 per SM), bf16 4096 x 2047
+// 38.0 -> 49.4 (4 per SM). The grid is a multiple of the phase period P when
+// it is below M, so that every residue class gets the same number of CTAs,
+// and never below min(P, M), so that every class has one.
+static bool plan_phase(const BwdProblem &p, const DeviceInfo &d, bool atomic, GenericPlan *plan) {
+    if (!generic_vec_ok(p, d)) return false;
+    const int64_t nvmax = (int64_t)p.N * elem_bytes(p.dtype) / 16;
+    if (nvmax > 1024) return false;
+    const int cpt = nvmax > 256 ? 2 : 1;
+    int threads = (int)((nvmax + cpt - 1) / cpt + 31) / 32 * 32;
+    if (threads < 32) threads = 32;
+    int per_sm = phase_blocks_per_sm(p.dtype, p.dres != nullptr, atomic, cpt, threads);
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > 2) per_sm = 2;
+    int64_t grid = (int64_t)per_sm * d.num_sms;
+    if (g_opts[RN_OPT_GRID] > 0 && grid > g_opts[RN_OPT_GRID]) grid = g_opts[RN_OPT_GRID];
+    // every residue class needs a CTA: at least min(P, M), whatever the grid option says
+    const int P = phase_period(p.N, p.dtype);
+    if (grid >= p.M) grid = p.M;
+    else if (grid >= P) grid = grid / P * P;
+    if (grid < P) grid = p.M < P ? p.M : P;
+    if (grid < 1) grid = 1;
+    plan->phase = cpt;
     plan->cpb = 0;
-    if (plan_realign(p, d, plan)) return;
+    plan->rows = 0;
+    plan->threads = threads;
+    plan->grid = (int)grid;
+    plan->smem_dw = atomic;
+    plan->smem = atomic ? (size_t)p.N * 4 : 0;  // the atomic mode's staged partial
+    plan->atomic = atomic;
+    return true;
+}
+
+static void plan_generic(const BwdProblem &p, const DeviceInfo &d, bool atomic, GenericPlan *plan) {
+    plan->cpb = 0;
+    plan->phase = 0;
+    // RN_OPT_GENERIC_KERNEL: 1 phase-class, 2 vector, 3 realigning, 4 element-wise
+    const int pick = g_opts[RN_OPT_GENERIC_KERNEL];
+    if (pick <= 1 && plan_phase(p, d, atomic, plan)) return;
+    if ((pick <= 1 || pick == 3) && plan_realign(p, d, plan)) return;
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
     plan->smem_dw = generic_smem_bytes(p.N, true) <= budget;
     plan->smem = generic_smem_bytes(p.N, plan->smem_dw);
     plan->rows = 0;
-    if (generic_vec_ok(p, d)) {
+    if (pick != 4 && generic_vec_ok(p, d)) {
         // rows in flight per CTA iteration: 4 when a row's chunks leave most
         // threads idle, else 2
         const int chunks = (int)((int64_t)p.N * elem_bytes(p.dtype) / 16);
@@ -443,7 +486,10 @@ static void plan_string_row(const RowPlan &rp, const char *engine, bool atomic) 
 }
 
 static void plan_string_generic(const GenericPlan &gp, const char *engine, bool atomic) {
-    if (gp.cpb)
+    if (gp.phase)
+        snprintf(g_plan, sizeof(g_plan), "engine=%s phase cpt=%d threads=%d grid=%d dw=%s",
+                 engine, gp.phase, gp.threads, gp.grid, atomic ? "atomic" : "scratch");
+    else if (gp.cpb)
         snprintf(g_plan, sizeof(g_plan), "engine=%s realign cpb=%d rows=%d threads=%d grid=%d dw=%s",
                  engine, gp.cpb, gp.rows, gp.threads, gp.grid, atomic ? "atomic" : "scratch");
     else if (gp.rows)
@@ -505,8 +551,8 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
                              partials, cp.clusters, p.N};
         return run_sequence(atomic, o, s, [&](bool pdl) { return launch_bwd_cluster(p, cp, s, pdl); });
     }
-    if (!use_row) plan_generic(p, d, &gp);
-    if (!use_row && atomic && !gp.rows && !gp.cpb &&
+    if (!use_row) plan_generic(p, d, atomic, &gp);
+    if (!use_row && atomic && !gp.rows && !gp.cpb && !gp.phase &&
         generic_smem_bytes(p.N, true) > d.smem_optin) {
         // the generic engine keeps its atomic-mode partial in shared memory
         if (g_opts[RN_OPT_DWEIGHT_MODE] == 2)
@@ -514,7 +560,7 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
         atomic = false;
     }
     rp.atomic = gp.atomic = atomic;
-    if (!use_row && atomic && !gp.rows && !gp.cpb) {
+    if (!use_row && atomic && !gp.rows && !gp.cpb && !gp.phase) {
         gp.smem_dw = true;
         gp.smem = generic_smem_bytes(p.N, true);
     }
@@ -524,6 +570,7 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
                          partials, use_row ? rp.grid : gp.grid, p.N};
     return run_sequence(atomic, o, s, [&](bool pdl) {
         if (use_row) return launch_bwd_row(p, rp, s, pdl);
+        if (gp.phase) return launch_bwd_phase(p, gp, s, pdl);
         return gp.cpb ? launch_bwd_realign(p, gp, s, pdl) : launch_bwd_generic(p, gp, s, pdl);
     });
 }

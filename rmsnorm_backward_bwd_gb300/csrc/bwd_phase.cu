@@ -1,0 +1,319 @@
+// Backward phase-class kernel: rows that are not 16-byte multiples (or whose
+// base is off a 16-byte boundary), x, dy, dx and dresidual_out at one
+// alignment phase, rows of at most 1024 16-byte chunks.
+//
+// Same math as the row engine (FlyDSL issue #769 "Math"; fused-add from
+// PR #800 "What's included"). Row r starts at byte r*N*s past the base, so its
+// alignment phase repeats with period P = 16 / gcd(16, N*s mod 16) rows (P = 1
+// when only the base is off a boundary). Each CTA takes the rows of one
+// residue class modulo P. Within a class every row splits the same way into
+// head elements, whole 16-byte chunks and tail elements, so a thread owns the
+// same columns in every row it touches. Its gamma chunks (packed, as loaded)
+// and its weight-gradient partial stay in registers, as in the row engine.
+// The row stays in registers between the two passes, and the class's next row
+// is loaded while the current one is computed. The generic vector kernel, by
+// contrast, lets any CTA take any row, so a column's owner changes with the
+// row's phase and gamma and the partial live in shared memory.
+#include "common.cuh"
+#include "launch.h"
+
+namespace rn {
+
+struct PhaseArgs {
+    const void *x;
+    const void *gamma;
+    const void *dy;
+    const float *rstd;
+    const void *dres;
+    void *dx;
+    float *dw_out;   // scratch: partial rows [gridDim.x][N]; atomic: dweight_f32 (16-byte aligned)
+    int64_t M;
+    int N;
+    float inv_n;
+    int period;      // P
+};
+
+int phase_period(int N, int dtype) {
+    const int d = (int)(((int64_t)N * elem_bytes(dtype)) & 15);
+    if (d == 0) return 1;
+    int g = 16, b = d;  // gcd(16, d)
+    while (b) {
+        const int t = g % b;
+        g = b;
+        b = t;
+    }
+    return 16 / g;
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 gather_chunk(const T *p) {
+    union {
+        T e[16 / sizeof(T)];
+        uint4 v;
+    } u;
+#pragma unroll
+    for (int k = 0; k < (int)(16 / sizeof(T)); ++k) u.e[k] = p[k];
+    return u.v;
+}
+
+template <typename T, bool HAS_DRES, bool ATOMIC, int J>
+__global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
+    constexpr int S = sizeof(T), V = 16 / S;
+    __shared__ float red[2][16];  // warp sums, alternating between rows
+    const T *x = static_cast<const T *>(a.x);
+    const T *g = static_cast<const T *>(a.gamma);
+    const T *dy = static_cast<const T *>(a.dy);
+    const T *dres = static_cast<const T *>(a.dres);
+    T *dx = static_cast<T *>(a.dx);
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    const int N = a.N, P = a.period;
+    const int cls = (int)(blockIdx.x % (unsigned)P);
+    const int64_t rank = blockIdx.x / (unsigned)P;
+    const int64_t nper = ((int64_t)gridDim.x - cls + P - 1) / P;  // CTAs of this class
+
+    // the class's split (address arithmetic on row cls; nothing is read there)
+    const uintptr_t start = reinterpret_cast<uintptr_t>(a.x) + (uintptr_t)cls * (uintptr_t)N * S;
+    int h = (int)(((16u - (unsigned)(start & 15u)) & 15u) / S);
+    if (h > N) h = N;
+    const int nv = (N - h) / V, tail = N - h - nv * V;
+
+    // this thread's chunks (i = tid + k*nthr) and its head or tail element
+    bool own[J];
+    int col[J];
+    uint4 gv[J];
+    float dwp[J][V];
+#pragma unroll
+    for (int k = 0; k < J; ++k) {
+        const int i = tid + k * nthr;
+        own[k] = i < nv;
+        col[k] = h + i * V;
+        gv[k] = own[k] ? gather_chunk<T>(g + col[k]) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < V; ++e) dwp[k][e] = 0.f;
+    }
+    const bool e_own = tid < h + tail;
+    const int je = tid < h ? tid : h + nv * V + (tid - h);
+    const float ge = e_own ? to_f(g[je]) : 0.f;
+    float dwe = 0.f;
+
+    auto load = [&](int64_t row, uint4 (&xv)[J], uint4 (&dv)[J], float &xe, float &de) {
+        const size_t base = (size_t)row * N;
+#pragma unroll
+        for (int k = 0; k < J; ++k) {
+            if (own[k]) {
+                xv[k] = ld_global_nc_v4(x + base + col[k]);
+                dv[k] = ld_global_nc_v4(dy + base + col[k]);
+            }
+        }
+        if (e_own) {
+            xe = to_f(x[base + je]);
+            de = to_f(dy[base + je]);
+        }
+    };
+
+    uint4 xc[J], dc[J];
+#pragma unroll
+    for (int k = 0; k < J; ++k) xc[k] = dc[k] = make_uint4(0, 0, 0, 0);
+    float xec = 0.f, dec = 0.f;
+    int64_t row = cls + rank * P;
+    if (row < a.M) load(row, xc, dc, xec, dec);
+    int buf = 0;
+    while (row < a.M) {
+        const int64_t nrow = row + nper * P;
+        uint4 xn[J], dn[J];
+#pragma unroll
+        for (int k = 0; k < J; ++k) xn[k] = dn[k] = make_uint4(0, 0, 0, 0);
+        float xen = 0.f, den = 0.f;
+        if (nrow < a.M) load(nrow, xn, dn, xen, den);
+        const size_t base = (size_t)row * N;
+        uint4 rv[J];
+        float re = 0.f;
+        if (HAS_DRES) {
+#pragma unroll
+            for (int k = 0; k < J; ++k)
+                rv[k] = own[k] ? *reinterpret_cast<const uint4 *>(dres + base + col[k])
+                               : make_uint4(0, 0, 0, 0);  // a plain load: dx may overwrite dres
+            if (e_own) re = to_f(dres[base + je]);
+        }
+        const float rs = __ldg(a.rstd + row);
+
+        // pass 1: sum_j x_j*dy_j*gamma_j
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < J; ++k) {
+            if (own[k]) {
+                float xf[V], df[V], gf[V];
+                chunk_to_float<T>(xc[k], xf);
+                chunk_to_float<T>(dc[k], df);
+                chunk_to_float<T>(gv[k], gf);
+#pragma unroll
+                for (int e = 0; e < V; ++e) s = fmaf(xf[e], df[e] * gf[e], s);
+            }
+        }
+        if (e_own) s = fmaf(xec, dec * ge, s);
+        s = warp_sum(s);
+        if (lane == 0) red[buf][warp] = s;
+        __syncthreads();  // also orders the reads of red[buf] two rows back before these writes
+        float tot = 0.f;
+        for (int w = 0; w < nwarps; ++w) tot += red[buf][w];
+        buf ^= 1;
+        const float c1 = rs * tot * a.inv_n;
+
+        // pass 2: dx = (wdy - x_hat*c1)*rstd (+ dres); partial += dy*x_hat
+#pragma unroll
+        for (int k = 0; k < J; ++k) {
+            if (own[k]) {
+                float xf[V], df[V], gf[V], o[V], rf[V];
+                chunk_to_float<T>(xc[k], xf);
+                chunk_to_float<T>(dc[k], df);
+                chunk_to_float<T>(gv[k], gf);
+                if (HAS_DRES) chunk_to_float<T>(rv[k], rf);
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const float xh = xf[e] * rs;
+                    o[e] = fmaf(-xh, c1, df[e] * gf[e]) * rs;
+                    if (HAS_DRES) o[e] += rf[e];
+                    dwp[k][e] = fmaf(df[e], xh, dwp[k][e]);
+                }
+                st_global_v4(dx + base + col[k], float_to_chunk<T>(o));
+            }
+        }
+        if (e_own) {
+            const float xh = xec * rs;
+            float d = fmaf(-xh, c1, dec * ge) * rs;
+            if (HAS_DRES) d += re;
+            dx[base + je] = from_f<T>(d);
+            dwe = fmaf(dec, xh, dwe);
+        }
+#pragma unroll
+        for (int k = 0; k < J; ++k) {
+            xc[k] = xn[k];
+            dc[k] = dn[k];
+        }
+        xec = xen;
+        dec = den;
+        row = nrow;
+    }
+    pdl_launch_dependents();
+    if (ATOMIC) {
+        // The partial goes through shared memory so that every class adds it
+        // with 16-byte atomics (dweight_f32 is 16-byte aligned; a class's own
+        // columns start at any element).
+        extern __shared__ __align__(16) float sdw[];  // N floats
+#pragma unroll
+        for (int k = 0; k < J; ++k)
+            if (own[k])
+#pragma unroll
+                for (int e = 0; e < V; ++e) sdw[col[k] + e] = dwp[k][e];
+        if (e_own) sdw[je] = dwe;
+        __syncthreads();
+        pdl_wait();
+        const int n4 = N >> 2;
+        for (int q = tid; q < n4; q += nthr)
+            atomicAdd(reinterpret_cast<float4 *>(a.dw_out) + q, reinterpret_cast<const float4 *>(sdw)[q]);
+        for (int j = (n4 << 2) + tid; j < N; j += nthr) atomicAdd(a.dw_out + j, sdw[j]);
+    } else {
+        float *part = a.dw_out + (size_t)blockIdx.x * N;
+#pragma unroll
+        for (int k = 0; k < J; ++k)
+            if (own[k])
+#pragma unroll
+                for (int e = 0; e < V; ++e) part[col[k] + e] = dwp[k][e];
+        if (e_own) part[je] = dwe;
+    }
+}
+
+template <typename T, bool HAS_DRES, bool ATOMIC, int J>
+static cudaError_t launch_phase_t(const PhaseArgs &args, const GenericPlan &plan, cudaStream_t s,
+                                  bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(plan.threads);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, bwd_phase_kernel<T, HAS_DRES, ATOMIC, J>, args);
+}
+
+template <typename T, bool HAS_DRES, bool ATOMIC>
+static cudaError_t launch_phase_j(const PhaseArgs &args, const GenericPlan &plan, cudaStream_t s,
+                                  bool pdl) {
+    return plan.phase == 2 ? launch_phase_t<T, HAS_DRES, ATOMIC, 2>(args, plan, s, pdl)
+                           : launch_phase_t<T, HAS_DRES, ATOMIC, 1>(args, plan, s, pdl);
+}
+
+template <typename T>
+static cudaError_t launch_phase_dt(const PhaseArgs &args, const GenericPlan &plan, bool has_dres,
+                                   cudaStream_t s, bool pdl) {
+    if (plan.atomic)
+        return has_dres ? launch_phase_j<T, true, true>(args, plan, s, pdl)
+                        : launch_phase_j<T, false, true>(args, plan, s, pdl);
+    return has_dres ? launch_phase_j<T, true, false>(args, plan, s, pdl)
+                    : launch_phase_j<T, false, false>(args, plan, s, pdl);
+}
+
+template <typename T>
+static const void *phase_kernel_ptr(bool dres, bool atomic, int cpt) {
+    if (cpt == 2)
+        return dres ? (atomic ? (const void *)bwd_phase_kernel<T, true, true, 2>
+                              : (const void *)bwd_phase_kernel<T, true, false, 2>)
+                    : (atomic ? (const void *)bwd_phase_kernel<T, false, true, 2>
+                              : (const void *)bwd_phase_kernel<T, false, false, 2>);
+    return dres ? (atomic ? (const void *)bwd_phase_kernel<T, true, true, 1>
+                          : (const void *)bwd_phase_kernel<T, true, false, 1>)
+                : (atomic ? (const void *)bwd_phase_kernel<T, false, true, 1>
+                          : (const void *)bwd_phase_kernel<T, false, false, 1>);
+}
+
+// Resident CTAs per SM of one instance at a CTA size (a multiple of 32 up to
+// 512), from the occupancy calculator without dynamic shared memory (the
+// atomic mode's N floats, at most 33 KB, leave room for the 2 CTAs per SM the
+// planner takes at most); cached per instance and size.
+int phase_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads) {
+    static int cache[3][2][2][2][17];
+    if (dtype < 0 || dtype > 2 || threads < 32 || threads > 512 || (threads & 31)) return 1;
+    int &c = cache[dtype][dres][atomic][cpt == 2][threads >> 5];
+    if (c > 0) return c;
+    const void *k = dtype == kF32 ? phase_kernel_ptr<float>(dres, atomic, cpt)
+                  : dtype == kF16 ? phase_kernel_ptr<__half>(dres, atomic, cpt)
+                                  : phase_kernel_ptr<__nv_bfloat16>(dres, atomic, cpt);
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, 0) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    c = n;
+    return n;
+}
+
+cudaError_t launch_bwd_phase(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
+                             bool pdl_after_zero) {
+    PhaseArgs a;
+    a.x = p.x;
+    a.gamma = p.gamma;
+    a.dy = p.dy;
+    a.rstd = p.rstd;
+    a.dres = p.dres;
+    a.dx = p.dx;
+    a.dw_out = plan.atomic ? p.dw_f32 : reinterpret_cast<float *>(p.ws + kWsHeaderBytes);
+    a.M = p.M;
+    a.N = p.N;
+    a.inv_n = 1.0f / (float)p.N;
+    a.period = phase_period(p.N, p.dtype);
+    // a residue class without a CTA would leave its rows unwritten
+    if (p.M > 0 && plan.grid < (p.M < a.period ? p.M : a.period)) return cudaErrorInvalidValue;
+    const bool has_dres = p.dres != nullptr;
+    switch (p.dtype) {
+    case kF32: return launch_phase_dt<float>(a, plan, has_dres, s, pdl_after_zero);
+    case kF16: return launch_phase_dt<__half>(a, plan, has_dres, s, pdl_after_zero);
+    case kBF16: return launch_phase_dt<__nv_bfloat16>(a, plan, has_dres, s, pdl_after_zero);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rn

@@ -59,6 +59,7 @@ struct GenericPlan {
     bool atomic;
     int rows = 0;      // vector variant: rows in flight per CTA iteration (2, 4); 0 = scalar
     int cpb = 0;       // realigning engine: column blocks per thread (2, 4); 0 = not used
+    int phase = 0;     // phase-class kernel: 16-byte chunks per thread (1, 2); 0 = not used
 };
 
 // Row engine: largest chunk count per row and CTA thread cap for a cpt.
@@ -73,6 +74,10 @@ cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_
 cudaError_t launch_bwd_generic(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
                                bool pdl_after_zero);
 // Rows that are not 16-byte multiples, all row tensors at one alignment phase.
+int phase_period(int N, int dtype);
+int phase_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads);
+cudaError_t launch_bwd_phase(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
+                             bool pdl_after_zero);
 size_t realign_smem_bytes(int N, int dtype, int rows, bool dres);
 cudaError_t launch_bwd_realign(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
                                bool pdl_after_zero);

@@ -17,8 +17,8 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "rmsnorm_gb300.h")
 RN_OK, RN_ERR_INVALID_ARG, RN_ERR_UNSUPPORTED, RN_ERR_CUDA, RN_ERR_WORKSPACE = range(5)
 RN_F32, RN_F16, RN_BF16 = 0, 1, 2
 (OPT_BWD_ENGINE, OPT_DWEIGHT_MODE, OPT_CHUNKS_PER_THREAD, OPT_TEAMS_PER_CTA, OPT_STAGES, OPT_GRID,
- OPT_CLUSTER_SIZE) = range(7)
-OPT_COUNT = 7
+ OPT_CLUSTER_SIZE, OPT_GENERIC_KERNEL) = range(8)
+OPT_COUNT = 8
 
 _lib = None
 

@@ -62,3 +62,21 @@ def test_reference_arm_prints_on_rank_zero_only():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_plan_names_the_timed_kernel():
+    """The bench's roofline names the row-pass kernel from the plan text of
+    every backward engine."""
+    sys.path.insert(0, ROOT)
+    import bench
+    cases = {
+        "engine=row cpt=4 team_threads=128 teams=4 stages=2 grid=152 smem=131328 dw=atomic":
+            "bwd_row_kernel",
+        "engine=cluster csize=2 cpt=4 threads=512 stages=2 clusters=76 dw=atomic": "bwd_cluster_kernel",
+        "engine=generic phase cpt=2 threads=256 grid=304 dw=atomic": "bwd_phase_kernel",
+        "engine=generic realign cpb=4 rows=1 threads=512 grid=152 dw=scratch": "bwd_realign_kernel",
+        "engine=generic vec rows=2 threads=512 grid=304 dw=atomic": "bwd_generic_vec_kernel",
+        "engine=generic threads=512 grid=304 smem_dw=1 dw=atomic": "bwd_generic_kernel",
+    }
+    for plan, kernel in cases.items():
+        assert bench.row_pass_kernel(plan) == kernel, plan

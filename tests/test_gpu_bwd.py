@@ -253,8 +253,10 @@ def test_generic_realigning_engine(M, N, dt, fused, cpb, mode):
     """Rows of 16 to 32 KB that are not 16-byte multiples, all tensors at one
     phase: aligned chunks through a shared row buffer, fixed column blocks
     read back by the row's phase, dx out as aligned chunks (2 and 4 blocks per
-    thread; both weight-gradient modes)."""
+    thread; both weight-gradient modes). The kernel is chosen by option where
+    the phase-class kernel would take the width."""
     native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    native.set_option(native.OPT_GENERIC_KERNEL, 3)
     ex = parity.expected_bwd(Case("realign %s" % dt, M, N, dt, fused=fused, with_dres=fused,
                                   seed=21))
     out = parity.run_gpu_bwd(ex)
@@ -275,8 +277,10 @@ def test_generic_vector_variant(M, N, dt, fused, rows, mode):
     16-byte multiples, all tensors at one phase: 16-byte chunks plus
     element-wise head and tail, several rows per CTA iteration (M not a
     multiple of them), shared partial with atomic adds; both weight-gradient
-    modes."""
+    modes. The kernel is chosen by option where another generic kernel would
+    take the width."""
     native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    native.set_option(native.OPT_GENERIC_KERNEL, 2)
     ex = parity.expected_bwd(Case("vec %s" % dt, M, N, dt, fused=fused, with_dres=fused, seed=23))
     out = parity.run_gpu_bwd(ex)
     plan = native.last_plan()
@@ -290,6 +294,7 @@ def test_generic_realigning_small_grid_and_dres_as_dx():
     dresidual_out in place."""
     import rmsnorm_backward_bwd_gb300 as rn
     native.set_option(native.OPT_GRID, 3)
+    native.set_option(native.OPT_GENERIC_KERNEL, 3)
     ex = parity.expected_bwd(Case("realign grid", 501, 8190, "bf16", fused=True, with_dres=True,
                                   seed=22))
     x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
@@ -302,18 +307,101 @@ def test_generic_realigning_small_grid_and_dres_as_dx():
     parity.check_bwd(ex, dx, dw, dw32)
 
 
+def _offset(t, shift):
+    """A copy of t on the GPU whose data starts `shift` elements past a
+    16-byte boundary."""
+    buf = torch.empty(t.numel() + shift, dtype=t.dtype, device="cuda")
+    v = buf[shift:].view(t.shape)
+    v.copy_(t.cuda())
+    return v
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("M,N,dt,fused,cpt,period", [
+    (1000, 4095, "bf16", False, 2, 8), (333, 4100, "bf16", True, 2, 2),
+    (97, 2999, "f32", False, 2, 4), (130, 1001, "f16", True, 1, 8), (5, 7, "bf16", False, 1, 8),
+    (3, 3, "f32", True, 1, 4), (64, 515, "bf16", True, 1, 8), (17, 8183, "bf16", False, 2, 8),
+    (33, 4095, "f32", True, 2, 4), (300, 2050, "f16", False, 1, 4), (9, 6, "f16", True, 1, 4)],
+    ids=lambda v: str(v))
+def test_generic_phase_kernel(M, N, dt, fused, cpt, period, mode):
+    """Rows that are not 16-byte multiples, all tensors at one phase: each CTA
+    takes the rows of one residue class modulo the phase period (M below,
+    above and not a multiple of it), with fixed columns per thread (1 and 2
+    chunks per thread); both weight-gradient modes."""
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    ex = parity.expected_bwd(Case("phase %s" % dt, M, N, dt, fused=fused, with_dres=fused,
+                                  seed=25))
+    out = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    assert "engine=generic phase cpt=%d" % cpt in plan, plan
+    assert ("atomic" if mode == 2 else "scratch") in plan, plan
+    grid = int(plan.split("grid=")[1].split()[0])
+    assert grid >= min(M, period) and (grid >= M or grid % period == 0), plan
+    parity.check_bwd(ex, *out, tag=" [%s]" % plan)
+
+
+@pytest.mark.parametrize("shift", [1, 3])
+@pytest.mark.parametrize("N,dt", [(4096, "bf16"), (1024, "f32"), (8192, "f16")])
+def test_generic_phase_kernel_aligned_rows_offset_base(N, dt, shift):
+    """Rows of whole 16-byte chunks whose tensors all start off a 16-byte
+    boundary: period 1, every row split the same way."""
+    import rmsnorm_backward_bwd_gb300 as rn
+    ex = parity.expected_bwd(Case("phase base %s" % dt, 77, N, dt, seed=26))
+    x, dy = _offset(ex.x, shift), _offset(ex.dy, shift)
+    dx = _offset(torch.zeros_like(ex.x), shift)
+    dx, dw, dw32 = rn.rmsnorm_bwd(x, ex.gamma.cuda(), dy, ex.rstd.cuda(), dx=dx)
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert "engine=generic phase" in plan, plan
+    parity.check_bwd(ex, dx, dw, dw32, tag=" [%s]" % plan)
+
+
+@pytest.mark.parametrize("grid", [1, 3, 9])
+def test_generic_phase_kernel_small_grid_and_dres_as_dx(grid):
+    """The grid option below the phase period still leaves one CTA per residue
+    class (bf16 N = 8190: period 4); above it, a multiple of it. dx is written
+    over dresidual_out in place."""
+    import rmsnorm_backward_bwd_gb300 as rn
+    native.set_option(native.OPT_GRID, grid)
+    ex = parity.expected_bwd(Case("phase grid", 501, 8190, "bf16", fused=True, with_dres=True,
+                                  seed=27))
+    x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
+    dres = ex.dres.cuda()
+    dx, dres_out, dw, dw32 = rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, dres, dx=dres)
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert "phase" in plan and "grid=%d" % max(4, grid // 4 * 4) in plan, plan
+    assert dx.data_ptr() == dres.data_ptr()
+    parity.check_bwd(ex, dx, dw, dw32)
+
+
+@pytest.mark.parametrize("kernel,name", [(1, "phase"), (2, "vec"), (3, "realign"), (4, "")])
+def test_generic_kernel_option(kernel, name):
+    """RN_OPT_GENERIC_KERNEL picks each generic kernel on one problem (f32
+    N = 4095: in every kernel's range)."""
+    native.set_option(native.OPT_GENERIC_KERNEL, kernel)
+    ex = parity.expected_bwd(Case("pick", 40, 4095, "f32", fused=True, with_dres=True, seed=28))
+    out = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    head = plan.split()
+    assert head[0] == "engine=generic" and (head[1] == name if name else "=" in head[1]), plan
+    parity.check_bwd(ex, *out, tag=" [%s]" % plan)
+
+
 @pytest.mark.parametrize("N,dt,engine", [
-    (8183, "bf16", "engine=generic vec"),        # 1023 column blocks: under the realigning range
-    (8185, "bf16", "engine=generic realign cpb=2"),  # 1024 blocks
+    (2055, "bf16", "engine=generic phase cpt=1"),   # 256 whole 16-byte chunks
+    (2057, "bf16", "engine=generic phase cpt=2"),   # 257
+    (8199, "bf16", "engine=generic phase cpt=2"),   # 1024: the phase-class kernel's widest rows
+    (8201, "bf16", "engine=generic realign cpb=4"),  # 1025 chunks, 1026 column blocks
     (16383, "bf16", "engine=generic realign cpb=4"),  # 2048 blocks
-    (16385, "bf16", "engine=generic vec"),       # 2049 blocks: past it
-    (4093, "f32", "engine=generic realign cpb=2"),   # 1024 blocks of f32
-    (4091, "f32", "engine=generic vec")],        # 1023
+    (16385, "bf16", "engine=generic vec"),       # 2049 blocks: past the realigning range
+    (4099, "f32", "engine=generic phase cpt=2"),    # 1024 chunks of f32
+    (4101, "f32", "engine=generic realign cpb=4")],  # 1025
     ids=lambda v: str(v))
 @pytest.mark.parametrize("M", [1, 3, 64])
 def test_generic_engine_thresholds(N, dt, engine, M):
-    """The width thresholds between the realigning engine and the vector
-    variant, on both sides, with few and several rows."""
+    """The width thresholds between the generic kernels (phase-class,
+    realigning, vector), on both sides, with few and several rows."""
     ex = parity.expected_bwd(Case("threshold", M, N, dt, fused=True, with_dres=True, seed=41))
     out = parity.run_gpu_bwd(ex)
     plan = native.last_plan()
