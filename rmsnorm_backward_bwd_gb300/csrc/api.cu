@@ -353,29 +353,41 @@ static bool plan_realign(const BwdProblem &p, const DeviceInfo &d, GenericPlan *
 // 38.0 -> 49.4 (4 per SM). The grid is a multiple of the phase period P when
 // it is below M, so that every residue class gets the same number of CTAs,
 // and never below min(P, M), so that every class has one.
-static bool plan_phase(const BwdProblem &p, const DeviceInfo &d, bool atomic, GenericPlan *plan) {
-    if (!generic_vec_ok(p, d)) return false;
-    const int64_t nvmax = (int64_t)p.N * elem_bytes(p.dtype) / 16;
-    if (nvmax > 1024) return false;
-    const int cpt = nvmax > 256 ? 2 : 1;
-    int threads = (int)((nvmax + cpt - 1) / cpt + 31) / 32 * 32;
-    if (threads < 32) threads = 32;
-    int per_sm = phase_blocks_per_sm(p.dtype, p.dres != nullptr, atomic, cpt, threads);
+static int phase_grid(int64_t M, int P, int per_sm, const DeviceInfo &d) {
     if (per_sm < 1) per_sm = 1;
     if (per_sm > 2) per_sm = 2;
     int64_t grid = (int64_t)per_sm * d.num_sms;
     if (g_opts[RN_OPT_GRID] > 0 && grid > g_opts[RN_OPT_GRID]) grid = g_opts[RN_OPT_GRID];
     // every residue class needs a CTA: at least min(P, M), whatever the grid option says
-    const int P = phase_period(p.N, p.dtype);
-    if (grid >= p.M) grid = p.M;
+    if (grid >= M) grid = M;
     else if (grid >= P) grid = grid / P * P;
-    if (grid < P) grid = p.M < P ? p.M : P;
+    if (grid < P) grid = M < P ? M : P;
     if (grid < 1) grid = 1;
+    return (int)grid;
+}
+
+// CTA size and chunks per thread of a phase-class kernel for a row of N
+// elements of s bytes: 1 chunk per thread up to 256 whole 16-byte chunks, else
+// 2, up to 1024 chunks. False past that.
+static bool phase_shape(int N, int dtype, int *cpt, int *threads) {
+    const int64_t nvmax = (int64_t)N * elem_bytes(dtype) / 16;
+    if (nvmax > 1024) return false;
+    *cpt = nvmax > 256 ? 2 : 1;
+    int t = (int)((nvmax + *cpt - 1) / *cpt + 31) / 32 * 32;
+    *threads = t < 32 ? 32 : t;
+    return true;
+}
+
+static bool plan_phase(const BwdProblem &p, const DeviceInfo &d, bool atomic, GenericPlan *plan) {
+    if (!generic_vec_ok(p, d)) return false;
+    int cpt, threads;
+    if (!phase_shape(p.N, p.dtype, &cpt, &threads)) return false;
+    const int per_sm = phase_blocks_per_sm(p.dtype, p.dres != nullptr, atomic, cpt, threads);
     plan->phase = cpt;
+    plan->grid = phase_grid(p.M, phase_period(p.N, p.dtype), per_sm, d);
     plan->cpb = 0;
     plan->rows = 0;
     plan->threads = threads;
-    plan->grid = (int)grid;
     plan->smem_dw = atomic;
     plan->smem = atomic ? (size_t)p.N * 4 : 0;  // the atomic mode's staged partial
     plan->atomic = atomic;
@@ -624,7 +636,35 @@ static bool plan_ln_cluster(const LnBwdProblem &p, const DeviceInfo &d, bool ato
     return cluster_count("ln", p.M, p.dtype, false, d, plan, ln_cluster_query, &p);
 }
 
-static void plan_ln_generic(const LnBwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
+// The LayerNorm phase-class kernel: x, dy and dx at one alignment phase and
+// the RMSNorm kernel's row-size range and grid rule.
+static bool plan_ln_phase(const LnBwdProblem &p, const DeviceInfo &d, bool atomic,
+                          GenericPlan *plan) {
+    const uintptr_t S = (uintptr_t)elem_bytes(p.dtype), ph = (uintptr_t)p.x & 15u;
+    for (const void *q : {p.x, p.dy, static_cast<const void *>(p.dx)})
+        if (((uintptr_t)q & 15u) != ph || ((uintptr_t)q % S) != 0) return false;
+    int cpt, threads;
+    if (!phase_shape(p.N, p.dtype, &cpt, &threads)) return false;
+    const size_t smem = ln_phase_smem_bytes(p.N, atomic);
+    if (smem > (size_t)d.smem_optin) return false;
+    const int per_sm = ln_phase_blocks_per_sm(p.dtype, atomic, cpt, threads, smem);
+    plan->phase = cpt;
+    plan->cpb = 0;
+    plan->rows = 0;
+    plan->threads = threads;
+    plan->grid = phase_grid(p.M, phase_period(p.N, p.dtype), per_sm, d);
+    plan->smem_dw = atomic;
+    plan->smem = smem;
+    plan->atomic = atomic;
+    return true;
+}
+
+static void plan_ln_generic(const LnBwdProblem &p, const DeviceInfo &d, bool atomic,
+                            GenericPlan *plan) {
+    plan->phase = 0;
+    // RN_OPT_GENERIC_KERNEL: 1 phase-class, 2 (or 3) vector, 4 element-wise
+    const int pick = g_opts[RN_OPT_GENERIC_KERNEL];
+    if (pick <= 1 && plan_ln_phase(p, d, atomic, plan)) return;
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
     plan->smem_dw = ln_generic_smem_bytes(p.N, true) <= budget;
@@ -633,7 +673,7 @@ static void plan_ln_generic(const LnBwdProblem &p, const DeviceInfo &d, GenericP
     plan->cpb = 0;
     // vector variant: x, dy and dx at one alignment phase (element-aligned)
     const uintptr_t S = (uintptr_t)elem_bytes(p.dtype), ph = (uintptr_t)p.x & 15u;
-    bool vec = ln_generic_vec_smem_bytes(p.N) <= budget;
+    bool vec = pick != 4 && ln_generic_vec_smem_bytes(p.N) <= budget;
     for (const void *q : {p.x, p.dy, static_cast<const void *>(p.dx)})
         vec = vec && ((uintptr_t)q & 15u) == ph && ((uintptr_t)q % S) == 0;
     if (vec) {
@@ -696,15 +736,16 @@ static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t
         return run_sequence(atomic, o, s,
                             [&](bool pdl) { return launch_ln_bwd_cluster(p, cp, s, pdl); });
     }
-    if (!use_row) plan_ln_generic(p, d, &gp);
-    if (!use_row && atomic && !gp.rows && ln_generic_smem_bytes(p.N, true) > d.smem_optin) {
+    if (!use_row) plan_ln_generic(p, d, atomic, &gp);
+    if (!use_row && atomic && !gp.rows && !gp.phase &&
+        ln_generic_smem_bytes(p.N, true) > d.smem_optin) {
         // the generic engine keeps its atomic-mode partials in shared memory
         if (g_opts[RN_OPT_DWEIGHT_MODE] == 2)
             return fail(RN_ERR_UNSUPPORTED, "atomic mode needs N*8 bytes of shared memory");
         atomic = false;
     }
     rp.atomic = gp.atomic = atomic;
-    if (!use_row && atomic && !gp.rows) {
+    if (!use_row && atomic && !gp.rows && !gp.phase) {
         gp.smem_dw = true;
         gp.smem = ln_generic_smem_bytes(p.N, true);
     }
@@ -713,7 +754,8 @@ static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t
     const DwOutputs o = {p.dg_f32, p.dg_cast, p.db_f32, p.db_cast, p.N, p.dtype,
                          partials, use_row ? rp.grid : gp.grid, 2 * p.N};
     return run_sequence(atomic, o, s, [&](bool pdl) {
-        return use_row ? launch_ln_bwd_row(p, rp, s, pdl) : launch_ln_bwd_generic(p, gp, s, pdl);
+        if (use_row) return launch_ln_bwd_row(p, rp, s, pdl);
+        return gp.phase ? launch_ln_bwd_phase(p, gp, s, pdl) : launch_ln_bwd_generic(p, gp, s, pdl);
     });
 }
 

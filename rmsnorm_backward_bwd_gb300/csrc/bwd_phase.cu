@@ -307,6 +307,7 @@ cudaError_t launch_bwd_phase(const BwdProblem &p, const GenericPlan &plan, cudaS
     a.period = phase_period(p.N, p.dtype);
     // a residue class without a CTA would leave its rows unwritten
     if (p.M > 0 && plan.grid < (p.M < a.period ? p.M : a.period)) return cudaErrorInvalidValue;
+    if (plan.atomic && plan.smem < (size_t)p.N * 4) return cudaErrorInvalidValue;
     const bool has_dres = p.dres != nullptr;
     switch (p.dtype) {
     case kF32: return launch_phase_dt<float>(a, plan, has_dres, s, pdl_after_zero);

@@ -76,6 +76,8 @@ cudaError_t launch_bwd_generic(const BwdProblem &p, const GenericPlan &plan, cud
 // Rows that are not 16-byte multiples, all row tensors at one alignment phase.
 int phase_period(int N, int dtype);
 int phase_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads);
+size_t ln_phase_smem_bytes(int N, bool atomic);
+int ln_phase_blocks_per_sm(int dtype, bool atomic, int cpt, int threads, size_t smem);
 cudaError_t launch_bwd_phase(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
                              bool pdl_after_zero);
 size_t realign_smem_bytes(int N, int dtype, int rows, bool dres);
@@ -171,6 +173,9 @@ struct LnBwdProblem {
     int N;
     int dtype;
 };
+
+cudaError_t launch_ln_bwd_phase(const LnBwdProblem &p, const GenericPlan &plan, cudaStream_t s,
+                                bool pdl_after_zero);
 
 // LayerNorm forward for unaligned rows (and rows longer than the row engine's tile).
 cudaError_t launch_ln_fwd(const LnFwdProblem &p, int num_sms, cudaStream_t s);

@@ -324,13 +324,47 @@ def test_layernorm_generic_vector_variant(M, N, dt, rows, with_dbeta, mode):
     """Rows that are not 16-byte multiples with x, dy and dx at one phase:
     16-byte chunks plus element-wise head and tail, several rows per CTA
     iteration, dgamma / dbeta partials in shared memory; both modes, with and
-    without the bias gradient."""
+    without the bias gradient. Chosen by option: the phase-class kernel takes
+    these widths by default."""
     native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    native.set_option(native.OPT_GENERIC_KERNEL, 2)
     ex = expected(Case("ln vec", M, N, dt, eps=1e-5, seed=33))
     out = run_gpu(ex, with_dbeta=with_dbeta)
     plan = native.last_plan()
     assert "engine=ln_generic vec rows=%d" % rows in plan, plan
     check(ex, out, with_dbeta=with_dbeta, tag=" [%s]" % plan)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("with_dbeta", [True, False])
+@pytest.mark.parametrize("M,N,dt,cpt", [(700, 4095, "bf16", 2), (97, 2999, "f32", 2),
+                                        (130, 1001, "f16", 1), (5, 7, "bf16", 1),
+                                        (40, 8190, "bf16", 2), (3, 3, "f32", 1),
+                                        (333, 4100, "bf16", 2), (64, 1022, "f32", 1)],
+                         ids=lambda v: str(v))
+def test_layernorm_generic_phase_kernel(M, N, dt, cpt, with_dbeta, mode):
+    """Rows that are not 16-byte multiples with x, dy and dx at one phase:
+    each CTA takes the rows of one residue class modulo the phase period, with
+    fixed columns per thread and both partials in registers; both modes, with
+    and without the bias gradient."""
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    ex = expected(Case("ln phase", M, N, dt, eps=1e-5, seed=35))
+    out = run_gpu(ex, with_dbeta=with_dbeta)
+    plan = native.last_plan()
+    assert "engine=ln_generic phase cpt=%d" % cpt in plan, plan
+    assert ("atomic" if mode == 2 else "scratch") in plan, plan
+    check(ex, out, with_dbeta=with_dbeta, tag=" [%s]" % plan)
+
+
+def test_layernorm_generic_phase_kernel_small_grid():
+    """The grid option below the phase period (bf16 N = 4095: period 8) still
+    leaves one CTA per residue class."""
+    native.set_option(native.OPT_GRID, 3)
+    ex = expected(Case("ln phase grid", 301, 4095, "bf16", eps=1e-5, seed=36))
+    out = run_gpu(ex)
+    plan = native.last_plan()
+    assert "phase" in plan and "grid=8" in plan, plan
+    check(ex, out, tag=" [%s]" % plan)
 
 
 def test_layernorm_mismatched_phases_take_the_scalar_generic_kernel():
