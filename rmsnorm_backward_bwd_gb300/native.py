@@ -70,9 +70,11 @@ def _bind(lib):
 # Process-wide overrides read from the environment when the library loads:
 #   RN_BWD_ENGINE   = auto | row | generic | cluster
 #   RN_DWEIGHT_MODE = auto | scratch (deterministic) | atomic
+#   RN_GENERIC_KERNEL = auto | phase | vec | realign | scalar (unaligned rows)
 ENV_OPTIONS = {
     "RN_BWD_ENGINE": (0, {"auto": 0, "row": 1, "generic": 2, "cluster": 3}),
     "RN_DWEIGHT_MODE": (1, {"auto": 0, "scratch": 1, "atomic": 2}),
+    "RN_GENERIC_KERNEL": (7, {"auto": 0, "phase": 1, "vec": 2, "realign": 3, "scalar": 4}),
 }
 
 
