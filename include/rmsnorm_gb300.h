@@ -27,6 +27,10 @@
  *     I/O dtype once, to nearest even.
  *   - Pointers are DEVICE pointers on the calling thread's current CUDA
  *     device; the caller owns every buffer. Nothing is allocated or freed.
+ *     Each buffer starts at a multiple of its element size (the I/O dtype's;
+ *     4 bytes for the fp32 ones), else RN_ERR_INVALID_ARG. Any further
+ *     alignment is optional: 16-byte aligned row tensors with 16-byte
+ *     multiple rows take the fastest engines.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
  *     asynchronous: they enqueue kernels on `stream` and return.
  *   - Errors: argument checks run before anything is enqueued and return
@@ -53,7 +57,8 @@ typedef enum rn_dtype { RN_F32 = 0, RN_F16 = 1, RN_BF16 = 2 } rn_dtype;
 
 typedef enum rn_status {
     RN_OK = 0,
-    RN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad dtype code, bad option */
+    RN_ERR_INVALID_ARG = 1,  /* null pointer, a buffer not aligned to its element size,
+                                bad size, bad dtype code, bad option */
     RN_ERR_UNSUPPORTED = 2,  /* shape/alignment no engine handles (e.g. N too large) */
     RN_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     RN_ERR_WORKSPACE = 4     /* workspace missing, misaligned or too small */

@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <string>
 #include <unordered_map>
@@ -768,6 +769,24 @@ static rn_status check_common(int64_t M, int64_t N, int dtype) {
     return RN_OK;
 }
 
+// Every buffer must start at a multiple of its element size (the dtype's for
+// row tensors, gamma, beta and the casts; 4 bytes for rstd, mean and the fp32
+// outputs): the kernels load and store whole elements, and a misaligned one
+// would fault on the GPU instead of failing here.
+struct Buf {
+    const void *p;
+    int bytes;
+    const char *name;
+};
+
+static rn_status check_alignment(std::initializer_list<Buf> bufs) {
+    for (const Buf &b : bufs)
+        if (b.p && ((uintptr_t)b.p % (uintptr_t)b.bytes) != 0)
+            return fail(RN_ERR_INVALID_ARG, "%s is not aligned to its element size (%d bytes)",
+                        b.name, b.bytes);
+    return RN_OK;
+}
+
 static rn_status bwd_entry(const void *x, const void *gamma, const void *dy, const float *rstd,
                            const void *dres, void *dx, float *dw_f32, void *dw_cast, void *ws,
                            size_t ws_bytes, int64_t M, int64_t N, int dtype, void *stream) {
@@ -780,6 +799,13 @@ static rn_status bwd_entry(const void *x, const void *gamma, const void *dy, con
         return fail(RN_ERR_INVALID_ARG, "x, dy, rstd and dx are required when M > 0");
     if (M > 0 && (dx == x || dx == dy || (void *)dx == (void *)rstd))
         return fail(RN_ERR_INVALID_ARG, "dx must not alias x, dy or rstd");
+    {
+        const int S = elem_bytes(dtype);
+        st = check_alignment({{x, S, "x"}, {gamma, S, "gamma"}, {dy, S, "dy"}, {dres, S, "dresidual_out"},
+                              {dx, S, "dx"}, {dw_cast, S, "dweight"}, {rstd, 4, "rstd"},
+                              {dw_f32, 4, "dweight_f32"}});
+        if (st != RN_OK) return st;
+    }
     BwdProblem p;
     p.x = x;
     p.gamma = gamma;
@@ -808,6 +834,13 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
     if (M > 0 && (!x || !y)) return fail(RN_ERR_INVALID_ARG, "input and output are required");
     if (fused && M > 0 && (!residual || !residual_out))
         return fail(RN_ERR_INVALID_ARG, "residual and residual_out are required");
+    {
+        const int S = elem_bytes(dtype);
+        st = check_alignment({{x, S, "x"}, {residual, S, "residual"}, {gamma, S, "gamma"},
+                              {y, S, "output"}, {residual_out, S, "residual_out"},
+                              {rstd, 4, "rstd"}});
+        if (st != RN_OK) return st;
+    }
     if (M == 0) return RN_OK;
     DeviceInfo d;
     cudaError_t e = device_info(&d, nullptr);
@@ -864,6 +897,12 @@ static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta
     if (!(eps >= 0.f)) return fail(RN_ERR_INVALID_ARG, "eps must be >= 0");
     if (!gamma) return fail(RN_ERR_INVALID_ARG, "gamma is required");
     if (M > 0 && (!x || !y)) return fail(RN_ERR_INVALID_ARG, "input and output are required");
+    {
+        const int S = elem_bytes(dtype);
+        st = check_alignment({{x, S, "x"}, {gamma, S, "gamma"}, {beta, S, "beta"}, {y, S, "y"},
+                              {mean, 4, "mean"}, {rstd, 4, "rstd"}});
+        if (st != RN_OK) return st;
+    }
     if (M == 0) return RN_OK;
     DeviceInfo d;
     cudaError_t e = device_info(&d, nullptr);
@@ -924,6 +963,14 @@ static rn_status ln_bwd_entry(const void *x, const void *gamma, const void *dy, 
         return fail(RN_ERR_INVALID_ARG, "x, dy, mean, rstd and dx are required when M > 0");
     if (M > 0 && (dx == x || dx == dy || (void *)dx == (void *)mean || (void *)dx == (void *)rstd))
         return fail(RN_ERR_INVALID_ARG, "dx must not alias x, dy, mean or rstd");
+    {
+        const int S = elem_bytes(dtype);
+        st = check_alignment({{x, S, "x"}, {gamma, S, "gamma"}, {dy, S, "dy"}, {dx, S, "dx"},
+                              {dg_cast, S, "dgamma"}, {db_cast, S, "dbeta"}, {mean, 4, "mean"},
+                              {rstd, 4, "rstd"}, {dg_f32, 4, "dgamma_f32"},
+                              {db_f32, 4, "dbeta_f32"}});
+        if (st != RN_OK) return st;
+    }
     LnBwdProblem p;
     p.x = x;
     p.gamma = gamma;

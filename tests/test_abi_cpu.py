@@ -46,6 +46,16 @@ def test_argument_checks_fail_before_any_launch():
     assert _bwd(lib, x=fake, g=fake, dy=fake, rstd=fake, dx=fake, dw32=fake) == \
         native.RN_ERR_INVALID_ARG                                          # dx aliases x
     assert _bwd(lib, N=1 << 40, g=fake, dw32=fake) == native.RN_ERR_UNSUPPORTED
+    # buffers off their element size fail before any launch (bf16: 2 bytes; fp32: 4)
+    odd = ctypes.c_void_p(0x1001)
+    assert _bwd(lib, g=odd, dw32=fake, M=0) == native.RN_ERR_INVALID_ARG
+    assert b"gamma is not aligned" in lib.rn_last_error()
+    assert _bwd(lib, g=fake, dw32=ctypes.c_void_p(0x1002), M=0) == native.RN_ERR_INVALID_ARG
+    assert b"dweight_f32" in lib.rn_last_error()
+    assert lib.rn_rmsnorm_fwd(odd, fake, 1e-6, fake, None, 4, 8, 2, None) == \
+        native.RN_ERR_INVALID_ARG
+    assert lib.rn_layernorm_fwd(fake, fake, None, 1e-5, fake, None, ctypes.c_void_p(0x1006), 4, 8,
+                                2, None) == native.RN_ERR_INVALID_ARG
     assert lib.rn_rmsnorm_fwd(None, None, 1e-6, None, None, 4, 8, 2, None) == native.RN_ERR_INVALID_ARG
     assert lib.rn_rmsnorm_fwd(fake, fake, -1.0, fake, None, 4, 8, 2, None) == native.RN_ERR_INVALID_ARG
     assert lib.rn_fused_add_rmsnorm_fwd(fake, None, fake, 1e-6, fake, fake, None, 4, 8, 2,
