@@ -15,6 +15,7 @@
 // contrast, lets any CTA take any row, so a column's owner changes with the
 // row's phase and gamma and the partial live in shared memory.
 #include "common.cuh"
+#include "unaligned.cuh"
 #include "launch.h"
 
 namespace rn {
@@ -43,17 +44,6 @@ int phase_period(int N, int dtype) {
         b = t;
     }
     return 16 / g;
-}
-
-template <typename T>
-__device__ __forceinline__ uint4 gather_chunk(const T *p) {
-    union {
-        T e[16 / sizeof(T)];
-        uint4 v;
-    } u;
-#pragma unroll
-    for (int k = 0; k < (int)(16 / sizeof(T)); ++k) u.e[k] = p[k];
-    return u.v;
 }
 
 template <typename T, bool HAS_DRES, bool ATOMIC, int J>

@@ -12,6 +12,7 @@
 // next row is loaded while the current one is computed; in atomic mode the
 // partials go out through shared memory as 16-byte atomic adds.
 #include "common.cuh"
+#include "unaligned.cuh"
 #include "launch.h"
 
 namespace rn {
@@ -32,17 +33,6 @@ struct LnPhaseArgs {
     float inv_n;
     int period;     // P
 };
-
-template <typename T>
-__device__ __forceinline__ uint4 ln_gather_chunk(const T *p) {
-    union {
-        T e[16 / sizeof(T)];
-        uint4 v;
-    } u;
-#pragma unroll
-    for (int k = 0; k < (int)(16 / sizeof(T)); ++k) u.e[k] = p[k];
-    return u.v;
-}
 
 // Padded length of the atomic mode's first staged partial: the second one
 // starts 16-byte aligned.
@@ -82,7 +72,7 @@ __global__ void __launch_bounds__(512) ln_bwd_phase_kernel(const LnPhaseArgs a) 
         const int i = tid + k * nthr;
         own[k] = i < nv;
         col[k] = h + i * V;
-        gv[k] = own[k] ? ln_gather_chunk<T>(g + col[k]) : make_uint4(0, 0, 0, 0);
+        gv[k] = own[k] ? gather_chunk<T>(g + col[k]) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int e = 0; e < V; ++e) dgp[k][e] = dbp[k][e] = 0.f;
     }

@@ -23,6 +23,19 @@ __device__ __forceinline__ uint4 shift_bytes(const uint4 &lo, const uint4 &hi, i
                       __funnelshift_r(a2, a3, b), __funnelshift_r(a3, a4, b));
 }
 
+// The 16 bytes of elements p[0 .. 16/sizeof(T)), loaded one element at a time
+// (p need only be element-aligned), packed as one 16-byte chunk.
+template <typename T>
+__device__ __forceinline__ uint4 gather_chunk(const T *p) {
+    union {
+        T e[16 / sizeof(T)];
+        uint4 v;
+    } u;
+#pragma unroll
+    for (int k = 0; k < (int)(16 / sizeof(T)); ++k) u.e[k] = p[k];
+    return u.v;
+}
+
 // The generic engines' per-column shared arrays are padded by one word per
 // 32 columns: a warp's lanes touch columns 16/s apart, which without the pad
 // share banks. vpad is column c's padded index; vec_words is the padded
