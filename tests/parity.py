@@ -15,11 +15,15 @@ from the seeded generator and the oracle, never from the GPU.
 
 Ill-conditioned elements: where dx is a near-total cancellation of its two
 terms (wdy - x_hat*c1; e.g. N = 1, where x_hat^2 = ms/(ms+eps) is 1 - O(eps)),
-fp32 arithmetic cannot reach a bound relative to |dx| itself. Such an element
-also passes when its error is within fp32 round-off of the terms it is made
-of: 2^-24 * rstd * (16*(|wdy| + |x_hat*c1|) + 4*sqrt(N)*|x_hat|*rstd*mean|x*wdy|)
-(pointwise roundings plus the c1 reduction); this scale is computed in fp64
-from the inputs for the failing elements only.
+fp32 arithmetic cannot reach a bound relative to |dx| itself. Only such an
+element may pass on a second, round-off bound: its cancellation ratio
+kappa = |dx| / (rstd * (|wdy| + |x_hat*c1|)) must be below KAPPA_ILL, and its
+error within fp32 round-off of the terms it is made of:
+2^-24 * rstd * (16*(|wdy| + |x_hat*c1|) + 4*sqrt(N)*|x_hat|*rstd*mean|x*wdy|)
+(pointwise roundings plus the c1 reduction), computed in fp64 from the
+inputs for the failing elements only. Every comparison returns how many
+elements passed that way; check_bwd asserts none unless the caller allows
+them (the degenerate widths), and the workload tests assert zero.
 """
 import numpy as np
 import torch
@@ -28,6 +32,8 @@ import oracle
 from rmsnorm_backward_bwd_gb300 import synth
 
 P_BITS = {"f32": 24, "f16": 11, "bf16": 8}
+# cancellation ratio below which an element counts as ill-conditioned
+KAPPA_ILL = 1e-3
 E_MIN = {"f32": -126, "f16": -14, "bf16": -126}
 
 
@@ -45,8 +51,10 @@ def to64(t):
 
 def check_tensor(name, got, ref, dtype, kind="dx", roundoff=None):
     """Compare one GPU output (torch tensor) with the fp64 reference (numpy).
-    roundoff(mask) -> per-element fp32 round-off bound for the masked
-    elements (dx only; see the module docstring)."""
+    roundoff(mask) -> (bound, terms): per-element fp32 round-off bound and the
+    magnitude of dx's terms (rstd * (|wdy| + |x_hat*c1|), plus |c2| for
+    LayerNorm) for the masked elements (dx only; see the module docstring).
+    Returns the number of elements that passed only on the round-off bound."""
     g = to64(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert g.shape == ref.shape, (name, g.shape, ref.shape)
@@ -54,32 +62,43 @@ def check_tensor(name, got, ref, dtype, kind="dx", roundoff=None):
     scale = float(np.max(np.abs(ref))) if ref.size else 0.0
     err = np.abs(g - ref)
     if ref.size == 0:
-        return
+        return 0
     if kind == "dweight_f32":
         rel = float(np.max(err)) / max(scale, 1e-30)
         assert rel <= 1e-4, "%s: max rel err %.3g > 1e-4" % (name, rel)
-        return
+        return 0
     if kind == "dweight":
         bound = ulp(ref, dtype) + 1e-4 * scale
         bad = err > bound
         assert not bad.any(), "%s: %d elements beyond 1 ulp (worst %.3g vs bound %.3g)" % (
             name, int(bad.sum()), float(err[bad].max()), float(bound[bad][np.argmax(err[bad])]))
-        return
+        return 0
+
+    def escape(bad, base):
+        """Elements of `bad` that are ill-conditioned and within the round-off
+        bound (added to `base`, the dtype's own allowance) pass."""
+        if not bad.any() or roundoff is None:
+            return 0
+        rb, terms = roundoff(bad)
+        kappa = np.abs(ref[bad]) / np.maximum(terms, 1e-300)
+        ok = (kappa < KAPPA_ILL) & (err[bad] <= base + rb)
+        bad[bad] = ~ok
+        return int(ok.sum())
+
     if dtype == "f32":
         bad = err > 1e-5 * scale
-        if bad.any() and roundoff is not None:
-            bad[bad] = err[bad] > roundoff(bad)
+        n_esc = escape(bad, 0.0)
         assert not bad.any(), "%s: %d elements beyond rel err 1e-5 (max rel %.3g)" % (
             name, int(bad.sum()), float(np.max(err)) / max(scale, 1e-30))
-        return
+        return n_esc
     loose = err <= 1e-2 + 1.6e-2 * np.abs(ref)
     assert loose.all(), "%s: %d elements outside atol 1e-2 / rtol 1.6e-2" % (name, int((~loose).sum()))
     bound = ulp(ref, dtype) + 1e-5 * scale
     bad = err > bound
-    if bad.any() and roundoff is not None:
-        bad[bad] = err[bad] > ulp(ref[bad], dtype) + roundoff(bad)
+    n_esc = escape(bad, ulp(ref[bad], dtype) if bad.any() else 0.0)
     assert not bad.any(), "%s: %d elements beyond 1 ulp (worst excess %.3g)" % (
         name, int(bad.sum()), float((err - bound)[bad].max()))
+    return n_esc
 
 
 class Expected:
@@ -122,7 +141,8 @@ def expected_bwd(case, nthreads=0):
 
 
 def roundoff_bound(ex):
-    """fp32 round-off scale of dx's terms, for the elements of a mask."""
+    """fp32 round-off bound of dx's terms and their magnitude, for the
+    elements of a mask."""
     def fn(mask):
         rows, cols = np.nonzero(mask.reshape(ex.a64.shape))
         urows = np.unique(rows)
@@ -136,8 +156,9 @@ def roundoff_bound(ex):
         xh = ex.a64[rows, cols] * ex.rstd64[rows]
         wdy = ex.dy64[rows, cols] * ex.g64[cols]
         rs = ex.rstd64[rows]
-        return 2.0**-24 * rs * (16 * (np.abs(wdy) + np.abs(xh * c1[pos]))
-                                + 4 * np.sqrt(N) * np.abs(xh) * rs * mabs[pos])
+        terms = np.abs(wdy) + np.abs(xh * c1[pos])
+        bound = 2.0**-24 * rs * (16 * terms + 4 * np.sqrt(N) * np.abs(xh) * rs * mabs[pos])
+        return bound, rs * terms
     return fn
 
 
@@ -157,9 +178,15 @@ def run_gpu_bwd(ex, dev="cuda", dx_out=None):
     return dx, dw, dw32
 
 
-def check_bwd(ex, dx, dw, dw32, tag=""):
+def check_bwd(ex, dx, dw, dw32, tag="", allow_ill_conditioned=False):
+    """dx, dweight_f32 and the cast dweight against the oracle. The round-off
+    escape for ill-conditioned dx elements is used only when the caller
+    allows it (degenerate widths such as N = 1); returns its count."""
     dt = ex.case.dtype
-    check_tensor("dx" + tag, dx, ex.dx, dt, "dx", roundoff=roundoff_bound(ex))
+    n_esc = check_tensor("dx" + tag, dx, ex.dx, dt, "dx", roundoff=roundoff_bound(ex))
+    assert allow_ill_conditioned or n_esc == 0, (
+        "dx%s: %d elements passed only on the round-off bound" % (tag, n_esc))
     check_tensor("dweight_f32" + tag, dw32, ex.dw, dt, "dweight_f32")
     if dw is not None:
         check_tensor("dweight" + tag, dw, ex.dw, dt, "dweight")
+    return n_esc

@@ -69,7 +69,7 @@ def test_backward_writes_stay_in_bounds(M, N, dt, fused, mode):
     plan = native.last_plan()
     for name, buf in (("dx", dx), ("dweight_f32", dw32), ("dweight", dw)):
         assert buf.margins_intact(), "%s margin overwritten [%s]" % (name, plan)
-    parity.check_bwd(ex, dx.t, dw.t, dw32.t, tag=" [%s]" % plan)
+    parity.check_bwd(ex, dx.t, dw.t, dw32.t, tag=" [%s]" % plan, allow_ill_conditioned=N == 1)
 
 
 @pytest.mark.parametrize("engine", [1, 3])

@@ -76,7 +76,7 @@ def test_random_backward(seed):
     plan = native.last_plan()
     _ENGINES.add(_engine(plan))
     parity.check_bwd(ex, dx, dw, dw32, tag=" [M=%d N=%d %s %s phases=%s: %s]" % (
-        M, N, dt, variant, ph, plan))
+        M, N, dt, variant, ph, plan), allow_ill_conditioned=N == 1)
 
 
 def test_random_backward_cases_reached_every_engine():
