@@ -215,8 +215,11 @@ rn_status rn_layernorm_bwd(const void *x, const void *gamma, const void *dy, con
  *   with RN_ERR_UNSUPPORTED and a message in rn_last_error(); nothing is
  *   launched. The call allocates nothing and frees nothing.
  *   The first call on a device looks up the array's device address on that
- *   device (cudaGetSymbolAddress); make that first call before any stream
- *   capture. All calls share the one array: nothing in it needs to start at
+ *   device (cudaGetSymbolAddress) and keeps it for the life of the process;
+ *   make that first call before any stream capture. A device reset
+ *   (cudaDeviceReset) while this library is loaded is not supported: it
+ *   reloads the device image, and the kept address would then be stale. All
+ *   calls share the one array: nothing in it needs to start at
  *   zero (every call overwrites the part it reads), but calls that could run
  *   at the same time on the GPU (different streams without ordering) race on
  *   it and give wrong results. Order such calls on one stream or with events.

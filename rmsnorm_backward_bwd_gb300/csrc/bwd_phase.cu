@@ -217,6 +217,11 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
 template <typename T, bool HAS_DRES, bool ATOMIC, int J>
 static cudaError_t launch_phase_t(const PhaseArgs &args, const GenericPlan &plan, cudaStream_t s,
                                   bool pdl) {
+    // the atomic mode stages N floats in dynamic shared memory: raise the
+    // kernel's cap when a plan asks for more than the default 48 KB
+    cudaError_t e = ensure_smem_attr((const void *)bwd_phase_kernel<T, HAS_DRES, ATOMIC, J>,
+                                     plan.smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(plan.threads);

@@ -13,7 +13,10 @@
 // library holds it until the process exits. In host code its name is only a
 // host-side handle, not a device address, so the device address is looked up
 // with cudaGetSymbolAddress once per device (with that device current) and
-// cached; that lookup happens on the first call on each device.
+// cached; that lookup happens on the first call on each device. The cache
+// assumes the device image stays loaded: a cudaDeviceReset while this library
+// is loaded would reload it at another address, so a reset is not supported
+// (the header says so).
 #include <cuda_runtime.h>
 
 #include <cstdio>
