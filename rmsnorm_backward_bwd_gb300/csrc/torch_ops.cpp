@@ -28,7 +28,10 @@
 #include <torch/csrc/autograd/custom_function.h>
 #include <torch/library.h>
 
+#include <map>
+#include <mutex>
 #include <tuple>
+#include <utility>
 #include <vector>
 
 #include "../../include/rmsnorm_gb300.h"
@@ -92,9 +95,27 @@ Tensor f32_vector(int64_t n, const Tensor &like) {
     return at::empty({n}, like.options().dtype(at::kFloat));
 }
 
+// The backward's workspace, kept per (device, stream) so that a call does
+// not allocate one each time (calls that share one are ordered on their
+// stream). A workspace replaced by a larger one stays allocated: a CUDA
+// graph captured on that stream may still use it. The map is never
+// destroyed, so no tensor outlives the CUDA context at process exit.
 Tensor workspace(size_t bytes, const Tensor &like) {
-    // the caching allocator's blocks are 512-byte aligned (the library wants 256)
-    return at::empty({(int64_t)bytes}, like.options().dtype(at::kByte));
+    struct Cache {
+        std::mutex mu;
+        std::map<std::pair<int, void *>, Tensor> live;
+        std::vector<Tensor> retired;
+    };
+    static Cache *cache = new Cache();
+    const std::pair<int, void *> key{like.get_device(), stream_of(like)};
+    std::lock_guard<std::mutex> lk(cache->mu);
+    Tensor &ws = cache->live[key];
+    if (!ws.defined() || (size_t)ws.numel() < bytes) {
+        if (ws.defined()) cache->retired.push_back(ws);
+        // the caching allocator's blocks are 512-byte aligned (the library wants 256)
+        ws = at::empty({(int64_t)bytes}, like.options().dtype(at::kByte));
+    }
+    return ws;
 }
 
 // ------------------------------------------------------------ raw calls
