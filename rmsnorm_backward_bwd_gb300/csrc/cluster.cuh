@@ -28,8 +28,11 @@ __device__ __forceinline__ uint32_t cluster_size_x() {
     return n;
 }
 // Every thread of every CTA of the cluster arrives; shared-memory writes
-// before it are visible to the cluster after it.
+// before it are visible to the cluster after it. The aligned cluster barrier
+// needs each warp converged when it gets there (see named_barrier_sync in
+// common.cuh): __syncwarp() first.
 __device__ __forceinline__ void cluster_sync_all() {
+    __syncwarp();
     asm volatile(
         "barrier.cluster.arrive.release.aligned;\n\t"
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");

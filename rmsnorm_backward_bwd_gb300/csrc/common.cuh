@@ -114,7 +114,17 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Named CTA barrier over `nthreads` threads (a multiple of 32). bar.sync is
+// the aligned form: every thread of a warp must execute it together, and
+// the PTX ISA leaves a diverged warp at an aligned barrier undefined. The
+// compiler cannot see that this inline asm needs a converged warp: code
+// such as `if (lane == 0) slot[w] = v;` just before it may be compiled as a
+// branch and leave the warp diverged here. On GB300 that stops the kernel
+// with "an illegal instruction was encountered". __syncwarp() is a
+// convergence point the compiler honours, so the whole warp reaches the
+// barrier together whatever the code before it compiled to.
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
