@@ -215,7 +215,8 @@ def workload_case(name):
              "fused_4096_nodres": synth.FUSED_4096_NODRES, "plain_16384x8192": synth.LARGE_PLAIN,
              "fused_16384x8192": synth.LARGE_FUSED, "layernorm_4096": synth.LN_4096,
              "layernorm_16384x8192": synth.LN_LARGE,
-             "plain_4096x32768": synth.LONG_ROWS, "plain_4096x4095": synth.UNALIGNED_ROWS}
+             "plain_4096x32768": synth.LONG_ROWS, "plain_4096x4095": synth.UNALIGNED_ROWS,
+             "plain_4096x12290": synth.UNALIGNED_WIDE_ROWS}
     return table[name]
 
 
@@ -622,6 +623,138 @@ def oracle_rate(case, seconds, nthreads=0):
     return nbytes * len(times) / sum(times) / 1e9, cores, len(times), sum(times)
 
 
+def oracle_sample_rate(case, kind, seconds, max_call_s=0.15):
+    """The fp64 CPU oracle (all host cores) on a bounded row sample of a
+    workload: the first rows of the case's inputs, as many as one call can
+    take in about max_call_s, called repeatedly for about `seconds`. Returns
+    (GB/s of the sample's algorithmic bytes, cores, rows, calls)."""
+    import numpy as np
+    import torch
+    import oracle
+    from rmsnorm_backward_bwd_gb300 import synth
+    inp = synth.make_inputs(case)
+    g = inp["gamma"].to(torch.float64).numpy()
+
+    def rows64(name, r):
+        return inp[name][:r].to(torch.float64).numpy() if name in inp else None
+
+    def prepare(r):
+        x = rows64("x", r)
+        if kind == "fwd":
+            return (x,)
+        dy = rows64("dy", r)
+        if case.fused:
+            _, a, rstd = oracle.fused_add_rmsnorm_fwd(x, rows64("residual", r), g,
+                                                      np.float32(case.eps), case.dtype)
+        else:
+            a = x
+            _, rstd = oracle.rmsnorm_fwd(x, g, np.float32(case.eps))
+        return a, dy, oracle.round_to(rstd, "f32"), rows64("dres", r)
+
+    def call(args):
+        if kind == "fwd":
+            oracle.rmsnorm_fwd(args[0], g, np.float32(case.eps))
+        elif case.fused:
+            oracle.fused_add_rmsnorm_bwd(args[0], g, args[1], args[2], args[3])
+        else:
+            oracle.rmsnorm_bwd(args[0], g, args[1], args[2])
+
+    probe = min(case.M, 64)
+    args = prepare(probe)
+    t = time.perf_counter()
+    call(args)
+    per_row = (time.perf_counter() - t) / probe
+    rows = int(min(case.M, max(1, max_call_s / max(per_row, 1e-9))))
+    args = prepare(rows)
+    call(args)
+    n, spent = 0, 0.0
+    t_end = time.time() + seconds
+    while True:
+        t = time.perf_counter()
+        call(args)
+        spent += time.perf_counter() - t
+        n += 1
+        if time.time() >= t_end:
+            break
+    if kind == "fwd":
+        s = synth.ELEM_BYTES[case.dtype]
+        nbytes = rows * case.N * s * 2 + case.N * s + 4 * rows
+    else:
+        nbytes = synth.algorithmic_bytes(rows, case.N, case.dtype, case.with_dres, True)
+    return nbytes * n / spent / 1e9, oracle.max_threads(), rows, n
+
+
+def workload_runs():
+    """The workloads of the benchmark table (besides the headline step): the
+    small f32 forward and backward, the edge shapes (plain and fused-add with
+    a residual gradient), fused-add 4096 x 4096 with and without it, and the
+    16384 x 8192 training shape, plain and fused."""
+    from rmsnorm_backward_bwd_gb300 import synth
+    runs = [(synth.SMALL_F32, "fwd"), (synth.SMALL_F32, "bwd")]
+    runs += [(c, "bwd") for c in synth.edge_cases()]
+    runs += [(synth.FUSED_4096, "bwd"), (synth.FUSED_4096_NODRES, "bwd"),
+             (synth.LARGE_PLAIN, "bwd"), (synth.LARGE_FUSED, "bwd")]
+    return runs
+
+
+class FwdProblem:
+    """Device-resident inputs/outputs of one RMSNorm forward, plus the call."""
+
+    def __init__(self, case, dev):
+        import torch
+        from rmsnorm_backward_bwd_gb300 import synth
+        self.case = case
+        inp = synth.make_inputs(case, device=str(dev))
+        self.x, self.g = inp["x"], inp["gamma"]
+        self.y = torch.empty_like(self.x)
+        self.rstd = torch.empty(case.M, dtype=torch.float32, device=dev)
+        s = synth.ELEM_BYTES[case.dtype]
+        self.bytes = case.M * case.N * s * 2 + case.N * s + 4 * case.M
+        torch.cuda.synchronize()
+
+    def call(self):
+        import rmsnorm_backward_bwd_gb300 as rn
+        rn.rmsnorm_fwd(self.x, self.g, self.case.eps, y=self.y, rstd=self.rstd)
+
+
+def time_workloads(dev, flush, peak, steps, warmup, ws, cpu_seconds, rank):
+    """Every workload run: device us per call (L2 flushed before each call,
+    CUDA events), algorithmic GB/s and % of peak, the row-pass kernel time
+    and the plan (backward), and the fp64 CPU oracle on the host cores beside
+    it (rank 0, single process only)."""
+    import numpy as np
+    import torch
+    from rmsnorm_backward_bwd_gb300 import native
+    rows = []
+    for case, kind in workload_runs():
+        prob = FwdProblem(case, dev) if kind == "fwd" else Problem(case, dev)
+        n = max(20, steps // 4)
+        cms, _, _ = time_calls(prob, n, warmup, flush, ws)
+        t = float(np.mean(cms))
+        row = {"workload": ("rmsnorm_fwd %s M=%d N=%d" % (case.dtype, case.M, case.N)
+                            if kind == "fwd" else case.name),
+               "kind": kind, "us_per_call": round(t * 1e3, 2),
+               "GBps": round(prob.bytes / (t * 1e-3) / 1e9, 1),
+               "pct_of_peak": round(100 * prob.bytes / (t * 1e-3) / 1e9 / peak, 1),
+               "algorithmic_bytes": prob.bytes}
+        if kind == "bwd":
+            _, kms, _ = time_calls(prob, n, 3, flush, ws, kernel_events=True)
+            k = float(np.mean(kms))
+            row["row_pass_us"] = round(k * 1e3, 2)
+            row["row_pass_GBps"] = round(prob.row_pass_bytes / (k * 1e-3) / 1e9, 1)
+        row["plan"] = native.last_plan()
+        if rank == 0 and ws == 1 and cpu_seconds > 0:
+            rate, cores, srows, calls = oracle_sample_rate(case, kind, cpu_seconds)
+            row["cpu_baseline"] = {
+                "value": round(rate, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "sample": "%d of %d rows, %d calls (fp64 C oracle, OpenMP)" % (
+                    srows, case.M, calls)}
+        rows.append(row)
+        del prob
+        torch.cuda.empty_cache()
+    return rows
+
+
 def run_reference(args):
     """The reference arm: the fp64 CPU oracle, timed as it stands."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -714,8 +847,7 @@ def run_ours(args):
 
     extra = []
     if not args.no_extra:
-        for name in ("fused_4096", "fused_4096_nodres", "plain_16384x8192", "fused_16384x8192",
-                     "plain_4096x32768", "plain_4096x4095"):
+        for name in ("plain_4096x32768", "plain_4096x4095", "plain_4096x12290"):
             if name == args.workload:
                 continue
             p2 = Problem(workload_case(name), dev)
@@ -748,6 +880,11 @@ def run_ours(args):
                           "plan": native.last_plan()})
             del p3
             torch.cuda.empty_cache()
+
+    workloads = []
+    if not args.no_extra:
+        workloads = time_workloads(dev, flush, peak, args.steps, args.warmup, ws,
+                                   0.0 if args.no_cpu else args.workload_cpu_seconds, rank)
 
     forward = []
     pages_table = []
@@ -818,6 +955,7 @@ def run_ours(args):
             "gpu_launches": launches_per_call(plan) * args.steps,
             "clocks": clocks,
             "plan": plan,
+            "workloads": workloads,
             "extra": extra,
             "autograd": autograd,
             "forward": forward,
@@ -837,10 +975,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="plain_4096",
                     choices=["plain_4096", "fused_4096", "fused_4096_nodres", "plain_16384x8192",
-                             "fused_16384x8192", "plain_4096x32768", "plain_4096x4095"])
+                             "fused_16384x8192", "plain_4096x32768", "plain_4096x4095",
+                             "plain_4096x12290"])
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload-cpu-seconds", type=float, default=1.0,
+                    help="oracle time per workload of the workload table")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
