@@ -291,8 +291,6 @@ class LnProblem:
 
 
 def launches_per_call(plan):
-    if "dw=grid" in plan:
-        return 1  # one cooperative row pass (partials, grid barrier, column sums, cast)
     if "dw=atomic" in plan:
         return 3  # zero, row pass, cast
     return 2      # row pass, finalize (+cast)

@@ -61,8 +61,7 @@ typedef enum rn_status {
                                 bad size, bad dtype code, bad option */
     RN_ERR_UNSUPPORTED = 2,  /* shape/alignment no engine handles (e.g. N too large) */
     RN_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
-    RN_ERR_WORKSPACE = 4,    /* workspace missing, misaligned or too small */
-    RN_ERR_TIMEOUT = 5       /* a kernel's bounded wait ran out (reported by rn_sync_status) */
+    RN_ERR_WORKSPACE = 4     /* workspace missing, misaligned or too small */
 } rn_status;
 
 /* Version of this ABI (increments on any incompatible change). */
@@ -103,14 +102,9 @@ rn_status rn_fused_add_rmsnorm_fwd(const void *x, const void *residual, const vo
  * Bytes of workspace the backward needs on the current device for an [M,N]
  * problem: a 256-byte header plus up to two fp32 rows of N per SM (the
  * per-CTA partials of the weight gradient). Needs a CUDA device; writes
- * *bytes. The workspace must be 256-byte aligned. Its partial rows are
- * scratch between calls and need no initialisation. The 256-byte header
- * belongs to the library: the grid weight-gradient mode keeps its barrier
- * counter there. The library zeroes the header itself the first time it
- * sees a workspace (a cudaMemsetAsync on the call's stream) and leaves it
- * valid after every call; the caller must not write it between calls. Calls
- * that share one workspace must be ordered on the GPU (one stream, or
- * events).
+ * *bytes. The workspace must be 256-byte aligned; its contents need no
+ * initialisation and are scratch between calls. Calls that share one
+ * workspace must be ordered on the GPU (one stream, or events).
  */
 rn_status rn_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes);
 
@@ -248,10 +242,8 @@ typedef enum rn_option {
                                  for aligned rows of more than 2048 16-byte chunks) */
     RN_OPT_DWEIGHT_MODE = 1,  /* 1 = scratch partials + finalize (deterministic dweight),
                                  2 = fp32 atomics + cast (summation order varies from call to
-                                 call), 3 = grid (row engine: one cooperative launch; partial
-                                 rows, a grid barrier bounded at 1 s, then fixed-order column
-                                 sums and the cast in the same kernel; deterministic). Other
-                                 engines take mode 2 when 3 is asked for. */
+                                 call). Automatic: scratch when a row tensor holds at most
+                                 2 MiB (fewer launches), else atomics where possible */
     RN_OPT_CHUNKS_PER_THREAD = 2, /* row engine: 16-byte chunks per thread per row: 1, 2, 4 */
     RN_OPT_TEAMS_PER_CTA = 3, /* row engine: rows processed at once per CTA (1..15) */
     RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8) */
@@ -262,11 +254,7 @@ typedef enum rn_option {
                                  kernel. A kernel that cannot take the problem (its row-size
                                  range, or tensors at different alignment phases) falls back
                                  to the next one the automatic choice would make. */
-    RN_OPT_GRID_SYNC_TEST = 8, /* test hook of the grid mode: v > 0 makes its barrier wait
-                                 for one arrival more than the grid has, with a v-millisecond
-                                 bound, so the wait runs out and the call reports
-                                 RN_ERR_TIMEOUT through rn_sync_status (dweight not written) */
-    RN_OPT_COUNT = 9
+    RN_OPT_COUNT = 8
 } rn_option;
 
 rn_status rn_set_option(int option, int value);
@@ -279,16 +267,6 @@ int rn_get_option(int option);
  * start with the operation ("rmsnorm_fwd", "fused_add_fwd", "layernorm_fwd").
  */
 const char *rn_last_plan(void);
-
-/*
- * Device status of bounded waits. Waits for all work on the current device
- * (cudaDeviceSynchronize), then returns RN_OK, or the status a kernel stored
- * when one of its bounded waits ran out (RN_ERR_TIMEOUT: the grid mode's
- * barrier; that call's dweight outputs were not written), and clears it.
- * After a reported error the library zeroes each workspace header again on
- * its next use. RN_ERR_CUDA if the device cannot be queried.
- */
-rn_status rn_sync_status(void);
 
 /*
  * Timing hook: while both are non-NULL, every backward call records

@@ -7,8 +7,6 @@
 // contract"):
 //   scratch mode: row pass (partials -> workspace) -> finalize (sum + cast)
 //   atomic mode:  zero dweight_f32 -> row pass (fp32 atomics) -> [cast]
-//   grid mode:    one cooperative row pass: partials -> grid barrier ->
-//                 column sums + cast (row engine only)
 // Kernels after the first are launched as programmatic dependents, so their
 // launch overlaps the tail of the kernel they wait for.
 #include <cuda_runtime.h>
@@ -20,7 +18,6 @@
 #include <mutex>
 #include <string>
 #include <unordered_map>
-#include <unordered_set>
 
 #include "../../include/rmsnorm_gb300.h"
 #include "common.cuh"
@@ -32,14 +29,6 @@ static thread_local char g_err[512] = "";
 static thread_local char g_plan[256] = "";
 static int g_opts[RN_OPT_COUNT] = {0};
 static cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
-
-// Device status word: a kernel whose bounded wait runs out stores its
-// rn_status here (first error wins); rn_sync_status reads and clears it. One
-// per device (the library's device image); the kernels get its address.
-static __device__ int g_dev_status;
-
-// Bound of the grid mode's barrier wait, and the shorter one of its test hook.
-constexpr unsigned long long kGridTimeoutNs = 1000000000ull;   // 1 s
 
 static rn_status fail(rn_status st, const char *fmt, ...) {
     va_list ap;
@@ -113,43 +102,6 @@ cudaError_t ensure_smem_attr(const void *func, size_t bytes) {
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_mu);
     g_smem_set[key] = cap;
-    return cudaSuccess;
-}
-
-// Address of g_dev_status on the current device (looked up once per device;
-// the device image stays loaded while the library is, so the address holds).
-static cudaError_t device_status_ptr(int dev, int **out) {
-    static std::unordered_map<int, int *> ptrs;
-    std::lock_guard<std::mutex> lk(g_mu);
-    auto it = ptrs.find(dev);
-    if (it != ptrs.end()) {
-        *out = it->second;
-        return cudaSuccess;
-    }
-    void *p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_dev_status);
-    if (e != cudaSuccess) return e;
-    ptrs[dev] = static_cast<int *>(p);
-    *out = static_cast<int *>(p);
-    return cudaSuccess;
-}
-
-// Workspaces whose header the library has zeroed (device, address). The grid
-// mode keeps its barrier counter there and leaves it zero after every call;
-// a workspace seen for the first time gets its header cleared on the call's
-// stream before the kernel.
-static std::unordered_set<unsigned long long> g_ws_ready;
-
-static cudaError_t prepare_ws_header(int dev, uint8_t *ws, cudaStream_t s) {
-    const unsigned long long key = ((unsigned long long)dev << 56) ^ (unsigned long long)ws;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (g_ws_ready.count(key)) return cudaSuccess;
-    }
-    cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeaderBytes, s);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(g_mu);
-    g_ws_ready.insert(key);
     return cudaSuccess;
 }
 
@@ -472,37 +424,24 @@ static void plan_generic(const BwdProblem &p, const DeviceInfo &d, bool atomic, 
     plan->atomic = false;
 }
 
-// Weight-gradient mode. Measured on GB300, fp32 vector atomics (zeroing and
-// cast overlapped by programmatic dependent launch) beat scratch partials +
-// a finalize kernel at every benchmarked shape (about 1.1-1.4 us per call at
-// 4096 x 4096), so they are the default where the engine can use them. The
-// scratch mode is deterministic (bitwise repeatable dweight) and is chosen
-// with RN_OPT_DWEIGHT_MODE = 1.
+// Weight-gradient mode. Measured on GB300 (L2 flushed, us per call, atomic
+// vs scratch): fp32 vector atomics (zeroing and cast overlapped by
+// programmatic dependent launch) win from a few MB up: bf16 4096 x 4096
+// 22.7 vs 23.3, fused +dres 27.1 vs 27.7, f32 512 x 3000 12.5 vs 12.6. On
+// the smallest problems the scratch mode's two launches (row pass, then a
+// finalize that sums the partial rows and casts) beat the atomic mode's
+// three: f16 128 x 4096 11.9 vs 10.4, bf16 512 x 2048 11.7 vs 10.7, f32
+// 128 x 1024 8.6 vs 8.4. So the automatic choice is scratch when a row
+// tensor holds at most 2 MiB, else atomics where dweight_f32 is 16-byte
+// aligned. RN_OPT_DWEIGHT_MODE = 1 / 2 forces scratch (deterministic,
+// bitwise repeatable) / atomics.
+constexpr int64_t kSmallProblemBytes = 2 << 20;
+
 static bool want_atomic(const BwdProblem &p) {
     const int m = g_opts[RN_OPT_DWEIGHT_MODE];
     if (m == 1) return false;
+    if (m == 0 && p.M * (int64_t)p.N * elem_bytes(p.dtype) <= kSmallProblemBytes) return false;
     return aligned16(p.dw_f32);
-}
-
-// Grid mode (RN_OPT_DWEIGHT_MODE = 3) for the row engine: cap the grid at the
-// CTAs that can be resident at once (the cooperative launch needs them all).
-static bool plan_grid_sync(const BwdProblem &p, const DeviceInfo &d, RowPlan *rp) {
-    if (g_opts[RN_OPT_DWEIGHT_MODE] != 3) return false;
-    rp->grid_sync = true;
-    int per_sm = 0;
-    if (row_grid_blocks_per_sm(p.dtype, p.dres != nullptr, *rp, &per_sm) != cudaSuccess) {
-        cudaGetLastError();
-        rp->grid_sync = false;
-        return false;
-    }
-    const int cap = per_sm * d.num_sms;
-    if (cap < 1) {
-        rp->grid_sync = false;
-        return false;
-    }
-    if (rp->grid > cap) rp->grid = cap;
-    rp->atomic = false;
-    return true;
 }
 
 // Outputs of the weight-gradient reduction: one or two length-N fp32 results
@@ -564,7 +503,7 @@ static void plan_string_row(const RowPlan &rp, const char *engine, bool atomic) 
     snprintf(g_plan, sizeof(g_plan),
              "engine=%s cpt=%d team_threads=%d teams=%d stages=%d grid=%d smem=%zu dw=%s",
              engine, rp.cpt, rp.team_threads, rp.teams, rp.stages, rp.grid, rp.smem,
-             rp.grid_sync ? "grid" : (atomic ? "atomic" : "scratch"));
+             atomic ? "atomic" : "scratch");
 }
 
 static void plan_string_generic(const GenericPlan &gp, const char *engine, bool atomic) {
@@ -645,26 +584,6 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
     if (!use_row && atomic && !gp.rows && !gp.cpb && !gp.phase) {
         gp.smem_dw = true;
         gp.smem = generic_smem_bytes(p.N, true);
-    }
-    if (use_row && plan_grid_sync(p, d, &rp)) {
-        // one cooperative launch: no zero, finalize or cast kernel
-        plan_string_row(rp, "row", false);
-        GridSync gs;
-        e = device_status_ptr(dev, &gs.status);
-        if (e != cudaSuccess) return cuda_fail(e, "device status lookup");
-        const int hook = g_opts[RN_OPT_GRID_SYNC_TEST];
-        gs.extra_arrivals = hook > 0 ? 1u : 0u;
-        gs.timeout_ns = hook > 0 ? (unsigned long long)hook * 1000000ull : kGridTimeoutNs;
-        e = prepare_ws_header(dev, p.ws, s);
-        if (e != cudaSuccess) return cuda_fail(e, "workspace header");
-        const bool prof = g_ev_begin && g_ev_end;
-        if (prof && (e = cudaEventRecord(g_ev_begin, s)) != cudaSuccess)
-            return cuda_fail(e, "profile event");
-        e = launch_bwd_row(p, rp, s, false, &gs);
-        if (e != cudaSuccess) return cuda_fail(e, "backward pass launch");
-        if (prof && (e = cudaEventRecord(g_ev_end, s)) != cudaSuccess)
-            return cuda_fail(e, "profile event");
-        return RN_OK;
     }
     if (use_row) plan_string_row(rp, "row", atomic);
     else plan_string_generic(gp, "generic", atomic);
@@ -1093,36 +1012,11 @@ const char *rn_status_string(int s) {
     case RN_ERR_UNSUPPORTED: return "unsupported shape or alignment";
     case RN_ERR_CUDA: return "CUDA error";
     case RN_ERR_WORKSPACE: return "bad workspace";
-    case RN_ERR_TIMEOUT: return "a bounded device wait ran out";
     default: return "unknown status";
     }
 }
 
 const char *rn_last_error(void) { return g_err; }
-
-rn_status rn_sync_status(void) {
-    g_err[0] = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-    int v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_dev_status, sizeof(v));
-    if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
-    if (v == RN_OK) return RN_OK;
-    const int zero = 0;
-    e = cudaMemcpyToSymbol(g_dev_status, &zero, sizeof(zero));
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the device status");
-    {
-        // a wait that ran out may have left a barrier counter mid-count: clear
-        // every workspace header of this device again on its next use
-        std::lock_guard<std::mutex> lk(g_mu);
-        for (auto it = g_ws_ready.begin(); it != g_ws_ready.end();)
-            it = (int)(*it >> 56) == dev ? g_ws_ready.erase(it) : std::next(it);
-    }
-    return fail((rn_status)v, "a kernel's bounded wait ran out on device %d", dev);
-}
 
 const char *rn_last_plan(void) { return g_plan; }
 

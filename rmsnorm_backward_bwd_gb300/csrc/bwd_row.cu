@@ -30,15 +30,6 @@
 //     one partial row to the workspace (deterministic; a finalize kernel sums
 //     the rows and casts) or adds it with fp32 vector atomics into a zeroed
 //     dweight_f32.
-//   * Grid mode (one launch for the whole backward, deterministic): the
-//     kernel is launched cooperatively, so all its CTAs are resident at
-//     once. Each CTA stores its partial row, then the CTAs meet at one grid
-//     barrier (an arrival counter and a generation word in the workspace
-//     header; the last arrival resets the counter, so every call leaves it
-//     zero); then CTA b sums the 16-byte columns b, b+G, ... of the G partial
-//     rows in a fixed order and writes dweight_f32 and its cast. The wait is
-//     bounded: after `timeout_ns` the CTA sets the device status word, skips
-//     its columns and returns.
 #include "common.cuh"
 #include "launch.h"
 #include "row_math.cuh"
@@ -64,14 +55,7 @@ struct RowArgs {
     const float *rstd;
     const uint8_t *dres;
     uint8_t *dx;
-    float *dw_out;   // scratch / grid: partial rows [gridDim.x][N]; atomic: dweight_f32
-    // grid mode only
-    float *dw_f32;          // the fp32 weight gradient
-    uint8_t *dw_cast;       // its cast to the I/O dtype (nullable)
-    unsigned int *bar;      // [0] arrival count (zero between calls), [1] generation
-    int *status;            // device status word (set on a timed-out wait)
-    unsigned long long timeout_ns;
-    unsigned int bar_expect;  // arrivals the barrier waits for (gridDim.x)
+    float *dw_out;   // scratch: partial rows [gridDim.x][N]; atomic: dweight_f32
     int64_t M;
     int N;
     int nchunks;
@@ -152,127 +136,6 @@ __device__ __forceinline__ void cta_partial_out(const f32x2 (&acc2)[CPT][RowMath
     }
 }
 
-// Grid barrier of the grid mode, run by one thread per CTA after the CTA's
-// stores and a fence. Count-and-generation: the thread reads the generation,
-// adds one arrival; the arrival that completes the count resets it to zero
-// and advances the generation; the others wait (bounded by timeout_ns) for
-// the generation to change. False on a timed-out wait (the status word is
-// set to RN_ERR_TIMEOUT, 5).
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Arrival half: returns the generation the caller must see advance.
-__device__ __forceinline__ unsigned int grid_arrive(unsigned int *bar, unsigned int expect) {
-    const unsigned int gen0 = ld_acquire_u32(bar + 1);
-    if (atomicAdd(bar, 1u) == expect - 1u) {
-        atomicExch(bar, 0u);
-        __threadfence();
-        atomicAdd(bar + 1, 1u);
-    }
-    return gen0;
-}
-// Waiting half (bounded).
-__device__ __forceinline__ bool grid_wait(const unsigned int *bar, unsigned int gen0,
-                                          unsigned long long timeout_ns, int *status) {
-    const unsigned long long t0 = global_ns();
-    while (ld_acquire_u32(bar + 1) == gen0) {
-        if (global_ns() - t0 > timeout_ns) {
-            atomicCAS(status, 0, 5);
-            return false;
-        }
-        __nanosleep(64);
-    }
-    __threadfence();
-    return true;
-}
-__device__ __forceinline__ bool grid_barrier(unsigned int *bar, unsigned int expect,
-                                             unsigned long long timeout_ns, int *status) {
-    return grid_wait(bar, grid_arrive(bar, expect), timeout_ns, status);
-}
-
-__device__ __forceinline__ void add4(float4 &a, const float4 &b) {
-    a.x += b.x;
-    a.y += b.y;
-    a.z += b.z;
-    a.w += b.w;
-}
-
-// The grid mode's end: every CTA has stored its partial row (dw_out row
-// blockIdx.x). After the barrier, CTA b owns the F = ceil(N/4 / G) 16-byte
-// columns [b*F, b*F + F) (fewer for the last CTAs), taken P = min(F,
-// blockDim) at a time. Thread t takes column t % P of the pass and the rows
-// t/P, t/P + R, ... (R = blockDim/P row groups), loaded with coalesced
-// 16-byte reads from L2; the R group sums of a column go through shared
-// memory (`sbuf`, blockDim float4s) and one warp per column adds them (lane
-// l takes groups l, l+32, ..., then a fixed xor butterfly). Every order is
-// fixed: the result is bitwise repeatable. `flag` is a shared int.
-template <typename T>
-__device__ __forceinline__ void grid_finish(const RowArgs &a, volatile int *flag, float4 *sbuf) {
-    __syncthreads();  // every thread's partial-row stores are issued
-    if (threadIdx.x == 0) {
-        __threadfence();
-        *flag = grid_barrier(a.bar, a.bar_expect, a.timeout_ns, a.status) ? 1 : 0;
-    }
-    __syncthreads();
-    if (!*flag) return;
-    const int G = gridDim.x;
-    const int nf4 = a.N >> 2;
-    const int F = (nf4 + G - 1) / G;
-    const int f0 = blockIdx.x * F;
-    const int nf = nf4 - f0 < F ? nf4 - f0 : F;
-    if (nf <= 0) return;
-    const int T_ = blockDim.x;
-    const int P = F < T_ ? F : T_;
-    const int R = T_ / P;
-    const int t = threadIdx.x, q = t % P, grp = t / P;
-    const int warp = t >> 5, lane = t & 31, nwarps = T_ >> 5;
-    const float4 *part = reinterpret_cast<const float4 *>(a.dw_out);
-    T *cast = reinterpret_cast<T *>(a.dw_cast);
-    for (int c0 = 0; c0 < nf; c0 += P) {
-        const int np = nf - c0 < P ? nf - c0 : P;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (grp < R && q < np) {
-#pragma unroll 4
-            for (int r = grp; r < G; r += R)
-                add4(acc, __ldcg(part + (size_t)r * nf4 + f0 + c0 + q));
-        }
-        if (grp < R) sbuf[grp * P + q] = acc;
-        __syncthreads();
-        for (int c = warp; c < np; c += nwarps) {
-            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int g = lane; g < R; g += 32) add4(s, sbuf[g * P + c]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                s.x += __shfl_xor_sync(0xFFFFFFFFu, s.x, o);
-                s.y += __shfl_xor_sync(0xFFFFFFFFu, s.y, o);
-                s.z += __shfl_xor_sync(0xFFFFFFFFu, s.z, o);
-                s.w += __shfl_xor_sync(0xFFFFFFFFu, s.w, o);
-            }
-            if (lane == 0) {
-                const size_t col = 4 * (size_t)(f0 + c0 + c);
-                a.dw_f32[col] = s.x;
-                a.dw_f32[col + 1] = s.y;
-                a.dw_f32[col + 2] = s.z;
-                a.dw_f32[col + 3] = s.w;
-                if (cast) {
-                    cast[col] = from_f<T>(s.x);
-                    cast[col + 1] = from_f<T>(s.y);
-                    cast[col + 2] = from_f<T>(s.z);
-                    cast[col + 3] = from_f<T>(s.w);
-                }
-            }
-        }
-        __syncthreads();  // sbuf is reused by the next pass
-    }
-}
-
 // Sum of one value per thread over a team of team_warps warps: warp
 // shuffles, then the warps' sums through shared memory (double-buffered by
 // `parity`) and one named barrier, then a second shuffle; every thread of
@@ -289,9 +152,7 @@ __device__ __forceinline__ float team_sum(float v, float *red, int parity, int t
     return warp_sum(w);
 }
 
-// DWM: weight-gradient mode, 0 scratch partial rows, 1 fp32 atomics into a
-// dweight_f32 zeroed by the kernel before, 2 grid.
-template <typename T, int CPT, bool HAS_DRES, int DWM>
+template <typename T, int CPT, bool HAS_DRES, bool ATOMIC>
 __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
     bwd_row_kernel(const RowArgs a) {
     constexpr int V = Traits<T>::kVec;
@@ -422,15 +283,13 @@ __global__ void __launch_bounds__(RowBounds<CPT>::kMaxThreads, 1)
 
     pdl_launch_dependents();
     __syncthreads();  // every team is done with its ring (all real copies waited for)
-    cta_partial_out<T, CPT, DWM == 1>(acc2, a, ring, team, tt);
-    if (DWM == 2) grid_finish<T>(a, reinterpret_cast<volatile int *>(red),
-                                 reinterpret_cast<float4 *>(ring));
+    cta_partial_out<T, CPT, ATOMIC>(acc2, a, ring, team, tt);
 }
 
-template <typename T, int CPT, bool HAS_DRES, int DWM>
+template <typename T, int CPT, bool HAS_DRES, bool ATOMIC>
 static cudaError_t launch_row_t(const RowArgs &args, const RowPlan &plan, cudaStream_t s,
                                 bool pdl) {
-    auto kern = bwd_row_kernel<T, CPT, HAS_DRES, DWM>;
+    auto kern = bwd_row_kernel<T, CPT, HAS_DRES, ATOMIC>;
     cudaError_t e = ensure_smem_attr((const void *)kern, plan.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -439,32 +298,21 @@ static cudaError_t launch_row_t(const RowArgs &args, const RowPlan &plan, cudaSt
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    if (DWM == 2) {
-        // the grid barrier needs every CTA resident at once
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-    } else {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-    }
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = (DWM == 2 || pdl) ? 1 : 0;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, args);
-}
-
-template <typename T, int CPT, bool HAS_DRES>
-static cudaError_t launch_row_mode(const RowArgs &args, const RowPlan &plan, cudaStream_t s,
-                                   bool pdl) {
-    if (plan.grid_sync) return launch_row_t<T, CPT, HAS_DRES, 2>(args, plan, s, false);
-    return plan.atomic ? launch_row_t<T, CPT, HAS_DRES, 1>(args, plan, s, pdl)
-                       : launch_row_t<T, CPT, HAS_DRES, 0>(args, plan, s, pdl);
 }
 
 template <typename T, int CPT>
 static cudaError_t launch_row_cpt(const RowArgs &args, const RowPlan &plan, bool has_dres,
                                   cudaStream_t s, bool pdl) {
-    return has_dres ? launch_row_mode<T, CPT, true>(args, plan, s, pdl)
-                    : launch_row_mode<T, CPT, false>(args, plan, s, pdl);
+    if (has_dres)
+        return plan.atomic ? launch_row_t<T, CPT, true, true>(args, plan, s, pdl)
+                           : launch_row_t<T, CPT, true, false>(args, plan, s, pdl);
+    return plan.atomic ? launch_row_t<T, CPT, false, true>(args, plan, s, pdl)
+                       : launch_row_t<T, CPT, false, false>(args, plan, s, pdl);
 }
 
 template <typename T>
@@ -478,40 +326,8 @@ static cudaError_t launch_row_dt(const RowArgs &args, const RowPlan &plan, bool 
     }
 }
 
-// Resident CTAs per SM of the kernel instance a plan launches (for the grid
-// mode's cooperative launch), from the occupancy calculator.
-template <typename T, int CPT>
-static cudaError_t row_occupancy_cpt(const RowPlan &plan, bool has_dres, int *blocks) {
-    const void *k = has_dres ? (const void *)bwd_row_kernel<T, CPT, true, 2>
-                             : (const void *)bwd_row_kernel<T, CPT, false, 2>;
-    cudaError_t e = ensure_smem_attr(k, plan.smem);
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, k,
-                                                         plan.teams * plan.team_threads,
-                                                         plan.smem);
-}
-
-template <typename T>
-static cudaError_t row_occupancy_dt(const RowPlan &plan, bool has_dres, int *blocks) {
-    switch (plan.cpt) {
-    case 1: return row_occupancy_cpt<T, 1>(plan, has_dres, blocks);
-    case 2: return row_occupancy_cpt<T, 2>(plan, has_dres, blocks);
-    case 4: return row_occupancy_cpt<T, 4>(plan, has_dres, blocks);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
-cudaError_t row_grid_blocks_per_sm(int dtype, bool has_dres, const RowPlan &plan, int *blocks) {
-    switch (dtype) {
-    case kF32: return row_occupancy_dt<float>(plan, has_dres, blocks);
-    case kF16: return row_occupancy_dt<__half>(plan, has_dres, blocks);
-    case kBF16: return row_occupancy_dt<__nv_bfloat16>(plan, has_dres, blocks);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
 cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_t s,
-                           bool pdl_after_zero, const GridSync *gs) {
+                           bool pdl_after_zero) {
     RowArgs a;
     const int eb = elem_bytes(p.dtype);
     a.x = static_cast<const uint8_t *>(p.x);
@@ -520,15 +336,7 @@ cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_
     a.rstd = p.rstd;
     a.dres = static_cast<const uint8_t *>(p.dres);
     a.dx = static_cast<uint8_t *>(p.dx);
-    a.dw_out = plan.atomic && !plan.grid_sync ? p.dw_f32
-                                              : reinterpret_cast<float *>(p.ws + kWsHeaderBytes);
-    a.dw_f32 = p.dw_f32;
-    a.dw_cast = static_cast<uint8_t *>(p.dw_cast);
-    a.bar = reinterpret_cast<unsigned int *>(p.ws);
-    a.status = gs ? gs->status : nullptr;
-    a.timeout_ns = gs ? gs->timeout_ns : 0;
-    a.bar_expect = (unsigned int)plan.grid + (gs ? gs->extra_arrivals : 0u);
-    if (plan.grid_sync && (!gs || !gs->status)) return cudaErrorInvalidValue;
+    a.dw_out = plan.atomic ? p.dw_f32 : reinterpret_cast<float *>(p.ws + kWsHeaderBytes);
     a.M = p.M;
     a.N = p.N;
     a.row_bytes = p.N * eb;

@@ -37,14 +37,6 @@ struct RowPlan {
     int grid;          // CTAs (persistent)
     size_t smem;       // dynamic shared memory bytes
     bool atomic;       // weight gradient via fp32 atomics (else scratch partials)
-    bool grid_sync = false;  // one cooperative launch: partial rows, grid barrier, column sums
-};
-
-// Device-side state the grid mode's barrier uses besides the workspace header.
-struct GridSync {
-    int *status;                     // device status word (RN_ERR_TIMEOUT on a timed-out wait)
-    unsigned long long timeout_ns;   // bound of the barrier wait
-    unsigned int extra_arrivals;     // test hook: arrivals the barrier waits for beyond the grid
 };
 
 // Launch shape of the cluster engine (rows longer than one CTA's tile).
@@ -78,9 +70,7 @@ size_t generic_smem_bytes(int N, bool smem_dw);
 size_t generic_vec_smem_bytes(int N);
 
 cudaError_t launch_bwd_row(const BwdProblem &p, const RowPlan &plan, cudaStream_t s,
-                           bool pdl_after_zero, const GridSync *gs = nullptr);
-// Resident CTAs per SM of the row kernel instance the grid mode would launch.
-cudaError_t row_grid_blocks_per_sm(int dtype, bool has_dres, const RowPlan &plan, int *blocks);
+                           bool pdl_after_zero);
 cudaError_t launch_bwd_generic(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
                                bool pdl_after_zero);
 // Rows that are not 16-byte multiples, all row tensors at one alignment phase.

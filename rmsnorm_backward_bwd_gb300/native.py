@@ -14,11 +14,11 @@ LIB_PATH = os.path.join(HERE, "_build", "librn_gb300.so")
 TORCH_LIB_PATH = os.path.join(HERE, "_build", "librn_torch.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "rmsnorm_gb300.h")
 
-RN_OK, RN_ERR_INVALID_ARG, RN_ERR_UNSUPPORTED, RN_ERR_CUDA, RN_ERR_WORKSPACE, RN_ERR_TIMEOUT = range(6)
+RN_OK, RN_ERR_INVALID_ARG, RN_ERR_UNSUPPORTED, RN_ERR_CUDA, RN_ERR_WORKSPACE = range(5)
 RN_F32, RN_F16, RN_BF16 = 0, 1, 2
 (OPT_BWD_ENGINE, OPT_DWEIGHT_MODE, OPT_CHUNKS_PER_THREAD, OPT_TEAMS_PER_CTA, OPT_STAGES, OPT_GRID,
- OPT_CLUSTER_SIZE, OPT_GENERIC_KERNEL, OPT_GRID_SYNC_TEST) = range(9)
-OPT_COUNT = 9
+ OPT_CLUSTER_SIZE, OPT_GENERIC_KERNEL) = range(8)
+OPT_COUNT = 8
 
 _lib = None
 
@@ -64,18 +64,16 @@ def _bind(lib):
     lib.rn_get_option.argtypes = [ci]
     lib.rn_set_profile_events.restype = ci
     lib.rn_set_profile_events.argtypes = [vp, vp]
-    lib.rn_sync_status.restype = ci
-    lib.rn_sync_status.argtypes = []
     return lib
 
 
 # Process-wide overrides read from the environment when the library loads:
 #   RN_BWD_ENGINE   = auto | row | generic | cluster
-#   RN_DWEIGHT_MODE = auto | scratch (deterministic) | atomic | grid (deterministic)
+#   RN_DWEIGHT_MODE = auto | scratch (deterministic) | atomic
 #   RN_GENERIC_KERNEL = auto | phase | vec | realign | scalar (unaligned rows)
 ENV_OPTIONS = {
     "RN_BWD_ENGINE": (0, {"auto": 0, "row": 1, "generic": 2, "cluster": 3}),
-    "RN_DWEIGHT_MODE": (1, {"auto": 0, "scratch": 1, "atomic": 2, "grid": 3}),
+    "RN_DWEIGHT_MODE": (1, {"auto": 0, "scratch": 1, "atomic": 2}),
     "RN_GENERIC_KERNEL": (7, {"auto": 0, "phase": 1, "vec": 2, "realign": 3, "scalar": 4}),
 }
 
@@ -142,12 +140,6 @@ def header_functions():
 
 def last_plan():
     return lib().rn_last_plan().decode()
-
-
-def sync_status():
-    """Wait for the current device, then return the status a kernel stored
-    when one of its bounded waits ran out (RN_OK if none), and clear it."""
-    return int(lib().rn_sync_status())
 
 
 def set_option(opt, value):

@@ -95,6 +95,33 @@ def test_row_engine_tile_shapes(cpt, teams, stages):
     assert "cpt=%d" % cpt in plan and "teams=%d" % teams in plan and "stages=%d" % stages in plan
 
 
+@pytest.mark.parametrize("M", [7, 513, 4096])
+def test_row_engine_warp_per_row(M):
+    """One warp per row: bf16 N = 1024 is 128 chunks, 4 chunks per thread of a
+    32-thread team (measured against the default team shapes: not faster)."""
+    native.set_option(native.OPT_BWD_ENGINE, 1)
+    native.set_option(native.OPT_CHUNKS_PER_THREAD, 4)
+    native.set_option(native.OPT_TEAMS_PER_CTA, 12)
+    ex = parity.expected_bwd(Case("bf16 M=%d N=1024 fused" % M, M, 1024, "bf16", fused=True,
+                                  with_dres=True))
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    assert "team_threads=32 " in plan and "cpt=4" in plan, plan
+    assert parity.check_bwd(ex, dx, dw, dw32) == 0
+
+
+def test_auto_weight_gradient_mode_by_size():
+    """Automatic mode: scratch partials for small problems, atomics for large."""
+    ex = parity.expected_bwd(Case("f16 M=128 N=4096", 128, 4096, "f16"))
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    assert "dw=scratch" in native.last_plan()
+    parity.check_bwd(ex, dx, dw, dw32)
+    ex = parity.expected_bwd(Case("bf16 M=1024 N=4096", 1024, 4096, "bf16"))
+    dx, dw, dw32 = parity.run_gpu_bwd(ex)
+    assert "dw=atomic" in native.last_plan()
+    parity.check_bwd(ex, dx, dw, dw32)
+
+
 @pytest.mark.parametrize("grid", [1, 3, 152])
 def test_row_engine_grid_caps(grid):
     native.set_option(native.OPT_GRID, grid)
@@ -183,91 +210,16 @@ def test_misaligned_pointers_take_generic_path():
     parity.check_bwd(ex, dx, dw, dw32)
 
 
-@pytest.mark.parametrize("mode", [1, 3])
-def test_workspace_contents_do_not_matter(mode):
-    """The workspace's partial rows are scratch: garbage left in them changes
-    nothing (the 256-byte header belongs to the library and is left alone)."""
+def test_workspace_contents_do_not_matter():
+    """The workspace is scratch: garbage left in it changes nothing."""
     import rmsnorm_backward_bwd_gb300 as rn
-    native.set_option(native.OPT_DWEIGHT_MODE, mode)  # the modes that use the workspace
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)  # the mode that uses the workspace
     ex = parity.expected_bwd(Case("bf16 M=512 N=4096", 512, 4096, "bf16"))
     a = parity.run_gpu_bwd(ex)
     ws = rn.bwd_workspace(512, 4096, torch.bfloat16, "cuda")
-    ws[256:].fill_(0x7F)
+    ws.fill_(0x7F)
     b = parity.run_gpu_bwd(ex)
-    assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2]) and torch.equal(a[1], b[1])
-
-
-GRID_CASES = [synth.PLAIN_4096, synth.FUSED_4096, synth.FUSED_4096_NODRES, synth.SMALL_F32,
-              Case("f16 M=128 N=4096 fused", 128, 4096, "f16", fused=True, with_dres=True),
-              Case("bf16 M=1 N=4096", 1, 4096, "bf16"),
-              Case("bf16 M=7 N=2048", 7, 2048, "bf16"),
-              Case("f32 M=300 N=8", 300, 8, "f32"),
-              Case("bf16 M=999 N=16384", 999, 16384, "bf16"),
-              Case("f32 M=5000 N=1020", 5000, 1020, "f32")]
-
-
-COOP_MODES = {3: "dw=grid"}
-
-
-@pytest.mark.parametrize("mode", [3], ids=["grid"])
-@pytest.mark.parametrize("case", GRID_CASES, ids=lambda c: c.name)
-def test_cooperative_modes_match_oracle(case, mode):
-    """The row engine's cooperative launch, the grid mode: partial rows, a grid
-    barrier, fixed-order column sums and the cast in one kernel."""
-    native.set_option(native.OPT_DWEIGHT_MODE, mode)
-    ex = parity.expected_bwd(case)
-    dx, dw, dw32 = parity.run_gpu_bwd(ex)
-    plan = native.last_plan()
-    assert "engine=row" in plan and COOP_MODES[mode] in plan, plan
-    assert parity.check_bwd(ex, dx, dw, dw32, tag=" [%s]" % plan) == 0
-    assert native.sync_status() == native.RN_OK
-
-
-def test_grid_mode_is_bitwise_repeatable():
-    native.set_option(native.OPT_DWEIGHT_MODE, 3)
-    ex = parity.expected_bwd(Case("bf16 M=4096 N=4096", 4096, 4096, "bf16"))
-    runs = [parity.run_gpu_bwd(ex) for _ in range(3)]
-    for r in runs[1:]:
-        for u, v in zip(runs[0], r):
-            assert torch.equal(u, v)
-
-
-@pytest.mark.parametrize("mode", [3], ids=["grid"])
-@pytest.mark.parametrize("grid", [1, 5, 152])
-def test_cooperative_modes_grid_sizes(grid, mode):
-    """Fewer CTAs than SMs (the barrier counts the launched grid)."""
-    native.set_option(native.OPT_DWEIGHT_MODE, mode)
-    native.set_option(native.OPT_GRID, grid)
-    ex = parity.expected_bwd(Case("bf16 M=600 N=4096 fused", 600, 4096, "bf16", fused=True,
-                                  with_dres=True))
-    dx, dw, dw32 = parity.run_gpu_bwd(ex)
-    plan = native.last_plan()
-    launched = int(plan.split("grid=")[1].split()[0])
-    assert COOP_MODES[mode] in plan and launched <= grid, plan
-    assert parity.check_bwd(ex, dx, dw, dw32) == 0
-
-
-@pytest.mark.parametrize("mode", [3], ids=["grid"])
-def test_cooperative_wait_that_runs_out_is_reported(mode):
-    """The barrier's bounded wait: with the test hook the barrier waits for
-    one arrival more than the grid has, gives up after 20 ms, and the call
-    reports RN_ERR_TIMEOUT through rn_sync_status; the next call (header
-    cleared again by the library) is correct."""
-    import rmsnorm_backward_bwd_gb300 as rn
-    native.set_option(native.OPT_DWEIGHT_MODE, mode)
-    ex = parity.expected_bwd(Case("bf16 M=256 N=4096", 256, 4096, "bf16"))
-    x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
-    assert native.sync_status() == native.RN_OK
-    native.set_option(native.OPT_GRID_SYNC_TEST, 20)
-    dw32 = torch.full((4096,), 7.0, device="cuda")
-    rn.rmsnorm_bwd(x, g, dy, rstd, dweight_f32=dw32)
-    assert native.sync_status() == native.RN_ERR_TIMEOUT
-    assert native.sync_status() == native.RN_OK        # read once, then cleared
-    assert torch.all(dw32 == 7.0)                       # the timed-out call wrote no dweight
-    native.set_option(native.OPT_GRID_SYNC_TEST, 0)
-    dx, dw, dw32 = parity.run_gpu_bwd(ex)
-    assert native.sync_status() == native.RN_OK
-    assert parity.check_bwd(ex, dx, dw, dw32) == 0
+    assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2])
 
 
 def test_invariant_holds_at_full_size():
