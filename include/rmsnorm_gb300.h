@@ -245,7 +245,9 @@ typedef enum rn_option {
                                  call). Automatic: scratch when a row tensor holds at most
                                  2 MiB (fewer launches), else atomics where possible */
     RN_OPT_CHUNKS_PER_THREAD = 2, /* row engine: 16-byte chunks per thread per row: 1, 2, 4 */
-    RN_OPT_TEAMS_PER_CTA = 3, /* row engine: rows processed at once per CTA (1..15) */
+    RN_OPT_TEAMS_PER_CTA = 3, /* row engine: rows processed at once per CTA (1..15);
+                                 RMSNorm backward phase-class kernel: rows per CTA
+                                 iteration (1 or 2) */
     RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8) */
     RN_OPT_GRID = 5,          /* CTAs of the row pass (default: one per SM; at most 2 per SM) */
     RN_OPT_CLUSTER_SIZE = 6,  /* cluster engine: CTAs per cluster, 2, 4, 8 or 16 */

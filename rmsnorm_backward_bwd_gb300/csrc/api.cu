@@ -383,8 +383,12 @@ static bool plan_phase(const BwdProblem &p, const DeviceInfo &d, bool atomic, Ge
     if (!generic_vec_ok(p, d)) return false;
     int cpt, threads;
     if (!phase_shape(p.N, p.dtype, &cpt, &threads)) return false;
-    const int per_sm = phase_blocks_per_sm(p.dtype, p.dres != nullptr, atomic, cpt, threads);
+    // rows per CTA iteration: RN_OPT_TEAMS_PER_CTA = 1 or 2 forces it
+    int rows = g_opts[RN_OPT_TEAMS_PER_CTA];
+    if (rows != 1 && rows != 2) rows = 2;
+    const int per_sm = phase_blocks_per_sm(p.dtype, p.dres != nullptr, atomic, cpt, rows, threads);
     plan->phase = cpt;
+    plan->phase_rows = rows;
     plan->grid = phase_grid(p.M, phase_period(p.N, p.dtype), per_sm, d);
     plan->cpb = 0;
     plan->rows = 0;
@@ -508,8 +512,9 @@ static void plan_string_row(const RowPlan &rp, const char *engine, bool atomic) 
 
 static void plan_string_generic(const GenericPlan &gp, const char *engine, bool atomic) {
     if (gp.phase)
-        snprintf(g_plan, sizeof(g_plan), "engine=%s phase cpt=%d threads=%d grid=%d dw=%s",
-                 engine, gp.phase, gp.threads, gp.grid, atomic ? "atomic" : "scratch");
+        snprintf(g_plan, sizeof(g_plan), "engine=%s phase cpt=%d rows=%d threads=%d grid=%d dw=%s",
+                 engine, gp.phase, gp.phase_rows, gp.threads, gp.grid,
+                 atomic ? "atomic" : "scratch");
     else if (gp.cpb)
         snprintf(g_plan, sizeof(g_plan), "engine=%s realign cpb=%d rows=%d threads=%d grid=%d dw=%s",
                  engine, gp.cpb, gp.rows, gp.threads, gp.grid, atomic ? "atomic" : "scratch");

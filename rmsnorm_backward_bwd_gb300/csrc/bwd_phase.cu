@@ -15,8 +15,9 @@
 // contrast, lets any CTA take any row, so a column's owner changes with the
 // row's phase and gamma and the partial live in shared memory.
 #include "common.cuh"
-#include "unaligned.cuh"
 #include "launch.h"
+#include "row_math.cuh"
+#include "unaligned.cuh"
 
 namespace rn {
 
@@ -46,10 +47,13 @@ int phase_period(int N, int dtype) {
     return 16 / g;
 }
 
-template <typename T, bool HAS_DRES, bool ATOMIC, int J>
+template <typename T, bool HAS_DRES, bool ATOMIC, int J, int R>
 __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
     constexpr int S = sizeof(T), V = 16 / S;
-    __shared__ float red[2][16];  // warp sums, alternating between rows
+    constexpr int P2 = RowMath<T>::kPairs;  // fp32 pairs per chunk
+    // gamma also as fp32 pairs when the math needs it or when that fits
+    constexpr bool kGammaF = RowMath<T>::kNeedsGammaF || J * V <= 8;
+    __shared__ float red[2][R][16];  // warp sums of the R rows, alternating between iterations
     const T *x = static_cast<const T *>(a.x);
     const T *g = static_cast<const T *>(a.gamma);
     const T *dy = static_cast<const T *>(a.dy);
@@ -61,6 +65,9 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
     const int cls = (int)(blockIdx.x % (unsigned)P);
     const int64_t rank = blockIdx.x / (unsigned)P;
     const int64_t nper = ((int64_t)gridDim.x - cls + P - 1) / P;  // CTAs of this class
+    // this CTA's rows: row0, row0 + rstride, ...; R of them per iteration
+    const int64_t rstride = nper * P;
+    const int64_t row0 = cls + rank * P;
 
     // the class's split (address arithmetic on row cls; nothing is read there)
     const uintptr_t start = reinterpret_cast<uintptr_t>(a.x) + (uintptr_t)cls * (uintptr_t)N * S;
@@ -72,15 +79,23 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
     bool own[J];
     int col[J];
     uint4 gv[J];
-    float dwp[J][V];
+    f32x2 g2[kGammaF ? J : 1][kGammaF ? P2 : 1];
+    f32x2 acc2[J][P2];
 #pragma unroll
     for (int k = 0; k < J; ++k) {
         const int i = tid + k * nthr;
         own[k] = i < nv;
         col[k] = h + i * V;
         gv[k] = own[k] ? gather_chunk<T>(g + col[k]) : make_uint4(0, 0, 0, 0);
+        if (kGammaF) {
+            float gf[V];
+            chunk_to_float<T>(gv[k], gf);
 #pragma unroll
-        for (int e = 0; e < V; ++e) dwp[k][e] = 0.f;
+            for (int q = 0; q < P2; ++q)
+                g2[kGammaF ? k : 0][kGammaF ? q : 0] = f2_make(gf[2 * q], gf[2 * q + 1]);
+        }
+#pragma unroll
+        for (int q = 0; q < P2; ++q) acc2[k][q] = f2_make(0.f, 0.f);
     }
     const bool e_own = tid < h + tail;
     const int je = tid < h ? tid : h + nv * V + (tid - h);
@@ -102,88 +117,106 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
         }
     };
 
-    uint4 xc[J], dc[J];
+    uint4 xc[R][J], dc[R][J];
+    float xec[R], dec[R];
 #pragma unroll
-    for (int k = 0; k < J; ++k) xc[k] = dc[k] = make_uint4(0, 0, 0, 0);
-    float xec = 0.f, dec = 0.f;
-    int64_t row = cls + rank * P;
-    if (row < a.M) load(row, xc, dc, xec, dec);
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int k = 0; k < J; ++k) xc[r][k] = dc[r][k] = make_uint4(0, 0, 0, 0);
+        xec[r] = dec[r] = 0.f;
+        const int64_t row = row0 + r * rstride;
+        if (row < a.M) load(row, xc[r], dc[r], xec[r], dec[r]);
+    }
     int buf = 0;
-    while (row < a.M) {
-        const int64_t nrow = row + nper * P;
-        uint4 xn[J], dn[J];
+    for (int64_t rb = row0; rb < a.M; rb += R * rstride) {
+        // the next iteration's rows, in flight while these are computed
+        uint4 xn[R][J], dn[R][J];
+        float xen[R], den[R];
 #pragma unroll
-        for (int k = 0; k < J; ++k) xn[k] = dn[k] = make_uint4(0, 0, 0, 0);
-        float xen = 0.f, den = 0.f;
-        if (nrow < a.M) load(nrow, xn, dn, xen, den);
-        const size_t base = (size_t)row * N;
-        uint4 rv[J];
-        float re = 0.f;
-        if (HAS_DRES) {
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+            for (int k = 0; k < J; ++k) xn[r][k] = dn[r][k] = make_uint4(0, 0, 0, 0);
+            xen[r] = den[r] = 0.f;
+            const int64_t nrow = rb + (R + r) * rstride;
+            if (nrow < a.M) load(nrow, xn[r], dn[r], xen[r], den[r]);
+        }
+
+        // dresidual_out (a plain load: dx may overwrite it) and rstd of these rows
+        uint4 rv[HAS_DRES ? R : 1][J];
+        float re[R], rs[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t row = rb + r * rstride;
+            const bool live = row < a.M;
+            const size_t base = (size_t)row * N;
+            re[r] = 0.f;
+            if (HAS_DRES) {
+#pragma unroll
+                for (int k = 0; k < J; ++k)
+                    rv[HAS_DRES ? r : 0][k] =
+                        own[k] && live ? *reinterpret_cast<const uint4 *>(dres + base + col[k])
+                                       : make_uint4(0, 0, 0, 0);
+                if (e_own && live) re[r] = to_f(dres[base + je]);
+            }
+            rs[r] = live ? __ldg(a.rstd + row) : 0.f;
+        }
+
+        // pass 1: sum_j x_j*dy_j*gamma_j of each row (a row past M sums zeros)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            f32x2 part2 = f2_make(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < J; ++k)
-                rv[k] = own[k] ? *reinterpret_cast<const uint4 *>(dres + base + col[k])
-                               : make_uint4(0, 0, 0, 0);  // a plain load: dx may overwrite dres
-            if (e_own) re = to_f(dres[base + je]);
+                if (own[k])
+                    part2 = RowMath<T>::pass1(xc[r][k], dc[r][k], gv[k],
+                                              kGammaF ? g2[kGammaF ? k : 0] : nullptr, part2);
+            float lo, hi;
+            f2_split(part2, lo, hi);
+            float s = lo + hi;
+            if (e_own) s = fmaf(xec[r] * dec[r], ge, s);
+            s = warp_sum(s);
+            if (lane == 0) red[buf][r][warp] = s;
         }
-        const float rs = __ldg(a.rstd + row);
+        __syncthreads();  // also orders the reads of red[buf] two iterations back before these writes
 
-        // pass 1: sum_j x_j*dy_j*gamma_j
-        float s = 0.f;
+        // pass 2: dx = wdy*rstd + x*b with b = -rstd^2*c1 (+ dres); partial += dy*x_hat
 #pragma unroll
-        for (int k = 0; k < J; ++k) {
-            if (own[k]) {
-                float xf[V], df[V], gf[V];
-                chunk_to_float<T>(xc[k], xf);
-                chunk_to_float<T>(dc[k], df);
-                chunk_to_float<T>(gv[k], gf);
+        for (int r = 0; r < R; ++r) {
+            const int64_t row = rb + r * rstride;
+            if (row >= a.M) break;  // uniform across the CTA
+            float tot = 0.f;
+            for (int w = 0; w < nwarps; ++w) tot += red[buf][r][w];
+            const float c1 = rs[r] * tot * a.inv_n;
+            const float b = -rs[r] * rs[r] * c1;
+            const f32x2 rs2 = f2_make(rs[r], rs[r]), b2 = f2_make(b, b);
+            const size_t base = (size_t)row * N;
 #pragma unroll
-                for (int e = 0; e < V; ++e) s = fmaf(xf[e], df[e] * gf[e], s);
-            }
-        }
-        if (e_own) s = fmaf(xec, dec * ge, s);
-        s = warp_sum(s);
-        if (lane == 0) red[buf][warp] = s;
-        __syncthreads();  // also orders the reads of red[buf] two rows back before these writes
-        float tot = 0.f;
-        for (int w = 0; w < nwarps; ++w) tot += red[buf][w];
-        buf ^= 1;
-        const float c1 = rs * tot * a.inv_n;
-
-        // pass 2: dx = (wdy - x_hat*c1)*rstd (+ dres); partial += dy*x_hat
-#pragma unroll
-        for (int k = 0; k < J; ++k) {
-            if (own[k]) {
-                float xf[V], df[V], gf[V], o[V], rf[V];
-                chunk_to_float<T>(xc[k], xf);
-                chunk_to_float<T>(dc[k], df);
-                chunk_to_float<T>(gv[k], gf);
-                if (HAS_DRES) chunk_to_float<T>(rv[k], rf);
-#pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const float xh = xf[e] * rs;
-                    o[e] = fmaf(-xh, c1, df[e] * gf[e]) * rs;
-                    if (HAS_DRES) o[e] += rf[e];
-                    dwp[k][e] = fmaf(df[e], xh, dwp[k][e]);
+            for (int k = 0; k < J; ++k) {
+                if (own[k]) {
+                    const uint4 o = RowMath<T>::template pass2<HAS_DRES>(
+                        xc[r][k], dc[r][k], HAS_DRES ? rv[HAS_DRES ? r : 0][k] : make_uint4(0, 0, 0, 0),
+                        gv[k], kGammaF ? g2[kGammaF ? k : 0] : nullptr, rs2, b2, acc2[k]);
+                    st_global_v4(dx + base + col[k], o);
                 }
-                st_global_v4(dx + base + col[k], float_to_chunk<T>(o));
+            }
+            if (e_own) {
+                float d = fmaf(xec[r], b, (dec[r] * ge) * rs[r]);
+                if (HAS_DRES) d += re[r];
+                dx[base + je] = from_f<T>(d);
+                dwe = fmaf(xec[r] * dec[r], rs[r], dwe);
             }
         }
-        if (e_own) {
-            const float xh = xec * rs;
-            float d = fmaf(-xh, c1, dec * ge) * rs;
-            if (HAS_DRES) d += re;
-            dx[base + je] = from_f<T>(d);
-            dwe = fmaf(dec, xh, dwe);
-        }
+        buf ^= 1;
 #pragma unroll
-        for (int k = 0; k < J; ++k) {
-            xc[k] = xn[k];
-            dc[k] = dn[k];
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+            for (int k = 0; k < J; ++k) {
+                xc[r][k] = xn[r][k];
+                dc[r][k] = dn[r][k];
+            }
+            xec[r] = xen[r];
+            dec[r] = den[r];
         }
-        xec = xen;
-        dec = den;
-        row = nrow;
     }
     pdl_launch_dependents();
     if (ATOMIC) {
@@ -195,7 +228,8 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
         for (int k = 0; k < J; ++k)
             if (own[k])
 #pragma unroll
-                for (int e = 0; e < V; ++e) sdw[col[k] + e] = dwp[k][e];
+                for (int q = 0; q < P2; ++q)
+                    f2_split(acc2[k][q], sdw[col[k] + 2 * q], sdw[col[k] + 2 * q + 1]);
         if (e_own) sdw[je] = dwe;
         __syncthreads();
         pdl_wait();
@@ -209,18 +243,19 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
         for (int k = 0; k < J; ++k)
             if (own[k])
 #pragma unroll
-                for (int e = 0; e < V; ++e) part[col[k] + e] = dwp[k][e];
+                for (int q = 0; q < P2; ++q)
+                    f2_split(acc2[k][q], part[col[k] + 2 * q], part[col[k] + 2 * q + 1]);
         if (e_own) part[je] = dwe;
     }
 }
 
-template <typename T, bool HAS_DRES, bool ATOMIC, int J>
+template <typename T, bool HAS_DRES, bool ATOMIC, int J, int R>
 static cudaError_t launch_phase_t(const PhaseArgs &args, const GenericPlan &plan, cudaStream_t s,
                                   bool pdl) {
+    auto kern = bwd_phase_kernel<T, HAS_DRES, ATOMIC, J, R>;
     // the atomic mode stages N floats in dynamic shared memory: raise the
     // kernel's cap when a plan asks for more than the default 48 KB
-    cudaError_t e = ensure_smem_attr((const void *)bwd_phase_kernel<T, HAS_DRES, ATOMIC, J>,
-                                     plan.smem);
+    cudaError_t e = ensure_smem_attr((const void *)kern, plan.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
@@ -232,14 +267,17 @@ static cudaError_t launch_phase_t(const PhaseArgs &args, const GenericPlan &plan
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, bwd_phase_kernel<T, HAS_DRES, ATOMIC, J>, args);
+    return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 template <typename T, bool HAS_DRES, bool ATOMIC>
 static cudaError_t launch_phase_j(const PhaseArgs &args, const GenericPlan &plan, cudaStream_t s,
                                   bool pdl) {
-    return plan.phase == 2 ? launch_phase_t<T, HAS_DRES, ATOMIC, 2>(args, plan, s, pdl)
-                           : launch_phase_t<T, HAS_DRES, ATOMIC, 1>(args, plan, s, pdl);
+    if (plan.phase_rows == 2)
+        return plan.phase == 2 ? launch_phase_t<T, HAS_DRES, ATOMIC, 2, 2>(args, plan, s, pdl)
+                               : launch_phase_t<T, HAS_DRES, ATOMIC, 1, 2>(args, plan, s, pdl);
+    return plan.phase == 2 ? launch_phase_t<T, HAS_DRES, ATOMIC, 2, 1>(args, plan, s, pdl)
+                           : launch_phase_t<T, HAS_DRES, ATOMIC, 1, 1>(args, plan, s, pdl);
 }
 
 template <typename T>
@@ -252,31 +290,37 @@ static cudaError_t launch_phase_dt(const PhaseArgs &args, const GenericPlan &pla
                     : launch_phase_j<T, false, false>(args, plan, s, pdl);
 }
 
-template <typename T>
-static const void *phase_kernel_ptr(bool dres, bool atomic, int cpt) {
+template <typename T, int R>
+static const void *phase_kernel_ptr_r(bool dres, bool atomic, int cpt) {
     if (cpt == 2)
-        return dres ? (atomic ? (const void *)bwd_phase_kernel<T, true, true, 2>
-                              : (const void *)bwd_phase_kernel<T, true, false, 2>)
-                    : (atomic ? (const void *)bwd_phase_kernel<T, false, true, 2>
-                              : (const void *)bwd_phase_kernel<T, false, false, 2>);
-    return dres ? (atomic ? (const void *)bwd_phase_kernel<T, true, true, 1>
-                          : (const void *)bwd_phase_kernel<T, true, false, 1>)
-                : (atomic ? (const void *)bwd_phase_kernel<T, false, true, 1>
-                          : (const void *)bwd_phase_kernel<T, false, false, 1>);
+        return dres ? (atomic ? (const void *)bwd_phase_kernel<T, true, true, 2, R>
+                              : (const void *)bwd_phase_kernel<T, true, false, 2, R>)
+                    : (atomic ? (const void *)bwd_phase_kernel<T, false, true, 2, R>
+                              : (const void *)bwd_phase_kernel<T, false, false, 2, R>);
+    return dres ? (atomic ? (const void *)bwd_phase_kernel<T, true, true, 1, R>
+                          : (const void *)bwd_phase_kernel<T, true, false, 1, R>)
+                : (atomic ? (const void *)bwd_phase_kernel<T, false, true, 1, R>
+                          : (const void *)bwd_phase_kernel<T, false, false, 1, R>);
+}
+
+template <typename T>
+static const void *phase_kernel_ptr(bool dres, bool atomic, int cpt, int rows) {
+    return rows == 2 ? phase_kernel_ptr_r<T, 2>(dres, atomic, cpt)
+                     : phase_kernel_ptr_r<T, 1>(dres, atomic, cpt);
 }
 
 // Resident CTAs per SM of one instance at a CTA size (a multiple of 32 up to
 // 512), from the occupancy calculator without dynamic shared memory (the
 // atomic mode's N floats, at most 33 KB, leave room for the 2 CTAs per SM the
 // planner takes at most); cached per instance and size.
-int phase_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads) {
-    static int cache[3][2][2][2][17];
+int phase_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int rows, int threads) {
+    static int cache[3][2][2][2][2][17];
     if (dtype < 0 || dtype > 2 || threads < 32 || threads > 512 || (threads & 31)) return 1;
-    int &c = cache[dtype][dres][atomic][cpt == 2][threads >> 5];
+    int &c = cache[dtype][dres][atomic][cpt == 2][rows == 2][threads >> 5];
     if (c > 0) return c;
-    const void *k = dtype == kF32 ? phase_kernel_ptr<float>(dres, atomic, cpt)
-                  : dtype == kF16 ? phase_kernel_ptr<__half>(dres, atomic, cpt)
-                                  : phase_kernel_ptr<__nv_bfloat16>(dres, atomic, cpt);
+    const void *k = dtype == kF32 ? phase_kernel_ptr<float>(dres, atomic, cpt, rows)
+                  : dtype == kF16 ? phase_kernel_ptr<__half>(dres, atomic, cpt, rows)
+                                  : phase_kernel_ptr<__nv_bfloat16>(dres, atomic, cpt, rows);
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, 0) != cudaSuccess || n < 1) {
         (void)cudaGetLastError();
@@ -303,6 +347,7 @@ cudaError_t launch_bwd_phase(const BwdProblem &p, const GenericPlan &plan, cudaS
     // a residue class without a CTA would leave its rows unwritten
     if (p.M > 0 && plan.grid < (p.M < a.period ? p.M : a.period)) return cudaErrorInvalidValue;
     if (plan.atomic && plan.smem < (size_t)p.N * 4) return cudaErrorInvalidValue;
+    if (plan.phase_rows != 1 && plan.phase_rows != 2) return cudaErrorInvalidValue;
     const bool has_dres = p.dres != nullptr;
     switch (p.dtype) {
     case kF32: return launch_phase_dt<float>(a, plan, has_dres, s, pdl_after_zero);

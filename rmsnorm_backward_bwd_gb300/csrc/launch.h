@@ -60,6 +60,7 @@ struct GenericPlan {
     int rows = 0;      // vector variant: rows in flight per CTA iteration (2, 4); 0 = scalar
     int cpb = 0;       // realigning engine: column blocks per thread (2, 4); 0 = not used
     int phase = 0;     // phase-class kernel: 16-byte chunks per thread (1, 2); 0 = not used
+    int phase_rows = 1;  // phase-class kernel: rows per CTA iteration (1, 2)
 };
 
 // Row engine: largest chunk count per row and CTA thread cap for a cpt.
@@ -75,7 +76,7 @@ cudaError_t launch_bwd_generic(const BwdProblem &p, const GenericPlan &plan, cud
                                bool pdl_after_zero);
 // Rows that are not 16-byte multiples, all row tensors at one alignment phase.
 int phase_period(int N, int dtype);
-int phase_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads);
+int phase_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int rows, int threads);
 size_t ln_phase_smem_bytes(int N, bool atomic);
 int ln_phase_blocks_per_sm(int dtype, bool atomic, int cpt, int threads, size_t smem);
 cudaError_t launch_bwd_phase(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,

@@ -383,6 +383,27 @@ def test_generic_phase_kernel(M, N, dt, fused, cpt, period, mode):
     parity.check_bwd(ex, *out, tag=" [%s]" % plan)
 
 
+@pytest.mark.parametrize("rows", [1, 2])
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("M,N,dt,fused", [
+    (1000, 4095, "bf16", False), (333, 4100, "bf16", True), (97, 2999, "f32", True),
+    (130, 1001, "f16", True), (5, 7, "bf16", False), (17, 8183, "f16", True), (9, 6, "f16", False),
+    (611, 8190, "bf16", False)],
+    ids=lambda v: str(v))
+def test_generic_phase_kernel_rows_per_iteration(M, N, dt, fused, mode, rows):
+    """One or two rows of the class per CTA iteration (RN_OPT_TEAMS_PER_CTA),
+    with M leaving the last iteration of some CTAs a single row; both
+    weight-gradient modes."""
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    native.set_option(native.OPT_TEAMS_PER_CTA, rows)
+    ex = parity.expected_bwd(Case("phase rows %s" % dt, M, N, dt, fused=fused, with_dres=fused,
+                                  seed=29))
+    out = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    assert "engine=generic phase" in plan and " rows=%d " % rows in plan, plan
+    assert parity.check_bwd(ex, *out, tag=" [%s]" % plan) == 0
+
+
 @pytest.mark.parametrize("shift", [1, 3])
 @pytest.mark.parametrize("N,dt", [(4096, "bf16"), (1024, "f32"), (8192, "f16")])
 def test_generic_phase_kernel_aligned_rows_offset_base(N, dt, shift):
