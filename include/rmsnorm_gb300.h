@@ -236,8 +236,9 @@ typedef enum rn_option {
     RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (async-copy ring), 2 = generic engines (the
                                  default for rows that are not 16-byte multiples or bases off
                                  16 bytes; which one runs depends on the row size and on whether
-                                 the row tensors share one alignment phase: realigning, vector
-                                 or element-wise kernel), 3 = cluster engine (RMSNorm backward:
+                                 the row tensors share one alignment phase: phase-class kernel up
+                                 to 2048 whole 16-byte chunks, vector kernel past that, element-
+                                 wise kernel for mixed phases), 3 = cluster engine (RMSNorm backward:
                                  a row split across a thread-block cluster; chosen by default
                                  for aligned rows of more than 2048 16-byte chunks) */
     RN_OPT_DWEIGHT_MODE = 1,  /* 1 = scratch partials + finalize (deterministic dweight),
@@ -252,10 +253,11 @@ typedef enum rn_option {
     RN_OPT_GRID = 5,          /* CTAs of the row pass (default: one per SM; at most 2 per SM) */
     RN_OPT_CLUSTER_SIZE = 6,  /* cluster engine: CTAs per cluster, 2, 4, 8 or 16 */
     RN_OPT_GENERIC_KERNEL = 7, /* RMSNorm backward, generic engines: 1 = phase-class kernel,
-                                 2 = vector kernel, 3 = realigning kernel, 4 = element-wise
-                                 kernel. A kernel that cannot take the problem (its row-size
-                                 range, or tensors at different alignment phases) falls back
-                                 to the next one the automatic choice would make. */
+                                 2 = vector kernel, 3 = realigning kernel (rows of 16 to 32 KB;
+                                 taken only when asked for), 4 = element-wise kernel. A kernel
+                                 that cannot take the problem (its row-size range, or tensors at
+                                 different alignment phases) falls back to the next one the
+                                 automatic choice would make. */
     RN_OPT_COUNT = 8
 } rn_option;
 

@@ -316,7 +316,12 @@ static bool generic_vec_ok(const BwdProblem &p, const DeviceInfo &d) {
 // flushed, us per call, vector variant -> realigning engine): bf16 16384 x
 // 8190 292 -> 233 (fused 321 -> 275), f32 4096 x 4095 68 -> 58 (fused
 // 77 -> 67); below 1024 blocks the vector variant was faster (bf16 4096 x
-// 4100 48 vs 56, 4096 x 4095 51 vs 53).
+// 4100 48 vs 56, 4096 x 4095 51 vs 53). Taken only when asked for
+// (RN_OPT_GENERIC_KERNEL = 3): the phase-class kernel with four chunks a thread
+// is faster at every width of its range (kernel us, realigning -> phase-class:
+// bf16 4096 x 12290 126.7 -> 87.1, fused 182.1 -> 132.8, 16384 x 12290
+// 424.4 -> 331.3, 16384 x 8201 365.4 -> 287.7, 4096 x 16383 138.4 -> 104.1,
+// f16 8192 x 10001 207.8 -> 157.2, f32 4096 x 6001 77.8 -> 66.3).
 static bool plan_realign(const BwdProblem &p, const DeviceInfo &d, GenericPlan *plan) {
     if (!generic_vec_ok(p, d)) return false;
     const int nb = (int)(((int64_t)p.N * elem_bytes(p.dtype) + 15) / 16);
@@ -345,8 +350,8 @@ static bool plan_realign(const BwdProblem &p, const DeviceInfo &d, GenericPlan *
 }
 
 // The phase-class kernel: the vector variant's conditions (one alignment
-// phase) and at most 1024 whole 16-byte chunks per row (bf16 N ~8K, f32 N
-// ~4K); 1 chunk per thread up to 256 chunks, else 2. Its grid is the
+// phase) and at most 2048 whole 16-byte chunks per row (bf16 N ~16K, f32 N
+// ~8K); 1 chunk per thread up to 256 chunks, 2 up to 1024, else 4. Its grid is the
 // kernel's resident CTAs on every SM, at most 2: scratch mode's partial rows
 // fill the workspace there, and in atomic mode every CTA adds N values at the
 // end. Measured on GB300 (L2 flushed, us per call, 2 CTAs per SM -> all
@@ -368,12 +373,12 @@ static int phase_grid(int64_t M, int P, int per_sm, const DeviceInfo &d) {
 }
 
 // CTA size and chunks per thread of a phase-class kernel for a row of N
-// elements of s bytes: 1 chunk per thread up to 256 whole 16-byte chunks, else
-// 2, up to 1024 chunks. False past that.
-static bool phase_shape(int N, int dtype, int *cpt, int *threads) {
+// elements of s bytes: 1 chunk per thread up to 256 whole 16-byte chunks, 2
+// up to 1024, else 4, up to max_chunks. False past that.
+static bool phase_shape(int N, int dtype, int max_chunks, int *cpt, int *threads) {
     const int64_t nvmax = (int64_t)N * elem_bytes(dtype) / 16;
-    if (nvmax > 1024) return false;
-    *cpt = nvmax > 256 ? 2 : 1;
+    if (nvmax > max_chunks) return false;
+    *cpt = nvmax > 1024 ? 4 : (nvmax > 256 ? 2 : 1);
     int t = (int)((nvmax + *cpt - 1) / *cpt + 31) / 32 * 32;
     *threads = t < 32 ? 32 : t;
     return true;
@@ -382,10 +387,12 @@ static bool phase_shape(int N, int dtype, int *cpt, int *threads) {
 static bool plan_phase(const BwdProblem &p, const DeviceInfo &d, bool atomic, GenericPlan *plan) {
     if (!generic_vec_ok(p, d)) return false;
     int cpt, threads;
-    if (!phase_shape(p.N, p.dtype, &cpt, &threads)) return false;
-    // rows per CTA iteration: RN_OPT_TEAMS_PER_CTA = 1 or 2 forces it
+    if (!phase_shape(p.N, p.dtype, 2048, &cpt, &threads)) return false;
+    // rows per CTA iteration: RN_OPT_TEAMS_PER_CTA = 1 or 2 forces it; one with four chunks a
+    // thread
     int rows = g_opts[RN_OPT_TEAMS_PER_CTA];
     if (rows != 1 && rows != 2) rows = 2;
+    if (cpt == 4) rows = 1;
     const int per_sm = phase_blocks_per_sm(p.dtype, p.dres != nullptr, atomic, cpt, rows, threads);
     plan->phase = cpt;
     plan->phase_rows = rows;
@@ -394,7 +401,10 @@ static bool plan_phase(const BwdProblem &p, const DeviceInfo &d, bool atomic, Ge
     plan->rows = 0;
     plan->threads = threads;
     plan->smem_dw = atomic;
-    plan->smem = atomic ? (size_t)p.N * 4 : 0;  // the atomic mode's staged partial
+    // the atomic mode's staged partial; with four 16-bit chunks a thread, first the gamma chunks
+    size_t smem = atomic ? (size_t)p.N * 4 : 0;
+    if (cpt == 4 && p.dtype != kF32 && smem < (size_t)threads * 4 * 16) smem = (size_t)threads * 4 * 16;
+    plan->smem = smem;
     plan->atomic = atomic;
     return true;
 }
@@ -405,7 +415,7 @@ static void plan_generic(const BwdProblem &p, const DeviceInfo &d, bool atomic, 
     // RN_OPT_GENERIC_KERNEL: 1 phase-class, 2 vector, 3 realigning, 4 element-wise
     const int pick = g_opts[RN_OPT_GENERIC_KERNEL];
     if (pick <= 1 && plan_phase(p, d, atomic, plan)) return;
-    if ((pick <= 1 || pick == 3) && plan_realign(p, d, plan)) return;
+    if (pick == 3 && plan_realign(p, d, plan)) return;
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
     plan->smem_dw = generic_smem_bytes(p.N, true) <= budget;
@@ -658,7 +668,7 @@ static bool plan_ln_phase(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
     for (const void *q : {p.x, p.dy, static_cast<const void *>(p.dx)})
         if (((uintptr_t)q & 15u) != ph || ((uintptr_t)q % S) != 0) return false;
     int cpt, threads;
-    if (!phase_shape(p.N, p.dtype, &cpt, &threads)) return false;
+    if (!phase_shape(p.N, p.dtype, 1024, &cpt, &threads)) return false;
     const size_t smem = ln_phase_smem_bytes(p.N, atomic);
     if (smem > (size_t)d.smem_optin) return false;
     const int per_sm = ln_phase_blocks_per_sm(p.dtype, atomic, cpt, threads, smem);

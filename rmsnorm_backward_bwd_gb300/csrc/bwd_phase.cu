@@ -1,6 +1,6 @@
 // Backward phase-class kernel: rows that are not 16-byte multiples (or whose
 // base is off a 16-byte boundary), x, dy, dx and dresidual_out at one
-// alignment phase, rows of at most 1024 16-byte chunks.
+// alignment phase, rows of at most 2048 whole 16-byte chunks.
 //
 // Same math as the row engine (FlyDSL issue #769 "Math"; fused-add from
 // PR #800 "What's included"). Row r starts at byte r*N*s past the base, so its
@@ -9,9 +9,13 @@
 // residue class modulo P. Within a class every row splits the same way into
 // head elements, whole 16-byte chunks and tail elements, so a thread owns the
 // same columns in every row it touches. Its gamma chunks (packed, as loaded)
-// and its weight-gradient partial stay in registers, as in the row engine.
-// The row stays in registers between the two passes, and the class's next row
-// is loaded while the current one is computed. The generic vector kernel, by
+// and its weight-gradient partial stay in registers, as in the row engine
+// (with four 16-bit chunks a thread the gamma chunks move to shared memory).
+// The rows stay in registers between the two passes: a CTA takes R rows of
+// its class per iteration (2, or 1 with four chunks a thread) under one CTA
+// barrier, and the class's next R rows are loaded while the current ones are
+// computed. The chunk arithmetic is the row engine's packed-pair RowMath. The
+// generic vector kernel, by
 // contrast, lets any CTA take any row, so a column's owner changes with the
 // row's phase and gamma and the partial live in shared memory.
 #include "common.cuh"
@@ -75,10 +79,14 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
     if (h > N) h = N;
     const int nv = (N - h) / V, tail = N - h - nv * V;
 
-    // this thread's chunks (i = tid + k*nthr) and its head or tail element
+    // this thread's chunks (i = tid + k*nthr) and its head or tail element. With four 16-bit
+    // chunks a thread the packed gamma chunks wait in dynamic shared memory (at i), not in
+    // registers: there are not enough.
+    constexpr bool kGammaSmem = J == 4 && !kGammaF;
+    extern __shared__ __align__(16) uint4 dyn[];
     bool own[J];
     int col[J];
-    uint4 gv[J];
+    uint4 gv[kGammaSmem ? 1 : J];
     f32x2 g2[kGammaF ? J : 1][kGammaF ? P2 : 1];
     f32x2 acc2[J][P2];
 #pragma unroll
@@ -86,10 +94,12 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
         const int i = tid + k * nthr;
         own[k] = i < nv;
         col[k] = h + i * V;
-        gv[k] = own[k] ? gather_chunk<T>(g + col[k]) : make_uint4(0, 0, 0, 0);
+        const uint4 gk = own[k] ? gather_chunk<T>(g + col[k]) : make_uint4(0, 0, 0, 0);
+        if (kGammaSmem) dyn[i] = gk;
+        else gv[kGammaSmem ? 0 : k] = gk;
         if (kGammaF) {
             float gf[V];
-            chunk_to_float<T>(gv[k], gf);
+            chunk_to_float<T>(gk, gf);
 #pragma unroll
             for (int q = 0; q < P2; ++q)
                 g2[kGammaF ? k : 0][kGammaF ? q : 0] = f2_make(gf[2 * q], gf[2 * q + 1]);
@@ -141,8 +151,10 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
             if (nrow < a.M) load(nrow, xn[r], dn[r], xen[r], den[r]);
         }
 
-        // dresidual_out (a plain load: dx may overwrite it) and rstd of these rows
-        uint4 rv[HAS_DRES ? R : 1][J];
+        // dresidual_out (a plain load: dx may overwrite it) and rstd of these rows; with four
+        // chunks a thread dresidual_out is loaded in pass 2 (registers)
+        constexpr bool kEarlyDres = HAS_DRES && J <= 2;
+        uint4 rv[kEarlyDres ? R : 1][J];
         float re[R], rs[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -150,14 +162,14 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
             const bool live = row < a.M;
             const size_t base = (size_t)row * N;
             re[r] = 0.f;
-            if (HAS_DRES) {
+            if (kEarlyDres) {
 #pragma unroll
                 for (int k = 0; k < J; ++k)
-                    rv[HAS_DRES ? r : 0][k] =
+                    rv[kEarlyDres ? r : 0][k] =
                         own[k] && live ? *reinterpret_cast<const uint4 *>(dres + base + col[k])
                                        : make_uint4(0, 0, 0, 0);
-                if (e_own && live) re[r] = to_f(dres[base + je]);
             }
+            if (HAS_DRES && e_own && live) re[r] = to_f(dres[base + je]);
             rs[r] = live ? __ldg(a.rstd + row) : 0.f;
         }
 
@@ -168,7 +180,8 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
 #pragma unroll
             for (int k = 0; k < J; ++k)
                 if (own[k])
-                    part2 = RowMath<T>::pass1(xc[r][k], dc[r][k], gv[k],
+                    part2 = RowMath<T>::pass1(xc[r][k], dc[r][k],
+                                              kGammaSmem ? dyn[tid + k * nthr] : gv[kGammaSmem ? 0 : k],
                                               kGammaF ? g2[kGammaF ? k : 0] : nullptr, part2);
             float lo, hi;
             f2_split(part2, lo, hi);
@@ -193,9 +206,13 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
 #pragma unroll
             for (int k = 0; k < J; ++k) {
                 if (own[k]) {
+                    uint4 rk = make_uint4(0, 0, 0, 0);
+                    if (kEarlyDres) rk = rv[kEarlyDres ? r : 0][k];
+                    else if (HAS_DRES) rk = *reinterpret_cast<const uint4 *>(dres + base + col[k]);
                     const uint4 o = RowMath<T>::template pass2<HAS_DRES>(
-                        xc[r][k], dc[r][k], HAS_DRES ? rv[HAS_DRES ? r : 0][k] : make_uint4(0, 0, 0, 0),
-                        gv[k], kGammaF ? g2[kGammaF ? k : 0] : nullptr, rs2, b2, acc2[k]);
+                        xc[r][k], dc[r][k], rk,
+                        kGammaSmem ? dyn[tid + k * nthr] : gv[kGammaSmem ? 0 : k],
+                        kGammaF ? g2[kGammaF ? k : 0] : nullptr, rs2, b2, acc2[k]);
                     st_global_v4(dx + base + col[k], o);
                 }
             }
@@ -222,8 +239,9 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
     if (ATOMIC) {
         // The partial goes through shared memory so that every class adds it
         // with 16-byte atomics (dweight_f32 is 16-byte aligned; a class's own
-        // columns start at any element).
-        extern __shared__ __align__(16) float sdw[];  // N floats
+        // columns start at any element). It takes the place of the gamma chunks.
+        float *sdw = reinterpret_cast<float *>(dyn);  // N floats
+        if (kGammaSmem) __syncthreads();  // every thread is done with the gamma chunks
 #pragma unroll
         for (int k = 0; k < J; ++k)
             if (own[k])
@@ -273,6 +291,8 @@ static cudaError_t launch_phase_t(const PhaseArgs &args, const GenericPlan &plan
 template <typename T, bool HAS_DRES, bool ATOMIC>
 static cudaError_t launch_phase_j(const PhaseArgs &args, const GenericPlan &plan, cudaStream_t s,
                                   bool pdl) {
+    // four chunks a thread: one row per iteration (two would not fit the registers)
+    if (plan.phase == 4) return launch_phase_t<T, HAS_DRES, ATOMIC, 4, 1>(args, plan, s, pdl);
     if (plan.phase_rows == 2)
         return plan.phase == 2 ? launch_phase_t<T, HAS_DRES, ATOMIC, 2, 2>(args, plan, s, pdl)
                                : launch_phase_t<T, HAS_DRES, ATOMIC, 1, 2>(args, plan, s, pdl);
@@ -292,6 +312,11 @@ static cudaError_t launch_phase_dt(const PhaseArgs &args, const GenericPlan &pla
 
 template <typename T, int R>
 static const void *phase_kernel_ptr_r(bool dres, bool atomic, int cpt) {
+    if (cpt == 4)
+        return dres ? (atomic ? (const void *)bwd_phase_kernel<T, true, true, 4, 1>
+                              : (const void *)bwd_phase_kernel<T, true, false, 4, 1>)
+                    : (atomic ? (const void *)bwd_phase_kernel<T, false, true, 4, 1>
+                              : (const void *)bwd_phase_kernel<T, false, false, 4, 1>);
     if (cpt == 2)
         return dres ? (atomic ? (const void *)bwd_phase_kernel<T, true, true, 2, R>
                               : (const void *)bwd_phase_kernel<T, true, false, 2, R>)
@@ -314,9 +339,9 @@ static const void *phase_kernel_ptr(bool dres, bool atomic, int cpt, int rows) {
 // atomic mode's N floats, at most 33 KB, leave room for the 2 CTAs per SM the
 // planner takes at most); cached per instance and size.
 int phase_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int rows, int threads) {
-    static int cache[3][2][2][2][2][17];
+    static int cache[3][2][2][3][2][17];
     if (dtype < 0 || dtype > 2 || threads < 32 || threads > 512 || (threads & 31)) return 1;
-    int &c = cache[dtype][dres][atomic][cpt == 2][rows == 2][threads >> 5];
+    int &c = cache[dtype][dres][atomic][cpt == 4 ? 2 : cpt == 2][rows == 2][threads >> 5];
     if (c > 0) return c;
     const void *k = dtype == kF32 ? phase_kernel_ptr<float>(dres, atomic, cpt, rows)
                   : dtype == kF16 ? phase_kernel_ptr<__half>(dres, atomic, cpt, rows)
@@ -347,6 +372,8 @@ cudaError_t launch_bwd_phase(const BwdProblem &p, const GenericPlan &plan, cudaS
     // a residue class without a CTA would leave its rows unwritten
     if (p.M > 0 && plan.grid < (p.M < a.period ? p.M : a.period)) return cudaErrorInvalidValue;
     if (plan.atomic && plan.smem < (size_t)p.N * 4) return cudaErrorInvalidValue;
+    if (plan.phase == 4 && p.dtype != kF32 && plan.smem < (size_t)plan.threads * 4 * 16)
+        return cudaErrorInvalidValue;
     if (plan.phase_rows != 1 && plan.phase_rows != 2) return cudaErrorInvalidValue;
     const bool has_dres = p.dres != nullptr;
     switch (p.dtype) {

@@ -404,6 +404,26 @@ def test_generic_phase_kernel_rows_per_iteration(M, N, dt, fused, mode, rows):
     assert parity.check_bwd(ex, *out, tag=" [%s]" % plan) == 0
 
 
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("M,N,dt,fused", [
+    (333, 12290, "bf16", False), (97, 16391, "bf16", True), (50, 8201, "f16", True),
+    (17, 6001, "f32", True), (5, 10001, "bf16", False), (300, 4101, "f32", False),
+    (9, 16390, "f16", False)],
+    ids=lambda v: str(v))
+def test_generic_phase_kernel_four_chunks(M, N, dt, fused, mode):
+    """Rows of 1025 to 2048 whole 16-byte chunks through the phase-class kernel
+    (RN_OPT_GENERIC_KERNEL = 1): four chunks a thread, one row per iteration,
+    gamma chunks in shared memory for 16-bit types; both weight-gradient modes."""
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    native.set_option(native.OPT_GENERIC_KERNEL, 1)
+    ex = parity.expected_bwd(Case("phase4 %s" % dt, M, N, dt, fused=fused, with_dres=fused,
+                                  seed=30))
+    out = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    assert "engine=generic phase cpt=4 rows=1 " in plan, plan
+    assert parity.check_bwd(ex, *out, tag=" [%s]" % plan) == 0
+
+
 @pytest.mark.parametrize("shift", [1, 3])
 @pytest.mark.parametrize("N,dt", [(4096, "bf16"), (1024, "f32"), (8192, "f16")])
 def test_generic_phase_kernel_aligned_rows_offset_base(N, dt, shift):
@@ -455,17 +475,18 @@ def test_generic_kernel_option(kernel, name):
 @pytest.mark.parametrize("N,dt,engine", [
     (2055, "bf16", "engine=generic phase cpt=1"),   # 256 whole 16-byte chunks
     (2057, "bf16", "engine=generic phase cpt=2"),   # 257
-    (8199, "bf16", "engine=generic phase cpt=2"),   # 1024: the phase-class kernel's widest rows
-    (8201, "bf16", "engine=generic realign cpb=4"),  # 1025 chunks, 1026 column blocks
-    (16383, "bf16", "engine=generic realign cpb=4"),  # 2048 blocks
-    (16385, "bf16", "engine=generic vec"),       # 2049 blocks: past the realigning range
+    (8199, "bf16", "engine=generic phase cpt=2"),   # 1024
+    (8201, "bf16", "engine=generic phase cpt=4"),   # 1025 whole chunks
+    (16385, "bf16", "engine=generic phase cpt=4"),  # 2048: the phase-class kernel's widest rows
+    (16393, "bf16", "engine=generic vec"),          # 2049 whole chunks
     (4099, "f32", "engine=generic phase cpt=2"),    # 1024 chunks of f32
-    (4101, "f32", "engine=generic realign cpb=4")],  # 1025
+    (4101, "f32", "engine=generic phase cpt=4")],   # 1025
     ids=lambda v: str(v))
 @pytest.mark.parametrize("M", [1, 3, 64])
 def test_generic_engine_thresholds(N, dt, engine, M):
-    """The width thresholds between the generic kernels (phase-class,
-    realigning, vector), on both sides, with few and several rows."""
+    """The width thresholds between the generic kernels (phase-class with 1,
+    2 or 4 chunks a thread, vector), on both sides, with few and several
+    rows."""
     ex = parity.expected_bwd(Case("threshold", M, N, dt, fused=True, with_dres=True, seed=41))
     out = parity.run_gpu_bwd(ex)
     plan = native.last_plan()
