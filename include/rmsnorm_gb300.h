@@ -115,10 +115,16 @@ rn_status rn_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes)
  *   dy           [M,N] dtype, in (gradient of y)
  *   rstd         [M] fp32, in: the statistic the forward saved (not recomputed)
  *   dx           [M,N] dtype, out
- *   dweight_f32  [N] fp32, out: fully overwritten with sum_m dy*x_hat
- *   dweight      [N] dtype, out, may be NULL: dweight_f32 rounded to dtype
+ *   dweight_f32  [N] fp32, out, may be NULL: fully overwritten with
+ *                sum_m dy*x_hat
+ *   dweight      [N] dtype, out, may be NULL: that sum rounded to dtype
  *   workspace    device buffer of >= rn_bwd_workspace_bytes(M,N,dtype) bytes
  * Every step (zero, row pass, cross-row reduction, cast) runs inside this call.
+ * Without dweight_f32 the fp32 sum is not stored and the weight gradient takes
+ * the deterministic scratch mode (per-CTA partial rows in the workspace, then
+ * one kernel that sums them in a fixed order and writes dweight): one launch
+ * fewer than the atomic mode's zero, row pass and cast. With neither
+ * dweight_f32 nor dweight no weight gradient is produced (the row pass alone).
  */
 rn_status rn_rmsnorm_bwd(const void *x, const void *gamma, const void *dy, const float *rstd,
                          void *dx, float *dweight_f32, void *dweight,
@@ -186,15 +192,18 @@ rn_status rn_layernorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size
  *   dy          [M,N] dtype, in (gradient of y)
  *   mean, rstd  [M] fp32, in: the statistics the forward saved (not recomputed)
  *   dx          [M,N] dtype, out; must not overlap any input
- *   dgamma_f32  [N] fp32, out: fully overwritten with sum_m dy*x_hat
- *   dbeta_f32   [N] fp32, out, may be NULL (no bias): sum_m dy; must not
- *               overlap dgamma_f32
- *   dgamma      [N] dtype, out, may be NULL: dgamma_f32 rounded to dtype
- *   dbeta       [N] dtype, out, may be NULL: dbeta_f32 rounded to dtype
- *               (needs dbeta_f32)
+ *   dgamma_f32  [N] fp32, out, may be NULL: fully overwritten with sum_m dy*x_hat
+ *   dbeta_f32   [N] fp32, out, may be NULL: sum_m dy; must not overlap
+ *               dgamma_f32
+ *   dgamma      [N] dtype, out, may be NULL: the dgamma sum rounded to dtype
+ *   dbeta       [N] dtype, out, may be NULL: the dbeta sum rounded to dtype
  *   workspace   >= rn_layernorm_bwd_workspace_bytes(M,N,dtype) bytes
  * Every step (zero, row pass, cross-row reduction, casts) runs inside this
- * call; RN_OPT_* options apply as for the RMSNorm backward.
+ * call; RN_OPT_* options apply as for the RMSNorm backward. The atomic mode
+ * needs the fp32 buffer of every gradient asked for (dgamma_f32, and
+ * dbeta_f32 when dbeta is asked for); otherwise the deterministic scratch mode
+ * runs, as for rn_rmsnorm_bwd without dweight_f32. Gradients whose two
+ * buffers are both NULL are not produced (dbeta: no bias).
  */
 rn_status rn_layernorm_bwd(const void *x, const void *gamma, const void *dy, const float *mean,
                            const float *rstd, void *dx, float *dgamma_f32, float *dbeta_f32,

@@ -452,6 +452,7 @@ static void plan_generic(const BwdProblem &p, const DeviceInfo &d, bool atomic, 
 constexpr int64_t kSmallProblemBytes = 2 << 20;
 
 static bool want_atomic(const BwdProblem &p) {
+    if (p.dw_f32 == nullptr) return false;  // no fp32 buffer to accumulate into
     const int m = g_opts[RN_OPT_DWEIGHT_MODE];
     if (m == 1) return false;
     if (m == 0 && p.M * (int64_t)p.N * elem_bytes(p.dtype) <= kSmallProblemBytes) return false;
@@ -498,9 +499,11 @@ static rn_status run_sequence(bool atomic, const DwOutputs &o, cudaStream_t s, P
     }
     if (atomic) {
         if (!o.cast_1 && !o.cast_2) return RN_OK;
+        // (the atomic mode runs only with the fp32 buffers of every requested output)
         e = launch_cast(o.f32_1, o.cast_1, o.N, o.dtype, s, !prof, o.f32_2, o.cast_2);
         return e == cudaSuccess ? RN_OK : cuda_fail(e, "cast launch");
     }
+    if (!o.f32_1 && !o.cast_1 && !o.f32_2 && !o.cast_2) return RN_OK;  // no weight gradient asked
     e = launch_finalize2(o.partials, o.G, o.ld, o.N, o.f32_1, o.cast_1, o.f32_2, o.cast_2, o.dtype,
                          s, !prof);
     return e == cudaSuccess ? RN_OK : cuda_fail(e, "finalize launch");
@@ -557,8 +560,9 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
         return fail(RN_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
 
     if (p.M == 0) {
-        e = launch_finalize(nullptr, 0, p.N, p.dw_f32, p.dw_cast, p.dtype, s, false);
         snprintf(g_plan, sizeof(g_plan), "empty batch: finalize only");
+        if (!p.dw_f32 && !p.dw_cast) return RN_OK;
+        e = launch_finalize(nullptr, 0, p.N, p.dw_f32, p.dw_cast, p.dtype, s, false);
         return e == cudaSuccess ? RN_OK : cuda_fail(e, "finalize launch");
     }
 
@@ -728,9 +732,10 @@ static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t
     const float *partials = reinterpret_cast<const float *>(p.ws + kWsHeaderBytes);
 
     if (p.M == 0) {
+        snprintf(g_plan, sizeof(g_plan), "empty batch: finalize only");
+        if (!p.dg_f32 && !p.dg_cast && !p.db_f32 && !p.db_cast) return RN_OK;
         e = launch_finalize2(nullptr, 0, 2 * p.N, p.N, p.dg_f32, p.dg_cast, p.db_f32, p.db_cast,
                              p.dtype, s, false);
-        snprintf(g_plan, sizeof(g_plan), "empty batch: finalize only");
         return e == cudaSuccess ? RN_OK : cuda_fail(e, "finalize launch");
     }
 
@@ -739,7 +744,9 @@ static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t
     GenericPlan gp;
     ClusterPlan cp;
     bool use_row = false, use_cluster = false;
-    bool atomic = g_opts[RN_OPT_DWEIGHT_MODE] != 1 && aligned16(p.dg_f32) &&
+    // atomics need the fp32 buffer of every requested output
+    bool atomic = g_opts[RN_OPT_DWEIGHT_MODE] != 1 && p.dg_f32 != nullptr &&
+                  aligned16(p.dg_f32) && (p.db_cast == nullptr || p.db_f32 != nullptr) &&
                   (p.db_f32 == nullptr || aligned16(p.db_f32));
     if (engine == 0 || engine == 1) {
         use_row = plan_ln_row(p, d, &rp);
@@ -817,7 +824,7 @@ static rn_status bwd_entry(const void *x, const void *gamma, const void *dy, con
     g_plan[0] = 0;
     rn_status st = check_common(M, N, dtype);
     if (st != RN_OK) return st;
-    if (!gamma || !dw_f32) return fail(RN_ERR_INVALID_ARG, "gamma and dweight_f32 are required");
+    if (!gamma) return fail(RN_ERR_INVALID_ARG, "gamma is required");
     if (M > 0 && (!x || !dy || !rstd || !dx))
         return fail(RN_ERR_INVALID_ARG, "x, dy, rstd and dx are required when M > 0");
     if (M > 0 && (dx == x || dx == dy || (void *)dx == (void *)rstd))
@@ -979,9 +986,9 @@ static rn_status ln_bwd_entry(const void *x, const void *gamma, const void *dy, 
     g_plan[0] = 0;
     rn_status st = check_common(M, N, dtype);
     if (st != RN_OK) return st;
-    if (!gamma || !dg_f32) return fail(RN_ERR_INVALID_ARG, "gamma and dgamma_f32 are required");
-    if (db_cast && !db_f32) return fail(RN_ERR_INVALID_ARG, "dbeta needs dbeta_f32");
-    if (db_f32 == dg_f32) return fail(RN_ERR_INVALID_ARG, "dbeta_f32 must not alias dgamma_f32");
+    if (!gamma) return fail(RN_ERR_INVALID_ARG, "gamma is required");
+    if (db_f32 && db_f32 == dg_f32)
+        return fail(RN_ERR_INVALID_ARG, "dbeta_f32 must not alias dgamma_f32");
     if (M > 0 && (!x || !dy || !mean || !rstd || !dx))
         return fail(RN_ERR_INVALID_ARG, "x, dy, mean, rstd and dx are required when M > 0");
     if (M > 0 && (dx == x || dx == dy || (void *)dx == (void *)mean || (void *)dx == (void *)rstd))

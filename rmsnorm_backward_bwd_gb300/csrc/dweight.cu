@@ -5,7 +5,8 @@
 // experiment").
 //
 //  * finalize: dweight_f32[j] = sum over the G partial rows, in a fixed
-//    order (deterministic), and the cast to the I/O dtype in the same pass.
+//    order (deterministic), and the cast to the I/O dtype in the same pass
+//    (either output may be absent).
 //    A CTA covers 32 columns with 32 x 32 threads: thread (cx, gy) sums rows
 //    gy, gy+32, ... of column cx; a fixed-shape tree in shared memory then
 //    adds the 32 column sums.
@@ -30,7 +31,7 @@ __global__ void __launch_bounds__(1024) finalize_kernel(const float *__restrict_
     __shared__ float sm[32][33];
     const int cx = threadIdx.x, gy = threadIdx.y;
     const int col = blockIdx.x * 32 + cx;
-    const int ncols = dw2_f32 ? 2 * N : N;
+    const int ncols = (dw2_f32 || dw2_cast) ? 2 * N : N;
     pdl_wait();  // the row pass has finished writing its partial rows
     float s = 0.f;
     if (col < ncols) {
@@ -57,10 +58,10 @@ __global__ void __launch_bounds__(1024) finalize_kernel(const float *__restrict_
     if (gy == 0 && col < ncols) {
         const float v = sm[0][cx];
         if (col < N) {
-            dw_f32[col] = v;
+            if (dw_f32) dw_f32[col] = v;
             if (dw_cast) dw_cast[col] = from_f<T>(v);
         } else {
-            dw2_f32[col - N] = v;
+            if (dw2_f32) dw2_f32[col - N] = v;
             if (dw2_cast) dw2_cast[col - N] = from_f<T>(v);
         }
     }
@@ -103,7 +104,7 @@ static cudaError_t launch_ex(K kern, dim3 grid, dim3 block, cudaStream_t s, bool
 cudaError_t launch_finalize2(const float *partials, int G, int ld, int N, float *dw_f32,
                              void *dw_cast, float *dw2_f32, void *dw2_cast, int dtype,
                              cudaStream_t s, bool pdl) {
-    const int ncols = dw2_f32 ? 2 * N : N;
+    const int ncols = (dw2_f32 || dw2_cast) ? 2 * N : N;
     dim3 grid((ncols + 31) / 32), block(32, 32);
     switch (dtype) {
     case kF32:

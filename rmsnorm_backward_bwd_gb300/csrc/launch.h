@@ -89,11 +89,12 @@ size_t cluster_smem_bytes(int stages, int ntensors, int cpt, int threads);
 cudaError_t cluster_max_active(const BwdProblem &p, const ClusterPlan &plan, int *clusters);
 cudaError_t launch_bwd_cluster(const BwdProblem &p, const ClusterPlan &plan, cudaStream_t s,
                                bool pdl_after_zero);
-// Scratch mode: dw_f32 = sum of G partial rows (fixed order), optional cast.
+// Scratch mode: dw_f32 = sum of G partial rows (fixed order), optional cast;
+// either output may be NULL.
 cudaError_t launch_finalize(const float *partials, int G, int N, float *dw_f32, void *dw_cast,
                             int dtype, cudaStream_t s, bool pdl);
 // The same over partial rows of ld floats holding two length-N outputs side
-// by side (dw2_f32 nullable: one output).
+// by side (dw2_f32 and dw2_cast both NULL: one output).
 cudaError_t launch_finalize2(const float *partials, int G, int ld, int N, float *dw_f32,
                              void *dw_cast, float *dw2_f32, void *dw2_cast, int dtype,
                              cudaStream_t s, bool pdl);

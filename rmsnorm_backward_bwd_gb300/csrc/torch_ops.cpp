@@ -151,10 +151,13 @@ std::tuple<Tensor, Tensor, Tensor> fused_add_rmsnorm_fwd(const Tensor &x, const 
 }
 
 // Shared by both RMSNorm backward calls; dres undefined = none.
-// Returns (dx, dweight [undefined unless want_cast], dweight_f32).
+// Returns (dx, dweight [undefined unless want_cast], dweight_f32 [undefined
+// unless want_f32]). Without the fp32 output the library sums the weight
+// gradient in its deterministic scratch mode (one launch fewer); without
+// either, no weight gradient is computed.
 std::tuple<Tensor, Tensor, Tensor> rms_bwd(const Tensor &x, const Tensor &w, const Tensor &dy,
                                            const Tensor &rstd, const Tensor &dres,
-                                           bool want_cast, bool fused) {
+                                           bool want_cast, bool fused, bool want_f32) {
     const char *xname = fused ? "added" : "x";
     need(xname, x, x, x.scalar_type());
     need("weight", w, x, x.scalar_type());
@@ -168,34 +171,36 @@ std::tuple<Tensor, Tensor, Tensor> rms_bwd(const Tensor &x, const Tensor &w, con
     check(rn_bwd_workspace_bytes(M, N, code, &ws_bytes), "rn_bwd_workspace_bytes");
     Tensor ws = workspace(ws_bytes, x);
     Tensor dx = at::empty(x.sizes(), x.options());
-    Tensor dw32 = f32_vector(N, x);
+    Tensor dw32 = want_f32 ? f32_vector(N, x) : Tensor();
     Tensor dw = want_cast ? at::empty({N}, x.options()) : Tensor();
     void *dwp = want_cast ? dw.data_ptr() : nullptr;
+    float *dw32p = want_f32 ? dw32.data_ptr<float>() : nullptr;
     if (fused)
         check(rn_fused_add_rmsnorm_bwd(x.data_ptr(), w.data_ptr(), dy.data_ptr(),
                                        rstd.data_ptr<float>(),
                                        dres.defined() ? dres.data_ptr() : nullptr, dx.data_ptr(),
-                                       dw32.data_ptr<float>(), dwp, ws.data_ptr(), ws_bytes, M, N,
-                                       code, stream_of(x)),
+                                       dw32p, dwp, ws.data_ptr(), ws_bytes, M, N, code,
+                                       stream_of(x)),
               "rn_fused_add_rmsnorm_bwd");
     else
         check(rn_rmsnorm_bwd(x.data_ptr(), w.data_ptr(), dy.data_ptr(), rstd.data_ptr<float>(),
-                             dx.data_ptr(), dw32.data_ptr<float>(), dwp, ws.data_ptr(), ws_bytes,
-                             M, N, code, stream_of(x)),
+                             dx.data_ptr(), dw32p, dwp, ws.data_ptr(), ws_bytes, M, N, code,
+                             stream_of(x)),
               "rn_rmsnorm_bwd");
     return {dx, dw, dw32};
 }
 
 std::tuple<Tensor, Tensor, Tensor> rmsnorm_bwd(const Tensor &x, const Tensor &w, const Tensor &dy,
-                                               const Tensor &rstd, bool want_cast) {
-    return rms_bwd(x, w, dy, rstd, Tensor(), want_cast, false);
+                                               const Tensor &rstd, bool want_cast, bool want_f32) {
+    return rms_bwd(x, w, dy, rstd, Tensor(), want_cast, false, want_f32);
 }
 
 std::tuple<Tensor, Tensor, Tensor> fused_add_rmsnorm_bwd(const Tensor &added, const Tensor &w,
                                                          const Tensor &dy, const Tensor &rstd,
                                                          const c10::optional<Tensor> &dres,
-                                                         bool want_cast) {
-    return rms_bwd(added, w, dy, rstd, dres.has_value() ? *dres : Tensor(), want_cast, true);
+                                                         bool want_cast, bool want_f32) {
+    return rms_bwd(added, w, dy, rstd, dres.has_value() ? *dres : Tensor(), want_cast, true,
+                   want_f32);
 }
 
 std::tuple<Tensor, Tensor, Tensor> layernorm_fwd(const Tensor &x, const Tensor &w,
@@ -216,10 +221,11 @@ std::tuple<Tensor, Tensor, Tensor> layernorm_fwd(const Tensor &x, const Tensor &
 }
 
 // Returns (dx, dgamma, dbeta, dgamma_f32, dbeta_f32); the casts are
-// undefined unless want_cast, the dbeta pair unless want_dbeta.
+// undefined unless want_cast, the fp32 sums unless want_f32, the dbeta pair
+// unless want_dbeta.
 std::tuple<Tensor, Tensor, Tensor, Tensor, Tensor> layernorm_bwd(
     const Tensor &x, const Tensor &w, const Tensor &dy, const Tensor &mean, const Tensor &rstd,
-    bool want_dbeta, bool want_cast) {
+    bool want_dbeta, bool want_cast, bool want_f32) {
     need("x", x, x, x.scalar_type());
     need("weight", w, x, x.scalar_type());
     need("dy", dy, x, x.scalar_type(), x.sizes(), true);
@@ -233,13 +239,14 @@ std::tuple<Tensor, Tensor, Tensor, Tensor, Tensor> layernorm_bwd(
           "rn_layernorm_bwd_workspace_bytes");
     Tensor ws = workspace(ws_bytes, x);
     Tensor dx = at::empty(x.sizes(), x.options());
-    Tensor dg32 = f32_vector(N, x);
-    Tensor db32 = want_dbeta ? f32_vector(N, x) : Tensor();
+    Tensor dg32 = want_f32 ? f32_vector(N, x) : Tensor();
+    Tensor db32 = want_f32 && want_dbeta ? f32_vector(N, x) : Tensor();
     Tensor dg = want_cast ? at::empty({N}, x.options()) : Tensor();
     Tensor db = want_cast && want_dbeta ? at::empty({N}, x.options()) : Tensor();
     check(rn_layernorm_bwd(x.data_ptr(), w.data_ptr(), dy.data_ptr(), mean.data_ptr<float>(),
-                           rstd.data_ptr<float>(), dx.data_ptr(), dg32.data_ptr<float>(),
-                           want_dbeta ? db32.data_ptr<float>() : nullptr,
+                           rstd.data_ptr<float>(), dx.data_ptr(),
+                           dg32.defined() ? dg32.data_ptr<float>() : nullptr,
+                           db32.defined() ? db32.data_ptr<float>() : nullptr,
                            dg.defined() ? dg.data_ptr() : nullptr,
                            db.defined() ? db.data_ptr() : nullptr, ws.data_ptr(), ws_bytes, M, N,
                            code, stream_of(x)),
@@ -282,16 +289,19 @@ struct RMSNormFunction : public torch::autograd::Function<RMSNormFunction> {
     static tensor_list backward(AutogradContext *ctx, tensor_list grads) {
         static auto op = raw<std::tuple<Tensor, Tensor, Tensor>(const Tensor &, const Tensor &,
                                                                 const Tensor &, const Tensor &,
-                                                                bool)>("rn_gb300::rmsnorm_bwd");
+                                                                bool, bool)>(
+            "rn_gb300::rmsnorm_bwd");
         BelowAutograd below;
         const auto saved = ctx->get_saved_variables();
         const bool need_x = ctx->needs_input_grad(0), need_w = ctx->needs_input_grad(1);
         if (!(need_x || need_w)) return {Tensor(), Tensor(), Tensor()};
         const Tensor &x2 = saved[0];
-        // an fp32 weight takes the fp32 accumulator itself: no cast launch
+        // an fp32 weight takes the fp32 sum itself (no cast launch); a 16-bit one only the
+        // cast (no fp32 output: the deterministic two-launch path); none when the weight
+        // needs no gradient
         const bool f32 = x2.scalar_type() == at::kFloat;
         auto [dx, dw, dw32] = op.call(x2, saved[1], rows2d(grads[0], x2.size(1)), saved[2],
-                                      need_w && !f32);
+                                      need_w && !f32, need_w && f32);
         const auto shape = ctx->saved_data["shape"].toIntVector();
         return {need_x ? dx.view(shape) : Tensor(), need_w ? (f32 ? dw32 : dw) : Tensor(),
                 Tensor()};
@@ -320,7 +330,7 @@ struct FusedAddRMSNormFunction : public torch::autograd::Function<FusedAddRMSNor
     static tensor_list backward(AutogradContext *ctx, tensor_list grads) {
         static auto op = raw<std::tuple<Tensor, Tensor, Tensor>(
             const Tensor &, const Tensor &, const Tensor &, const Tensor &,
-            const c10::optional<Tensor> &, bool)>("rn_gb300::fused_add_rmsnorm_bwd");
+            const c10::optional<Tensor> &, bool, bool)>("rn_gb300::fused_add_rmsnorm_bwd");
         BelowAutograd below;
         const auto saved = ctx->get_saved_variables();
         const bool need_x = ctx->needs_input_grad(0), need_r = ctx->needs_input_grad(1),
@@ -340,7 +350,7 @@ struct FusedAddRMSNormFunction : public torch::autograd::Function<FusedAddRMSNor
         if (d_res.defined()) dres = rows2d(d_res, N);
         const bool f32 = added.scalar_type() == at::kFloat;
         auto [dx, dw, dw32] = op.call(added, saved[1], rows2d(d_out, N), saved[2], dres,
-                                      need_w && !f32);
+                                      need_w && !f32, need_w && f32);
         const auto shape = ctx->saved_data["shape"].toIntVector();
         const Tensor g = dx.view(shape);
         return {need_x ? g : Tensor(), need_r ? g : Tensor(),
@@ -371,7 +381,7 @@ struct LayerNormFunction : public torch::autograd::Function<LayerNormFunction> {
     static tensor_list backward(AutogradContext *ctx, tensor_list grads) {
         static auto op = raw<std::tuple<Tensor, Tensor, Tensor, Tensor, Tensor>(
             const Tensor &, const Tensor &, const Tensor &, const Tensor &, const Tensor &, bool,
-            bool)>("rn_gb300::layernorm_bwd");
+            bool, bool)>("rn_gb300::layernorm_bwd");
         BelowAutograd below;
         const auto saved = ctx->get_saved_variables();
         const bool need_x = ctx->needs_input_grad(0), need_w = ctx->needs_input_grad(1);
@@ -381,7 +391,8 @@ struct LayerNormFunction : public torch::autograd::Function<LayerNormFunction> {
         const bool f32 = x2.scalar_type() == at::kFloat;
         auto [dx, dg, db, dg32, db32] = op.call(x2, saved[1], rows2d(grads[0], x2.size(1)),
                                                 saved[2], saved[3], need_b,
-                                                (need_w || need_b) && !f32);
+                                                (need_w || need_b) && !f32,
+                                                (need_w || need_b) && f32);
         const auto shape = ctx->saved_data["shape"].toIntVector();
         return {need_x ? dx.view(shape) : Tensor(), need_w ? (f32 ? dg32 : dg) : Tensor(),
                 need_b ? (f32 ? db32 : db) : Tensor(), Tensor()};
@@ -408,16 +419,17 @@ Tensor layernorm(const Tensor &x, const Tensor &w, const c10::optional<Tensor> &
 
 TORCH_LIBRARY(rn_gb300, m) {
     m.def("rmsnorm_fwd(Tensor x, Tensor weight, float eps) -> (Tensor, Tensor)");
-    m.def("rmsnorm_bwd(Tensor x, Tensor weight, Tensor dy, Tensor rstd, bool want_cast) "
-          "-> (Tensor, Tensor, Tensor)");
+    m.def("rmsnorm_bwd(Tensor x, Tensor weight, Tensor dy, Tensor rstd, bool want_cast, "
+          "bool want_f32=True) -> (Tensor, Tensor, Tensor)");
     m.def("fused_add_rmsnorm_fwd(Tensor x, Tensor residual, Tensor weight, float eps) "
           "-> (Tensor, Tensor, Tensor)");
     m.def("fused_add_rmsnorm_bwd(Tensor added, Tensor weight, Tensor dy, Tensor rstd, "
-          "Tensor? dresidual_out, bool want_cast) -> (Tensor, Tensor, Tensor)");
+          "Tensor? dresidual_out, bool want_cast, bool want_f32=True) -> (Tensor, Tensor, Tensor)");
     m.def("layernorm_fwd(Tensor x, Tensor weight, Tensor? bias, float eps) "
           "-> (Tensor, Tensor, Tensor)");
     m.def("layernorm_bwd(Tensor x, Tensor weight, Tensor dy, Tensor mean, Tensor rstd, "
-          "bool want_dbeta, bool want_cast) -> (Tensor, Tensor, Tensor, Tensor, Tensor)");
+          "bool want_dbeta, bool want_cast, bool want_f32=True) "
+          "-> (Tensor, Tensor, Tensor, Tensor, Tensor)");
     m.def("rmsnorm(Tensor x, Tensor weight, float eps) -> Tensor");
     m.def("fused_add_rmsnorm(Tensor x, Tensor residual, Tensor weight, float eps) "
           "-> (Tensor, Tensor)");

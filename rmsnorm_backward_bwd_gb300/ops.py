@@ -186,10 +186,12 @@ def fused_add_rmsnorm_fwd(x, residual, gamma, eps, *, out=None, residual_out=Non
     return out, residual_out, rstd
 
 
-def _bwd_outputs(x, M, N, dx, dweight_f32, dweight, want_cast):
+def _bwd_outputs(x, M, N, dx, dweight_f32, dweight, want_cast, want_f32):
     dx = torch.empty_like(x) if dx is None else _need("dx", dx, x, x.shape)
-    dweight_f32 = (torch.empty(N, dtype=torch.float32, device=x.device) if dweight_f32 is None
-                   else _need("dweight_f32", dweight_f32, x, (N,), torch.float32))
+    if dweight_f32 is not None:
+        _need("dweight_f32", dweight_f32, x, (N,), torch.float32)
+    elif want_f32:
+        dweight_f32 = torch.empty(N, dtype=torch.float32, device=x.device)
     if dweight is None and want_cast:
         dweight = torch.empty(N, dtype=x.dtype, device=x.device)
     elif dweight is not None:
@@ -198,17 +200,20 @@ def _bwd_outputs(x, M, N, dx, dweight_f32, dweight, want_cast):
 
 
 def rmsnorm_bwd(x, gamma, dy, rstd, *, dx=None, dweight_f32=None, dweight=None,
-                want_cast=True, workspace=None):
+                want_cast=True, want_f32=True, workspace=None):
     """Gradients of y = rmsnorm(x) * gamma given dy and the saved fp32 rstd.
-    Returns (dx, dweight, dweight_f32); dweight is dweight_f32 cast to the
-    I/O dtype (None when want_cast is False and no buffer was passed)."""
+    Returns (dx, dweight, dweight_f32); dweight is the weight gradient cast
+    to the I/O dtype (None when want_cast is False and no buffer was passed),
+    dweight_f32 its fp32 sum (None when want_f32 is False and no buffer was
+    passed: the library then sums in its deterministic scratch mode)."""
     _need("x", x, x)
     _need("gamma", gamma, x)
     _need("dy", dy, x, x.shape)
     M, N = _rows(x, gamma)
     _need("rstd", rstd, x, (M,), torch.float32)
     with _on_device(x.get_device()):
-        dx, dweight_f32, dweight = _bwd_outputs(x, M, N, dx, dweight_f32, dweight, want_cast)
+        dx, dweight_f32, dweight = _bwd_outputs(x, M, N, dx, dweight_f32, dweight, want_cast,
+                                                want_f32)
         ws = _workspace(M, N, _code(x), x.get_device()) if workspace is None else workspace
         native.check(native.lib().rn_rmsnorm_bwd(
             _ptr(x), _ptr(gamma), _ptr(dy), _ptr(rstd), _ptr(dx), _ptr(dweight_f32),
@@ -217,7 +222,8 @@ def rmsnorm_bwd(x, gamma, dy, rstd, *, dx=None, dweight_f32=None, dweight=None,
 
 
 def fused_add_rmsnorm_bwd(added, gamma, dy, rstd, dresidual_out=None, *, dx=None,
-                          dweight_f32=None, dweight=None, want_cast=True, workspace=None):
+                          dweight_f32=None, dweight=None, want_cast=True, want_f32=True,
+                          workspace=None):
     """Backward of the fused-add (prenorm) RMSNorm. `added` is the saved
     residual_out; dresidual_out (may be None) is the gradient flowing into
     residual_out. Returns (dx, dresidual, dweight, dweight_f32) where
@@ -230,7 +236,8 @@ def fused_add_rmsnorm_bwd(added, gamma, dy, rstd, dresidual_out=None, *, dx=None
     if dresidual_out is not None:
         _need("dresidual_out", dresidual_out, added, added.shape)
     with _on_device(added.get_device()):
-        dx, dweight_f32, dweight = _bwd_outputs(added, M, N, dx, dweight_f32, dweight, want_cast)
+        dx, dweight_f32, dweight = _bwd_outputs(added, M, N, dx, dweight_f32, dweight, want_cast,
+                                                want_f32)
         ws = (_workspace(M, N, _code(added), added.get_device()) if workspace is None
               else workspace)
         native.check(native.lib().rn_fused_add_rmsnorm_bwd(
@@ -266,11 +273,13 @@ def layernorm_fwd(x, gamma, beta, eps, *, y=None, mean=None, rstd=None, store_st
 
 
 def layernorm_bwd(x, gamma, dy, mean, rstd, *, dx=None, dgamma_f32=None, dbeta_f32=None,
-                  dgamma=None, dbeta=None, want_dbeta=True, want_cast=True, workspace=None):
+                  dgamma=None, dbeta=None, want_dbeta=True, want_cast=True, want_f32=True,
+                  workspace=None):
     """Gradients of y = layernorm(x) * gamma (+ beta) given dy and the saved
     fp32 mean and rstd. Returns (dx, dgamma, dbeta, dgamma_f32, dbeta_f32):
-    the casts to the I/O dtype are None when want_cast is False (and no buffer
-    was passed); the dbeta pair is None when want_dbeta is False."""
+    the casts to the I/O dtype are None when want_cast is False, the fp32
+    sums when want_f32 is False (and no buffer was passed); the dbeta pair is
+    None when want_dbeta is False."""
     _need("x", x, x)
     _need("gamma", gamma, x)
     _need("dy", dy, x, x.shape)
@@ -280,11 +289,15 @@ def layernorm_bwd(x, gamma, dy, mean, rstd, *, dx=None, dgamma_f32=None, dbeta_f
     with _on_device(x.get_device()):
         dx = torch.empty_like(x) if dx is None else _need("dx", dx, x, x.shape)
         f32 = dict(dtype=torch.float32, device=x.device)
-        dgamma_f32 = (torch.empty(N, **f32) if dgamma_f32 is None
-                      else _need("dgamma_f32", dgamma_f32, x, (N,), torch.float32))
+        if dgamma_f32 is not None:
+            _need("dgamma_f32", dgamma_f32, x, (N,), torch.float32)
+        elif want_f32:
+            dgamma_f32 = torch.empty(N, **f32)
         if want_dbeta:
-            dbeta_f32 = (torch.empty(N, **f32) if dbeta_f32 is None
-                         else _need("dbeta_f32", dbeta_f32, x, (N,), torch.float32))
+            if dbeta_f32 is not None:
+                _need("dbeta_f32", dbeta_f32, x, (N,), torch.float32)
+            elif want_f32:
+                dbeta_f32 = torch.empty(N, **f32)
         else:
             dbeta_f32 = dbeta = None
         if dgamma is None and want_cast:

@@ -44,20 +44,22 @@ class OracleKernels:
         return (torch.from_numpy(out).to(x.dtype), torch.from_numpy(added).to(x.dtype),
                 torch.from_numpy(oracle.round_to(rstd, "f32")).to(torch.float32))
 
-    def rmsnorm_bwd(self, x, gamma, dy, rstd, want_cast):
-        self.calls.append(("bwd", tuple(x.shape), want_cast))
+    def rmsnorm_bwd(self, x, gamma, dy, rstd, want_cast, want_f32=True):
+        self.calls.append(("bwd", tuple(x.shape), want_cast, want_f32))
         assert dy.is_contiguous() and dy.shape == x.shape
         dx, dw = oracle.rmsnorm_bwd(_np(x), _np(gamma), _np(dy), _np(rstd))
         dw32 = torch.from_numpy(dw).to(torch.float32)
-        return (torch.from_numpy(dx).to(x.dtype), dw32.to(x.dtype) if want_cast else None, dw32)
+        return (torch.from_numpy(dx).to(x.dtype), dw32.to(x.dtype) if want_cast else None,
+                dw32 if want_f32 else None)
 
-    def fused_add_rmsnorm_bwd(self, added, gamma, dy, rstd, dres, want_cast):
-        self.calls.append(("fused_bwd", tuple(added.shape), dres is not None, want_cast))
+    def fused_add_rmsnorm_bwd(self, added, gamma, dy, rstd, dres, want_cast, want_f32=True):
+        self.calls.append(("fused_bwd", tuple(added.shape), dres is not None, want_cast,
+                           want_f32))
         dx, dw = oracle.fused_add_rmsnorm_bwd(_np(added), _np(gamma), _np(dy), _np(rstd),
                                               None if dres is None else _np(dres))
         dx = torch.from_numpy(dx).to(added.dtype)
         dw32 = torch.from_numpy(dw).to(torch.float32)
-        return dx, dw32.to(added.dtype) if want_cast else None, dw32
+        return dx, dw32.to(added.dtype) if want_cast else None, dw32 if want_f32 else None
 
     def layernorm_fwd(self, x, gamma, beta, eps):
         self.calls.append(("ln_fwd", tuple(x.shape), beta is not None))
@@ -66,13 +68,14 @@ class OracleKernels:
         f32 = lambda a: torch.from_numpy(oracle.round_to(a, "f32")).to(torch.float32)  # noqa: E731
         return torch.from_numpy(y).to(x.dtype), f32(mean), f32(rstd)
 
-    def layernorm_bwd(self, x, gamma, dy, mean, rstd, want_dbeta, want_cast):
-        self.calls.append(("ln_bwd", tuple(x.shape), want_dbeta, want_cast))
+    def layernorm_bwd(self, x, gamma, dy, mean, rstd, want_dbeta, want_cast, want_f32=True):
+        self.calls.append(("ln_bwd", tuple(x.shape), want_dbeta, want_cast, want_f32))
         dx, dg, db = oracle.layernorm_bwd(_np(x), _np(gamma), _np(dy), _np(mean), _np(rstd))
         dg32 = torch.from_numpy(dg).to(torch.float32)
         db32 = torch.from_numpy(db).to(torch.float32) if want_dbeta else None
         return (torch.from_numpy(dx).to(x.dtype), dg32.to(x.dtype) if want_cast else None,
-                db32.to(x.dtype) if (want_cast and want_dbeta) else None, dg32, db32)
+                db32.to(x.dtype) if (want_cast and want_dbeta) else None,
+                dg32 if want_f32 else None, db32 if want_f32 else None)
 
 
 _RAW = ("rmsnorm_fwd", "rmsnorm_bwd", "fused_add_rmsnorm_fwd", "fused_add_rmsnorm_bwd",
@@ -131,23 +134,24 @@ def test_rmsnorm_grads_any_rank(fake, shape):
     _close(xa.grad, x64.grad)
     _close(wa.grad, w64.grad)
     M = int(np.prod(shape[:-1]))
-    # fp32 weight: its gradient is the fp32 accumulator itself (no cast asked for)
-    assert fake.calls == [("fwd", (M, shape[-1])), ("bwd", (M, shape[-1]), False)]
+    # fp32 weight: its gradient is the fp32 sum itself (no cast asked for)
+    assert fake.calls == [("fwd", (M, shape[-1])), ("bwd", (M, shape[-1]), False, True)]
 
 
 def test_bf16_weight_gradient_is_the_cast(fake):
-    """A 16-bit weight's gradient is the fp32 accumulator cast to its dtype;
-    an fp32 weight's is the accumulator itself."""
+    """A 16-bit weight's gradient is the cast alone (no fp32 output is asked
+    for, so the library takes its two-launch scratch path); an fp32 weight's
+    is the fp32 sum itself."""
     x, r, w, dy, _ = _draw((4, 32), seed=6)
     for dt, cast in ((torch.bfloat16, True), (torch.float32, False)):
         xa = x.to(dt).requires_grad_()
         wa = w.to(dt).requires_grad_()
         (rn.rmsnorm(xa, wa, 1e-6) * dy.to(dt)).sum().backward()
-        assert fake.calls[-1] == ("bwd", (4, 32), cast)
+        assert fake.calls[-1] == ("bwd", (4, 32), cast, not cast)
         assert wa.grad.dtype == dt
         out, _ = rn.fused_add_rmsnorm(xa.detach().requires_grad_(), r.to(dt), wa, 1e-6)
         (out * dy.to(dt)).sum().backward()
-        assert fake.calls[-1] == ("fused_bwd", (4, 32), False, cast)
+        assert fake.calls[-1] == ("fused_bwd", (4, 32), False, cast, not cast)
 
 
 def test_rmsnorm_weight_grad_not_needed(fake):
@@ -155,7 +159,8 @@ def test_rmsnorm_weight_grad_not_needed(fake):
     xa = x.clone().requires_grad_()
     y = rn.rmsnorm(xa, w, 1e-6)
     y.backward(dy)
-    assert fake.calls[-1] == ("bwd", (4, 32), False)
+    # no weight gradient asked for at all
+    assert fake.calls[-1] == ("bwd", (4, 32), False, False)
     assert xa.grad is not None
 
 
@@ -216,7 +221,7 @@ def test_fused_prenorm_false_returns_out_only(fake):
     (out * dy).sum().backward()
     _, _, gx, _, _ = _fused_reference(x, r, w, dy, dy, 1e-6, True, False)
     _close(xa.grad, gx)
-    assert fake.calls[-1] == ("fused_bwd", (3, 16), False, False)
+    assert fake.calls[-1] == ("fused_bwd", (3, 16), False, False, False)
 
 
 def test_real_calls_refuse_cpu_tensors():
@@ -259,7 +264,7 @@ def test_layernorm_grads(fake, shape, with_bias):
         _close(ba.grad, b64.grad)
     M = int(np.prod(shape[:-1]))
     assert fake.calls == [("ln_fwd", (M, shape[-1]), with_bias),
-                          ("ln_bwd", (M, shape[-1]), with_bias, False)]   # fp32: no cast
+                          ("ln_bwd", (M, shape[-1]), with_bias, False, True)]   # fp32: no cast
 
 
 def test_layernorm_only_x_grad(fake):
@@ -267,7 +272,7 @@ def test_layernorm_only_x_grad(fake):
     xa = x.clone().requires_grad_()
     rn.layernorm(xa, w, b[0]).backward(dy)
     # neither weight nor bias needs a gradient: no dbeta, no casts
-    assert fake.calls[-1] == ("ln_bwd", (4, 16), False, False)
+    assert fake.calls[-1] == ("ln_bwd", (4, 16), False, False, False)
     x64 = x.double().requires_grad_()
     (_torch_ln(x64, w.double(), b[0].double(), 1e-5) * dy.double()).sum().backward()
     _close(xa.grad, x64.grad)

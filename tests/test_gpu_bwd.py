@@ -503,3 +503,60 @@ def test_generic_engines_empty_batch():
         dx, dw, dw32 = rn.rmsnorm_bwd(x, g, x, torch.empty(0, device="cuda"))
         torch.cuda.synchronize()
         assert dx.shape == (0, N) and torch.count_nonzero(dw32).item() == 0
+
+
+def _run_kw(ex, **kw):
+    import rmsnorm_backward_bwd_gb300 as rn
+    x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
+    if ex.case.fused:
+        dres = ex.dres.cuda() if ex.dres is not None else None
+        dx, _, dw, dw32 = rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, dres, **kw)
+    else:
+        dx, dw, dw32 = rn.rmsnorm_bwd(x, g, dy, rstd, **kw)
+    torch.cuda.synchronize()
+    return dx, dw, dw32
+
+
+@pytest.mark.parametrize("case", [
+    synth.PLAIN_4096, synth.FUSED_4096, Case("bf16 M=33 N=4095", 33, 4095, "bf16"),
+    Case("f16 M=9 N=40000 fused", 9, 40000, "f16", fused=True, with_dres=True),
+    Case("bf16 M=300 N=12290", 300, 12290, "bf16"), Case("bf16 M=5 N=70001", 5, 70001, "bf16")],
+    ids=lambda c: c.name)
+def test_cast_only_weight_gradient_takes_the_scratch_mode(case):
+    """dweight_f32 = NULL with dweight given: the fp32 sum is not stored and
+    the scratch mode runs even with atomics forced; dweight matches the oracle
+    and equals, bit for bit, the cast of the scratch mode's fp32 sum (the same
+    fixed summation order)."""
+    ex = parity.expected_bwd(case)
+    native.set_option(native.OPT_DWEIGHT_MODE, 2)
+    dx, dw, dw32 = _run_kw(ex, want_f32=False)
+    plan = native.last_plan()
+    assert dw32 is None and "dw=scratch" in plan, plan
+    n_esc = parity.check_tensor("dx", dx, ex.dx, case.dtype, "dx",
+                                roundoff=parity.roundoff_bound(ex))
+    assert n_esc == 0
+    parity.check_tensor("dweight", dw, ex.dw, case.dtype, "dweight")
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)
+    dx1, dw1, _ = _run_kw(ex)
+    assert torch.equal(dx, dx1) and torch.equal(dw, dw1)
+
+
+def test_no_weight_gradient_asked():
+    """Neither dweight_f32 nor dweight: dx alone, no weight gradient."""
+    ex = parity.expected_bwd(Case("bf16 M=777 N=4096 fused", 777, 4096, "bf16", fused=True,
+                                  with_dres=True))
+    dx, dw, dw32 = _run_kw(ex, want_f32=False, want_cast=False)
+    assert dw is None and dw32 is None
+    assert parity.check_tensor("dx", dx, ex.dx, "bf16", "dx",
+                               roundoff=parity.roundoff_bound(ex)) == 0
+
+
+def test_cast_only_empty_batch():
+    import rmsnorm_backward_bwd_gb300 as rn
+    x = torch.empty(0, 4095, dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(4095, dtype=torch.bfloat16, device="cuda")
+    dw = torch.full((4095,), 7.0, dtype=torch.bfloat16, device="cuda")
+    dx, dw, dw32 = rn.rmsnorm_bwd(x, g, x, torch.empty(0, device="cuda"), dweight=dw,
+                                  want_f32=False)
+    torch.cuda.synchronize()
+    assert dw32 is None and torch.count_nonzero(dw).item() == 0

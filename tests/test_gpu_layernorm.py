@@ -385,3 +385,28 @@ def test_layernorm_mismatched_phases_take_the_scalar_generic_kernel():
     plan = native.last_plan()
     assert plan.startswith("engine=ln_generic") and "vec" not in plan, plan
     check(ex, out)
+
+
+@pytest.mark.parametrize("M,N,dt", [(4096, 4096, "bf16"), (33, 4095, "f16"), (7, 40000, "bf16"),
+                                    (64, 3000, "f32")], ids=lambda v: str(v))
+def test_layernorm_casts_without_fp32_outputs(M, N, dt):
+    """dgamma and dbeta asked for without their fp32 buffers: the scratch mode
+    runs (even with atomics forced) and the casts match the oracle and the
+    scratch mode's own casts bit for bit."""
+    ex = expected(Case("ln cast only", M, N, dt, eps=1e-5, seed=44))
+    native.set_option(native.OPT_DWEIGHT_MODE, 2)
+    x, g, dy = (ex.inp[k].cuda() for k in ("x", "gamma", "dy"))
+    mean = torch.from_numpy(ex.mean32).float().cuda()
+    rstd = torch.from_numpy(ex.rstd32).float().cuda()
+    dx, dg, db, dg32, db32 = rn.layernorm_bwd(x, g, dy, mean, rstd, want_f32=False)
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert dg32 is None and db32 is None and "dw=scratch" in plan, plan
+    parity.check_tensor("dgamma", dg, ex.dg, dt, "dweight")
+    parity.check_tensor("dbeta", db, ex.db, dt, "dweight")
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)
+    out = rn.layernorm_bwd(x, g, dy, mean, rstd)
+    torch.cuda.synchronize()
+    check(ex, out)
+    assert torch.equal(dx, out[0]) and torch.equal(dg, out[1]) and torch.equal(db, out[2])
+
