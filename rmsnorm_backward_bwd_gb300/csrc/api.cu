@@ -120,7 +120,7 @@ static size_t ws_bytes_for(const DeviceInfo &d, int64_t N) {
 // `max_cpt` caps the default chunks per thread.
 static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int max_cpt,
                           int (*max_threads)(int cpt), const DeviceInfo &d, RowPlan *plan,
-                          bool use_options = true) {
+                          bool use_options = true, size_t ring_soft_cap = 0) {
     if (nchunks > kRowMaxChunks) return false;
     // RN_OPT_* shape the backward only
     auto opt = [&](int o) { return use_options ? g_opts[o] : 0; };
@@ -149,6 +149,8 @@ static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int 
         if (teams > 15) teams = 15;
         // room for at least 2 slots per team
         while (teams > 1 && smem_for(teams, 2) > budget) --teams;
+        // a softer cap on the ring while at least 3 teams remain
+        while (ring_soft_cap && teams > 3 && smem_for(teams, 2) > ring_soft_cap) --teams;
         // no more teams than rows per SM
         int64_t rows_per_sm = (M + d.num_sms - 1) / d.num_sms;
         if (rows_per_sm < 1) rows_per_sm = 1;
@@ -197,9 +199,14 @@ static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
         (p.dres && !aligned16(p.dres)))
         return false;
     const int nt = p.dres ? 3 : 2;
+    // Measured on GB300 (bf16 fused-add with dresidual_out, 4096-wide rows, us per call): a ring
+    // above ~150 KB costs more than a fourth team gains. 3 teams (147 KB) vs 4 (196 KB): 25.5 vs
+    // 26.1 at M = 4096, 40.0 vs 42.9 at 8192, 79.5 vs 83.2 at 16384, 18.9 vs 19.3 at 2048.
+    // With fewer teams left the larger ring stays (16384 x 8192: 2 teams 159.5, 1 team 173.3).
+    constexpr size_t kRingSoftCap = 160 * 1024;
     // the kernel's reduction slots precede its ring: row_smem_bytes with no ring
     return plan_row_tile(p.M, row_bytes / 16, nt, row_smem_bytes(0, 0, nt, 0), 4,
-                         row_max_threads, d, plan);
+                         row_max_threads, d, plan, true, kRingSoftCap);
 }
 
 // Cluster engine: the row split over `csize` CTAs of up to 2048 chunks each.
