@@ -118,9 +118,16 @@ static size_t ws_bytes_for(const DeviceInfo &d, int64_t N) {
 // Tile of the persistent row engine for rows of `nchunks` 16-byte chunks and
 // `nt` streamed tensors; `red_bytes` of shared memory precede the ring and
 // `max_cpt` caps the default chunks per thread.
+// Extra tile rules of the RMSNorm backward (measured there only).
+struct RowTuning {
+    size_t ring_cap_3;    // ring cap while at least 3 teams remain
+    size_t ring_cap_5;    // ring cap while at least 5 teams remain
+    int min_rows_per_team;  // on problems of at least 16 rows per SM
+};
+
 static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int max_cpt,
                           int (*max_threads)(int cpt), const DeviceInfo &d, RowPlan *plan,
-                          bool use_options = true, size_t ring_soft_cap = 0) {
+                          bool use_options = true, const RowTuning *tune = nullptr) {
     if (nchunks > kRowMaxChunks) return false;
     // RN_OPT_* shape the backward only
     auto opt = [&](int o) { return use_options ? g_opts[o] : 0; };
@@ -128,20 +135,20 @@ static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int 
     // Tile (measured on GB300): 4 chunks per thread for rows of 512+ chunks
     // (bf16 N >= 4096), else 2, else 1 for very short rows.
     int cpt = opt(RN_OPT_CHUNKS_PER_THREAD);
-    if (cpt != 1 && cpt != 2 && cpt != 4) {
+    const bool cpt_forced = cpt == 1 || cpt == 2 || cpt == 4;
+    if (!cpt_forced) {
         cpt = nchunks >= 512 ? 4 : (nchunks >= 64 ? 2 : 1);
         while (cpt > max_cpt) cpt /= 2;
         // more chunks per thread when the row does not fit the capped tile
         while (cpt < 4 && ((nchunks + cpt - 1) / cpt + 31) / 32 * 32 > max_threads(cpt)) cpt *= 2;
     }
-    int team = ((nchunks + cpt - 1) / cpt + 31) / 32 * 32;
+    auto team_of = [&](int c) { return ((nchunks + c - 1) / c + 31) / 32 * 32; };
+    int team = team_of(cpt);
     if (team > max_threads(cpt)) return false;
 
     const size_t budget = (d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024);
-    const int tc = cpt * team;  // 16-byte chunks per tensor row in a team's slot
-    const size_t stage = (size_t)nt * tc * 16;
     auto smem_for = [&](int teams_, int stages_) {
-        return red_bytes + (size_t)teams_ * stages_ * stage;
+        return red_bytes + (size_t)teams_ * stages_ * nt * (size_t)(cpt * team) * 16;
     };
     int teams = opt(RN_OPT_TEAMS_PER_CTA);
     if (teams <= 0) {
@@ -149,13 +156,27 @@ static bool plan_row_tile(int64_t M, int nchunks, int nt, size_t red_bytes, int 
         if (teams > 15) teams = 15;
         // room for at least 2 slots per team
         while (teams > 1 && smem_for(teams, 2) > budget) --teams;
-        // a softer cap on the ring while at least 3 teams remain
-        while (ring_soft_cap && teams > 3 && smem_for(teams, 2) > ring_soft_cap) --teams;
+        if (tune) {
+            // softer caps on the ring while enough teams remain
+            while (teams > 4 && smem_for(teams, 2) > tune->ring_cap_5) --teams;
+            while (teams > 3 && smem_for(teams, 2) > tune->ring_cap_3) --teams;
+        }
         // no more teams than rows per SM
         int64_t rows_per_sm = (M + d.num_sms - 1) / d.num_sms;
         if (rows_per_sm < 1) rows_per_sm = 1;
         if (teams > rows_per_sm) teams = (int)rows_per_sm;
+        // with enough rows, each team gets a few: fewer teams, and then fewer chunks per
+        // thread (more threads on a row) while the CTA still fits
+        if (tune && rows_per_sm >= 16 && teams > rows_per_sm / tune->min_rows_per_team) {
+            teams = (int)(rows_per_sm / tune->min_rows_per_team);
+            while (!cpt_forced && cpt > 1 && team_of(cpt / 2) * teams <= max_threads(cpt / 2)) {
+                cpt /= 2;
+                team = team_of(cpt);
+            }
+        }
     }
+    const int tc = cpt * team;  // 16-byte chunks per tensor row in a team's slot
+    const size_t stage = (size_t)nt * tc * 16;
     if (teams < 1 || teams > 15 || teams * team > max_threads(cpt)) return false;
 
     // one CTA per SM unless the grid option asks for another count
@@ -199,14 +220,21 @@ static bool plan_row(const BwdProblem &p, const DeviceInfo &d, RowPlan *plan) {
         (p.dres && !aligned16(p.dres)))
         return false;
     const int nt = p.dres ? 3 : 2;
-    // Measured on GB300 (bf16 fused-add with dresidual_out, 4096-wide rows, us per call): a ring
-    // above ~150 KB costs more than a fourth team gains. 3 teams (147 KB) vs 4 (196 KB): 25.5 vs
-    // 26.1 at M = 4096, 40.0 vs 42.9 at 8192, 79.5 vs 83.2 at 16384, 18.9 vs 19.3 at 2048.
-    // With fewer teams left the larger ring stays (16384 x 8192: 2 teams 159.5, 1 team 173.3).
-    constexpr size_t kRingSoftCap = 160 * 1024;
+    // Measured on GB300 (L2 flushed, us per call):
+    //  * a ring above ~150 KB costs more than a fourth team gains (bf16 fused-add with
+    //    dresidual_out, 4096-wide rows; 3 teams and 147 KB vs 4 and 196 KB): 25.5 vs 26.1 at
+    //    M = 4096, 40.0 vs 42.9 at 8192, 79.5 vs 83.2 at 16384, 18.9 vs 19.3 at 2048. With
+    //    fewer teams left the larger ring stays (16384 x 8192: 2 teams 159.5, 1 team 173.3);
+    //  * with five or more teams, above ~125 KB (fused with dres; 5 teams and 123 KB vs 6 and
+    //    147 KB): bf16 4096 x 2048 18.8 vs 21.4, 16384 x 2048 39.9 vs 41.0, f32 16384 x 1024
+    //    39.3 vs 40.6;
+    //  * at least 4 rows a team once there are 16 rows per SM, with the spare threads put on
+    //    each row: bf16 4096 x 1024 (1 chunk x 128 threads, 6 teams vs 2 x 64, 12 teams) 13.3
+    //    vs 15.2, fused 14.4 vs 16.3.
+    static const RowTuning kTune = {160 * 1024, 125 * 1024, 4};
     // the kernel's reduction slots precede its ring: row_smem_bytes with no ring
     return plan_row_tile(p.M, row_bytes / 16, nt, row_smem_bytes(0, 0, nt, 0), 4,
-                         row_max_threads, d, plan, true, kRingSoftCap);
+                         row_max_threads, d, plan, true, &kTune);
 }
 
 // Cluster engine: the row split over `csize` CTAs of up to 2048 chunks each.

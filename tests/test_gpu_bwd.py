@@ -560,3 +560,22 @@ def test_cast_only_empty_batch():
                                   want_f32=False)
     torch.cuda.synchronize()
     assert dw32 is None and torch.count_nonzero(dw).item() == 0
+
+
+@pytest.mark.parametrize("M,N,dt,fused,want", [
+    (4096, 1024, "bf16", False, "cpt=1 team_threads=128 teams=6 "),   # >= 4 rows a team
+    (4096, 4096, "bf16", True, "cpt=4 team_threads=128 teams=3 "),    # ring under 160 KB
+    (4096, 2048, "bf16", True, "cpt=2 team_threads=128 teams=5 "),    # ring under 125 KB
+    (4096, 4096, "bf16", False, "cpt=4 team_threads=128 teams=4 "),   # 131 KB ring kept
+    (16384, 8192, "bf16", True, "cpt=4 team_threads=256 teams=2 "),   # too few teams to cap
+    (512, 2048, "bf16", False, "cpt=2 team_threads=128 teams=4 ")],   # too few rows per SM
+    ids=lambda v: str(v))
+def test_row_engine_default_tiles(M, N, dt, fused, want):
+    """The planner's measured tile rules pick these shapes by default, and
+    the results match the oracle."""
+    ex = parity.expected_bwd(Case("tile %s" % dt, M, N, dt, fused=fused, with_dres=fused,
+                                  seed=45))
+    out = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    assert plan.startswith("engine=row ") and want in plan, plan
+    assert parity.check_bwd(ex, *out) == 0
