@@ -37,6 +37,7 @@ struct PhaseArgs {
     int N;
     float inv_n;
     int period;      // P
+    int prefetch;    // 1: L2 prefetch of the rows two iterations ahead
 };
 
 int phase_period(int N, int dtype) {
@@ -149,6 +150,24 @@ __global__ void __launch_bounds__(512) bwd_phase_kernel(const PhaseArgs a) {
             xen[r] = den[r] = 0.f;
             const int64_t nrow = rb + (R + r) * rstride;
             if (nrow < a.M) load(nrow, xn[r], dn[r], xen[r], den[r]);
+        }
+        // the rows after those into L2 (when the planner asks): their loads next iteration
+        // then wait on L2, not DRAM (the rows in flight in registers are all the registers
+        // allow)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t prow = rb + (2 * R + r) * rstride;
+            if (a.prefetch && prow < a.M) {
+                const size_t base = (size_t)prow * N;
+#pragma unroll
+                for (int k = 0; k < J; ++k) {
+                    if (own[k]) {
+                        prefetch_l2(x + base + col[k]);
+                        prefetch_l2(dy + base + col[k]);
+                        if (HAS_DRES) prefetch_l2(dres + base + col[k]);
+                    }
+                }
+            }
         }
 
         // dresidual_out (a plain load: dx may overwrite it) and rstd of these rows; with four
@@ -369,6 +388,7 @@ cudaError_t launch_bwd_phase(const BwdProblem &p, const GenericPlan &plan, cudaS
     a.N = p.N;
     a.inv_n = 1.0f / (float)p.N;
     a.period = phase_period(p.N, p.dtype);
+    a.prefetch = plan.prefetch ? 1 : 0;
     // a residue class without a CTA would leave its rows unwritten
     if (p.M > 0 && plan.grid < (p.M < a.period ? p.M : a.period)) return cudaErrorInvalidValue;
     if (plan.atomic && plan.smem < (size_t)p.N * 4) return cudaErrorInvalidValue;

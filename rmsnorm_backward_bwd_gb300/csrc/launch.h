@@ -61,6 +61,7 @@ struct GenericPlan {
     int cpb = 0;       // realigning engine: column blocks per thread (2, 4); 0 = not used
     int phase = 0;     // phase-class kernel: 16-byte chunks per thread (1, 2); 0 = not used
     int phase_rows = 1;  // phase-class kernel: rows per CTA iteration (1, 2)
+    bool prefetch = false;  // phase-class kernel: L2 prefetch two iterations ahead
 };
 
 // Row engine: largest chunk count per row and CTA thread cap for a cpt.

@@ -579,3 +579,22 @@ def test_row_engine_default_tiles(M, N, dt, fused, want):
     plan = native.last_plan()
     assert plan.startswith("engine=row ") and want in plan, plan
     assert parity.check_bwd(ex, *out) == 0
+
+
+@pytest.mark.parametrize("M,N,dt,fused,want", [
+    (600, 8183, "f16", True, "cpt=2 rows=2 "),      # wide rows of three tensors: prefetch
+    (12288, 2999, "bf16", False, "cpt=2 rows=2 "),  # >= 40 rows per CTA: prefetch
+    (1000, 1001, "f16", False, "cpt=1 rows=2 "),    # one chunk a thread: prefetch
+    (500, 4095, "bf16", False, "cpt=2 rows=2 ")],   # neither: no prefetch
+    ids=lambda v: str(v))
+def test_generic_phase_kernel_prefetch(M, N, dt, fused, want):
+    """The planner's L2-prefetch choice for the phase-class kernel, and the
+    results with and without it."""
+    ex = parity.expected_bwd(Case("phase prefetch %s" % dt, M, N, dt, fused=fused,
+                                  with_dres=fused, seed=46))
+    out = parity.run_gpu_bwd(ex)
+    plan = native.last_plan()
+    assert want in plan, plan
+    expect = 0 if (N == 4095 and M == 500) else 1
+    assert " prefetch=%d " % expect in plan, plan
+    assert parity.check_bwd(ex, *out, tag=" [%s]" % plan) == 0
