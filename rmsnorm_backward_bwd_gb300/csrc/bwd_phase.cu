@@ -25,6 +25,12 @@
 
 namespace rn {
 
+// Ask L2 to fetch the line holding p (no register result, no completion to
+// wait for; p must be a valid global address).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 struct PhaseArgs {
     const void *x;
     const void *gamma;

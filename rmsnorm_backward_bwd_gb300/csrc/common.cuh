@@ -146,12 +146,6 @@ __device__ __forceinline__ uint4 ld_global_nc_v4_hint(const void *p, uint64_t po
     return v;
 }
 
-// Ask L2 to fetch the line holding p (no register result, no completion to
-// wait for; p must be a valid global address).
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ void st_global_v4(void *p, const uint4 &v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
