@@ -1,6 +1,8 @@
 // Backward realigning engine: rows whose byte length is not a multiple of 16
 // (so consecutive rows start at different offsets within a 16-byte line),
-// with x, dy, dx and dresidual_out at one common alignment phase.
+// with x, dy, dx and dresidual_out at one common alignment phase. Run only
+// when asked for (RN_OPT_GENERIC_KERNEL = 3): the phase-class kernel covers
+// its 16-32 KB rows faster.
 //
 // Same math as the row engine (FlyDSL issue #769 "Math"; fused-add from
 // PR #800 "What's included"), and the same per-chunk arithmetic (RowMath).

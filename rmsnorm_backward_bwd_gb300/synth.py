@@ -113,9 +113,9 @@ LN_4096 = Case("layernorm_bwd bf16 M=4096 N=4096", 4096, 4096, "bf16", eps=1e-5)
 LN_LARGE = Case("layernorm_bwd bf16 M=16384 N=8192", 16384, 8192, "bf16", eps=1e-5)
 # rows longer than one CTA's tile (the cluster engine's range)
 LONG_ROWS = Case("rmsnorm_bwd bf16 M=4096 N=32768", 4096, 32768, "bf16")
-# rows that are not 16-byte multiples (the generic engine's range)
+# rows that are not 16-byte multiples (the generic engines' range: phase-class kernel)
 UNALIGNED_ROWS = Case("rmsnorm_bwd bf16 M=4096 N=4095", 4096, 4095, "bf16")
-# rows of 24 KB that are not 16-byte multiples (the realigning engine's range)
+# rows of 24 KB that are not 16-byte multiples (phase-class kernel, four chunks a thread)
 UNALIGNED_WIDE_ROWS = Case("rmsnorm_bwd bf16 M=4096 N=12290", 4096, 12290, "bf16")
 
 

@@ -316,8 +316,8 @@ def test_generic_realigning_engine(M, N, dt, fused, cpb, mode):
     (64, 515, "bf16", True, 4), (24, 20001, "bf16", False, 2), (16, 18001, "f16", True, 2)],
     ids=lambda v: str(v))
 def test_generic_vector_variant(M, N, dt, fused, rows, mode):
-    """Rows under 16 KB (or past the realigning engine's 32 KB) that are not
-    16-byte multiples, all tensors at one phase: 16-byte chunks plus
+    """Rows that are not 16-byte multiples, all tensors at one phase (past
+    2048 whole chunks it is the default; below, forced): 16-byte chunks plus
     element-wise head and tail, several rows per CTA iteration (M not a
     multiple of them), shared partial with atomic adds; both weight-gradient
     modes. The kernel is chosen by option where another generic kernel would
