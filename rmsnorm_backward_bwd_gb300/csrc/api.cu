@@ -587,7 +587,22 @@ static void plan_string_generic(const GenericPlan &gp, const char *engine, bool 
                  gp.threads, gp.grid, (int)gp.smem_dw, atomic ? "atomic" : "scratch");
 }
 
-static void plan_string_fwd(const char *op, bool vec, bool row, bool gvec, const RowPlan &rp) {
+// The phase-class forward's launch shape: 1 chunk a thread up to 256 whole
+// 16-byte chunks, else 2; the backward phase-class kernel's grid rule (two
+// CTAs per SM, a multiple of the period, never below min(P, M)).
+struct FwdPhasePlan {
+    int cpt, threads, grid;
+};
+
+static FwdPhasePlan plan_fwd_phase(const FwdRowProblem &q, const DeviceInfo &d);
+
+static void plan_string_fwd(const char *op, bool vec, bool row, bool gvec, const RowPlan &rp,
+                            const FwdPhasePlan *fp = nullptr) {
+    if (fp) {
+        snprintf(g_plan, sizeof(g_plan), "%s engine=generic phase cpt=%d threads=%d grid=%d", op,
+                 fp->cpt, fp->threads, fp->grid);
+        return;
+    }
     if (vec && row)
         snprintf(g_plan, sizeof(g_plan), "%s engine=row cpt=%d team_threads=%d teams=%d stages=%d "
                  "grid=%d", op, rp.cpt, rp.team_threads, rp.teams, rp.stages, rp.grid);
@@ -956,13 +971,40 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
     q.N = (int)N;
     q.dtype = dtype;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const char *op = fused ? "fused_add_fwd" : "rmsnorm_fwd";
+    // The RMSNorm forwards keep the vector kernel where it can run (see plan_fwd_phase); the
+    // phase-class kernel takes gamma at any alignment.
+    if (!vec && !fwd_generic_vec_ok(q) && fwd_phase_ok(q)) {
+        const FwdPhasePlan fp = plan_fwd_phase(q, d);
+        plan_string_fwd(op, vec, row, false, rp, &fp);
+        e = launch_fwd_phase(q, fp.cpt, fp.grid, fp.threads, cs);
+        return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
+    }
     const bool gvec = !vec && fwd_generic_vec_ok(q);
-    plan_string_fwd(fused ? "fused_add_fwd" : "rmsnorm_fwd", vec, row, gvec, rp);
+    plan_string_fwd(op, vec, row, gvec, rp);
     if (vec)
         e = row ? launch_fwd_row(q, rp, cs) : launch_fwd_long(q, d.num_sms, cs);
     else
         e = gvec ? launch_fwd_generic_vec(q, d.num_sms, cs) : launch_fwd(p, d.num_sms, cs);
     return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
+}
+
+// Measured on GB300 (L2 flushed, us per call; vector kernel -> phase-class kernel): the
+// LayerNorm forward in 16-bit types gains (bf16 4096 x 4095 32.5 -> 24.5, 4096 x 4100 30.8 ->
+// 24.6, 16384 x 8190 186.6 -> 175.4, f16 16384 x 1001 62.8 -> 61.3), its rows staying in
+// registers through the mean and variance passes. The RMSNorm forwards lose (bf16 4096 x 4095
+// 19.2 -> 20.5, fused 23.1 -> 24.6, 16384 x 8190 98.5 -> 149.4) and so does the f32 LayerNorm
+// (4096 x 4095 32.8 -> 43.0): the vector kernel's eight CTAs per SM keep more rows in flight.
+// So the phase-class forward runs for the 16-bit LayerNorm, and for the others only where the
+// vector kernel cannot (gamma or beta off a 16-byte boundary).
+static FwdPhasePlan plan_fwd_phase(const FwdRowProblem &q, const DeviceInfo &d) {
+    FwdPhasePlan fp;
+    const int64_t nvmax = (int64_t)q.N * elem_bytes(q.dtype) / 16;
+    fp.cpt = nvmax > 256 ? 2 : 1;
+    const int t = (int)((nvmax + fp.cpt - 1) / fp.cpt + 31) / 32 * 32;
+    fp.threads = t < 32 ? 32 : t;
+    fp.grid = phase_grid(q.M, phase_period(q.N, q.dtype), 2, d);
+    return fp;
 }
 
 static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta, float eps,
@@ -1017,6 +1059,12 @@ static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta
     q.N = (int)N;
     q.dtype = dtype;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (!vec && fwd_phase_ok(q) && (dtype != kF32 || !fwd_generic_vec_ok(q))) {
+        const FwdPhasePlan fp = plan_fwd_phase(q, d);
+        plan_string_fwd("layernorm_fwd", vec, row, false, rp, &fp);
+        e = launch_fwd_phase(q, fp.cpt, fp.grid, fp.threads, cs);
+        return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
+    }
     const bool gvec = !vec && fwd_generic_vec_ok(q);
     plan_string_fwd("layernorm_fwd", vec, row, gvec, rp);
     if (vec)

@@ -144,6 +144,11 @@ cudaError_t launch_fwd_long(const FwdRowProblem &p, int num_sms, cudaStream_t s)
 // Rows that are not 16-byte multiples, row tensors at one alignment phase and
 // gamma (beta) 16-byte aligned: 16-byte chunks plus element-wise head and tail.
 bool fwd_generic_vec_ok(const FwdRowProblem &p);
+// The same rows, each CTA on one alignment class of rows (row tensors at one
+// phase, at most 1024 whole 16-byte chunks; gamma and beta at any alignment).
+bool fwd_phase_ok(const FwdRowProblem &p);
+cudaError_t launch_fwd_phase(const FwdRowProblem &p, int cpt, int grid, int threads,
+                             cudaStream_t s);
 cudaError_t launch_fwd_generic_vec(const FwdRowProblem &p, int num_sms, cudaStream_t s);
 
 // LayerNorm.

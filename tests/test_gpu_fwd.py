@@ -101,7 +101,8 @@ def test_fwd_3d_input_and_guards():
 
 
 UNALIGNED = [(300, 4095, "bf16"), (97, 2999, "f32"), (64, 1001, "f16"), (5, 7, "bf16"),
-             (3, 3, "f32"), (40, 8190, "bf16"), (9, 16385, "f16")]
+             (3, 3, "f32"), (40, 8190, "bf16"), (9, 16385, "f16"), (1000, 4100, "bf16"),
+             (17, 515, "bf16"), (600, 2050, "f16"), (33, 4095, "f32"), (1, 4095, "bf16")]
 
 
 def _shifted_like(t, shift):
@@ -117,9 +118,11 @@ def _shifted_like(t, shift):
 @pytest.mark.parametrize("phase", ["same", "mismatched"])
 def test_fwds_on_unaligned_rows(M, N, dt, phase):
     """Rows that are not 16-byte multiples: with all row tensors at one phase
-    (16-byte chunks plus element-wise head and tail), and with the output one
-    element off the input's phase (element-wise kernel). RMSNorm, fused-add
-    and LayerNorm against the oracle."""
+    (16-byte chunks plus element-wise head and tail: the vector kernel, or for
+    the 16-bit LayerNorm the phase-class kernel, each CTA on one alignment
+    class of rows), and with the output one element off the input's phase
+    (element-wise kernel). RMSNorm, fused-add and LayerNorm against the
+    oracle."""
     inp = synth.make_inputs(Case("unaligned fwd", M, N, dt, fused=True, seed=31))
     x64, r64, g64 = (parity.to64(inp[k]) for k in ("x", "residual", "gamma"))
     x, r, g = inp["x"].cuda(), inp["residual"].cuda(), inp["gamma"].cuda()
@@ -128,6 +131,10 @@ def test_fwds_on_unaligned_rows(M, N, dt, phase):
         z = torch.empty(M, N, dtype=x.dtype)
         return _shifted_like(z, 1) if phase == "mismatched" else z.cuda()
 
+    # one phase: the vector kernel, except the 16-bit LayerNorm up to 1024 whole 16-byte
+    # chunks (the phase-class kernel)
+    wide = N * synth.ELEM_BYTES[dt] // 16 > 1024
+    ln_phase = phase == "same" and not wide and dt != "f32"
     engine = "engine=generic vec" if phase == "same" else "engine=generic"
     plans = []
     y, rstd = rn.rmsnorm_fwd(x, g, 1e-6, y=out_buf())
@@ -138,7 +145,8 @@ def test_fwds_on_unaligned_rows(M, N, dt, phase):
     plans.append(native.last_plan())
     torch.cuda.synchronize()
     for op, plan in zip(("rmsnorm_fwd", "fused_add_fwd", "layernorm_fwd"), plans):
-        assert plan == "%s %s" % (op, engine), plan
+        want = "engine=generic phase" if (op == "layernorm_fwd" and ln_phase) else engine
+        assert plan == "%s %s" % (op, want) or plan.startswith("%s %s " % (op, want)), plan
     y64, rstd64 = oracle.rmsnorm_fwd(x64, g64, np.float32(1e-6))
     o64, a64, frstd64 = oracle.fused_add_rmsnorm_fwd(x64, r64, g64, np.float32(1e-6), dt)
     yl64, mean64, lrstd64 = oracle.layernorm_fwd(x64, g64, g64, np.float32(1e-5))
@@ -154,13 +162,15 @@ def test_fwds_on_unaligned_rows(M, N, dt, phase):
 
 
 def test_unaligned_fwd_gamma_off_16_bytes():
-    """gamma itself off 16-byte alignment: the element-wise kernel."""
+    """gamma itself off 16-byte alignment: the phase-class kernel gathers it
+    element by element."""
     M, N, dt = 33, 1001, "bf16"
     inp = synth.make_inputs(Case("unaligned gamma", M, N, dt, seed=32))
     x64, g64 = parity.to64(inp["x"]), parity.to64(inp["gamma"])
     g = _shifted_like(inp["gamma"], 3)
     y, rstd = rn.rmsnorm_fwd(inp["x"].cuda(), g, 1e-6)
     torch.cuda.synchronize()
+    assert native.last_plan().startswith("rmsnorm_fwd engine=generic phase"), native.last_plan()
     y64, rstd64 = oracle.rmsnorm_fwd(x64, g64, np.float32(1e-6))
     parity.check_tensor("y", y, y64, dt, "y")
     _check_rstd(rstd, rstd64)
