@@ -744,6 +744,12 @@ static bool plan_ln_phase(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
     plan->rows = 0;
     plan->threads = threads;
     plan->grid = phase_grid(p.M, phase_period(p.N, p.dtype), per_sm, d);
+    // L2 prefetch of the row after the next one, by the RMSNorm phase-class kernel's rule
+    {
+        const int64_t rows_per_cta = (p.M + plan->grid - 1) / plan->grid;
+        plan->prefetch = cpt != 2 || rows_per_cta >= 40 ||
+                         (int64_t)2 * p.N * elem_bytes(p.dtype) >= 40 * 1024;
+    }
     plan->smem_dw = atomic;
     plan->smem = smem;
     plan->atomic = atomic;

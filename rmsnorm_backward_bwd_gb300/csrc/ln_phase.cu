@@ -32,6 +32,7 @@ struct LnPhaseArgs {
     int N;
     float inv_n;
     int period;     // P
+    int prefetch;   // 1: L2 prefetch of the row after the next one
 };
 
 // Padded length of the atomic mode's first staged partial: the second one
@@ -110,6 +111,19 @@ __global__ void __launch_bounds__(512) ln_bwd_phase_kernel(const LnPhaseArgs a) 
         for (int k = 0; k < J; ++k) xn[k] = dn[k] = make_uint4(0, 0, 0, 0);
         float xen = 0.f, den = 0.f;
         if (nrow < a.M) load(nrow, xn, dn, xen, den);
+        // the row after that into L2 (when the planner asks): its loads next iteration then
+        // wait on L2, not DRAM
+        const int64_t prow = nrow + nper * P;
+        if (a.prefetch && prow < a.M) {
+            const size_t pbase = (size_t)prow * N;
+#pragma unroll
+            for (int k = 0; k < J; ++k) {
+                if (own[k]) {
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(x + pbase + col[k]));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(dy + pbase + col[k]));
+                }
+            }
+        }
         const size_t base = (size_t)row * N;
         const float mu = __ldg(a.mean + row), rs = __ldg(a.rstd + row);
 
@@ -312,6 +326,7 @@ cudaError_t launch_ln_bwd_phase(const LnBwdProblem &p, const GenericPlan &plan, 
     a.N = p.N;
     a.inv_n = 1.0f / (float)p.N;
     a.period = phase_period(p.N, p.dtype);
+    a.prefetch = plan.prefetch ? 1 : 0;
     // a residue class without a CTA would leave its rows unwritten
     if (p.M > 0 && plan.grid < (p.M < a.period ? p.M : a.period)) return cudaErrorInvalidValue;
     if (plan.atomic && plan.smem < ln_phase_smem_bytes(p.N, true)) return cudaErrorInvalidValue;
