@@ -959,6 +959,15 @@ def run_ours(args):
             "forward": forward,
             "autograd_pages_shapes": pages_table,
         }
+        # every backward workload's device time and % of peak also as flat top-level keys, so
+        # that a record keeping only scalars keeps them too
+        for w in workloads or []:
+            if w.get("kind") != "bwd":
+                continue
+            slug = re.sub(r"[^0-9a-z]+", "_", w["workload"].lower().replace(" m=", " ")
+                          .replace(" n=", "x")).strip("_")
+            line["us_per_call__" + slug] = w["us_per_call"]
+            line["pct_of_peak__" + slug] = w["pct_of_peak"]
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
