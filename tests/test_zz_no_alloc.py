@@ -76,3 +76,22 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     st = _noalloc(x, g, x, rstd, torch.empty_like(x), dw32, None)
     assert st == native.RN_ERR_UNSUPPORTED
     assert b"scratch" in native.lib().rn_last_error()
+
+
+def test_noalloc_cast_only_weight_gradient():
+    """dweight_f32 = NULL: the fp32 sum stays in the fixed scratch (scratch
+    mode) and only the cast is written; equal, bit for bit, to the workspace
+    entry point's scratch-mode cast."""
+    native.set_option(native.OPT_DWEIGHT_MODE, 1)
+    ex = parity.expected_bwd(Case("bf16 M=2048 N=4096", 2048, 4096, "bf16"))
+    x, g, dy, rstd = (t.cuda() for t in (ex.x, ex.gamma, ex.dy, ex.rstd))
+    ref_dx, ref_dw, _ = rn.rmsnorm_bwd(x, g, dy, rstd)
+    native.set_option(native.OPT_DWEIGHT_MODE, 0)
+    dx = torch.full_like(x, float("nan"))
+    dw = torch.full_like(ref_dw, float("nan"))
+    st = _noalloc(x, g, dy, rstd, dx, None, dw)
+    assert st == native.RN_OK, native.lib().rn_last_error()
+    torch.cuda.synchronize()
+    assert "dw=scratch" in native.last_plan()
+    assert torch.equal(dx, ref_dx) and torch.equal(dw, ref_dw)
+    parity.check_tensor("dweight", dw, ex.dw, "bf16", "dweight")
