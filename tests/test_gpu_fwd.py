@@ -174,3 +174,23 @@ def test_unaligned_fwd_gamma_off_16_bytes():
     y64, rstd64 = oracle.rmsnorm_fwd(x64, g64, np.float32(1e-6))
     parity.check_tensor("y", y, y64, dt, "y")
     _check_rstd(rstd, rstd64)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+def test_unaligned_layernorm_fwd_params_off_16_bytes(dt):
+    """LayerNorm forward on rows that are not 16-byte multiples with gamma and
+    beta off 16-byte alignment: the phase-class kernel gathers both."""
+    M, N = 77, 2999
+    inp = synth.make_inputs(Case("unaligned ln params", M, N, dt, seed=33))
+    x64, g64 = parity.to64(inp["x"]), parity.to64(inp["gamma"])
+    b = (inp["gamma"].float() * 0.5 - 0.25).to(inp["gamma"].dtype)
+    b64 = parity.to64(b)
+    g, bb = _shifted_like(inp["gamma"], 1), _shifted_like(b, 3)
+    y, mean, rstd = rn.layernorm_fwd(inp["x"].cuda(), g, bb, 1e-5)
+    torch.cuda.synchronize()
+    assert native.last_plan().startswith("layernorm_fwd engine=generic phase"), native.last_plan()
+    y64, mean64, rstd64 = oracle.layernorm_fwd(x64, g64, b64, np.float32(1e-5))
+    parity.check_tensor("layernorm y", y, y64, dt, "y")
+    tol = 2.0**-24 * (8 + 4 * np.sqrt(N))
+    assert np.all(np.abs(parity.to64(mean) - mean64) <= tol * np.mean(np.abs(x64), axis=1))
+    assert np.all(np.abs(parity.to64(rstd) - rstd64) <= tol * rstd64)
