@@ -61,6 +61,7 @@ def measured_peak():
 
 # The row-pass kernel each engine launches (from the plan string).
 ENGINE_KERNELS = {"row": "bwd_row_kernel", "cluster": "bwd_cluster_kernel",
+                  "generic staged": "bwd_stage_kernel",
                   "generic phase": "bwd_phase_kernel", "generic realign": "bwd_realign_kernel",
                   "generic vec": "bwd_generic_vec_kernel", "generic": "bwd_generic_kernel"}
 

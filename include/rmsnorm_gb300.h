@@ -245,29 +245,40 @@ typedef enum rn_option {
     RN_OPT_BWD_ENGINE = 0,    /* 1 = row engine (async-copy ring), 2 = generic engines (the
                                  default for rows that are not 16-byte multiples or bases off
                                  16 bytes; which one runs depends on the row size and on whether
-                                 the row tensors share one alignment phase: phase-class kernel up
-                                 to 2048 whole 16-byte chunks, vector kernel past that, element-
-                                 wise kernel for mixed phases), 3 = cluster engine (RMSNorm backward:
-                                 a row split across a thread-block cluster; chosen by default
-                                 for aligned rows of more than 2048 16-byte chunks) */
+                                 the row tensors share one alignment phase: the staged
+                                 phase-class kernel up to 2048 whole 16-byte chunks, vector
+                                 kernel past that, element-wise kernel for mixed phases),
+                                 3 = cluster engine (RMSNorm backward: a row split across a
+                                 thread-block cluster; chosen by default for aligned rows of
+                                 more than 2048 16-byte chunks) */
     RN_OPT_DWEIGHT_MODE = 1,  /* 1 = scratch partials + finalize (deterministic dweight),
                                  2 = fp32 atomics + cast (summation order varies from call to
                                  call). Automatic: scratch when a row tensor holds at most
                                  2 MiB (fewer launches), else atomics where possible */
-    RN_OPT_CHUNKS_PER_THREAD = 2, /* row engine: 16-byte chunks per thread per row: 1, 2, 4 */
-    RN_OPT_TEAMS_PER_CTA = 3, /* row engine: rows processed at once per CTA (1..15);
-                                 RMSNorm backward phase-class kernel: rows per CTA
-                                 iteration (1 or 2) */
-    RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8) */
+    RN_OPT_CHUNKS_PER_THREAD = 2, /* row engine and staged phase-class kernel: 16-byte chunks
+                                 per thread per row: 1, 2, 4 */
+    RN_OPT_TEAMS_PER_CTA = 3, /* row engine and staged phase-class kernel: rows processed at
+                                 once per CTA (1..15); RMSNorm backward phase-class kernel:
+                                 rows per CTA iteration (1 or 2) */
+    RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8); staged
+                                 phase-class kernel: shared-memory slots per team (2..4) */
     RN_OPT_GRID = 5,          /* CTAs of the row pass (default: one per SM; at most 2 per SM) */
     RN_OPT_CLUSTER_SIZE = 6,  /* cluster engine: CTAs per cluster, 2, 4, 8 or 16 */
-    RN_OPT_GENERIC_KERNEL = 7, /* RMSNorm backward, generic engines: 1 = phase-class kernel,
-                                 2 = vector kernel, 3 = realigning kernel (rows of 16 to 32 KB;
-                                 taken only when asked for), 4 = element-wise kernel. A kernel
-                                 that cannot take the problem (its row-size range, or tensors at
-                                 different alignment phases) falls back to the next one the
-                                 automatic choice would make. */
-    RN_OPT_COUNT = 8
+    RN_OPT_GENERIC_KERNEL = 7, /* RMSNorm backward, generic engines: 1 = phase-class kernel
+                                 (rows held in registers), 2 = vector kernel, 3 = realigning
+                                 kernel (rows of 16 to 32 KB; taken only when asked for),
+                                 4 = element-wise kernel, 5 = staged phase-class kernel (rows
+                                 staged in shared memory by bulk copies; the automatic
+                                 choice). A kernel that cannot take the problem (its row-size
+                                 range, or tensors at different alignment phases) falls back
+                                 to the next one the automatic choice would make. */
+    RN_OPT_TEST_WAIT_TIMEOUT = 8, /* test hook, RMSNorm backward, staged phase-class kernel:
+                                 v > 0 makes the first CTA's first team leave its row v-1
+                                 (counted from 0 among that team's rows) uncopied, so that
+                                 the team's bounded wait (250 ms) runs out. The call then
+                                 leaves dx rows and the weight gradient incomplete and
+                                 rn_take_device_status() reports bit 0. */
+    RN_OPT_COUNT = 9
 } rn_option;
 
 rn_status rn_set_option(int option, int value);
@@ -280,6 +291,17 @@ int rn_get_option(int option);
  * start with the operation ("rmsnorm_fwd", "fused_add_fwd", "layernorm_fwd").
  */
 const char *rn_last_plan(void);
+
+/*
+ * Device status word of the current device (kernels OR bits into it):
+ *   bit 0 = a bounded wait inside a kernel ran out (the staged phase-class
+ *           kernel waits at most 250 ms for a row's bulk copies). The team that
+ *           waited stopped: the dx rows it had not reached and the weight
+ *           gradient of that call are not valid. The CUDA context stays usable.
+ * Synchronizes the device, stores the word in *status and clears it.
+ * Returns RN_ERR_INVALID_ARG for a NULL status, RN_ERR_CUDA if a CUDA call fails.
+ */
+rn_status rn_take_device_status(unsigned int *status);
 
 /*
  * Timing hook: while both are non-NULL, every backward call records

@@ -456,12 +456,67 @@ static bool plan_phase(const BwdProblem &p, const DeviceInfo &d, bool atomic, Ge
     return true;
 }
 
+// The staged phase-class kernel: the phase-class kernel's conditions (one
+// alignment phase, at most 2048 whole 16-byte chunks per row); 4 chunks a
+// thread (RN_OPT_CHUNKS_PER_THREAD forces 1 or 2), teams of the fewest whole
+// warps that cover a row, 2 shared-memory slots a team (RN_OPT_STAGES forces
+// 2..4), as many teams as fit 512 threads, 15 named barriers and 200 KB of
+// ring (RN_OPT_TEAMS_PER_CTA forces 1..15), and the phase-class kernel's grid
+// rule at the resident CTAs per SM. The automatic choice takes it from 2048
+// rows: with fewer, a CTA has too few rows to fill its pipeline and the
+// phase-class kernel is as fast or faster. Measured on GB300 (L2 flushed, us
+// per call, phase-class -> staged): bf16 4096 x 4095 29.2 -> 27.6, fused +dres
+// 37.7 -> 31.4, 16384 x 4095 81.7 -> 71.4, 4096 x 12290 80.8 -> 66.8, 16384 x
+// 2047 63.0 -> 40.8, 32768 x 1001 94.3 -> 42.5, 4096 x 255 20.5 -> 13.9, f32
+// 4096 x 4095 34.9 -> 31.9, f16 2048 x 3001 19.3 -> 17.9; with fewer rows
+// 1024 x 4095 15.6 -> 15.9, 1000 x 4095 15.5 -> 15.9, 128 x 2047 10.4 ->
+// 12.6, 64 x 4095 12.1 -> 12.6.
+constexpr int64_t kStageMinRows = 2048;
+
+static bool plan_stage(const BwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
+                       StagePlan *plan) {
+    if (!forced && p.M < kStageMinRows) return false;
+    if (!generic_vec_ok(p, d)) return false;
+    const int64_t maxnv = (int64_t)p.N * elem_bytes(p.dtype) / 16;
+    if (maxnv > kRowMaxChunks) return false;
+    int cpt = g_opts[RN_OPT_CHUNKS_PER_THREAD];
+    if (cpt != 1 && cpt != 2) cpt = 4;
+    int tthr = (int)((maxnv + cpt - 1) / cpt + 31) / 32 * 32;
+    if (tthr < 32) tthr = 32;
+    if (tthr > 512) return false;
+    int slots = g_opts[RN_OPT_STAGES];
+    if (slots < 2 || slots > 4) slots = 2;
+    const bool dres = p.dres != nullptr;
+    const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
+    int teams = 512 / tthr;
+    if (teams > 15) teams = 15;
+    const int want_teams = g_opts[RN_OPT_TEAMS_PER_CTA];
+    if (want_teams >= 1 && want_teams <= 15 && want_teams * tthr <= 512) teams = want_teams;
+    size_t smem = stage_smem_bytes(p.N, p.dtype, dres, teams, slots, cpt, tthr, nullptr, nullptr);
+    while (teams > 1 && smem > budget) {
+        --teams;
+        smem = stage_smem_bytes(p.N, p.dtype, dres, teams, slots, cpt, tthr, nullptr, nullptr);
+    }
+    if (smem > d.smem_optin) return false;
+    plan->cpt = cpt;
+    plan->team_threads = tthr;
+    plan->teams = teams;
+    plan->slots = slots;
+    plan->smem = smem;
+    plan->atomic = atomic;
+    const int per_sm = stage_blocks_per_sm(p.dtype, dres, atomic, cpt, teams * tthr, smem);
+    plan->grid = phase_grid(p.M, phase_period(p.N, p.dtype), per_sm, d);
+    plan->skip_row = g_opts[RN_OPT_TEST_WAIT_TIMEOUT] > 0 ? g_opts[RN_OPT_TEST_WAIT_TIMEOUT] - 1 : -1;
+    return true;
+}
+
 static void plan_generic(const BwdProblem &p, const DeviceInfo &d, bool atomic, GenericPlan *plan) {
     plan->cpb = 0;
     plan->phase = 0;
-    // RN_OPT_GENERIC_KERNEL: 1 phase-class, 2 vector, 3 realigning, 4 element-wise
+    // RN_OPT_GENERIC_KERNEL: 1 phase-class, 2 vector, 3 realigning, 4 element-wise (5, the
+    // staged phase-class kernel, is planned before this)
     const int pick = g_opts[RN_OPT_GENERIC_KERNEL];
-    if (pick <= 1 && plan_phase(p, d, atomic, plan)) return;
+    if ((pick <= 1 || pick == 5) && plan_phase(p, d, atomic, plan)) return;
     if (pick == 3 && plan_realign(p, d, plan)) return;
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
@@ -570,6 +625,13 @@ static void plan_string_row(const RowPlan &rp, const char *engine, bool atomic) 
              atomic ? "atomic" : "scratch");
 }
 
+static void plan_string_stage(const StagePlan &sp, const char *engine, bool atomic) {
+    snprintf(g_plan, sizeof(g_plan),
+             "engine=%s staged cpt=%d team_threads=%d teams=%d slots=%d grid=%d smem=%zu dw=%s",
+             engine, sp.cpt, sp.team_threads, sp.teams, sp.slots, sp.grid, sp.smem,
+             atomic ? "atomic" : "scratch");
+}
+
 static void plan_string_generic(const GenericPlan &gp, const char *engine, bool atomic) {
     if (gp.phase)
         snprintf(g_plan, sizeof(g_plan),
@@ -653,6 +715,15 @@ static rn_status run_bwd(const BwdProblem &p, size_t ws_bytes, cudaStream_t s) {
         const DwOutputs o = {p.dw_f32, p.dw_cast, nullptr, nullptr, p.N, p.dtype,
                              partials, cp.clusters, p.N};
         return run_sequence(atomic, o, s, [&](bool pdl) { return launch_bwd_cluster(p, cp, s, pdl); });
+    }
+    // the staged phase-class kernel first (RN_OPT_GENERIC_KERNEL automatic or 5)
+    StagePlan sp;
+    const int gpick = g_opts[RN_OPT_GENERIC_KERNEL];
+    if (!use_row && (gpick == 0 || gpick == 5) && plan_stage(p, d, atomic, gpick == 5, &sp)) {
+        plan_string_stage(sp, "generic", atomic);
+        const DwOutputs o = {p.dw_f32, p.dw_cast, nullptr, nullptr, p.N, p.dtype,
+                             partials, sp.grid, p.N};
+        return run_sequence(atomic, o, s, [&](bool pdl) { return launch_bwd_stage(p, sp, s, pdl); });
     }
     if (!use_row) plan_generic(p, d, atomic, &gp);
     if (!use_row && atomic && !gp.rows && !gp.cpb && !gp.phase &&
@@ -760,8 +831,8 @@ static void plan_ln_generic(const LnBwdProblem &p, const DeviceInfo &d, bool ato
                             GenericPlan *plan) {
     plan->phase = 0;
     // RN_OPT_GENERIC_KERNEL: 1 phase-class, 2 (or 3) vector, 4 element-wise
-    const int pick = g_opts[RN_OPT_GENERIC_KERNEL];
-    if (pick <= 1 && plan_ln_phase(p, d, atomic, plan)) return;
+    const int pick = g_opts[RN_OPT_GENERIC_KERNEL];  // 5 (staged, RMSNorm only) as automatic
+    if ((pick <= 1 || pick == 5) && plan_ln_phase(p, d, atomic, plan)) return;
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
     plan->smem_dw = ln_generic_smem_bytes(p.N, true) <= budget;
@@ -1154,6 +1225,13 @@ rn_status rn_set_option(int option, int value) {
 int rn_get_option(int option) {
     if (option < 0 || option >= RN_OPT_COUNT) return -1;
     return g_opts[option];
+}
+
+rn_status rn_take_device_status(unsigned int *status) {
+    g_err[0] = 0;
+    if (!status) return fail(RN_ERR_INVALID_ARG, "status is NULL");
+    cudaError_t e = take_device_status(status);
+    return e == cudaSuccess ? RN_OK : cuda_fail(e, "device status");
 }
 
 rn_status rn_set_profile_events(void *ev_begin, void *ev_end) {

@@ -64,6 +64,19 @@ struct GenericPlan {
     bool prefetch = false;  // phase-class kernel: L2 prefetch two iterations ahead
 };
 
+// Launch shape of the staged phase-class kernel (rows that are not 16-byte
+// multiples, staged in shared memory by bulk copies).
+struct StagePlan {
+    int cpt;           // 16-byte chunks per thread (1, 2, 4)
+    int team_threads;  // threads that share one row (multiple of 32)
+    int teams;         // rows in progress per CTA (1..15)
+    int slots;         // shared-memory slots per team (2..4): rows in flight + 1
+    int grid;          // CTAs (persistent)
+    size_t smem;       // dynamic shared memory bytes
+    bool atomic;
+    int64_t skip_row = -1;  // test hook (see RN_OPT_TEST_WAIT_TIMEOUT); -1 = off
+};
+
 // Row engine: largest chunk count per row and CTA thread cap for a cpt.
 constexpr int kRowMaxChunks = 2048;
 int row_max_threads(int cpt);
@@ -82,6 +95,19 @@ size_t ln_phase_smem_bytes(int N, bool atomic);
 int ln_phase_blocks_per_sm(int dtype, bool atomic, int cpt, int threads, size_t smem);
 cudaError_t launch_bwd_phase(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
                              bool pdl_after_zero);
+// Staged phase-class kernel: its shared memory for a tile (the ring, or the
+// teams' weight-gradient regions if larger), and the per-tensor slot size and
+// one team's region in words it lays out.
+uint32_t stage_ring_offset(int slots);
+size_t stage_smem_bytes(int N, int dtype, bool dres, int teams, int slots, int cpt,
+                        int team_threads, uint32_t *tensor_bytes, uint32_t *region_words);
+// Resident CTAs per SM of one instance at a CTA size and dynamic shared memory.
+int stage_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads, size_t smem);
+cudaError_t launch_bwd_stage(const BwdProblem &p, const StagePlan &plan, cudaStream_t s,
+                             bool pdl_after_zero);
+// Read and clear the device status word (bit 0: a bounded wait in a kernel ran
+// out); synchronizes the device first.
+cudaError_t take_device_status(unsigned int *status);
 size_t realign_smem_bytes(int N, int dtype, int rows, bool dres);
 cudaError_t launch_bwd_realign(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
                                bool pdl_after_zero);

@@ -17,8 +17,8 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "rmsnorm_gb300.h")
 RN_OK, RN_ERR_INVALID_ARG, RN_ERR_UNSUPPORTED, RN_ERR_CUDA, RN_ERR_WORKSPACE = range(5)
 RN_F32, RN_F16, RN_BF16 = 0, 1, 2
 (OPT_BWD_ENGINE, OPT_DWEIGHT_MODE, OPT_CHUNKS_PER_THREAD, OPT_TEAMS_PER_CTA, OPT_STAGES, OPT_GRID,
- OPT_CLUSTER_SIZE, OPT_GENERIC_KERNEL) = range(8)
-OPT_COUNT = 8
+ OPT_CLUSTER_SIZE, OPT_GENERIC_KERNEL, OPT_TEST_WAIT_TIMEOUT) = range(9)
+OPT_COUNT = 9
 
 _lib = None
 
@@ -64,17 +64,20 @@ def _bind(lib):
     lib.rn_get_option.argtypes = [ci]
     lib.rn_set_profile_events.restype = ci
     lib.rn_set_profile_events.argtypes = [vp, vp]
+    lib.rn_take_device_status.restype = ci
+    lib.rn_take_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     return lib
 
 
 # Process-wide overrides read from the environment when the library loads:
 #   RN_BWD_ENGINE   = auto | row | generic | cluster
 #   RN_DWEIGHT_MODE = auto | scratch (deterministic) | atomic
-#   RN_GENERIC_KERNEL = auto | phase | vec | realign | scalar (unaligned rows)
+#   RN_GENERIC_KERNEL = auto | phase | vec | realign | scalar | staged (unaligned rows)
 ENV_OPTIONS = {
     "RN_BWD_ENGINE": (0, {"auto": 0, "row": 1, "generic": 2, "cluster": 3}),
     "RN_DWEIGHT_MODE": (1, {"auto": 0, "scratch": 1, "atomic": 2}),
-    "RN_GENERIC_KERNEL": (7, {"auto": 0, "phase": 1, "vec": 2, "realign": 3, "scalar": 4}),
+    "RN_GENERIC_KERNEL": (7, {"auto": 0, "phase": 1, "vec": 2, "realign": 3, "scalar": 4,
+                              "staged": 5}),
 }
 
 
@@ -140,6 +143,14 @@ def header_functions():
 
 def last_plan():
     return lib().rn_last_plan().decode()
+
+
+def take_device_status():
+    """Read and clear the current device's status word (bit 0: a bounded wait
+    in a kernel ran out). Synchronizes the device."""
+    v = ctypes.c_uint(0)
+    check(lib().rn_take_device_status(ctypes.byref(v)))
+    return int(v.value)
 
 
 def set_option(opt, value):

@@ -97,7 +97,8 @@ def test_python_guards_refuse_host_tensors():
                                           ({"RN_BWD_ENGINE": "generic"}, 0, 2),
                                           ({"RN_DWEIGHT_MODE": "scratch"}, 1, 1),
                                           ({"RN_DWEIGHT_MODE": "ATOMIC"}, 1, 2),
-                                          ({"RN_GENERIC_KERNEL": "realign"}, 7, 3)])
+                                          ({"RN_GENERIC_KERNEL": "realign"}, 7, 3),
+                                          ({"RN_GENERIC_KERNEL": "staged"}, 7, 5)])
 def test_environment_overrides_options(env, opt, want):
     import subprocess
     import sys

@@ -588,8 +588,10 @@ def test_row_engine_default_tiles(M, N, dt, fused, want):
     (500, 4095, "bf16", False, "cpt=2 rows=2 ")],   # neither: no prefetch
     ids=lambda v: str(v))
 def test_generic_phase_kernel_prefetch(M, N, dt, fused, want):
-    """The planner's L2-prefetch choice for the phase-class kernel, and the
-    results with and without it."""
+    """The planner's L2-prefetch choice for the phase-class kernel (forced:
+    from 2048 rows the staged kernel is the default), and the results with
+    and without it."""
+    native.set_option(native.OPT_GENERIC_KERNEL, 1)
     ex = parity.expected_bwd(Case("phase prefetch %s" % dt, M, N, dt, fused=fused,
                                   with_dres=fused, seed=46))
     out = parity.run_gpu_bwd(ex)

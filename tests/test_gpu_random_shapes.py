@@ -38,6 +38,13 @@ def _draw(seed):
     return M, N, dt, variant, phases
 
 
+@pytest.fixture(autouse=True)
+def _reset_options():
+    yield
+    for opt in range(native.OPT_COUNT):
+        native.set_option(opt, 0)
+
+
 _ENGINES = set()   # the backward engines the random cases took (checked by the last test)
 
 
@@ -45,7 +52,8 @@ def _engine(plan):
     head = plan.split()
     if not head:
         return ""
-    if head[0] == "engine=generic" and len(head) > 1 and head[1] in ("phase", "realign", "vec"):
+    if head[0] == "engine=generic" and len(head) > 1 and head[1] in ("phase", "realign", "vec",
+                                                                      "staged"):
         return "generic " + head[1]
     return head[0].split("=", 1)[1]
 
@@ -59,6 +67,10 @@ def _placed(t, shift):
 
 @pytest.mark.parametrize("seed", range(48))
 def test_random_backward(seed):
+    """Odd seeds ask for the staged phase-class kernel (below 2048 rows the
+    automatic choice is the phase-class kernel): it takes the one-phase
+    unaligned ones; the rest fall back as the automatic choice would."""
+    native.set_option(native.OPT_GENERIC_KERNEL, 5 if seed % 2 else 0)
     M, N, dt, variant, ph = _draw(seed)
     fused = variant != "plain"
     case = Case("random %d" % seed, M, N, dt, fused=fused, with_dres=variant == "fused",
@@ -82,7 +94,7 @@ def test_random_backward(seed):
 def test_random_backward_cases_reached_every_engine():
     """The sweep above is only worth its seeds if it reaches every engine."""
     # (the realigning engine is taken only when asked for: its own tests cover it)
-    want = {"row", "cluster", "generic phase", "generic vec", "generic"}
+    want = {"row", "cluster", "generic staged", "generic phase", "generic vec", "generic"}
     assert want <= _ENGINES, "engines not reached: %s (reached %s)" % (want - _ENGINES, _ENGINES)
 
 
