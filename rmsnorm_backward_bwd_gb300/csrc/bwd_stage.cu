@@ -22,9 +22,13 @@
 //     issued by lane 0, completing on the warp's own mbarrier of the slot).
 //     A team has `Sq` slots; at the top of row j the warp refills the slot it
 //     finished with in row j-1 with row j+Sq-1, so no barrier guards the
-//     ring: only the warp itself reads what it copied. The head and tail
-//     elements (fewer than 16 per row, all in the team's first warp) and
-//     rstd are loaded one row ahead into registers.
+//     ring: only the warp itself reads what it copied. The 16-byte blocks
+//     that hold the row's head and tail elements (fewer than 16 per row)
+//     ride on the first warp's and the last warp's copies, which start 16
+//     bytes early and end 16 bytes late; lanes of those warps own the
+//     elements. A block that would reach outside the tensor (the first and
+//     last rows) is not copied and its lanes read their elements from global
+//     memory. rstd is loaded one row ahead.
 //   * Pass 1 sums x*dy*gamma over the row (warp shuffles, then the team's
 //     named barrier); pass 2 reads the slot again and stores dx with 16-byte
 //     stores (the class's chunks are 16-byte aligned in every row tensor).
@@ -92,6 +96,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         if ((n & 255u) == 0 && global_ns() - t0 > limit) return false;
     }
 }
+// One element of a row tensor from shared memory, widened to fp32.
+template <typename T> __device__ __forceinline__ float lds_elem(uint32_t addr);
+template <> __device__ __forceinline__ float lds_elem<float>(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+template <> __device__ __forceinline__ float lds_elem<__nv_bfloat16>(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return __bfloat162float(__ushort_as_bfloat16(v));
+}
+template <> __device__ __forceinline__ float lds_elem<__half>(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return __half2float(__ushort_as_half(v));
+}
+
 // Bulk copy global -> this CTA's shared memory, completing `bytes` of the
 // mbarrier's transaction count (addresses 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
@@ -106,8 +128,13 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
 // Shared memory: [0,256) warp sums [2 parities][32 warps]; [256,512) wait
 // outcomes, same layout; [512, 512 + 8*16*Sq) the warps' full barriers
 // (warp w, slot u at w*Sq + u); the ring from stage_ring_offset(Sq): team t's
-// slot u at (t*Sq + u)*stage_bytes, tensor k of a slot at k*tensor_bytes.
+// slot u at (t*Sq + u)*stage_bytes, tensor k of a slot at k*tensor_bytes;
+// within a tensor the head block at 0, whole chunk i at 16 + 16i and the
+// tail block after the last whole chunk.
 constexpr uint32_t kStageBarOffset = 512;
+// Within a tensor's slot: the whole chunks from byte kMid (128-byte aligned, as the bulk copies
+// of the chunks land), the head block just before them, the tail block just after.
+constexpr uint32_t kMid = 128;
 
 }  // namespace
 
@@ -162,11 +189,17 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
     const int64_t rstride = nper * P;
     const int64_t row0 = cls + (int64_t)(blockIdx.x / (unsigned)P) * P;
     const int64_t nrows = row0 < a.M ? (a.M - 1 - row0) / rstride + 1 : 0;
-    // the class's split (address arithmetic on row cls; nothing is read there)
+    // the class's split (address arithmetic on row cls; nothing is read there): h head
+    // elements before the first 16-byte boundary, nv whole chunks, `tail` elements after
     const uintptr_t start = reinterpret_cast<uintptr_t>(a.x) + (uintptr_t)cls * (uintptr_t)N * S;
-    int h = (int)(((16u - (unsigned)(start & 15u)) & 15u) / S);
-    if (h > N) h = N;
+    const int h_free = (int)(((16u - (unsigned)(start & 15u)) & 15u) / S);
+    // A row that holds a 16-byte boundary has its head in the 16-byte block that ends at the
+    // first boundary and its tail in the block that starts at the last one; those blocks are
+    // copied with the row wherever they lie inside the tensor.
+    const bool blocks = h_free <= N;
+    const int h = blocks ? h_free : N;
     const int nv = (N - h) / V, tail = N - h - nv * V;
+    const int64_t total = a.M * (int64_t)N;  // elements of a row tensor
 
     const int team_warps = a.team_threads >> 5;
     const int team = tid / a.team_threads;
@@ -189,29 +222,39 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
     }
     __syncthreads();
 
-    // Lane 0: copies of this warp's span of the team's rows, in order.
+    // Lane 0: copies of this warp's span of the team's rows, in order; the team's first warp
+    // also copies the row's head and tail blocks (those inside the tensor).
     const uint64_t policy = l2_policy_evict_first();
     const uint32_t bytes = (uint32_t)wn * 16u;
+    // The team's first warp also copies the head block (its copy starts 16 bytes early), the
+    // warp holding the last whole chunk the tail block (its copy ends 16 bytes late).
+    const int w_last = nv > 0 ? (nv - 1) / (32 * J) : 0;
+    const bool w_head = warp == first_warp, w_tail = warp == first_warp + w_last;
     const bool skipper = a.skip_row >= 0 && blockIdx.x == 0 && tid == 0;
-    int64_t issued = 0;                              // rows issued
-    int64_t ioff = trow0 * N + h + (int64_t)c0 * V;  // element offset of row `issued`'s span
-    int iu = 0;                                      // its slot
+    int64_t issued = 0;                   // rows issued
+    int64_t irow_e0 = trow0 * N + h;      // element of row `issued`'s first 16-byte boundary
+    int iu = 0;                           // its slot
     auto issue = [&]() {
         const uint32_t bar = wbar + 8u * (uint32_t)iu;
-        const size_t off = (size_t)ioff;
+        const int64_t e0 = irow_e0;
+        const bool hb = w_head && blocks && h > 0 && e0 - V >= 0;
+        const bool tb = w_tail && blocks && tail > 0 && e0 + (int64_t)(nv + 1) * V <= total;
+        const uint32_t nbytes = bytes + (hb ? 16u : 0u) + (tb ? 16u : 0u);
         if (skipper && issued == a.skip_row) {
             // test hook: nothing arrives, so this slot's wait runs out
-        } else if (bytes == 0) {
+        } else if (nbytes == 0) {
             mbar_arrive(bar);
         } else {
-            const uint32_t dst = tring + (uint32_t)iu * a.stage_bytes + 16u * (uint32_t)c0;
-            mbar_arrive_expect_tx(bar, NT * bytes);
-            bulk_copy_g2s(dst, x + off, bytes, bar, policy);
-            bulk_copy_g2s(dst + a.tensor_bytes, dy + off, bytes, bar, policy);
-            if (HAS_DRES) bulk_copy_g2s(dst + 2 * a.tensor_bytes, dres + off, bytes, bar, policy);
+            const size_t off = (size_t)(e0 + (int64_t)c0 * V - (hb ? V : 0));
+            const uint32_t dst =
+                tring + (uint32_t)iu * a.stage_bytes + kMid + 16u * (uint32_t)c0 - (hb ? 16u : 0u);
+            mbar_arrive_expect_tx(bar, NT * nbytes);
+            bulk_copy_g2s(dst, x + off, nbytes, bar, policy);
+            bulk_copy_g2s(dst + a.tensor_bytes, dy + off, nbytes, bar, policy);
+            if (HAS_DRES) bulk_copy_g2s(dst + 2 * a.tensor_bytes, dres + off, nbytes, bar, policy);
         }
         ++issued;
-        ioff += tstep;
+        irow_e0 += tstep;
         if (++iu == Sq) iu = 0;
     };
     if (lane == 0)
@@ -238,23 +281,21 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
 #pragma unroll
         for (int q = 0; q < P2; ++q) acc2[k][q] = f2_make(0.f, 0.f);
     }
-    const bool e_own = tt < h + tail;
-    const int je = tt < h ? tt : h + nv * V + (tt - h);
+    // the head or tail element of this thread: head elements on the first lanes of the team's
+    // first warp, tail elements on the last lanes of the warp that copies the tail block (each
+    // reads only what its own warp copied); the element's column and its byte offset in a
+    // tensor's slot
+    const bool e_head = w_head && lane < h;
+    const bool e_tail = w_tail && lane >= 32 - tail;
+    const bool e_own = e_head || e_tail;
+    const int je = e_head ? lane : h + nv * V + (lane - (32 - tail));
+    const uint32_t e_soff = e_head ? kMid - 16u + (uint32_t)(S * (V - h + lane))
+                                   : kMid + 16u * (uint32_t)nv + (uint32_t)(S * (lane - (32 - tail)));
     const float ge = e_own ? to_f(g[je]) : 0.f;
     float dwe = 0.f;
 
-    // rstd and the head or tail element of the team's next row, one row ahead
-    float rs_n = 0.f, xe_n = 0.f, de_n = 0.f, re_n = 0.f;
-    auto scalars = [&](int64_t row) {
-        rs_n = __ldg(a.rstd + row);
-        if (e_own) {
-            const size_t e = (size_t)row * N + je;
-            xe_n = to_f(x[e]);
-            de_n = to_f(dy[e]);
-            if (HAS_DRES) re_n = to_f(dres[e]);
-        }
-    };
-    if (tn > 0) scalars(trow0);
+    // rstd of the team's next row, one row ahead
+    float rs_n = tn > 0 ? __ldg(a.rstd + trow0) : 0.f;
 
     bool failed = false;
     int64_t j = 0;
@@ -266,17 +307,34 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
         // every lane of this warp is done with row j-1: its slot takes row j+Sq-1
         __syncwarp();
         if (lane == 0 && issued < tn) issue();
-        const float rs = rs_n, xe = xe_n, de = de_n, re = re_n;
-        if (j + 1 < tn) scalars(row + tstride);
+        const float rs = rs_n;
+        if (j + 1 < tn) rs_n = __ldg(a.rstd + row + tstride);
         const bool ok = mbar_wait_bounded(wbar + 8u * (uint32_t)u, ph, kWaitLimitNs);
         const uint32_t sb = tring + (uint32_t)u * a.stage_bytes;
+        const uint32_t sm = sb + kMid;  // the row's whole chunks
+        // this row's head or tail element: from its copied block, or (a block that would
+        // reach outside the tensor: the first and last rows) from global memory
+        bool e_smem = false;
+        float xe = 0.f, de = 0.f;
+        if (e_own) {
+            const int64_t e0 = row * N + h;
+            e_smem = blocks && (e_head ? e0 - V >= 0 : e0 + (int64_t)(nv + 1) * V <= total);
+            if (e_smem) {
+                xe = lds_elem<T>(sb + e_soff);
+                de = lds_elem<T>(sb + a.tensor_bytes + e_soff);
+            } else {
+                const size_t e = (size_t)row * N + je;
+                xe = to_f(x[e]);
+                de = to_f(dy[e]);
+            }
+        }
 
         f32x2 part2 = f2_make(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < J; ++k) {
             const uint32_t c16 = 16u * (uint32_t)(c0 + lane + 32 * k);
             if (own[k])
-                part2 = RowMath<T>::pass1(ld_shared_v4(sb + c16), ld_shared_v4(sb + a.tensor_bytes + c16),
+                part2 = RowMath<T>::pass1(ld_shared_v4(sm + c16), ld_shared_v4(sm + a.tensor_bytes + c16),
                                           gp[k], kGammaF ? g2[kGammaF ? k : 0] : nullptr, part2);
         }
         float plo, phi;
@@ -308,17 +366,19 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
         for (int k = 0; k < J; ++k) {
             if (own[k]) {
                 const uint32_t c16 = 16u * (uint32_t)(c0 + lane + 32 * k);
-                const uint4 r = HAS_DRES ? ld_shared_v4(sb + 2 * a.tensor_bytes + c16)
+                const uint4 r = HAS_DRES ? ld_shared_v4(sm + 2 * a.tensor_bytes + c16)
                                          : make_uint4(0, 0, 0, 0);
                 const uint4 out = RowMath<T>::template pass2<HAS_DRES>(
-                    ld_shared_v4(sb + c16), ld_shared_v4(sb + a.tensor_bytes + c16), r, gp[k],
+                    ld_shared_v4(sm + c16), ld_shared_v4(sm + a.tensor_bytes + c16), r, gp[k],
                     kGammaF ? g2[kGammaF ? k : 0] : nullptr, rs2, b2, acc2[k]);
                 st_global_v4(dxr + col[k], out);
             }
         }
         if (e_own) {
             float d = fmaf(xe, b, (de * ge) * rs);
-            if (HAS_DRES) d += re;
+            if (HAS_DRES)
+                d += e_smem ? lds_elem<T>(sb + 2 * a.tensor_bytes + e_soff)
+                            : to_f(dres[(size_t)row * N + je]);
             dxr[je] = from_f<T>(d);
             dwe = fmaf(xe * de, rs, dwe);
         }
@@ -405,7 +465,8 @@ size_t stage_smem_bytes(int N, int dtype, bool dres, int teams, int slots, int c
     const int64_t maxnv = (int64_t)N / V;  // whole chunks of any class's row
     (void)cpt;
     (void)team_threads;
-    const uint32_t tb = (uint32_t)((maxnv * 16 + 127) / 128 * 128);
+    // a tensor's slot: the head block, the whole chunks, the tail block
+    const uint32_t tb = (uint32_t)((kMid + (maxnv + 1) * 16 + 127) / 128 * 128);
     const uint32_t rwords = (uint32_t)((vec_words(N) + 31) / 32 * 32);
     if (tensor_bytes) *tensor_bytes = tb;
     if (region_words) *region_words = rwords;
