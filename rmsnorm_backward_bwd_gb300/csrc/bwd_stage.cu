@@ -172,6 +172,12 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
     constexpr int NT = HAS_DRES ? 3 : 2;
     // gamma also as fp32 pairs when the math needs it or when that fits
     constexpr bool kGammaF = RowMath<T>::kNeedsGammaF || J * V <= 8;
+    // The head and tail elements come with the bulk copies (kFold) or are loaded one row ahead
+    // into registers by lanes of the team's first warp. Measured on GB300 (us per call, registers
+    // -> folded): bf16 4096 x 4095 27.6 -> 25.1, 4096 x 12290 66.6 -> 58.3, f16 16384 x 1001
+    // 28.4 -> 27.2, f32 fused 4096 x 4095 +dres 43.3 -> 40.5; plain f32 loses (4096 x 4095
+    // 31.9 -> 35.0, 8192 x 6001 94.1 -> 101.5, 4096 x 2047 21.5 -> 23.6), so it keeps registers.
+    constexpr bool kFold = S == 2 || HAS_DRES;
     extern __shared__ __align__(128) uint8_t smem[];
     float *red = reinterpret_cast<float *>(smem);
     int *okf = reinterpret_cast<int *>(smem + 256);
@@ -222,12 +228,12 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
     }
     __syncthreads();
 
-    // Lane 0: copies of this warp's span of the team's rows, in order; the team's first warp
-    // also copies the row's head and tail blocks (those inside the tensor).
+    // Lane 0: copies of this warp's span of the team's rows, in order. Folded edges: the team's
+    // first warp also copies the head block (its copy starts 16 bytes early), the warp holding
+    // the last whole chunk the tail block (its copy ends 16 bytes late), where they lie inside
+    // the tensor.
     const uint64_t policy = l2_policy_evict_first();
     const uint32_t bytes = (uint32_t)wn * 16u;
-    // The team's first warp also copies the head block (its copy starts 16 bytes early), the
-    // warp holding the last whole chunk the tail block (its copy ends 16 bytes late).
     const int w_last = nv > 0 ? (nv - 1) / (32 * J) : 0;
     const bool w_head = warp == first_warp, w_tail = warp == first_warp + w_last;
     const bool skipper = a.skip_row >= 0 && blockIdx.x == 0 && tid == 0;
@@ -237,8 +243,8 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
     auto issue = [&]() {
         const uint32_t bar = wbar + 8u * (uint32_t)iu;
         const int64_t e0 = irow_e0;
-        const bool hb = w_head && blocks && h > 0 && e0 - V >= 0;
-        const bool tb = w_tail && blocks && tail > 0 && e0 + (int64_t)(nv + 1) * V <= total;
+        const bool hb = kFold && w_head && blocks && h > 0 && e0 - V >= 0;
+        const bool tb = kFold && w_tail && blocks && tail > 0 && e0 + (int64_t)(nv + 1) * V <= total;
         const uint32_t nbytes = bytes + (hb ? 16u : 0u) + (tb ? 16u : 0u);
         if (skipper && issued == a.skip_row) {
             // test hook: nothing arrives, so this slot's wait runs out
@@ -281,18 +287,30 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
 #pragma unroll
         for (int q = 0; q < P2; ++q) acc2[k][q] = f2_make(0.f, 0.f);
     }
-    // the head or tail element of this thread: head elements on the first lanes of the team's
-    // first warp, tail elements on the last lanes of the warp that copies the tail block (each
-    // reads only what its own warp copied); the element's column and its byte offset in a
-    // tensor's slot
-    const bool e_head = w_head && lane < h;
-    const bool e_tail = w_tail && lane >= 32 - tail;
+    // the head or tail element of this thread and its column. Folded: head elements on the
+    // first lanes of the team's first warp, tail elements on the last lanes of the warp that
+    // copies the tail block (each reads only what its own warp copied), with the element's byte
+    // offset in a tensor's slot. Otherwise: the first h + tail threads of the team.
+    const bool e_head = kFold ? w_head && lane < h : tt < h;
+    const bool e_tail = kFold ? w_tail && lane >= 32 - tail : tt >= h && tt < h + tail;
     const bool e_own = e_head || e_tail;
-    const int je = e_head ? lane : h + nv * V + (lane - (32 - tail));
+    const int je = e_head ? (kFold ? lane : tt)
+                          : h + nv * V + (kFold ? lane - (32 - tail) : tt - h);
     const uint32_t e_soff = e_head ? kMid - 16u + (uint32_t)(S * (V - h + lane))
                                    : kMid + 16u * (uint32_t)nv + (uint32_t)(S * (lane - (32 - tail)));
     const float ge = e_own ? to_f(g[je]) : 0.f;
     float dwe = 0.f;
+    // registers: the team's next row's head or tail element
+    float xe_n = 0.f, de_n = 0.f, re_n = 0.f;
+    auto edge_next = [&](int64_t r) {
+        if (!kFold && e_own) {
+            const size_t e = (size_t)r * N + je;
+            xe_n = to_f(x[e]);
+            de_n = to_f(dy[e]);
+            if (HAS_DRES) re_n = to_f(dres[e]);
+        }
+    };
+    if (tn > 0) edge_next(trow0);
 
     // rstd of the team's next row, one row ahead
     float rs_n = tn > 0 ? __ldg(a.rstd + trow0) : 0.f;
@@ -308,27 +326,31 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
         __syncwarp();
         if (lane == 0 && issued < tn) issue();
         const float rs = rs_n;
-        if (j + 1 < tn) rs_n = __ldg(a.rstd + row + tstride);
+        float xe = xe_n, de = de_n, re = re_n;
+        if (j + 1 < tn) {
+            rs_n = __ldg(a.rstd + row + tstride);
+            edge_next(row + tstride);
+        }
         const bool ok = mbar_wait_bounded(wbar + 8u * (uint32_t)u, ph, kWaitLimitNs);
         const uint32_t sb = tring + (uint32_t)u * a.stage_bytes;
         const uint32_t sm = sb + kMid;  // the row's whole chunks
-        // this row's head or tail element: from its copied block, or (a block that would
+        // folded: this row's head or tail element from its copied block, or (a block that would
         // reach outside the tensor: the first and last rows) from global memory
         bool e_smem = false;
-        float xe = 0.f, de = 0.f;
-        if (e_own) {
+        if (kFold && e_own) {
             const int64_t e0 = row * N + h;
             e_smem = blocks && (e_head ? e0 - V >= 0 : e0 + (int64_t)(nv + 1) * V <= total);
             if (e_smem) {
                 xe = lds_elem<T>(sb + e_soff);
                 de = lds_elem<T>(sb + a.tensor_bytes + e_soff);
+                if (HAS_DRES) re = lds_elem<T>(sb + 2 * a.tensor_bytes + e_soff);
             } else {
                 const size_t e = (size_t)row * N + je;
                 xe = to_f(x[e]);
                 de = to_f(dy[e]);
+                if (HAS_DRES) re = to_f(dres[e]);
             }
         }
-
         f32x2 part2 = f2_make(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < J; ++k) {
@@ -376,9 +398,7 @@ __global__ void __launch_bounds__(512, 1) bwd_stage_kernel(const StageArgs a) {
         }
         if (e_own) {
             float d = fmaf(xe, b, (de * ge) * rs);
-            if (HAS_DRES)
-                d += e_smem ? lds_elem<T>(sb + 2 * a.tensor_bytes + e_soff)
-                            : to_f(dres[(size_t)row * N + je]);
+            if (HAS_DRES) d += re;
             dxr[je] = from_f<T>(d);
             dwe = fmaf(xe * de, rs, dwe);
         }
