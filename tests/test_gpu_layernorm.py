@@ -217,6 +217,31 @@ def test_layernorm_fwd_matches_oracle(M, N, dt, with_bias):
     assert np.all(np.abs(parity.to64(rstd) - ex.rstd64) <= tol * ex.rstd64)
 
 
+@pytest.mark.parametrize("shift,M,N,dt", [(1000.0, 64, 4096, "f32"), (-300.0, 33, 1000, "f32"),
+                                          (48.0, 128, 4096, "bf16"), (12.0, 40, 8192, "f16"),
+                                          (1000.0, 17, 16384, "f32")],
+                         ids=lambda v: str(v))
+def test_layernorm_fwd_large_mean(shift, M, N, dt):
+    """Rows whose mean is far larger than their spread (x = shift + N(0, 1)): the
+    statistics merged pairwise over the team (count, mean, centred sum of
+    squares) keep mean and rstd within the same bound as centred rows."""
+    case = Case("ln large mean", M, N, dt, eps=1e-5, seed=13)
+    inp = synth.make_ln_inputs(case, x_shift=shift)
+    x64, g64, b64 = (parity.to64(inp[k]) for k in ("x", "gamma", "beta"))
+    y64, mean64, rstd64 = oracle.layernorm_fwd(x64, g64, b64, np.float32(case.eps))
+    y, mean, rstd = rn.layernorm_fwd(inp["x"].cuda(), inp["gamma"].cuda(), inp["beta"].cuda(),
+                                     1e-5)
+    torch.cuda.synchronize()
+    tol = _stat_tol(N)
+    assert np.all(np.abs(parity.to64(mean) - mean64) <= tol * np.mean(np.abs(x64), axis=1))
+    assert np.all(np.abs(parity.to64(rstd) - rstd64) <= tol * rstd64)
+    # y = (x - mean)*rstd*gamma + beta: an fp32 mean of values near `shift` is off by about
+    # shift*2^-24*log2(N) absolute, which y carries relative to |x - mean| ~ 1; below the
+    # 16-bit dtypes' unit in the last place, far above the f32 bound
+    if dt != "f32":
+        parity.check_tensor("y", y, y64, dt, "y")
+
+
 def test_layernorm_fwd_guards():
     x = torch.randn(4, 256, device="cuda", dtype=torch.bfloat16)
     g = torch.ones(256, device="cuda", dtype=torch.bfloat16)
