@@ -264,20 +264,21 @@ typedef enum rn_option {
                                  phase-class kernel: shared-memory slots per team (2..4) */
     RN_OPT_GRID = 5,          /* CTAs of the row pass (default: one per SM; at most 2 per SM) */
     RN_OPT_CLUSTER_SIZE = 6,  /* cluster engine: CTAs per cluster, 2, 4, 8 or 16 */
-    RN_OPT_GENERIC_KERNEL = 7, /* RMSNorm backward, generic engines: 1 = phase-class kernel
-                                 (rows held in registers), 2 = vector kernel, 3 = realigning
-                                 kernel (rows of 16 to 32 KB; taken only when asked for),
-                                 4 = element-wise kernel, 5 = staged phase-class kernel (rows
-                                 staged in shared memory by bulk copies; the automatic
-                                 choice). A kernel that cannot take the problem (its row-size
-                                 range, or tensors at different alignment phases) falls back
-                                 to the next one the automatic choice would make. */
-    RN_OPT_TEST_WAIT_TIMEOUT = 8, /* test hook, RMSNorm backward, staged phase-class kernel:
-                                 v > 0 makes the first CTA's first team leave its row v-1
-                                 (counted from 0 among that team's rows) uncopied, so that
-                                 the team's bounded wait (250 ms) runs out. The call then
-                                 leaves dx rows and the weight gradient incomplete and
-                                 rn_take_device_status() reports bit 0. */
+    RN_OPT_GENERIC_KERNEL = 7, /* backward generic engines: 1 = phase-class kernel (rows held
+                                 in registers), 2 = vector kernel, 3 = realigning kernel (RMSNorm,
+                                 rows of 16 to 32 KB; taken only when asked for), 4 = element-wise
+                                 kernel, 5 = staged phase-class kernel (rows staged in shared
+                                 memory by bulk copies; chosen automatically from 2048 rows,
+                                 LayerNorm: unless its tile is two teams). A kernel that cannot
+                                 take the problem (its row-size range, or tensors at different
+                                 alignment phases) falls back to the next one the automatic
+                                 choice would make. */
+    RN_OPT_TEST_WAIT_TIMEOUT = 8, /* test hook, RMSNorm and LayerNorm backward, staged
+                                 phase-class kernels: v > 0 makes the first CTA's first team
+                                 leave its row v-1 (counted from 0 among that team's rows)
+                                 uncopied, so that the team's bounded wait (250 ms) runs out.
+                                 The call then leaves dx rows and the weight gradients
+                                 incomplete and rn_take_device_status() reports bit 0. */
     RN_OPT_COUNT = 9
 } rn_option;
 
@@ -295,9 +296,10 @@ const char *rn_last_plan(void);
 /*
  * Device status word of the current device (kernels OR bits into it):
  *   bit 0 = a bounded wait inside a kernel ran out (the staged phase-class
- *           kernel waits at most 250 ms for a row's bulk copies). The team that
- *           waited stopped: the dx rows it had not reached and the weight
- *           gradient of that call are not valid. The CUDA context stays usable.
+ *           kernels, RMSNorm and LayerNorm, wait at most 250 ms for a row's
+ *           bulk copies). The team that waited stopped: the dx rows it had not
+ *           reached and the weight gradients of that call are not valid. The
+ *           CUDA context stays usable.
  * Synchronizes the device, stores the word in *status and clears it.
  * Returns RN_ERR_INVALID_ARG for a NULL status, RN_ERR_CUDA if a CUDA call fails.
  */

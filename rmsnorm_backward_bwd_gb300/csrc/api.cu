@@ -827,11 +827,64 @@ static bool plan_ln_phase(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
     return true;
 }
 
+// The LayerNorm staged phase-class kernel: x, dy and dx at one alignment
+// phase, at most 1024 whole 16-byte chunks a row, 2 chunks a thread
+// (RN_OPT_CHUNKS_PER_THREAD = 1 forces 1: two fp32 partials a column leave no
+// registers for 4), teams of the fewest whole warps that cover a row, 2 slots
+// a team (RN_OPT_STAGES 2..4), as many teams as fit 512 threads, 15 named
+// barriers and 200 KB (RN_OPT_TEAMS_PER_CTA forces 1..15), the phase-class
+// grid rule. Taken automatically from 2048 rows, as the RMSNorm staged kernel,
+// except where its tile is two teams. Measured on GB300 (L2 flushed, us per
+// call, phase-class -> staged): f16 16384 x 1001 62.1 -> 34.3 (8 teams), bf16
+// 16384 x 509 54.5 -> 25.7 (15), 4096 x 2047 27.5 -> 23.6 (4), 4096 x 8190 64.7
+// -> 58.4 (1), 16384 x 8190 211.2 -> 193.1 (1), f32 4096 x 4095 54.7 -> 43.9 (1),
+// f32 8192 x 2999 80.7 -> 67.0 (1); two teams of 256 threads: bf16 4096 x 4095
+// 35.7 -> 35.6, 16384 x 4095 97.0 -> 102.5, 4096 x 4100 35.5 -> 35.7 (3 or 4
+// slots a team no better); below 2048 rows 1024 x 4095 18.3 -> 19.5, 512 x 4095
+// 15.1 -> 16.8.
+static bool plan_ln_stage(const LnBwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
+                          StagePlan *plan) {
+    if (!forced && p.M < kStageMinRows) return false;
+    const uintptr_t S = (uintptr_t)elem_bytes(p.dtype), ph = (uintptr_t)p.x & 15u;
+    for (const void *q : {p.x, p.dy, static_cast<const void *>(p.dx)})
+        if (((uintptr_t)q & 15u) != ph || ((uintptr_t)q % S) != 0) return false;
+    const int64_t maxnv = (int64_t)p.N * elem_bytes(p.dtype) / 16;
+    if (maxnv > 1024) return false;
+    const int cpt = g_opts[RN_OPT_CHUNKS_PER_THREAD] == 1 ? 1 : 2;
+    int tthr = (int)((maxnv + cpt - 1) / cpt + 31) / 32 * 32;
+    if (tthr < 32) tthr = 32;
+    if (tthr > 512) return false;
+    int slots = g_opts[RN_OPT_STAGES];
+    if (slots < 2 || slots > 4) slots = 2;
+    const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
+    int teams = 512 / tthr;
+    if (teams > 15) teams = 15;
+    const int want_teams = g_opts[RN_OPT_TEAMS_PER_CTA];
+    if (want_teams >= 1 && want_teams <= 15 && want_teams * tthr <= 512) teams = want_teams;
+    size_t smem = ln_stage_smem_bytes(p.N, p.dtype, teams, slots, nullptr, nullptr);
+    while (teams > 1 && smem > budget) {
+        --teams;
+        smem = ln_stage_smem_bytes(p.N, p.dtype, teams, slots, nullptr, nullptr);
+    }
+    if (smem > d.smem_optin) return false;
+    if (!forced && teams == 2) return false;  // the phase-class kernel is as fast there
+    plan->cpt = cpt;
+    plan->team_threads = tthr;
+    plan->teams = teams;
+    plan->slots = slots;
+    plan->smem = smem;
+    plan->atomic = atomic;
+    const int per_sm = ln_stage_blocks_per_sm(p.dtype, atomic, cpt, teams * tthr, smem);
+    plan->grid = phase_grid(p.M, phase_period(p.N, p.dtype), per_sm, d);
+    plan->skip_row = g_opts[RN_OPT_TEST_WAIT_TIMEOUT] > 0 ? g_opts[RN_OPT_TEST_WAIT_TIMEOUT] - 1 : -1;
+    return true;
+}
+
 static void plan_ln_generic(const LnBwdProblem &p, const DeviceInfo &d, bool atomic,
                             GenericPlan *plan) {
     plan->phase = 0;
     // RN_OPT_GENERIC_KERNEL: 1 phase-class, 2 (or 3) vector, 4 element-wise
-    const int pick = g_opts[RN_OPT_GENERIC_KERNEL];  // 5 (staged, RMSNorm only) as automatic
+    const int pick = g_opts[RN_OPT_GENERIC_KERNEL];  // 5 (staged, planned before this) as 0
     if ((pick <= 1 || pick == 5) && plan_ln_phase(p, d, atomic, plan)) return;
     plan->threads = p.N >= 4096 ? 512 : 256;
     const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
@@ -906,6 +959,16 @@ static rn_status run_ln_bwd(const LnBwdProblem &p, size_t ws_bytes, cudaStream_t
                              partials, cp.clusters, 2 * p.N};
         return run_sequence(atomic, o, s,
                             [&](bool pdl) { return launch_ln_bwd_cluster(p, cp, s, pdl); });
+    }
+    // the staged phase-class kernel first (RN_OPT_GENERIC_KERNEL automatic or 5)
+    StagePlan sp;
+    const int gpick = g_opts[RN_OPT_GENERIC_KERNEL];
+    if (!use_row && (gpick == 0 || gpick == 5) && plan_ln_stage(p, d, atomic, gpick == 5, &sp)) {
+        plan_string_stage(sp, "ln_generic", atomic);
+        const DwOutputs o = {p.dg_f32, p.dg_cast, p.db_f32, p.db_cast, p.N, p.dtype,
+                             partials, sp.grid, 2 * p.N};
+        return run_sequence(atomic, o, s,
+                            [&](bool pdl) { return launch_ln_bwd_stage(p, sp, s, pdl); });
     }
     if (!use_row) plan_ln_generic(p, d, atomic, &gp);
     if (!use_row && atomic && !gp.rows && !gp.phase &&

@@ -48,6 +48,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "row_math.cuh"
+#include "stage.cuh"
 #include "unaligned.cuh"
 
 namespace rn {
@@ -58,79 +59,12 @@ __device__ unsigned int g_device_status;
 
 namespace {
 
-// Time limit of one mbarrier wait (ns of %globaltimer).
-constexpr uint64_t kWaitLimitNs = 250ull * 1000 * 1000;
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// True once the phase of `parity` has completed; false if that takes longer
-// than `limit` ns (the clock is read every 256 polls).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 255u) == 0 && global_ns() - t0 > limit) return false;
-    }
-}
-// One element of a row tensor from shared memory, widened to fp32.
-template <typename T> __device__ __forceinline__ float lds_elem(uint32_t addr);
-template <> __device__ __forceinline__ float lds_elem<float>(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-template <> __device__ __forceinline__ float lds_elem<__nv_bfloat16>(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
-    return __bfloat162float(__ushort_as_bfloat16(v));
-}
-template <> __device__ __forceinline__ float lds_elem<__half>(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
-    return __half2float(__ushort_as_half(v));
-}
-
-// Bulk copy global -> this CTA's shared memory, completing `bytes` of the
-// mbarrier's transaction count (addresses 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                              uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-        : "memory");
-}
-
 // Shared memory: [0,256) warp sums [2 parities][32 warps]; [256,512) wait
 // outcomes, same layout; [512, 512 + 8*16*Sq) the warps' full barriers
 // (warp w, slot u at w*Sq + u); the ring from stage_ring_offset(Sq): team t's
 // slot u at (t*Sq + u)*stage_bytes, tensor k of a slot at k*tensor_bytes;
-// within a tensor the head block at 0, whole chunk i at 16 + 16i and the
-// tail block after the last whole chunk.
+// within a tensor whole chunk i at kMid + 16i, the head block just before
+// chunk 0 and the tail block just after the last whole chunk.
 constexpr uint32_t kStageBarOffset = 512;
 // Within a tensor's slot: the whole chunks from byte kMid (128-byte aligned, as the bulk copies
 // of the chunks land), the head block just before them, the tail block just after.
@@ -612,14 +546,16 @@ int stage_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads,
 }
 
 cudaError_t take_device_status(unsigned int *status) {
-    unsigned int v = 0, zero = 0;
+    unsigned int v = 0, zero = 0, ln = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return e;
     e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v));
     if (e != cudaSuccess) return e;
     e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero));
     if (e != cudaSuccess) return e;
-    *status = v;
+    e = take_ln_device_status(&ln);  // the LayerNorm staged kernel's word
+    if (e != cudaSuccess) return e;
+    *status = v | ln;
     return cudaSuccess;
 }
 

@@ -106,8 +106,11 @@ int stage_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads,
 cudaError_t launch_bwd_stage(const BwdProblem &p, const StagePlan &plan, cudaStream_t s,
                              bool pdl_after_zero);
 // Read and clear the device status word (bit 0: a bounded wait in a kernel ran
-// out); synchronizes the device first.
+// out); synchronizes the device first. The LayerNorm staged kernel keeps its
+// own word (device variables are per translation unit), read and cleared by
+// the second call without synchronizing.
 cudaError_t take_device_status(unsigned int *status);
+cudaError_t take_ln_device_status(unsigned int *status);
 size_t realign_smem_bytes(int N, int dtype, int rows, bool dres);
 cudaError_t launch_bwd_realign(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
                                bool pdl_after_zero);
@@ -209,6 +212,14 @@ struct LnBwdProblem {
 };
 
 cudaError_t launch_ln_bwd_phase(const LnBwdProblem &p, const GenericPlan &plan, cudaStream_t s,
+                                bool pdl_after_zero);
+// LayerNorm staged phase-class kernel (at most 1024 whole chunks a row, 1 or 2
+// chunks a thread): shared memory of a tile and the launch.
+uint32_t ln_stage_ring_offset(int slots);
+size_t ln_stage_smem_bytes(int N, int dtype, int teams, int slots, uint32_t *tensor_bytes,
+                           uint32_t *region_words);
+int ln_stage_blocks_per_sm(int dtype, bool atomic, int cpt, int threads, size_t smem);
+cudaError_t launch_ln_bwd_stage(const LnBwdProblem &p, const StagePlan &plan, cudaStream_t s,
                                 bool pdl_after_zero);
 
 // LayerNorm forward for unaligned rows (and rows longer than the row engine's tile).

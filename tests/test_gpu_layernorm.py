@@ -435,3 +435,105 @@ def test_layernorm_casts_without_fp32_outputs(M, N, dt):
     check(ex, out)
     assert torch.equal(dx, out[0]) and torch.equal(dg, out[1]) and torch.equal(db, out[2])
 
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("with_dbeta", [True, False])
+@pytest.mark.parametrize("M,N,dt", [(1000, 4095, "bf16"), (333, 4100, "bf16"), (97, 2999, "f32"),
+                                    (130, 1001, "f16"), (5, 7, "bf16"), (3, 3, "f32"),
+                                    (64, 515, "bf16"), (17, 8183, "bf16"), (33, 4095, "f32"),
+                                    (300, 2050, "f16"), (9, 6, "f16"), (1, 4095, "bf16"),
+                                    (2, 1, "f32"), (611, 8190, "bf16"), (40, 4099, "f32")],
+                         ids=lambda v: str(v))
+def test_layernorm_staged_kernel(M, N, dt, with_dbeta, mode):
+    """The LayerNorm staged phase-class kernel (RN_OPT_GENERIC_KERNEL = 5): each CTA
+    on one residue class of rows, every warp staging its own span of the rows (with
+    the head and tail blocks for 16-bit types), one to fifteen teams a CTA; both
+    weight-gradient modes, with and without the bias gradient. No wait runs out."""
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    native.set_option(native.OPT_GENERIC_KERNEL, 5)
+    ex = expected(Case("ln staged", M, N, dt, eps=1e-5, seed=37))
+    out = run_gpu(ex, with_dbeta=with_dbeta)
+    plan = native.last_plan()
+    assert plan.startswith("engine=ln_generic staged "), plan
+    assert ("atomic" if mode == 2 else "scratch") in plan, plan
+    check(ex, out, with_dbeta=with_dbeta, tag=" [%s]" % plan)
+    assert native.take_device_status() == 0
+
+
+@pytest.mark.parametrize("cpt,teams,slots", [(1, 0, 0), (0, 1, 0), (0, 0, 3), (0, 0, 4),
+                                             (1, 3, 3)])
+@pytest.mark.parametrize("M,N,dt", [(1000, 4095, "bf16"), (130, 1001, "f16"), (97, 2050, "f32")],
+                         ids=lambda v: str(v))
+def test_layernorm_staged_kernel_forced_tiles(M, N, dt, cpt, teams, slots):
+    """Chunks per thread, teams per CTA and slots per team forced through the options."""
+    native.set_option(native.OPT_GENERIC_KERNEL, 5)
+    native.set_option(native.OPT_CHUNKS_PER_THREAD, cpt)
+    native.set_option(native.OPT_TEAMS_PER_CTA, teams)
+    native.set_option(native.OPT_STAGES, slots)
+    ex = expected(Case("ln staged tile", M, N, dt, eps=1e-5, seed=38))
+    out = run_gpu(ex)
+    plan = native.last_plan()
+    chunks = N * (4 if dt == "f32" else 2) // 16
+    if cpt == 1 and chunks > 512:
+        # a team of more than 512 threads: the phase-class kernel takes the rows instead
+        assert plan.startswith("engine=ln_generic phase "), plan
+    else:
+        assert plan.startswith("engine=ln_generic staged "), plan
+    check(ex, out, tag=" [%s]" % plan)
+    assert native.take_device_status() == 0
+
+
+@pytest.mark.parametrize("shift", [1, 3])
+@pytest.mark.parametrize("N,dt", [(4096, "bf16"), (1024, "f32"), (4095, "f16")])
+def test_layernorm_staged_kernel_offset_base(N, dt, shift):
+    """x, dy and dx all starting off a 16-byte boundary (one phase)."""
+    native.set_option(native.OPT_GENERIC_KERNEL, 5)
+    ex = expected(Case("ln staged base", 77, N, dt, eps=1e-5, seed=39))
+
+    def placed(t):
+        buf = torch.empty(t.numel() + shift, dtype=t.dtype, device="cuda")
+        v = buf[shift:].view(t.shape)
+        v.copy_(t.cuda())
+        return v
+    x, dy = placed(ex.inp["x"]), placed(ex.inp["dy"])
+    dx = placed(torch.zeros_like(ex.inp["x"]))
+    mean = torch.from_numpy(ex.mean32).float().cuda()
+    rstd = torch.from_numpy(ex.rstd32).float().cuda()
+    out = rn.layernorm_bwd(x, ex.inp["gamma"].cuda(), dy, mean, rstd, dx=dx)
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert plan.startswith("engine=ln_generic staged "), plan
+    check(ex, out, tag=" [%s]" % plan)
+
+
+@pytest.mark.parametrize("skip", [1, 3])
+def test_layernorm_staged_kernel_wait_runs_out(skip):
+    """The test hook leaves one row of the first team uncopied: the bounded wait
+    runs out, rn_take_device_status() reports bit 0, and the next call is correct."""
+    native.set_option(native.OPT_GENERIC_KERNEL, 5)
+    # bf16 N = 4095: period 8, 152 CTAs, 2 teams: CTA 0's first team has 7 rows of 2000
+    ex = expected(Case("ln staged timeout", 2000, 4095, "bf16", eps=1e-5, seed=40))
+    native.set_option(native.OPT_TEST_WAIT_TIMEOUT, skip)
+    run_gpu(ex)
+    assert native.take_device_status() == 1
+    assert native.take_device_status() == 0
+    native.set_option(native.OPT_TEST_WAIT_TIMEOUT, 0)
+    check(ex, run_gpu(ex))
+    assert native.take_device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,dt,engine", [(2048, 2047, "bf16", "staged"),
+                                           (2047, 2047, "bf16", "phase"),
+                                           (4096, 1001, "f16", "staged"),
+                                           (2048, 4095, "f32", "staged"),
+                                           (2048, 4095, "bf16", "phase")],   # two teams
+                         ids=lambda v: str(v))
+def test_layernorm_staged_kernel_default_choice(M, N, dt, engine):
+    """The automatic choice: the staged kernel from 2048 rows unless its tile is two
+    teams (bf16 N = 4095: 256-thread teams), the phase-class kernel otherwise."""
+    ex = expected(Case("ln default", M, N, dt, eps=1e-5, seed=41))
+    out = run_gpu(ex)
+    plan = native.last_plan()
+    assert plan.startswith("engine=ln_generic %s " % engine), plan
+    check(ex, out, tag=" [%s]" % plan)
