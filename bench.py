@@ -864,7 +864,7 @@ def run_ours(args):
             del p2
             torch.cuda.empty_cache()
         from rmsnorm_backward_bwd_gb300 import synth as _synth
-        for ln_case in (_synth.LN_4096, _synth.LN_LARGE):
+        for ln_case in (_synth.LN_4096, _synth.LN_LARGE, _synth.LN_UNALIGNED):
             p3 = LnProblem(ln_case, dev)
             n3 = max(20, args.steps // 4)
             cms, _, _ = time_calls(p3, n3, args.warmup, flush, ws)

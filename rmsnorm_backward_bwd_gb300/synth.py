@@ -111,6 +111,8 @@ LARGE_FUSED = Case("fused_add_rmsnorm_bwd bf16 M=16384 N=8192 +dres", 16384, 819
 
 LN_4096 = Case("layernorm_bwd bf16 M=4096 N=4096", 4096, 4096, "bf16", eps=1e-5)
 LN_LARGE = Case("layernorm_bwd bf16 M=16384 N=8192", 16384, 8192, "bf16", eps=1e-5)
+# rows that are not 16-byte multiples (the staged phase-class kernel, one team of 512 threads)
+LN_UNALIGNED = Case("layernorm_bwd bf16 M=4096 N=8190", 4096, 8190, "bf16", eps=1e-5)
 # rows longer than one CTA's tile (the cluster engine's range)
 LONG_ROWS = Case("rmsnorm_bwd bf16 M=4096 N=32768", 4096, 32768, "bf16")
 # rows that are not 16-byte multiples (the generic engines' range: phase-class kernel)

@@ -527,7 +527,8 @@ def test_layernorm_staged_kernel_wait_runs_out(skip):
                                            (2047, 2047, "bf16", "phase"),
                                            (4096, 1001, "f16", "staged"),
                                            (2048, 4095, "f32", "staged"),
-                                           (2048, 4095, "bf16", "phase")],   # two teams
+                                           (2048, 4095, "bf16", "phase"),    # two teams
+                                           (4096, 8190, "bf16", "staged")],  # one team
                          ids=lambda v: str(v))
 def test_layernorm_staged_kernel_default_choice(M, N, dt, engine):
     """The automatic choice: the staged kernel from 2048 rows unless its tile is two
