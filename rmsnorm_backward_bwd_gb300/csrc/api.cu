@@ -78,7 +78,7 @@ static cudaError_t device_info(DeviceInfo *out, int *dev_out) {
 }
 
 cudaError_t ensure_smem_attr(const void *func, size_t bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    if (bytes == 0) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -88,13 +88,22 @@ cudaError_t ensure_smem_attr(const void *func, size_t bytes) {
         auto it = g_smem_set.find(key);
         if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
     }
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, func);
+    if (e != cudaSuccess) return e;
+    // Without the opt-in a launch may use 48 KB of shared memory, the kernel's static shared
+    // memory and the dynamic bytes together.
+    const size_t base_cap = 48 * 1024 > fa.sharedSizeBytes ? 48 * 1024 - fa.sharedSizeBytes : 0;
+    if (bytes <= base_cap) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        size_t &known = g_smem_set[key];
+        if (known < base_cap) known = base_cap;
+        return cudaSuccess;
+    }
     // Set the kernel's cap to the most dynamic shared memory it can have:
     // the device's opt-in limit minus the kernel's own static shared memory.
     DeviceInfo d;
     e = device_info(&d, nullptr);
-    if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, func);
     if (e != cudaSuccess) return e;
     const size_t cap = d.smem_optin - fa.sharedSizeBytes;
     if (bytes > cap) return cudaErrorInvalidValue;

@@ -600,3 +600,21 @@ def test_generic_phase_kernel_prefetch(M, N, dt, fused, want):
     expect = 0 if (N == 4095 and M == 500) else 1
     assert " prefetch=%d " % expect in plan, plan
     assert parity.check_bwd(ex, *out, tag=" [%s]" % plan) == 0
+
+
+@pytest.mark.parametrize("N", [12288, 12280])
+def test_phase_kernel_near_48k_of_shared_memory(N):
+    """bf16 rows off a 16-byte boundary through the phase-class kernel in atomic mode: its
+    staged partial is 4N bytes of dynamic shared memory, which with the kernel's static
+    shared memory passes the 48 KB a launch may use without the opt-in."""
+    import rmsnorm_backward_bwd_gb300 as rn
+    native.set_option(native.OPT_DWEIGHT_MODE, 2)
+    native.set_option(native.OPT_GENERIC_KERNEL, 1)
+    ex = parity.expected_bwd(Case("phase 48k", 97, N, "bf16", seed=57))
+    x, dy = _offset(ex.x, 1), _offset(ex.dy, 1)
+    dx = _offset(torch.zeros_like(ex.x), 1)
+    dx, dw, dw32 = rn.rmsnorm_bwd(x, ex.gamma.cuda(), dy, ex.rstd.cuda(), dx=dx)
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert "engine=generic phase" in plan and "atomic" in plan, plan
+    assert parity.check_bwd(ex, dx, dw, dw32, tag=" [%s]" % plan) == 0

@@ -538,3 +538,24 @@ def test_layernorm_staged_kernel_default_choice(M, N, dt, engine):
     plan = native.last_plan()
     assert plan.startswith("engine=ln_generic %s " % engine), plan
     check(ex, out, tag=" [%s]" % plan)
+
+
+@pytest.mark.parametrize("N,dt", [(6144, "f16"), (6120, "bf16"), (6140, "bf16")])
+def test_layernorm_phase_kernel_near_48k_of_shared_memory(N, dt):
+    """The phase-class kernel's atomic-mode partials take 8N bytes of dynamic shared
+    memory: at N = 6120..6144 that and the kernel's static shared memory together pass
+    the 48 KB a launch may use without the opt-in, which the launch must then set."""
+    native.set_option(native.OPT_DWEIGHT_MODE, 2)
+    ex = expected(Case("ln 48k", 275, N, dt, eps=1e-5, seed=42))
+    x = torch.empty(275 * N + 1, dtype=ex.inp["x"].dtype, device="cuda")[1:].view(275, N)
+    x.copy_(ex.inp["x"].cuda())
+    dy = torch.empty(275 * N + 1, dtype=ex.inp["dy"].dtype, device="cuda")[1:].view(275, N)
+    dy.copy_(ex.inp["dy"].cuda())
+    dx = torch.empty(275 * N + 1, dtype=ex.inp["x"].dtype, device="cuda")[1:].view(275, N)
+    mean = torch.from_numpy(ex.mean32).float().cuda()
+    rstd = torch.from_numpy(ex.rstd32).float().cuda()
+    out = rn.layernorm_bwd(x, ex.inp["gamma"].cuda(), dy, mean, rstd, dx=dx)
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert "ln_generic phase" in plan and "atomic" in plan, plan
+    check(ex, out, tag=" [%s]" % plan)

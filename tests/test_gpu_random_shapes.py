@@ -125,3 +125,33 @@ def test_random_forwards(seed):
     tol = 2.0**-24 * (8 + 4 * np.sqrt(N))
     assert np.all(np.abs(parity.to64(mean) - mean64) <= tol * np.mean(np.abs(x64), axis=1))
     assert np.all(np.abs(parity.to64(lrstd) - lrstd64) <= tol * lrstd64)
+
+
+LN_WIDTHS = [1, 2, 7, 31, 64, 129, 1000, 1001, 2048, 2999, 4095, 4096, 4100, 6144, 8190, 8191,
+             8192, 12289, 16384]
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_layernorm_backward(seed):
+    """Seeded random LayerNorm backward problems (dtype, width, rows, a base off 16 bytes,
+    with or without the bias gradient) against the oracle; odd seeds ask for the staged
+    phase-class kernel, the rest take the automatic choice."""
+    import test_gpu_layernorm as lnt
+    rng = np.random.default_rng(3000 + seed)
+    dt = ["f32", "f16", "bf16"][rng.integers(3)]
+    N = int(rng.choice(LN_WIDTHS))
+    M = int(rng.integers(1, 64 if N > 8000 else 300))
+    shift = int(rng.choice([0, 0, 1, 3]))
+    with_dbeta = bool(rng.integers(2))
+    native.set_option(native.OPT_GENERIC_KERNEL, 5 if seed % 2 else 0)
+    ex = lnt.expected(Case("random ln %d" % seed, M, N, dt, eps=1e-5, seed=seed), with_dbeta)
+    x, dy = _placed(ex.inp["x"], shift), _placed(ex.inp["dy"], shift)
+    dx = _placed(torch.zeros_like(ex.inp["x"]), shift)
+    mean = torch.from_numpy(ex.mean32).float().cuda()
+    rstd = torch.from_numpy(ex.rstd32).float().cuda()
+    out = rn.layernorm_bwd(x, ex.inp["gamma"].cuda(), dy, mean, rstd, dx=dx,
+                           want_dbeta=with_dbeta)
+    torch.cuda.synchronize()
+    lnt.check(ex, out, with_dbeta=with_dbeta,
+              tag=" [M=%d N=%d %s shift=%d: %s]" % (M, N, dt, shift, native.last_plan()))
+    assert native.take_device_status() == 0
