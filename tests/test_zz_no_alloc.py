@@ -43,7 +43,9 @@ def _default_options():
 @pytest.mark.parametrize("mode", [1, 2], ids=["scratch-partials", "atomics"])
 @pytest.mark.parametrize("case", [Case("bf16 M=4096 N=4096", 4096, 4096, "bf16"),
                                   Case("f32 M=300 N=1000", 300, 1000, "f32"),
-                                  Case("f16 M=7 N=1003", 7, 1003, "f16")],
+                                  Case("f16 M=7 N=1003", 7, 1003, "f16"),
+                                  # rows that are not 16-byte multiples: the staged kernel
+                                  Case("bf16 M=2048 N=4095", 2048, 4095, "bf16")],
                          ids=lambda c: c.name)
 def test_noalloc_matches_workspace_entry_point_twice(case, mode):
     # weight-gradient mode 1 keeps the per-CTA partials in the fixed scratch array
@@ -59,6 +61,8 @@ def test_noalloc_matches_workspace_entry_point_twice(case, mode):
         st = _noalloc(x, g, dy, rstd, dx, dw32, dw)
         assert st == native.RN_OK, native.lib().rn_last_error()
         torch.cuda.synchronize()
+        if case.N == 4095:
+            assert "staged" in native.last_plan(), native.last_plan()
         # against the workspace entry point, with the parity tolerances
         parity.check_tensor("dx", dx, parity.to64(ref_dx), case.dtype, "dx")
         parity.check_tensor("dweight_f32", dw32, parity.to64(ref_dw32), case.dtype, "dweight_f32")
