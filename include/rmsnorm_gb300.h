@@ -272,13 +272,19 @@ typedef enum rn_option {
                                  LayerNorm: unless its tile is two teams). A kernel that cannot
                                  take the problem (its row-size range, or tensors at different
                                  alignment phases) falls back to the next one the automatic
-                                 choice would make. */
-    RN_OPT_TEST_WAIT_TIMEOUT = 8, /* test hook, RMSNorm and LayerNorm backward, staged
-                                 phase-class kernels: v > 0 makes the first CTA's first team
-                                 leave its row v-1 (counted from 0 among that team's rows)
-                                 uncopied, so that the team's bounded wait (250 ms) runs out.
-                                 The call then leaves dx rows and the weight gradients
-                                 incomplete and rn_take_device_status() reports bit 0. */
+                                 choice would make. The forwards on such rows read 5 as "the
+                                 staged forward wherever it can run" and any other non-zero
+                                 value as "not the staged forward"; their automatic choice
+                                 takes the staged forward from 2048 rows (RMSNorm with at least
+                                 6 rows a team, fused-add with one team a CTA, either way also
+                                 for rows of at most 256 chunks). */
+    RN_OPT_TEST_WAIT_TIMEOUT = 8, /* test hook, staged phase-class kernels (RMSNorm and
+                                 LayerNorm backward, the forwards): v > 0 makes the first CTA's
+                                 first team leave its row v-1 (counted from 0 among that team's
+                                 rows) uncopied, so that the team's bounded wait (250 ms) runs
+                                 out. The call then leaves output rows (and the weight
+                                 gradients) incomplete and rn_take_device_status() reports
+                                 bit 0. */
     RN_OPT_COUNT = 9
 } rn_option;
 
@@ -296,10 +302,11 @@ const char *rn_last_plan(void);
 /*
  * Device status word of the current device (kernels OR bits into it):
  *   bit 0 = a bounded wait inside a kernel ran out (the staged phase-class
- *           kernels, RMSNorm and LayerNorm, wait at most 250 ms for a row's
- *           bulk copies). The team that waited stopped: the dx rows it had not
- *           reached and the weight gradients of that call are not valid. The
- *           CUDA context stays usable.
+ *           kernels, the RMSNorm and LayerNorm backwards and the forwards, wait
+ *           at most 250 ms for a row's bulk copies). The team that waited
+ *           stopped: the output rows it had not reached (dx, or y, residual_out
+ *           and the statistics) and the weight gradients of that call are not
+ *           valid. The CUDA context stays usable.
  * Synchronizes the device, stores the word in *status and clears it.
  * Returns RN_ERR_INVALID_ARG for a NULL status, RN_ERR_CUDA if a CUDA call fails.
  */

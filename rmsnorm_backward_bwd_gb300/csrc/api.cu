@@ -667,6 +667,78 @@ struct FwdPhasePlan {
 
 static FwdPhasePlan plan_fwd_phase(const FwdRowProblem &q, const DeviceInfo &d);
 
+// The forward staged phase-class kernel: row tensors at one alignment phase, at most 2048
+// whole 16-byte chunks per row; 4 chunks a thread (RN_OPT_CHUNKS_PER_THREAD forces 1 or 2),
+// teams of the fewest whole warps that cover a row, 2 shared-memory slots a team
+// (RN_OPT_STAGES forces 2..4), as many teams as fit 512 threads, 15 named barriers and 200 KB
+// of ring (RN_OPT_TEAMS_PER_CTA forces 1..15), and the phase-class grid rule at the resident
+// CTAs per SM. RN_OPT_GENERIC_KERNEL = 5 forces it; any other non-zero pick leaves the rows to
+// the vector or phase-class forward.
+// The automatic choice, measured on GB300 (L2 flushed, us per call, vector or phase-class ->
+// staged), takes it from 2048 rows:
+//  * LayerNorm, always: bf16 4096 x 4095 24.6 -> 22.5, 16384 x 8190 177.7 -> 117.3, 4096 x
+//    16383 87.9 -> 63.4, 16384 x 2047 71.6 -> 36.4, 32768 x 509 108.0 -> 34.6, f32 4096 x 4095
+//    32.8 -> 26.6, f16 2048 x 1001 14.2 -> 10.6; 2048 x 4095 16.4 -> 16.3 (1024 x 4095 12.2 ->
+//    13.3: too few rows).
+//  * RMSNorm, with at least 6 rows a team or rows of at most 256 chunks (where the vector
+//    kernel's CTA per row leaves most threads idle): bf16 4096 x 4095 19.5 -> 18.2, 16384 x
+//    8190 98.8 -> 89.1, 32768 x 4095 115.6 -> 86.5, 16384 x 2047 44.8 -> 26.4, f16 16384 x 1001
+//    45.2 -> 19.9, f32 4096 x 4095 28.4 -> 24.3; fewer rows a team lose (2048 x 4095 13.1 ->
+//    14.1, 3072 x 4095 16.1 -> 16.3), and so do the one-team rows of bf16 12290 (4096 rows 39.1
+//    -> 41.3, 16384 rows 142.1 -> 147.1), which keep it for simplicity.
+//  * Fused-add, with one team a CTA or rows of at most 256 chunks: bf16 8192 x 16383 176.4 ->
+//    169.6, 4096 x 12290 65.7 -> 64.4, f32 16384 x 6001 249.7 -> 241.1, bf16 16384 x 2047 50.6
+//    -> 44.2, f16 16384 x 1001 51.2 -> 24.4. With two or more teams the vector kernel's
+//    four streams keep the copy engines busier (bf16 16384 x 8190 162.3 vs 171.6, 32768 x 4095
+//    165.0 vs 171.2, 16384 x 4095 83.9 vs 86.3, f32 8192 x 4095 82.9 vs 84.2).
+constexpr int64_t kFwdStageMinRows = 2048;
+
+static bool plan_fwd_stage(const FwdRowProblem &q, const DeviceInfo &d, StagePlan *plan) {
+    const int pick = g_opts[RN_OPT_GENERIC_KERNEL];
+    if (pick != 0 && pick != 5) return false;
+    if (pick == 0 && q.M < kFwdStageMinRows) return false;
+    if (!fwd_stage_ok(q)) return false;
+    const int64_t maxnv = (int64_t)q.N * elem_bytes(q.dtype) / 16;
+    int cpt = g_opts[RN_OPT_CHUNKS_PER_THREAD];
+    if (cpt != 1 && cpt != 2) cpt = 4;
+    int tthr = (int)((maxnv + cpt - 1) / cpt + 31) / 32 * 32;
+    if (tthr < 32) tthr = 32;
+    if (tthr > 512) return false;
+    int slots = g_opts[RN_OPT_STAGES];
+    if (slots < 2 || slots > 4) slots = 2;
+    const size_t budget = d.smem_optin < 200 * 1024 ? d.smem_optin : 200 * 1024;
+    int teams = 512 / tthr;
+    if (teams > 15) teams = 15;
+    const int want_teams = g_opts[RN_OPT_TEAMS_PER_CTA];
+    if (want_teams >= 1 && want_teams <= 15 && want_teams * tthr <= 512) teams = want_teams;
+    size_t smem = fwd_stage_smem_bytes(q.N, q.dtype, q.mode, teams, slots);
+    while (teams > 1 && smem > budget) {
+        --teams;
+        smem = fwd_stage_smem_bytes(q.N, q.dtype, q.mode, teams, slots);
+    }
+    if (smem > d.smem_optin) return false;
+    plan->cpt = cpt;
+    plan->team_threads = tthr;
+    plan->teams = teams;
+    plan->slots = slots;
+    plan->smem = smem;
+    plan->atomic = false;
+    const int per_sm = fwd_stage_blocks_per_sm(q.dtype, q.mode, cpt, teams * tthr, smem);
+    plan->grid = phase_grid(q.M, phase_period(q.N, q.dtype), per_sm, d);
+    plan->skip_row = g_opts[RN_OPT_TEST_WAIT_TIMEOUT] > 0 ? g_opts[RN_OPT_TEST_WAIT_TIMEOUT] - 1 : -1;
+    if (pick == 0 && maxnv > 256) {
+        if (q.mode == kFwdRms && q.M < 6 * (int64_t)plan->grid * teams) return false;
+        if (q.mode == kFwdFused && teams > 1) return false;
+    }
+    return true;
+}
+
+static void plan_string_fwd_stage(const char *op, const StagePlan &sp) {
+    snprintf(g_plan, sizeof(g_plan),
+             "%s engine=generic staged cpt=%d team_threads=%d teams=%d slots=%d grid=%d smem=%zu", op,
+             sp.cpt, sp.team_threads, sp.teams, sp.slots, sp.grid, sp.smem);
+}
+
 static void plan_string_fwd(const char *op, bool vec, bool row, bool gvec, const RowPlan &rp,
                             const FwdPhasePlan *fp = nullptr) {
     if (fp) {
@@ -1121,6 +1193,12 @@ static rn_status fwd_entry(const void *x, const void *residual, const void *gamm
     q.dtype = dtype;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const char *op = fused ? "fused_add_fwd" : "rmsnorm_fwd";
+    StagePlan sp;
+    if (!vec && plan_fwd_stage(q, d, &sp)) {
+        plan_string_fwd_stage(op, sp);
+        e = launch_fwd_stage(q, sp, cs);
+        return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
+    }
     // The RMSNorm forwards keep the vector kernel where it can run (see plan_fwd_phase); the
     // phase-class kernel takes gamma at any alignment.
     if (!vec && !fwd_generic_vec_ok(q) && fwd_phase_ok(q)) {
@@ -1208,6 +1286,12 @@ static rn_status ln_fwd_entry(const void *x, const void *gamma, const void *beta
     q.N = (int)N;
     q.dtype = dtype;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    StagePlan sp;
+    if (!vec && plan_fwd_stage(q, d, &sp)) {
+        plan_string_fwd_stage("layernorm_fwd", sp);
+        e = launch_fwd_stage(q, sp, cs);
+        return e == cudaSuccess ? RN_OK : cuda_fail(e, "forward launch");
+    }
     if (!vec && fwd_phase_ok(q) && (dtype != kF32 || !fwd_generic_vec_ok(q))) {
         const FwdPhasePlan fp = plan_fwd_phase(q, d);
         plan_string_fwd("layernorm_fwd", vec, row, false, rp, &fp);

@@ -546,7 +546,7 @@ int stage_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads,
 }
 
 cudaError_t take_device_status(unsigned int *status) {
-    unsigned int v = 0, zero = 0, ln = 0;
+    unsigned int v = 0, zero = 0, ln = 0, fw = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return e;
     e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v));
@@ -555,7 +555,9 @@ cudaError_t take_device_status(unsigned int *status) {
     if (e != cudaSuccess) return e;
     e = take_ln_device_status(&ln);  // the LayerNorm staged kernel's word
     if (e != cudaSuccess) return e;
-    *status = v | ln;
+    e = take_fwd_device_status(&fw);  // the forward staged kernel's word
+    if (e != cudaSuccess) return e;
+    *status = v | ln | fw;
     return cudaSuccess;
 }
 

@@ -106,11 +106,12 @@ int stage_blocks_per_sm(int dtype, bool dres, bool atomic, int cpt, int threads,
 cudaError_t launch_bwd_stage(const BwdProblem &p, const StagePlan &plan, cudaStream_t s,
                              bool pdl_after_zero);
 // Read and clear the device status word (bit 0: a bounded wait in a kernel ran
-// out); synchronizes the device first. The LayerNorm staged kernel keeps its
-// own word (device variables are per translation unit), read and cleared by
-// the second call without synchronizing.
+// out); synchronizes the device first. The LayerNorm and forward staged
+// kernels keep their own words (device variables are per translation unit),
+// read and cleared by the other two calls without synchronizing.
 cudaError_t take_device_status(unsigned int *status);
 cudaError_t take_ln_device_status(unsigned int *status);
+cudaError_t take_fwd_device_status(unsigned int *status);
 size_t realign_smem_bytes(int N, int dtype, int rows, bool dres);
 cudaError_t launch_bwd_realign(const BwdProblem &p, const GenericPlan &plan, cudaStream_t s,
                                bool pdl_after_zero);
@@ -179,6 +180,13 @@ bool fwd_phase_ok(const FwdRowProblem &p);
 cudaError_t launch_fwd_phase(const FwdRowProblem &p, int cpt, int grid, int threads,
                              cudaStream_t s);
 cudaError_t launch_fwd_generic_vec(const FwdRowProblem &p, int num_sms, cudaStream_t s);
+// The same rows staged in shared memory by per-warp bulk copies (row tensors
+// at one phase, at most 2048 whole 16-byte chunks; gamma and beta at any
+// alignment): the backward staged kernel's work split, with the forward math.
+bool fwd_stage_ok(const FwdRowProblem &p);
+size_t fwd_stage_smem_bytes(int N, int dtype, int mode, int teams, int slots);
+int fwd_stage_blocks_per_sm(int dtype, int mode, int cpt, int threads, size_t smem);
+cudaError_t launch_fwd_stage(const FwdRowProblem &p, const StagePlan &plan, cudaStream_t s);
 
 // LayerNorm.
 struct LnFwdProblem {
