@@ -515,9 +515,10 @@ def autograd_pages_table(dev, steps=100, warmup=10):
 
 def time_forwards(dev, flush, steps, warmup, peak):
     """The forwards (RMSNorm, fused-add, LayerNorm; bf16) at 4096x4096 and
-    16384x8192: mean device time per call with an L2 flush before each, the
+    16384x8192, and on rows that are not 16-byte multiples at 4096x4095 and
+    16384x8190: mean device time per call with an L2 flush before each, the
     algorithmic bytes (inputs read once, outputs and statistics written once)
-    over that time, and torch eager rms_norm on the same inputs beside them."""
+    over that time, the plan, and torch eager on the same inputs beside them."""
     import numpy as np
     import torch
     import rmsnorm_backward_bwd_gb300 as rn
@@ -541,7 +542,8 @@ def time_forwards(dev, flush, steps, warmup, peak):
         return float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3
 
     rows = []
-    for M, N in ((4096, 4096), (16384, 8192)):
+    from rmsnorm_backward_bwd_gb300 import native
+    for M, N in ((4096, 4096), (16384, 8192), (4096, 4095), (16384, 8190)):
         inp = synth.make_inputs(Case("forward", M, N, "bf16", fused=True), device=str(dev))
         x, r, g = inp["x"], inp["residual"], inp["gamma"]
         y, ro = torch.empty_like(x), torch.empty_like(x)
@@ -560,7 +562,8 @@ def time_forwards(dev, flush, steps, warmup, peak):
             us = timed(fn)
             rows.append({"workload": "%s bf16 M=%d N=%d" % (name, M, N), "us_per_call": round(us, 2),
                          "GBps": round(nbytes / us / 1e3, 1),
-                         "pct_of_peak": round(100 * nbytes / us / 1e3 / peak, 1)})
+                         "pct_of_peak": round(100 * nbytes / us / 1e3 / peak, 1),
+                         "plan": native.last_plan()})
         us = timed(lambda: torch.nn.functional.rms_norm(x, (N,), g, 1e-6))
         rows.append({"workload": "torch eager rms_norm bf16 M=%d N=%d" % (M, N),
                      "us_per_call": round(us, 2)})
