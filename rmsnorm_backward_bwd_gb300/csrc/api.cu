@@ -482,6 +482,19 @@ static bool plan_phase(const BwdProblem &p, const DeviceInfo &d, bool atomic, Ge
 // 12.6, 64 x 4095 12.1 -> 12.6.
 constexpr int64_t kStageMinRows = 2048;
 
+// A staged tile of two teams of 192-256 threads runs as one team a CTA at two CTAs an SM
+// (unless RN_OPT_TEAMS_PER_CTA asks for a count). Measured on GB300 (L2 flushed, us per
+// call, two teams -> one team at two CTAs an SM): RMSNorm backward bf16 4096 x 8190 38.3 ->
+// 37.8, fused +dres 44.0 -> 42.5, 16384 x 8190 129.0 -> 127.9, f32 8192 x 2999 49.0 -> 48.7;
+// forwards bf16 4096 x 8190 27.6 -> 26.5 (fused 44.3 -> 43.1, LayerNorm 36.8 -> 36.1), f32 4096
+// x 4095 24.4 -> 22.3 (LayerNorm 26.9 -> 25.8), bf16 16384 x 8190 LayerNorm 117.6 -> 113.0;
+// LayerNorm backward bf16 4096 x 4095 35.8 -> 33.5 (the phase-class kernel: 35.7), 8192 x 2999
+// 50.7 -> 49.7. Smaller teams lose that way (128 threads, bf16 4096 x 4095: 25.6 -> 31.8).
+static int stage_teams_split(int teams, int team_threads) {
+    const int want = g_opts[RN_OPT_TEAMS_PER_CTA];
+    return (want == 0 && teams == 2 && team_threads >= 192) ? 1 : teams;
+}
+
 static bool plan_stage(const BwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
                        StagePlan *plan) {
     if (!forced && p.M < kStageMinRows) return false;
@@ -507,6 +520,8 @@ static bool plan_stage(const BwdProblem &p, const DeviceInfo &d, bool atomic, bo
         smem = stage_smem_bytes(p.N, p.dtype, dres, teams, slots, cpt, tthr, nullptr, nullptr);
     }
     if (smem > d.smem_optin) return false;
+    teams = stage_teams_split(teams, tthr);
+    smem = stage_smem_bytes(p.N, p.dtype, dres, teams, slots, cpt, tthr, nullptr, nullptr);
     plan->cpt = cpt;
     plan->team_threads = tthr;
     plan->teams = teams;
@@ -730,6 +745,13 @@ static bool plan_fwd_stage(const FwdRowProblem &q, const DeviceInfo &d, StagePla
         if (q.mode == kFwdRms && q.M < 6 * (int64_t)plan->grid * teams) return false;
         if (q.mode == kFwdFused && teams > 1) return false;
     }
+    const int split = stage_teams_split(teams, tthr);
+    if (split != teams) {
+        plan->teams = split;
+        plan->smem = fwd_stage_smem_bytes(q.N, q.dtype, q.mode, split, slots);
+        const int per = fwd_stage_blocks_per_sm(q.dtype, q.mode, cpt, split * tthr, plan->smem);
+        plan->grid = phase_grid(q.M, phase_period(q.N, q.dtype), per, d);
+    }
     return true;
 }
 
@@ -914,15 +936,17 @@ static bool plan_ln_phase(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
 // registers for 4), teams of the fewest whole warps that cover a row, 2 slots
 // a team (RN_OPT_STAGES 2..4), as many teams as fit 512 threads, 15 named
 // barriers and 200 KB (RN_OPT_TEAMS_PER_CTA forces 1..15), the phase-class
-// grid rule. Taken automatically from 2048 rows, as the RMSNorm staged kernel,
-// except where its tile is two teams. Measured on GB300 (L2 flushed, us per
-// call, phase-class -> staged): f16 16384 x 1001 62.1 -> 34.3 (8 teams), bf16
-// 16384 x 509 54.5 -> 25.7 (15), 4096 x 2047 27.5 -> 23.6 (4), 4096 x 8190 64.7
-// -> 58.4 (1), 16384 x 8190 211.2 -> 193.1 (1), f32 4096 x 4095 54.7 -> 43.9 (1),
-// f32 8192 x 2999 80.7 -> 67.0 (1); two teams of 256 threads: bf16 4096 x 4095
-// 35.7 -> 35.6, 16384 x 4095 97.0 -> 102.5, 4096 x 4100 35.5 -> 35.7 (3 or 4
-// slots a team no better); below 2048 rows 1024 x 4095 18.3 -> 19.5, 512 x 4095
-// 15.1 -> 16.8.
+// grid rule. Taken automatically from 2048 rows, as the RMSNorm staged kernel.
+// Measured on GB300 (L2 flushed, us per call, phase-class -> staged): f16 16384
+// x 1001 62.1 -> 34.3 (8 teams), bf16 16384 x 509 54.5 -> 25.7 (15), 4096 x 2047
+// 27.5 -> 23.6 (4), 4096 x 8190 64.7 -> 58.4 (1), 16384 x 8190 211.2 -> 193.1
+// (1), f32 4096 x 4095 54.7 -> 43.9 (1), f32 8192 x 2999 80.7 -> 67.0 (1); a tile
+// of two 256-thread teams split into one team at two CTAs an SM
+// (stage_teams_split): bf16 4096 x 4095 35.7 -> 33.5, 4096 x 4100 35.5 -> 34.8,
+// 8192 x 2999 51.1 -> 50.2, but 16384 x 4095 97.7 -> 99.5, where the phase-class
+// kernel has 40+ rows a CTA and prefetches, so it keeps those (as two teams in
+// one CTA: 35.8, 35.8, 50.5, 102.5; 3 or 4 slots a team no better); below 2048
+// rows 1024 x 4095 18.3 -> 19.5, 512 x 4095 15.1 -> 16.8.
 static bool plan_ln_stage(const LnBwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
                           StagePlan *plan) {
     if (!forced && p.M < kStageMinRows) return false;
@@ -948,7 +972,14 @@ static bool plan_ln_stage(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
         smem = ln_stage_smem_bytes(p.N, p.dtype, teams, slots, nullptr, nullptr);
     }
     if (smem > d.smem_optin) return false;
-    if (!forced && teams == 2) return false;  // the phase-class kernel is as fast there
+    if (!forced && stage_teams_split(teams, tthr) != teams) {
+        // with 40 or more rows a CTA the phase-class kernel's L2 prefetch pays and it is the
+        // faster one there (bf16 16384 x 4095: 97.7 vs 99.5)
+        const int64_t g2 = 2 * (int64_t)d.num_sms;
+        if ((p.M + g2 - 1) / g2 >= 40) return false;
+    }
+    teams = stage_teams_split(teams, tthr);
+    smem = ln_stage_smem_bytes(p.N, p.dtype, teams, slots, nullptr, nullptr);
     plan->cpt = cpt;
     plan->team_threads = tthr;
     plan->teams = teams;

@@ -527,16 +527,21 @@ def test_layernorm_staged_kernel_wait_runs_out(skip):
                                            (2047, 2047, "bf16", "phase"),
                                            (4096, 1001, "f16", "staged"),
                                            (2048, 4095, "f32", "staged"),
-                                           (2048, 4095, "bf16", "phase"),    # two teams
+                                           (2048, 4095, "bf16", "staged"),   # two teams: split
+                                           (12160, 4095, "bf16", "phase"),   # 40 rows a CTA
                                            (4096, 8190, "bf16", "staged")],  # one team
                          ids=lambda v: str(v))
 def test_layernorm_staged_kernel_default_choice(M, N, dt, engine):
-    """The automatic choice: the staged kernel from 2048 rows unless its tile is two
-    teams (bf16 N = 4095: 256-thread teams), the phase-class kernel otherwise."""
+    """The automatic choice: the staged kernel from 2048 rows, the phase-class kernel
+    below; a tile of two 256-thread teams (bf16 N = 4095) runs as one team a CTA, up
+    to 40 rows a CTA of two CTAs an SM (the phase-class kernel, which prefetches,
+    beyond)."""
     ex = expected(Case("ln default", M, N, dt, eps=1e-5, seed=41))
     out = run_gpu(ex)
     plan = native.last_plan()
     assert plan.startswith("engine=ln_generic %s " % engine), plan
+    if N == 4095 and dt == "bf16" and engine == "staged":
+        assert " teams=1 " in plan and " grid=304 " in plan, plan
     check(ex, out, tag=" [%s]" % plan)
 
 
