@@ -3,9 +3,10 @@ range must be formed in 64 bits. The inputs repeat a block of B rows (row r
 holds base row r mod B), so each output row equals the oracle's output for its
 base row, and the weight gradient is (M / B) times the oracle's over the block.
 Sampled rows cover the start, the rows around element 2^31 and the end; the
-weight gradient covers every row. Backward (row engine and staged kernel,
-plain and fused with dresidual_out, both weight-gradient modes) and forwards
-(row engine and staged forward)."""
+weight gradient covers every row. Backward (row, staged, cluster and vector
+engines, plain and fused with dresidual_out, both weight-gradient modes),
+LayerNorm backward (row engine and staged kernel) and forwards (row engine and
+staged forward)."""
 import numpy as np
 import pytest
 import torch
@@ -42,7 +43,8 @@ def _tile(t, reps):
     return t.cuda().repeat(reps, *([1] * (t.dim() - 1)))
 
 
-@pytest.mark.parametrize("N,engine", [(8192, "row"), (8190, "generic staged")])
+@pytest.mark.parametrize("N,engine", [(8192, "row"), (8190, "generic staged"), (32768, "cluster"),
+                                      (16393, "generic vec")])
 @pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("mode", [1, 2])
 def test_backward_past_2_31_elements(N, engine, fused, mode):
@@ -107,3 +109,27 @@ def test_forwards_past_2_31_elements(N, engine):
     del x, r
     assert np.array_equal(parity.to64(ro[rows]), a64[base])
     parity.check_tensor("out", o[rows].cpu(), o64[base], "bf16", "y")
+
+
+@pytest.mark.parametrize("N,engine", [(8192, "ln_row"), (8190, "ln_generic staged")])
+def test_layernorm_backward_past_2_31_elements(N, engine):
+    reps = ((1 << 31) // N) // B + 3
+    M = B * reps
+    inp = synth.make_ln_inputs(Case("large ln base", B, N, "bf16", eps=1e-5, seed=73))
+    x64, g64, dy64 = (parity.to64(inp[k]) for k in ("x", "gamma", "dy"))
+    _, mean64, rstd64 = oracle.layernorm_fwd(x64, g64, None, np.float32(1e-5))
+    mean32, rstd32 = oracle.round_to(mean64, "f32"), oracle.round_to(rstd64, "f32")
+    dx64, dg64, db64 = oracle.layernorm_bwd(x64, g64, dy64, mean32, rstd32)
+    x, dy = _tile(inp["x"], reps), _tile(inp["dy"], reps)
+    mean = _tile(torch.from_numpy(mean32).float(), reps)
+    rstd = _tile(torch.from_numpy(rstd32).float(), reps)
+    dx, dg, db, dg32, db32 = rn.layernorm_bwd(x, inp["gamma"].cuda(), dy, mean, rstd)
+    torch.cuda.synchronize()
+    plan = native.last_plan()
+    assert plan.startswith("engine=%s " % engine), plan
+    del x, dy
+    rows = _rows_to_check(M, N)
+    parity.check_tensor("dx rows [%s]" % plan, dx[rows].cpu(), dx64[[r % B for r in rows]],
+                        "bf16", "dx")
+    parity.check_tensor("dgamma_f32 [%s]" % plan, dg32, dg64 * reps, "bf16", "dweight_f32")
+    parity.check_tensor("dbeta_f32 [%s]" % plan, db32, db64 * reps, "bf16", "dweight_f32")
