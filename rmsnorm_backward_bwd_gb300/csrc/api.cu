@@ -931,9 +931,10 @@ static bool plan_ln_phase(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
 }
 
 // The LayerNorm staged phase-class kernel: x, dy and dx at one alignment
-// phase, at most 1024 whole 16-byte chunks a row, 2 chunks a thread
-// (RN_OPT_CHUNKS_PER_THREAD = 1 forces 1: two fp32 partials a column leave no
-// registers for 4), teams of the fewest whole warps that cover a row, 2 slots
+// phase, at most 2048 whole 16-byte chunks a row; 2 chunks a thread up to 512
+// chunks a row, else 4 (RN_OPT_CHUNKS_PER_THREAD forces 1, 2 or 4; at 4 the two
+// fp32 partials a column fill the register budget and ptxas spills 40 bytes, which
+// the measurements below include), teams of the fewest whole warps that cover a row, 2 slots
 // a team (RN_OPT_STAGES 2..4), as many teams as fit 512 threads, 15 named
 // barriers and 200 KB (RN_OPT_TEAMS_PER_CTA forces 1..15), the phase-class
 // grid rule. Taken automatically from 2048 rows, as the RMSNorm staged kernel.
@@ -946,7 +947,12 @@ static bool plan_ln_phase(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
 // 8192 x 2999 51.1 -> 50.2, but 16384 x 4095 97.7 -> 99.5, where the phase-class
 // kernel has 40+ rows a CTA and prefetches, so it keeps those (as two teams in
 // one CTA: 35.8, 35.8, 50.5, 102.5; 3 or 4 slots a team no better); below 2048
-// rows 1024 x 4095 18.3 -> 19.5, 512 x 4095 15.1 -> 16.8.
+// rows 1024 x 4095 18.3 -> 19.5, 512 x 4095 15.1 -> 16.8. Four chunks a thread
+// against two (us per call): bf16 4096 x 8190 58.3 -> 57.5, 16384 x 8190 193.1 ->
+// 184.1, f32 4096 x 4095 44.0 -> 37.9; rows of 1025-2048 chunks, which only 4
+// chunks a thread can take, against the vector kernel: bf16 4096 x 12290 216.2 ->
+// 91.0, 4096 x 16383 295.4 -> 103.4; shorter rows lose with 4 (4096 x 4095 34.7 ->
+// 36.9, 4096 x 2047 23.5 -> 26.0).
 static bool plan_ln_stage(const LnBwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
                           StagePlan *plan) {
     if (!forced && p.M < kStageMinRows) return false;
@@ -954,8 +960,9 @@ static bool plan_ln_stage(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
     for (const void *q : {p.x, p.dy, static_cast<const void *>(p.dx)})
         if (((uintptr_t)q & 15u) != ph || ((uintptr_t)q % S) != 0) return false;
     const int64_t maxnv = (int64_t)p.N * elem_bytes(p.dtype) / 16;
-    if (maxnv > 1024) return false;
-    const int cpt = g_opts[RN_OPT_CHUNKS_PER_THREAD] == 1 ? 1 : 2;
+    const int copt = g_opts[RN_OPT_CHUNKS_PER_THREAD];
+    const int cpt = (copt == 1 || copt == 2 || copt == 4) ? copt : (maxnv <= 512 ? 2 : 4);
+    if (maxnv > 512 * (int64_t)cpt) return false;
     int tthr = (int)((maxnv + cpt - 1) / cpt + 31) / 32 * 32;
     if (tthr < 32) tthr = 32;
     if (tthr > 512) return false;
@@ -972,7 +979,7 @@ static bool plan_ln_stage(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
         smem = ln_stage_smem_bytes(p.N, p.dtype, teams, slots, nullptr, nullptr);
     }
     if (smem > d.smem_optin) return false;
-    if (!forced && stage_teams_split(teams, tthr) != teams) {
+    if (!forced && cpt == 2 && stage_teams_split(teams, tthr) != teams) {
         // with 40 or more rows a CTA the phase-class kernel's L2 prefetch pays and it is the
         // faster one there (bf16 16384 x 4095: 97.7 vs 99.5)
         const int64_t g2 = 2 * (int64_t)d.num_sms;

@@ -444,14 +444,19 @@ template <typename T>
 static cudaError_t launch_ln_stage_dt(const LnStageArgs &args, const StagePlan &plan,
                                       cudaStream_t s, bool pdl) {
     if (plan.atomic)
-        return plan.cpt == 2 ? launch_ln_stage_t<T, true, 2>(args, plan, s, pdl)
-                             : launch_ln_stage_t<T, true, 1>(args, plan, s, pdl);
-    return plan.cpt == 2 ? launch_ln_stage_t<T, false, 2>(args, plan, s, pdl)
-                         : launch_ln_stage_t<T, false, 1>(args, plan, s, pdl);
+        return plan.cpt == 4   ? launch_ln_stage_t<T, true, 4>(args, plan, s, pdl)
+               : plan.cpt == 2 ? launch_ln_stage_t<T, true, 2>(args, plan, s, pdl)
+                               : launch_ln_stage_t<T, true, 1>(args, plan, s, pdl);
+    return plan.cpt == 4   ? launch_ln_stage_t<T, false, 4>(args, plan, s, pdl)
+           : plan.cpt == 2 ? launch_ln_stage_t<T, false, 2>(args, plan, s, pdl)
+                           : launch_ln_stage_t<T, false, 1>(args, plan, s, pdl);
 }
 
 template <typename T>
 static const void *ln_stage_kernel_ptr(bool atomic, int cpt) {
+    if (cpt == 4)
+        return atomic ? (const void *)ln_bwd_stage_kernel<T, true, 4>
+                      : (const void *)ln_bwd_stage_kernel<T, false, 4>;
     if (cpt == 2)
         return atomic ? (const void *)ln_bwd_stage_kernel<T, true, 2>
                       : (const void *)ln_bwd_stage_kernel<T, false, 2>;
@@ -499,7 +504,7 @@ cudaError_t launch_ln_bwd_stage(const LnBwdProblem &p, const StagePlan &plan, cu
     a.ring_off = ln_stage_ring_offset(plan.slots);
     // the launch shape the kernel relies on (as for the RMSNorm staged kernel)
     const int64_t maxnv = (int64_t)p.N / V;
-    if (plan.cpt != 1 && plan.cpt != 2) return cudaErrorInvalidValue;
+    if (plan.cpt != 1 && plan.cpt != 2 && plan.cpt != 4) return cudaErrorInvalidValue;
     if (plan.team_threads < 32 || plan.team_threads % 32 || plan.teams < 1 || plan.teams > 15 ||
         plan.teams * plan.team_threads > 512)
         return cudaErrorInvalidValue;

@@ -208,10 +208,8 @@ def test_staged_kernels_write_stay_in_bounds(M, N, dt, mode):
     y64, _ = oracle.rmsnorm_fwd(parity.to64(finp["x"]), parity.to64(finp["gamma"]),
                                 np.float32(1e-6))
     parity.check_tensor("y", outs["y"].t, y64, dt, "y")
-    # rows that are not 16-byte multiples, of at most 2048 whole chunks (LayerNorm backward:
-    # 1024), took the staged kernels
+    # rows that are not 16-byte multiples, of at most 2048 whole chunks, took the staged kernels
     row_bytes = N * synth.ELEM_BYTES[dt]
     chunks, ragged = row_bytes // 16, row_bytes % 16 != 0
-    want = ([ragged and chunks <= 2048] * 2 + [ragged and chunks <= 1024] +
-            [ragged and chunks <= 2048] * 3)
+    want = [ragged and chunks <= 2048] * 6
     assert [("staged" in p) for p in plans] == want, plans

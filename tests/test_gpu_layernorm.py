@@ -443,7 +443,9 @@ def test_layernorm_casts_without_fp32_outputs(M, N, dt):
                                     (130, 1001, "f16"), (5, 7, "bf16"), (3, 3, "f32"),
                                     (64, 515, "bf16"), (17, 8183, "bf16"), (33, 4095, "f32"),
                                     (300, 2050, "f16"), (9, 6, "f16"), (1, 4095, "bf16"),
-                                    (2, 1, "f32"), (611, 8190, "bf16"), (40, 4099, "f32")],
+                                    (2, 1, "f32"), (611, 8190, "bf16"), (40, 4099, "f32"),
+                                    (97, 12290, "bf16"), (33, 16383, "bf16"), (17, 8191, "f32"),
+                                    (50, 6001, "f32"), (9, 16390, "f16")],
                          ids=lambda v: str(v))
 def test_layernorm_staged_kernel(M, N, dt, with_dbeta, mode):
     """The LayerNorm staged phase-class kernel (RN_OPT_GENERIC_KERNEL = 5): each CTA
@@ -457,13 +459,16 @@ def test_layernorm_staged_kernel(M, N, dt, with_dbeta, mode):
     plan = native.last_plan()
     assert plan.startswith("engine=ln_generic staged "), plan
     assert ("atomic" if mode == 2 else "scratch") in plan, plan
+    chunks = N * (4 if dt == "f32" else 2) // 16
+    assert (" cpt=4 " in plan) == (chunks > 512), plan   # 2 chunks a thread up to 512 a row
     check(ex, out, with_dbeta=with_dbeta, tag=" [%s]" % plan)
     assert native.take_device_status() == 0
 
 
 @pytest.mark.parametrize("cpt,teams,slots", [(1, 0, 0), (0, 1, 0), (0, 0, 3), (0, 0, 4),
-                                             (1, 3, 3)])
-@pytest.mark.parametrize("M,N,dt", [(1000, 4095, "bf16"), (130, 1001, "f16"), (97, 2050, "f32")],
+                                             (1, 3, 3), (4, 0, 0), (2, 0, 0), (4, 3, 3)])
+@pytest.mark.parametrize("M,N,dt", [(1000, 4095, "bf16"), (130, 1001, "f16"), (97, 2050, "f32"),
+                                    (77, 8190, "bf16")],
                          ids=lambda v: str(v))
 def test_layernorm_staged_kernel_forced_tiles(M, N, dt, cpt, teams, slots):
     """Chunks per thread, teams per CTA and slots per team forced through the options."""
@@ -475,11 +480,13 @@ def test_layernorm_staged_kernel_forced_tiles(M, N, dt, cpt, teams, slots):
     out = run_gpu(ex)
     plan = native.last_plan()
     chunks = N * (4 if dt == "f32" else 2) // 16
-    if cpt == 1 and chunks > 512:
+    if (cpt or (2 if chunks <= 512 else 4)) * 512 < chunks:
         # a team of more than 512 threads: the phase-class kernel takes the rows instead
         assert plan.startswith("engine=ln_generic phase "), plan
     else:
         assert plan.startswith("engine=ln_generic staged "), plan
+        if cpt:
+            assert " cpt=%d " % cpt in plan, plan
     check(ex, out, tag=" [%s]" % plan)
     assert native.take_device_status() == 0
 
@@ -529,7 +536,9 @@ def test_layernorm_staged_kernel_wait_runs_out(skip):
                                            (2048, 4095, "f32", "staged"),
                                            (2048, 4095, "bf16", "staged"),   # two teams: split
                                            (12160, 4095, "bf16", "phase"),   # 40 rows a CTA
-                                           (4096, 8190, "bf16", "staged")],  # one team
+                                           (4096, 8190, "bf16", "staged"),   # 4 chunks, split
+                                           (2048, 12290, "bf16", "staged"),  # 4 chunks a thread
+                                           (2048, 16393, "bf16", "vec")],    # 2049 chunks
                          ids=lambda v: str(v))
 def test_layernorm_staged_kernel_default_choice(M, N, dt, engine):
     """The automatic choice: the staged kernel from 2048 rows, the phase-class kernel
