@@ -952,14 +952,18 @@ static bool plan_ln_phase(const LnBwdProblem &p, const DeviceInfo &d, bool atomi
 // 184.1, f32 4096 x 4095 44.0 -> 37.9; rows of 1025-2048 chunks, which only 4
 // chunks a thread can take, against the vector kernel: bf16 4096 x 12290 216.2 ->
 // 91.0, 4096 x 16383 295.4 -> 103.4; shorter rows lose with 4 (4096 x 4095 34.7 ->
-// 36.9, 4096 x 2047 23.5 -> 26.0).
+// 36.9, 4096 x 2047 23.5 -> 26.0). Rows past 1024 chunks take it at any row count
+// (the vector kernel is the alternative there): bf16 1 x 12290 20.0 -> 15.6, 64 x
+// 12290 26.4 -> 15.7, 1024 x 12290 74.7 -> 34.8, 1024 x 16383 95.4 -> 39.6, f32
+// 512 x 6001 26.1 -> 18.0.
 static bool plan_ln_stage(const LnBwdProblem &p, const DeviceInfo &d, bool atomic, bool forced,
                           StagePlan *plan) {
-    if (!forced && p.M < kStageMinRows) return false;
+    const int64_t maxnv = (int64_t)p.N * elem_bytes(p.dtype) / 16;
+    // below 2048 rows the phase-class kernel, where it can take the rows (up to 1024 chunks)
+    if (!forced && p.M < kStageMinRows && maxnv <= 1024) return false;
     const uintptr_t S = (uintptr_t)elem_bytes(p.dtype), ph = (uintptr_t)p.x & 15u;
     for (const void *q : {p.x, p.dy, static_cast<const void *>(p.dx)})
         if (((uintptr_t)q & 15u) != ph || ((uintptr_t)q % S) != 0) return false;
-    const int64_t maxnv = (int64_t)p.N * elem_bytes(p.dtype) / 16;
     const int copt = g_opts[RN_OPT_CHUNKS_PER_THREAD];
     const int cpt = (copt == 1 || copt == 2 || copt == 4) ? copt : (maxnv <= 512 ? 2 : 4);
     if (maxnv > 512 * (int64_t)cpt) return false;

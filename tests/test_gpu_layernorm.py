@@ -538,13 +538,15 @@ def test_layernorm_staged_kernel_wait_runs_out(skip):
                                            (12160, 4095, "bf16", "phase"),   # 40 rows a CTA
                                            (4096, 8190, "bf16", "staged"),   # 4 chunks, split
                                            (2048, 12290, "bf16", "staged"),  # 4 chunks a thread
+                                           (300, 12290, "bf16", "staged"),   # past 1024 chunks
+                                           (300, 4095, "bf16", "phase"),
                                            (2048, 16393, "bf16", "vec")],    # 2049 chunks
                          ids=lambda v: str(v))
 def test_layernorm_staged_kernel_default_choice(M, N, dt, engine):
     """The automatic choice: the staged kernel from 2048 rows, the phase-class kernel
-    below; a tile of two 256-thread teams (bf16 N = 4095) runs as one team a CTA, up
-    to 40 rows a CTA of two CTAs an SM (the phase-class kernel, which prefetches,
-    beyond)."""
+    below (rows past its 1024 chunks: the staged kernel at any row count); a tile of
+    two 256-thread teams (bf16 N = 4095) runs as one team a CTA, up to 40 rows a CTA
+    of two CTAs an SM (the phase-class kernel, which prefetches, beyond)."""
     ex = expected(Case("ln default", M, N, dt, eps=1e-5, seed=41))
     out = run_gpu(ex)
     plan = native.last_plan()
