@@ -693,8 +693,11 @@ static FwdPhasePlan plan_fwd_phase(const FwdRowProblem &q, const DeviceInfo &d);
 // staged), takes it from 2048 rows:
 //  * LayerNorm, always: bf16 4096 x 4095 24.6 -> 22.5, 16384 x 8190 177.7 -> 117.3, 4096 x
 //    16383 87.9 -> 63.4, 16384 x 2047 71.6 -> 36.4, 32768 x 509 108.0 -> 34.6, f32 4096 x 4095
-//    32.8 -> 26.6, f16 2048 x 1001 14.2 -> 10.6; 2048 x 4095 16.4 -> 16.3 (1024 x 4095 12.2 ->
-//    13.3: too few rows).
+//    32.8 -> 26.6, f16 2048 x 1001 14.2 -> 10.6; 2048 x 4095 16.4 -> 16.3. Below 2048 rows the
+//    16-bit phase-class forward is faster (1024 x 4095 11.9 vs 13.0, 64 x 4095 8.3 vs 10.1, 512
+//    x 1001 8.3 vs 10.1), but the vector kernel is not, from 256 rows: f32 300 x 2999 9.7 ->
+//    8.4, 512 x 4095 11.3 -> 10.1, 1024 x 6001 17.8 -> 16.2, bf16 256 x 12290 13.0 -> 12.1,
+//    1024 x 12290 23.3 -> 20.7, 1024 x 16383 29.0 -> 23.8.
 //  * RMSNorm, with at least 6 rows a team or rows of at most 256 chunks (where the vector
 //    kernel's CTA per row leaves most threads idle): bf16 4096 x 4095 19.5 -> 18.2, 16384 x
 //    8190 98.8 -> 89.1, 32768 x 4095 115.6 -> 86.5, 16384 x 2047 44.8 -> 26.4, f16 16384 x 1001
@@ -711,7 +714,12 @@ constexpr int64_t kFwdStageMinRows = 2048;
 static bool plan_fwd_stage(const FwdRowProblem &q, const DeviceInfo &d, StagePlan *plan) {
     const int pick = g_opts[RN_OPT_GENERIC_KERNEL];
     if (pick != 0 && pick != 5) return false;
-    if (pick == 0 && q.M < kFwdStageMinRows) return false;
+    if (pick == 0 && q.M < kFwdStageMinRows) {
+        // below 2048 rows: only the LayerNorm forward from 256 rows, and only where the vector
+        // kernel would take the rows (fp32, or rows past the phase-class kernel's 1024 chunks)
+        const bool ln_phase = fwd_phase_ok(q) && (q.dtype != kF32 || !fwd_generic_vec_ok(q));
+        if (q.mode != kFwdLn || ln_phase || q.M < 256) return false;
+    }
     if (!fwd_stage_ok(q)) return false;
     const int64_t maxnv = (int64_t)q.N * elem_bytes(q.dtype) / 16;
     int cpt = g_opts[RN_OPT_CHUNKS_PER_THREAD];

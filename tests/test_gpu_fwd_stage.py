@@ -196,13 +196,17 @@ def test_staged_forward_wait_runs_out(skip):
     (2048, 4095, "bf16", (False, False, True)), (2047, 4095, "bf16", (False, False, False)),
     (4096, 4095, "bf16", (True, False, True)), (4096, 1001, "f16", (True, True, True)),
     (4096, 2999, "f32", (True, False, True)), (2048, 12290, "bf16", (True, True, True)),
-    (2048, 16393, "bf16", (False, False, False))],   # 2049 whole chunks
+    (2048, 16393, "bf16", (False, False, False)),   # 2049 whole chunks
+    (300, 2999, "f32", (False, False, True)), (300, 4095, "bf16", (False, False, False)),
+    (255, 2999, "f32", (False, False, False)), (300, 12290, "bf16", (False, False, True))],
     ids=lambda v: str(v))
 def test_staged_forward_default_choice(M, N, dt, staged):
     """The automatic choice (RMSNorm, fused-add, LayerNorm): the staged forward
     from 2048 rows within 2048 whole chunks a row; RMSNorm with at least 6 rows
     a team or rows of at most 256 chunks, fused-add with one team a CTA or rows
-    of at most 256 chunks; the vector or phase-class forward otherwise."""
+    of at most 256 chunks; the vector or phase-class forward otherwise. Below
+    2048 rows the LayerNorm forward takes it from 256 rows where the vector
+    kernel would run (fp32, rows past 1024 chunks)."""
     inp = synth.make_inputs(Case("fwd default %s" % dt, M, N, dt, fused=True, seed=66))
     for plan, want in zip(_run_all(inp, dt), staged):
         assert ("engine=generic staged " in plan) == want, plan
