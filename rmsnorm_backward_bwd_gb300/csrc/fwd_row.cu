@@ -15,7 +15,12 @@
 // next rows into a private shared-memory ring with cp.async (no barrier
 // guards the ring: a thread reads back only what it copied). The row sums are
 // reduced over the team (warp shuffles, one named barrier, double-buffered
-// slots). Every input byte is read from HBM once.
+// slots). Every input byte is read from HBM once. The LayerNorm forward reads
+// its chunks from the ring once into registers and takes both sums and the
+// output from there on packed fp32 pairs (measured on GB300, us per call, three
+// passes over the ring -> registers: bf16 4096^2 20.4 -> 18.3, 16384 x 8192
+// 107.6 -> 94.5, 4096 x 8192 33.0 -> 30.3, 16384 x 2048 34.6 -> 30.7, f32 4096^2
+// 26.1 -> 24.5; f16 4096 x 1024 10.8 -> 11.6 the one loss measured).
 #include "common.cuh"
 #include "launch.h"
 
@@ -142,36 +147,67 @@ __global__ void __launch_bounds__(FwdBounds<CPT>::kMaxThreads, 1) fwd_row_kernel
 
         float mu = 0.f, rs;
         if (MODE == kFwdLn) {
-            float s = 0.f;
+            // the row's chunks read once into registers; sums on packed fp32 pairs
+            uint4 xv[CPT];
+            f32x2 s2 = f2_make(0.f, 0.f);
 #pragma unroll
             for (int kk = 0; kk < CPT; ++kk) {
+                xv[kk] = cok[kk] ? ld_shared_v4(sb + kk * kk_bytes) : make_uint4(0, 0, 0, 0);
                 if (cok[kk]) {
                     float v[V];
-                    chunk_to_float<T>(ld_shared_v4(sb + kk * kk_bytes), v);
+                    chunk_to_float<T>(xv[kk], v);
 #pragma unroll
-                    for (int e = 0; e < V; ++e) s += v[e];
+                    for (int e = 0; e < V; e += 2) s2 = f2_add(f2_make(v[e], v[e + 1]), s2);
                 }
             }
-            mu = fwd_team_sum(s, red, parity, team, warp, lane, team_warps, first_warp,
+            float slo, shi;
+            f2_split(s2, slo, shi);
+            mu = fwd_team_sum(slo + shi, red, parity, team, warp, lane, team_warps, first_warp,
                               a.team_threads) * a.inv_n;
             parity ^= 1;
-            float q = 0.f;
+            const f32x2 m2 = f2_make(-mu, -mu);
+            f32x2 q2 = f2_make(0.f, 0.f);
 #pragma unroll
             for (int kk = 0; kk < CPT; ++kk) {
                 if (cok[kk]) {
                     float v[V];
-                    chunk_to_float<T>(ld_shared_v4(sb + kk * kk_bytes), v);
+                    chunk_to_float<T>(xv[kk], v);
 #pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        const float d = v[e] - mu;
-                        q = fmaf(d, d, q);
+                    for (int e = 0; e < V; e += 2) {
+                        const f32x2 d = f2_add(f2_make(v[e], v[e + 1]), m2);
+                        q2 = f2_fma(d, d, q2);
                     }
                 }
             }
-            q = fwd_team_sum(q, red, parity, team, warp, lane, team_warps, first_warp,
-                             a.team_threads);
+            f2_split(q2, slo, shi);
+            const float q = fwd_team_sum(slo + shi, red, parity, team, warp, lane, team_warps,
+                                         first_warp, a.team_threads);
             parity ^= 1;
             rs = rsqrtf(q * a.inv_n + a.eps);
+            if (tt == 0) {
+                if (a.mean) a.mean[row] = mu;
+                if (a.rstd) a.rstd[row] = rs;
+            }
+            const f32x2 rs2 = f2_make(rs, rs);
+#pragma unroll
+            for (int kk = 0; kk < CPT; ++kk) {
+                if (cok[kk]) {
+                    float v[V], g[V], b[V], o[V];
+                    chunk_to_float<T>(xv[kk], v);
+                    chunk_to_float<T>(gp[kk], g);
+                    chunk_to_float<T>(bp[kk], b);
+#pragma unroll
+                    for (int e = 0; e < V; e += 2) {
+                        const f32x2 t = f2_fma(f2_mul(f2_add(f2_make(v[e], v[e + 1]), m2), rs2),
+                                               f2_make(g[e], g[e + 1]), f2_make(b[e], b[e + 1]));
+                        f2_split(t, o[e], o[e + 1]);
+                    }
+                    st_global_v4(a.y + off + coff[kk], float_to_chunk<T>(o));
+                }
+            }
+            if (++slot == S) slot = 0;
+            if (++fill == S) fill = 0;
+            continue;
         } else {
             float ss = 0.f;
 #pragma unroll
