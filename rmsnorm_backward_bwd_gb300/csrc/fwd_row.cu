@@ -15,25 +15,22 @@
 // next rows into a private shared-memory ring with cp.async (no barrier
 // guards the ring: a thread reads back only what it copied). The row sums are
 // reduced over the team (warp shuffles, one named barrier, double-buffered
-// slots). Every input byte is read from HBM once. The LayerNorm forward reads
-// its chunks from the ring once into registers and takes both sums and the
-// output from there on packed fp32 pairs (measured on GB300, us per call, three
-// passes over the ring -> registers: bf16 4096^2 20.4 -> 18.3, 16384 x 8192
+// slots). Every input byte is read from HBM once. A thread reads its chunks
+// from the ring once into registers (fused-add: the rounded sum, which is also
+// stored as residual_out) and takes the sums and the output from there on
+// packed fp32 pairs. Measured on GB300 (us per call, passes over the ring with
+// scalar sums -> registers): LayerNorm bf16 4096^2 20.4 -> 18.3, 16384 x 8192
 // 107.6 -> 94.5, 4096 x 8192 33.0 -> 30.3, 16384 x 2048 34.6 -> 30.7, f32 4096^2
-// 26.1 -> 24.5; f16 4096 x 1024 10.8 -> 11.6 the one loss measured).
+// 26.1 -> 24.5 (f16 4096 x 1024 10.8 -> 11.6); RMSNorm bf16 4096^2 16.1 -> 14.6,
+// 16384 x 8192 83.4 -> 81.9, 16384 x 2048 24.3 -> 22.3, 16384 x 1024 16.2 -> 14.9;
+// fused-add within 2 % either way (16384 x 8192 165.8 -> 164.0, 16384 x 1024 20.4
+// -> 20.8).
 #include "common.cuh"
 #include "launch.h"
 
 namespace rn {
 
 constexpr int kFwdRingOffset = 256;  // [2 parities][32 warps] fp32 warp sums first
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 &v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};"
-                 :
-                 : "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
 
 size_t fwd_row_smem_bytes(int teams, int stages, int ntensors, int team_chunks) {
     return (size_t)kFwdRingOffset + (size_t)teams * stages * ntensors * (size_t)team_chunks * 16;
@@ -209,54 +206,54 @@ __global__ void __launch_bounds__(FwdBounds<CPT>::kMaxThreads, 1) fwd_row_kernel
             if (++fill == S) fill = 0;
             continue;
         } else {
-            float ss = 0.f;
+            // the row's chunks once into registers (fused-add: the rounded sum, also stored as
+            // residual_out); the sum of squares and the output on packed fp32 pairs
+            uint4 xv[CPT];
+            f32x2 s2 = f2_make(0.f, 0.f);
 #pragma unroll
             for (int kk = 0; kk < CPT; ++kk) {
+                xv[kk] = cok[kk] ? ld_shared_v4(sb + kk * kk_bytes) : make_uint4(0, 0, 0, 0);
                 if (cok[kk]) {
                     float v[V];
-                    uint4 xv = ld_shared_v4(sb + kk * kk_bytes);
+                    chunk_to_float<T>(xv[kk], v);
                     if (MODE == kFwdFused) {
-                        // added = x + residual, rounded to the dtype: stored as
-                        // residual_out and kept (in place of x) for the output
                         float r[V];
-                        chunk_to_float<T>(xv, v);
                         chunk_to_float<T>(ld_shared_v4(sb + tensor_bytes + kk * kk_bytes), r);
 #pragma unroll
                         for (int e = 0; e < V; ++e) v[e] = v[e] + r[e];
-                        xv = float_to_chunk<T>(v);
-                        st_shared_v4(sb + kk * kk_bytes, xv);
-                        st_global_v4(a.res_out + off + coff[kk], xv);
+                        xv[kk] = float_to_chunk<T>(v);
+                        st_global_v4(a.res_out + off + coff[kk], xv[kk]);
+                        chunk_to_float<T>(xv[kk], v);
                     }
-                    chunk_to_float<T>(xv, v);
 #pragma unroll
-                    for (int e = 0; e < V; ++e) ss = fmaf(v[e], v[e], ss);
+                    for (int e = 0; e < V; e += 2) {
+                        const f32x2 p2 = f2_make(v[e], v[e + 1]);
+                        s2 = f2_fma(p2, p2, s2);
+                    }
                 }
             }
-            ss = fwd_team_sum(ss, red, parity, team, warp, lane, team_warps, first_warp,
-                              a.team_threads);
+            float slo, shi;
+            f2_split(s2, slo, shi);
+            const float ss = fwd_team_sum(slo + shi, red, parity, team, warp, lane, team_warps,
+                                          first_warp, a.team_threads);
             parity ^= 1;
             rs = rsqrtf(ss * a.inv_n + a.eps);
-        }
-        if (tt == 0) {
-            if (MODE == kFwdLn && a.mean) a.mean[row] = mu;
-            if (a.rstd) a.rstd[row] = rs;
-        }
+            if (tt == 0 && a.rstd) a.rstd[row] = rs;
+            const f32x2 rs2 = f2_make(rs, rs);
 #pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            if (cok[kk]) {
-                float v[V], g[V], o[V];
-                chunk_to_float<T>(ld_shared_v4(sb + kk * kk_bytes), v);
-                chunk_to_float<T>(gp[kk], g);
-                if (MODE == kFwdLn) {
-                    float b[V];
-                    chunk_to_float<T>(bp[kk], b);
+            for (int kk = 0; kk < CPT; ++kk) {
+                if (cok[kk]) {
+                    float v[V], g[V], o[V];
+                    chunk_to_float<T>(xv[kk], v);
+                    chunk_to_float<T>(gp[kk], g);
 #pragma unroll
-                    for (int e = 0; e < V; ++e) o[e] = fmaf((v[e] - mu) * rs, g[e], b[e]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < V; ++e) o[e] = v[e] * rs * g[e];
+                    for (int e = 0; e < V; e += 2) {
+                        const f32x2 t = f2_mul(f2_mul(f2_make(v[e], v[e + 1]), rs2),
+                                               f2_make(g[e], g[e + 1]));
+                        f2_split(t, o[e], o[e + 1]);
+                    }
+                    st_global_v4(a.y + off + coff[kk], float_to_chunk<T>(o));
                 }
-                st_global_v4(a.y + off + coff[kk], float_to_chunk<T>(o));
             }
         }
         if (++slot == S) slot = 0;
