@@ -122,3 +122,48 @@ def test_graph_keeps_its_workspace_after_the_cache_grows():
     parity.check_bwd(ex, dx, None, dw32)
     for c in canaries:
         assert bool((c == 0x5A).all()), "a graph replay wrote into a later tensor"
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_staged_kernels_captured_in_a_cuda_graph(mode):
+    """The staged phase-class kernels (mbarriers initialised by every launch)
+    replayed from a CUDA graph: the RMSNorm backward and the three forwards on
+    rows that are not 16-byte multiples; every replay rewrites every output and
+    matches the eager call bit for bit."""
+    native.set_option(native.OPT_DWEIGHT_MODE, mode)
+    native.set_option(native.OPT_GENERIC_KERNEL, 5)
+    ex = parity.expected_bwd(Case("graph staged", 2048, 4095, "bf16", fused=True, with_dres=True,
+                                  seed=81))
+    t = _device_inputs(ex)
+    x, g, dy, rstd, dres = t["x"], t["g"], t["dy"], t["rstd"], t["dres"]
+    outs = {k: torch.empty_like(x) for k in ("dx", "y", "lny")}
+    dw32 = torch.empty(4095, dtype=torch.float32, device="cuda")
+    dw = torch.empty(4095, dtype=x.dtype, device="cuda")
+    st1 = {k: torch.empty(2048, dtype=torch.float32, device="cuda") for k in ("rstd", "mean", "lrstd")}
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ws = rn.bwd_workspace(2048, 4095, x.dtype, x.device)
+
+        def call():
+            rn.fused_add_rmsnorm_bwd(x, g, dy, rstd, dres, dx=outs["dx"], dweight_f32=dw32,
+                                     dweight=dw, workspace=ws)
+            rn.rmsnorm_fwd(x, g, 1e-6, y=outs["y"], rstd=st1["rstd"])
+            rn.layernorm_fwd(x, g, g, 1e-5, y=outs["lny"], mean=st1["mean"], rstd=st1["lrstd"])
+        call()   # first call outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert "staged" in native.last_plan(), native.last_plan()
+    eager = {k: v.clone() for k, v in list(outs.items()) + list(st1.items())}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        call()
+    for _ in range(2):
+        for buf in list(outs.values()) + list(st1.values()) + [dw32, dw]:
+            buf.fill_(7)      # every replay must rewrite every output
+        graph.replay()
+        torch.cuda.synchronize()
+        for k, v in list(outs.items()) + list(st1.items()):
+            assert torch.equal(v, eager[k]), k   # dx, y and the statistics are deterministic
+        parity.check_bwd(ex, outs["dx"], dw, dw32)
+    assert native.take_device_status() == 0
