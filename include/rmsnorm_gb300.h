@@ -255,11 +255,13 @@ typedef enum rn_option {
                                  2 = fp32 atomics + cast (summation order varies from call to
                                  call). Automatic: scratch when a row tensor holds at most
                                  2 MiB (fewer launches), else atomics where possible */
-    RN_OPT_CHUNKS_PER_THREAD = 2, /* row engine and staged phase-class kernel: 16-byte chunks
-                                 per thread per row: 1, 2, 4 */
-    RN_OPT_TEAMS_PER_CTA = 3, /* row engine and staged phase-class kernel: rows processed at
-                                 once per CTA (1..15); RMSNorm backward phase-class kernel:
-                                 rows per CTA iteration (1 or 2) */
+    RN_OPT_CHUNKS_PER_THREAD = 2, /* row engine and staged phase-class kernels: 16-byte chunks
+                                 per thread per row: 1, 2, 4 (default: by row length) */
+    RN_OPT_TEAMS_PER_CTA = 3, /* row engine and staged phase-class kernels: rows processed at
+                                 once per CTA (1..15; the staged kernels otherwise run a tile of
+                                 two teams of 192-256 threads as one team a CTA at two CTAs an
+                                 SM); RMSNorm backward phase-class kernel: rows per CTA
+                                 iteration (1 or 2) */
     RN_OPT_STAGES = 4,        /* row engine: rows in flight per team (2..8); staged
                                  phase-class kernel: shared-memory slots per team (2..4) */
     RN_OPT_GRID = 5,          /* CTAs of the row pass (default: one per SM; at most 2 per SM) */
